@@ -1,0 +1,499 @@
+/*
+ * laya_oracle.c -- plain, slow CPU definition of the Laya encoder forward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the checker that the CUDA library is
+ * compared against.  Only the test-suite, the smoke check and the benchmark's
+ * CPU-baseline leg may load it.  It shares no code, header, table generator or
+ * helper with the CUDA library: everything below (BF16 rounding, RoPE tables,
+ * LayerNorm, attention, GeGLU) is written out here on its own.
+ *
+ * What is computed (sources):
+ *  - "Run Laya encoder and decision layers on CUDA" (PR #49), section
+ *    "H800 comparison": the timed scope is token embedding + 28 encoder layers
+ *    + 2 decision transformer layers; hidden states are the output (section
+ *    "Purpose": they stay on the GPU for the scorer).
+ *  - "[RFC]: Native Laya inference with Rust and CUDA #14", section "Design":
+ *    each layer runs a QKV projection, then RoPE, then attention as separate
+ *    steps.
+ *  - "[Performance]: Optimize native Rust/CUDA Laya inference #66", section
+ *    "Starting evidence": separate global and local rotary tables.
+ *  - "Laya native CUDA worker", section "Prepare the checkpoint and bundle":
+ *    rotary tables reproduce a BF16 rounding of their values.
+ *  - "perf(model): exact Metal speed-ups of the forward pass - #45": the
+ *    encoder has no biases; the attention mask is one (b,1,1,s) key-padding
+ *    row broadcast over every query.
+ *  - PR #49, section "Test Result": query rows whose keys are all padding are
+ *    excluded from equality checks (here: their context is defined as 0).
+ *
+ * Readings where the pages are silent (each one is a choice, not a quotation):
+ *  pre-norm residual layers; LayerNorm (no bias) right after the embedding
+ *  gather; identity attention-norm at encoder layer 0; one final LayerNorm
+ *  after the last encoder layer and none after the decision layers; GeGLU with
+ *  the first half of the up-projection through exact (erf) GELU times the
+ *  second half; rotate-half RoPE pairs (i, i + D/2); positions are indices in
+ *  the padded row; attention scale 1/sqrt(D); a local layer lets query i see
+ *  key j iff |i - j| <= half_window; encoder layer l is global iff
+ *  l % global_every == 0 and decision layers are always global.
+ *
+ * Precision: fp32 arithmetic; values are rounded to BF16 (round to nearest
+ * even) exactly where the GPU path stores BF16.  Dot products are sequential
+ * fp32 sums over k ascending (or fp64 when cfg.accum_f64 is set: a diagnostic
+ * used to size the rounding floor).  Build with -ffp-contract=off so that no
+ * multiply-add is fused.
+ *
+ * Parity status: every step function below is pinned by the CPU tests in
+ * tests/test_oracle_*.py (closed forms, exact integer cases, invariants, fp64
+ * brute force on tiny inputs).  The full-stack output at the real sizes has no
+ * published value to pin it to: "parity unpinned" beyond the pinned steps and
+ * the stack invariants (padding, permutation, truncation, structure tests).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_ABI 1
+
+typedef struct {
+  int32_t hidden, heads, head_dim, intermediate, vocab;
+  int32_t n_encoder_layers, n_decision_layers;
+  int32_t global_every, local_half_window;
+  float theta_global, theta_local, ln_eps;
+  int32_t max_seq;
+  int32_t rope_table_bf16;
+  int32_t first_attn_norm_identity, final_norm;
+  int32_t accum_f64;
+} orc_config;
+
+int orc_abi(void) { return ORC_ABI; }
+
+int orc_set_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+  return omp_get_max_threads();
+#else
+  (void)n;
+  return 1;
+#endif
+}
+
+/* ---------------------------------------------------------------- BF16 --- */
+
+/* Round an fp32 value to the nearest BF16 value, ties to even; NaN stays NaN. */
+float orc_bf16_round(float x) {
+  uint32_t u;
+  memcpy(&u, &x, 4);
+  if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu) != 0u) {
+    u = (u | 0x00400000u) & 0xffff0000u; /* quiet NaN, keep sign */
+  } else {
+    uint32_t lsb = (u >> 16) & 1u;
+    u = (u + 0x7fffu + lsb) & 0xffff0000u;
+  }
+  float y;
+  memcpy(&y, &u, 4);
+  return y;
+}
+
+uint16_t orc_f32_to_bf16_bits(float x) {
+  float r = orc_bf16_round(x);
+  uint32_t u;
+  memcpy(&u, &r, 4);
+  return (uint16_t)(u >> 16);
+}
+
+float orc_bf16_bits_to_f32(uint16_t h) {
+  uint32_t u = ((uint32_t)h) << 16;
+  float y;
+  memcpy(&y, &u, 4);
+  return y;
+}
+
+static void bits_to_f32(const uint16_t* src, size_t n, float* dst) {
+  for (size_t i = 0; i < n; ++i) dst[i] = orc_bf16_bits_to_f32(src[i]);
+}
+
+static void f32_to_bits(const float* src, size_t n, uint16_t* dst) {
+  for (size_t i = 0; i < n; ++i) dst[i] = orc_f32_to_bf16_bits(src[i]);
+}
+
+/* ----------------------------------------------------------- LayerNorm --- */
+
+/* y = (x - mean) * (1 / sqrt(var + eps)) * gamma, no bias, two passes in fp32
+ * (mean first, then the mean of squared deviations), one BF16 rounding. */
+void orc_layernorm_row(const float* x, const float* gamma, int n, float eps,
+                       float* y) {
+  float sum = 0.0f;
+  for (int i = 0; i < n; ++i) sum += x[i];
+  float mean = sum / (float)n;
+  float sq = 0.0f;
+  for (int i = 0; i < n; ++i) {
+    float d = x[i] - mean;
+    sq += d * d;
+  }
+  float var = sq / (float)n;
+  float rstd = 1.0f / sqrtf(var + eps);
+  for (int i = 0; i < n; ++i) y[i] = orc_bf16_round(((x[i] - mean) * rstd) * gamma[i]);
+}
+
+static void layernorm_rows(const float* x, const float* gamma, int rows, int n,
+                           float eps, float* y) {
+#pragma omp parallel for schedule(static)
+  for (int r = 0; r < rows; ++r)
+    orc_layernorm_row(x + (size_t)r * n, gamma, n, eps, y + (size_t)r * n);
+}
+
+/* -------------------------------------------------------------- Linear --- */
+
+/* y[r][o] = sum_k x[r][k] * w[o][k]   (nn.Linear layout: w is [out][in]).
+ * Sequential sum over k ascending; the result is NOT rounded here. */
+static void linear_rows(const float* x, int rows, int in, const float* w,
+                        int out, float* y, int f64) {
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int r = 0; r < rows; ++r) {
+    for (int o = 0; o < out; ++o) {
+      const float* xr = x + (size_t)r * in;
+      const float* wo = w + (size_t)o * in;
+      if (f64) {
+        double acc = 0.0;
+        for (int k = 0; k < in; ++k) acc += (double)xr[k] * (double)wo[k];
+        y[(size_t)r * out + o] = (float)acc;
+      } else {
+        float acc = 0.0f;
+        for (int k = 0; k < in; ++k) acc += xr[k] * wo[k];
+        y[(size_t)r * out + o] = acc;
+      }
+    }
+  }
+}
+
+/* ---------------------------------------------------------------- GELU --- */
+
+/* Exact GELU: 0.5 * z * (1 + erf(z / sqrt(2))), with the C library's erff. */
+float orc_gelu(float z) {
+  return (0.5f * z) * (1.0f + erff(z * 0.70710678118654752f));
+}
+
+/* ---------------------------------------------------------------- RoPE --- */
+
+/* Table of cos/sin for positions [0, max_seq) and pair index i in [0, half):
+ * frequency theta^(-2i / (2*half)) and angle p * frequency, both in fp64;
+ * cos and sin are taken in fp64, rounded to fp32 and, if bf16 is set, then to
+ * BF16 (kept as fp32 values).  Layout: [pos][i]. */
+void orc_rope_table(double theta, int max_seq, int half, int bf16, float* cos_t,
+                    float* sin_t) {
+  for (int p = 0; p < max_seq; ++p) {
+    for (int i = 0; i < half; ++i) {
+      double freq = pow(theta, -2.0 * (double)i / (double)(2 * half));
+      double ang = (double)p * freq;
+      float c = (float)cos(ang);
+      float s = (float)sin(ang);
+      if (bf16) {
+        c = orc_bf16_round(c);
+        s = orc_bf16_round(s);
+      }
+      cos_t[(size_t)p * half + i] = c;
+      sin_t[(size_t)p * half + i] = s;
+    }
+  }
+}
+
+/* Rotate one head vector of length 2*half in place, pairs (i, i + half):
+ *   y[i]        = bf16( x1*c - x2*s )
+ *   y[i + half] = bf16( x2*c + x1*s )
+ * each product and the sum rounded to fp32 separately (no fused multiply-add).
+ */
+void orc_rope_vec(float* v, const float* c, const float* s, int half) {
+  for (int i = 0; i < half; ++i) {
+    float x1 = v[i], x2 = v[i + half];
+    float a = x1 * c[i];
+    float b = x2 * s[i];
+    float d = x2 * c[i];
+    float e = x1 * s[i];
+    v[i] = orc_bf16_round(a - b);
+    v[i + half] = orc_bf16_round(d + e);
+  }
+}
+
+/* ----------------------------------------------------------- Attention --- */
+
+/* Context for one (row b, head n): q, k, v are rows of the packed [S, 3H]
+ * projection (q at column n*D, k at H + n*D, v at 2H + n*D).  Query i sees key
+ * j iff j < len and (global or |i - j| <= half_window).  Scores are
+ * dot(q_i, k_j) / sqrt(D); softmax with the maximum subtracted; the context is
+ * the probability-weighted sum of v, rounded to BF16.  A query with no visible
+ * key gets context 0. */
+static void attention_head(const float* qkv, int S, int H, int D, int n,
+                           int len, int global, int half_window, float* ctx,
+                           float* scores /* scratch [S] */) {
+  const float scale = 1.0f / sqrtf((float)D);
+  const size_t ld = (size_t)3 * H;
+  for (int i = 0; i < S; ++i) {
+    const float* q = qkv + (size_t)i * ld + (size_t)n * D;
+    float* out = ctx + (size_t)i * H + (size_t)n * D;
+    int lo = 0, hi = len; /* keys [lo, hi) */
+    if (!global) {
+      if (i - half_window > lo) lo = i - half_window;
+      if (i + half_window + 1 < hi) hi = i + half_window + 1;
+    }
+    if (lo >= hi) {
+      for (int d = 0; d < D; ++d) out[d] = 0.0f;
+      continue;
+    }
+    float m = -INFINITY;
+    for (int j = lo; j < hi; ++j) {
+      const float* k = qkv + (size_t)j * ld + H + (size_t)n * D;
+      float dot = 0.0f;
+      for (int d = 0; d < D; ++d) dot += q[d] * k[d];
+      scores[j] = dot * scale;
+      if (scores[j] > m) m = scores[j];
+    }
+    float sum = 0.0f;
+    for (int j = lo; j < hi; ++j) {
+      scores[j] = expf(scores[j] - m);
+      sum += scores[j];
+    }
+    for (int j = lo; j < hi; ++j) scores[j] = scores[j] / sum;
+    for (int d = 0; d < D; ++d) {
+      float acc = 0.0f;
+      for (int j = lo; j < hi; ++j) {
+        const float* v = qkv + (size_t)j * ld + 2 * (size_t)H + (size_t)n * D;
+        acc += scores[j] * v[d];
+      }
+      out[d] = orc_bf16_round(acc);
+    }
+  }
+}
+
+static void attention_rows(const float* qkv, const int32_t* lengths, int B,
+                           int S, int H, int heads, int D, int global,
+                           int half_window, float* ctx) {
+#pragma omp parallel
+  {
+    float* scores = (float*)malloc(sizeof(float) * (size_t)(S > 0 ? S : 1));
+#pragma omp for collapse(2) schedule(static)
+    for (int b = 0; b < B; ++b)
+      for (int n = 0; n < heads; ++n)
+        attention_head(qkv + (size_t)b * S * 3 * H, S, H, D, n, lengths[b],
+                       global, half_window, ctx + (size_t)b * S * H, scores);
+    free(scores);
+  }
+}
+
+/* ------------------------------------------------- step entry points ----- */
+/* Each takes BF16 bit patterns (uint16) in and out, so that the GPU steps can
+ * be compared with the same storage points.  They exist for the per-step
+ * parity tests; orc_forward below composes the same pieces. */
+
+void orc_step_layernorm(const uint16_t* x, const uint16_t* gamma, int rows,
+                        int n, float eps, uint16_t* y) {
+  float* xf = (float*)malloc(sizeof(float) * (size_t)rows * n);
+  float* gf = (float*)malloc(sizeof(float) * (size_t)n);
+  float* yf = (float*)malloc(sizeof(float) * (size_t)rows * n);
+  bits_to_f32(x, (size_t)rows * n, xf);
+  bits_to_f32(gamma, (size_t)n, gf);
+  layernorm_rows(xf, gf, rows, n, eps, yf);
+  f32_to_bits(yf, (size_t)rows * n, y);
+  free(xf); free(gf); free(yf);
+}
+
+/* y = x . w^T in fp32, returned unrounded (fp32) for checks of the sums. */
+void orc_step_linear_f32(const uint16_t* x, int rows, int in, const uint16_t* w,
+                         int out, int f64, float* y) {
+  float* xf = (float*)malloc(sizeof(float) * (size_t)rows * in);
+  float* wf = (float*)malloc(sizeof(float) * (size_t)out * in);
+  bits_to_f32(x, (size_t)rows * in, xf);
+  bits_to_f32(w, (size_t)out * in, wf);
+  linear_rows(xf, rows, in, wf, out, y, f64);
+  free(xf); free(wf);
+}
+
+/* Epilogue kinds of the three stored projections:
+ *   0: y = bf16(x . w^T)                      (QKV)
+ *   1: y = bf16(r + x . w^T), r given as BF16  (attention output, MLP down)
+ *   2: y = bf16(gelu(a[:, :I]) * a[:, I:]), a = x . w^T with out = 2I (GeGLU) */
+void orc_step_linear(const uint16_t* x, int rows, int in, const uint16_t* w,
+                     int out, int kind, const uint16_t* residual, uint16_t* y) {
+  float* a = (float*)malloc(sizeof(float) * (size_t)rows * out);
+  orc_step_linear_f32(x, rows, in, w, out, 0, a);
+  if (kind == 2) {
+    int I = out / 2;
+    for (int r = 0; r < rows; ++r)
+      for (int j = 0; j < I; ++j) {
+        float u = a[(size_t)r * out + j];
+        float g = a[(size_t)r * out + I + j];
+        y[(size_t)r * I + j] = orc_f32_to_bf16_bits(orc_gelu(u) * g);
+      }
+  } else {
+    for (size_t e = 0; e < (size_t)rows * out; ++e) {
+      float v = a[e];
+      if (kind == 1) v = orc_bf16_bits_to_f32(residual[e]) + v;
+      y[e] = orc_f32_to_bf16_bits(v);
+    }
+  }
+  free(a);
+}
+
+/* RoPE on the q and k slices of a packed [B*S, 3H] projection, in place; the
+ * v slice is not touched.  Position of token (b, s) is s. */
+void orc_step_rope(uint16_t* qkv, int B, int S, int H, int heads, int D,
+                   const float* cos_t, const float* sin_t) {
+  int half = D / 2;
+  float* v = (float*)malloc(sizeof(float) * (size_t)D);
+  for (int b = 0; b < B; ++b)
+    for (int s = 0; s < S; ++s)
+      for (int part = 0; part < 2; ++part)
+        for (int n = 0; n < heads; ++n) {
+          uint16_t* p = qkv + ((size_t)b * S + s) * 3 * H + (size_t)part * H + (size_t)n * D;
+          bits_to_f32(p, (size_t)D, v);
+          orc_rope_vec(v, cos_t + (size_t)s * half, sin_t + (size_t)s * half, half);
+          f32_to_bits(v, (size_t)D, p);
+        }
+  free(v);
+}
+
+void orc_step_attention(const uint16_t* qkv, const int32_t* lengths, int B,
+                        int S, int H, int heads, int D, int global,
+                        int half_window, uint16_t* ctx) {
+  size_t M = (size_t)B * S;
+  float* qf = (float*)malloc(sizeof(float) * M * 3 * H);
+  float* cf = (float*)malloc(sizeof(float) * M * H);
+  bits_to_f32(qkv, M * 3 * H, qf);
+  attention_rows(qf, lengths, B, S, H, heads, D, global, half_window, cf);
+  f32_to_bits(cf, M * H, ctx);
+  free(qf); free(cf);
+}
+
+/* Embedding gather followed by LayerNorm: x[t] = bf16(LN(E[ids[t]], gamma)). */
+void orc_step_embed_layernorm(const uint16_t* emb, const uint16_t* gamma,
+                              const int32_t* ids, int M, int H, float eps,
+                              uint16_t* x) {
+  float* row = (float*)malloc(sizeof(float) * (size_t)H);
+  float* gf = (float*)malloc(sizeof(float) * (size_t)H);
+  float* y = (float*)malloc(sizeof(float) * (size_t)H);
+  bits_to_f32(gamma, (size_t)H, gf);
+  for (int t = 0; t < M; ++t) {
+    bits_to_f32(emb + (size_t)ids[t] * H, (size_t)H, row);
+    orc_layernorm_row(row, gf, H, eps, y);
+    f32_to_bits(y, (size_t)H, x + (size_t)t * H);
+  }
+  free(row); free(gf); free(y);
+}
+
+/* --------------------------------------------------------- full stack ---- */
+
+/* Weights per layer, in this order (all BF16 bit patterns, nn.Linear layout):
+ *   0 attn_norm [H] (may be NULL at encoder layer 0 when the identity reading
+ *     is on), 1 wqkv [3H, H], 2 wo [H, H], 3 mlp_norm [H], 4 wup [2I, H],
+ *   5 wdown [H, I].
+ * Output: out[B*S*H] fp32 holding BF16 values, the residual stream after the
+ * last decision layer.  If capture_layer >= 0, the residual stream after that
+ * layer (0-based over encoder then decision layers, before the final norm) is
+ * copied to capture.  Returns 0, or -1 on a bad argument. */
+int orc_forward(const orc_config* cfg, const uint16_t* tok_emb,
+                const uint16_t* emb_norm, const uint16_t* final_norm,
+                const uint16_t* const* layer_w, const int32_t* ids,
+                const int32_t* lengths, int B, int S, float* out,
+                int capture_layer, float* capture) {
+  const int H = cfg->hidden, NH = cfg->heads, D = cfg->head_dim;
+  const int I = cfg->intermediate;
+  const int L = cfg->n_encoder_layers + cfg->n_decision_layers;
+  if (B < 1 || S < 1 || S > cfg->max_seq || NH * D != H || (D % 2) != 0)
+    return -1;
+  for (int b = 0; b < B; ++b)
+    if (lengths[b] < 1 || lengths[b] > S) return -1;
+  for (int t = 0; t < B * S; ++t)
+    if (ids[t] < 0 || ids[t] >= cfg->vocab) return -1;
+
+  const size_t M = (size_t)B * S;
+  const int half = D / 2;
+  float* cos_g = (float*)malloc(sizeof(float) * (size_t)cfg->max_seq * half);
+  float* sin_g = (float*)malloc(sizeof(float) * (size_t)cfg->max_seq * half);
+  float* cos_l = (float*)malloc(sizeof(float) * (size_t)cfg->max_seq * half);
+  float* sin_l = (float*)malloc(sizeof(float) * (size_t)cfg->max_seq * half);
+  orc_rope_table(cfg->theta_global, cfg->max_seq, half, cfg->rope_table_bf16, cos_g, sin_g);
+  orc_rope_table(cfg->theta_local, cfg->max_seq, half, cfg->rope_table_bf16, cos_l, sin_l);
+
+  float* x = (float*)malloc(sizeof(float) * M * H);
+  float* h = (float*)malloc(sizeof(float) * M * H);
+  float* qkv = (float*)malloc(sizeof(float) * M * 3 * H);
+  float* ctx = (float*)malloc(sizeof(float) * M * H);
+  float* acc = (float*)malloc(sizeof(float) * M * (size_t)(2 * I > 3 * H ? 2 * I : 3 * H));
+  float* g = (float*)malloc(sizeof(float) * M * I);
+  float* gam = (float*)malloc(sizeof(float) * (size_t)H);
+  size_t wmax = (size_t)3 * H * H;
+  if ((size_t)2 * I * H > wmax) wmax = (size_t)2 * I * H;
+  float* wbuf = (float*)malloc(sizeof(float) * wmax);
+
+  /* token embedding + embedding LayerNorm */
+  {
+    float* row = (float*)malloc(sizeof(float) * (size_t)H);
+    bits_to_f32(emb_norm, (size_t)H, gam);
+    for (size_t t = 0; t < M; ++t) {
+      bits_to_f32(tok_emb + (size_t)ids[t] * H, (size_t)H, row);
+      orc_layernorm_row(row, gam, H, cfg->ln_eps, x + t * H);
+    }
+    free(row);
+  }
+
+  for (int l = 0; l < L; ++l) {
+    const uint16_t* const* w = layer_w + (size_t)6 * l;
+    const int dec = l >= cfg->n_encoder_layers;
+    const int glob = dec || (l % cfg->global_every == 0);
+
+    if (l == cfg->n_encoder_layers && cfg->final_norm) {
+      bits_to_f32(final_norm, (size_t)H, gam);
+      layernorm_rows(x, gam, (int)M, H, cfg->ln_eps, h);
+      memcpy(x, h, sizeof(float) * M * H);
+    }
+
+    /* attention sub-layer: h = LN(x); qkv = h W^T; RoPE; attention; x += ctx Wo^T */
+    if (l == 0 && cfg->first_attn_norm_identity) {
+      memcpy(h, x, sizeof(float) * M * H);
+    } else {
+      bits_to_f32(w[0], (size_t)H, gam);
+      layernorm_rows(x, gam, (int)M, H, cfg->ln_eps, h);
+    }
+    bits_to_f32(w[1], (size_t)3 * H * H, wbuf);
+    linear_rows(h, (int)M, H, wbuf, 3 * H, qkv, cfg->accum_f64);
+    for (size_t e = 0; e < M * 3 * H; ++e) qkv[e] = orc_bf16_round(qkv[e]);
+
+    {
+      const float* ct = glob ? cos_g : cos_l;
+      const float* st = glob ? sin_g : sin_l;
+      for (int b = 0; b < B; ++b)
+        for (int s = 0; s < S; ++s)
+          for (int part = 0; part < 2; ++part)
+            for (int n = 0; n < NH; ++n)
+              orc_rope_vec(qkv + ((size_t)b * S + s) * 3 * H + (size_t)part * H + (size_t)n * D,
+                           ct + (size_t)s * half, st + (size_t)s * half, half);
+    }
+
+    attention_rows(qkv, lengths, B, S, H, NH, D, glob, cfg->local_half_window, ctx);
+
+    bits_to_f32(w[2], (size_t)H * H, wbuf);
+    linear_rows(ctx, (int)M, H, wbuf, H, acc, cfg->accum_f64);
+    for (size_t e = 0; e < M * H; ++e) x[e] = orc_bf16_round(x[e] + acc[e]);
+
+    /* MLP sub-layer: h = LN(x); a = h Wup^T; g = gelu(a_in) * a_gate; x += g Wdn^T */
+    bits_to_f32(w[3], (size_t)H, gam);
+    layernorm_rows(x, gam, (int)M, H, cfg->ln_eps, h);
+    bits_to_f32(w[4], (size_t)2 * I * H, wbuf);
+    linear_rows(h, (int)M, H, wbuf, 2 * I, acc, cfg->accum_f64);
+    for (size_t t = 0; t < M; ++t)
+      for (int j = 0; j < I; ++j)
+        g[t * I + j] = orc_bf16_round(orc_gelu(acc[t * 2 * I + j]) * acc[t * 2 * I + I + j]);
+    bits_to_f32(w[5], (size_t)H * I, wbuf);
+    linear_rows(g, (int)M, I, wbuf, H, acc, cfg->accum_f64);
+    for (size_t e = 0; e < M * H; ++e) x[e] = orc_bf16_round(x[e] + acc[e]);
+
+    if (l == capture_layer && capture) memcpy(capture, x, sizeof(float) * M * H);
+  }
+
+  memcpy(out, x, sizeof(float) * M * H);
+  free(cos_g); free(sin_g); free(cos_l); free(sin_l);
+  free(x); free(h); free(qkv); free(ctx); free(acc); free(g); free(gam); free(wbuf);
+  return 0;
+}
