@@ -1,0 +1,186 @@
+/*
+ * laya_enc.h -- C ABI of the Laya BF16 encoder forward pass on one GB300 (sm_103a).
+ *
+ * The library runs token embedding, the encoder layers and the decision layers
+ * of a bidirectional transformer encoder over a right-padded batch of rows
+ * (at most max_batch rows of at most max_seq tokens, with per-row lengths used
+ * as a key-padding mask) and leaves the final hidden states in a caller-owned
+ * device buffer.
+ *
+ * Sources for the operation:
+ *  - "Run Laya encoder and decision layers on CUDA" (PR #49), sections
+ *    "Purpose" and "H800 comparison": embedding + 28 encoder layers + 2
+ *    decision transformer layers, hidden states left on the GPU.
+ *  - "[RFC]: Native Laya inference with Rust and CUDA #14", section "Design"
+ *    and the C-ABI discussion under "Activity": an ABI version call, int
+ *    return codes, work queued on a caller-supplied stream so that it can be
+ *    captured in a CUDA Graph; per-shape graph capture and replay with an LRU
+ *    cache of at most four shapes and 512 MiB of workspaces.
+ *  - "Laya native CUDA worker", section "Start and check": at most 16 rows and
+ *    512 tokens per row; invalid input is a client error; a native failure
+ *    stops the executor.
+ *  - "[Performance]: Optimize native Rust/CUDA Laya inference #66", section
+ *    "Implementation priorities": group uploads and keep safe host-buffer
+ *    lifetimes.
+ * The per-layer arithmetic (pre-norm layers, GeGLU MLP, rotate-half RoPE with
+ * separate global and local tables, local layers with a sliding window) is the
+ * same definition as the CPU oracle of this repository; see laya_ops.h for
+ * each step.
+ *
+ * Conventions.  Every function returns 0 on success and a negative LAYA_E_*
+ * code on failure.  On an argument error nothing is enqueued and the output
+ * buffer is untouched.  Device pointers must be 16-byte aligned.  A handle is
+ * not thread-safe: calls on one handle must be serialised by the caller.
+ */
+#ifndef LAYA_ENC_H_
+#define LAYA_ENC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LAYA_ENC_ABI_VERSION 1
+
+/* Error codes (negative). */
+#define LAYA_OK 0
+#define LAYA_E_INVAL (-1)       /* bad argument or configuration */
+#define LAYA_E_NOMEM (-2)       /* device or pinned host allocation failed */
+#define LAYA_E_CUDA (-3)        /* a CUDA call failed; the handle is poisoned */
+#define LAYA_E_POISONED (-4)    /* the handle saw an earlier CUDA/device error */
+#define LAYA_E_UNSUPPORTED (-5) /* device is not compute capability 10.3 */
+#define LAYA_E_DEVICE (-6)      /* a kernel reported an error (bounded wait expired,
+                                   id out of range); the handle is poisoned */
+
+/* Model shape.  Plain old data; all fields must be set.
+ * Full model: hidden 1024, heads 16, head_dim 64, intermediate 2624,
+ * vocab 50368, 28 encoder + 2 decision layers, global_every 3,
+ * local_half_window 64, theta_global 160000, theta_local 10000, ln_eps 1e-5,
+ * max_batch 16, max_seq 512, rope_table_bf16 1, first_attn_norm_identity 1,
+ * final_norm 1.
+ * Supported: hidden a multiple of 256 and at most 2048, head_dim 64,
+ * heads * head_dim == hidden, intermediate a multiple of 64,
+ * max_seq <= 512, max_batch <= 16. */
+typedef struct {
+  int32_t hidden, heads, head_dim, intermediate, vocab;
+  int32_t n_encoder_layers, n_decision_layers;
+  int32_t global_every;      /* encoder layer l is global iff l % global_every == 0;
+                                decision layers are always global */
+  int32_t local_half_window; /* local layers: query i sees key j iff |i - j| <= this */
+  float theta_global, theta_local, ln_eps;
+  int32_t max_batch, max_seq;
+  int32_t rope_table_bf16;          /* 1: RoPE table values rounded to BF16 (kept fp32) */
+  int32_t first_attn_norm_identity; /* 1: encoder layer 0 projects x without LayerNorm */
+  int32_t final_norm;               /* 1: LayerNorm after the last encoder layer */
+} laya_enc_config;
+
+/* Per-layer weights: device pointers to BF16 data in nn.Linear layout
+ * [out_features, in_features], row-major.  Caller-owned; they must stay valid
+ * and unchanged until laya_enc_destroy. */
+typedef struct {
+  const void* attn_norm; /* [hidden]; NULL at encoder layer 0 when
+                            first_attn_norm_identity is set */
+  const void* wqkv;      /* [3*hidden, hidden]: rows q | k | v, head-major inside */
+  const void* wo;        /* [hidden, hidden] */
+  const void* mlp_norm;  /* [hidden] */
+  const void* wup;       /* [2*intermediate, hidden]: rows [0, I) go through
+                            GELU, rows [I, 2I) are the gate */
+  const void* wdown;     /* [hidden, intermediate] */
+} laya_enc_layer_weights;
+
+typedef struct {
+  const void* tok_emb;    /* [vocab, hidden] */
+  const void* emb_norm;   /* [hidden] */
+  const void* final_norm; /* [hidden] (may be NULL if final_norm == 0) */
+  int32_t n_layers;       /* must equal n_encoder_layers + n_decision_layers */
+  const laya_enc_layer_weights* layers; /* host array of n_layers entries */
+} laya_enc_weights;
+
+typedef struct laya_enc_handle laya_enc_handle;
+
+/* Returns LAYA_ENC_ABI_VERSION. */
+int laya_enc_abi_version(void);
+
+/* Validates the configuration without touching a GPU.  0 or LAYA_E_INVAL. */
+int laya_enc_validate_config(const laya_enc_config* cfg);
+
+/* Creates a handle on the current CUDA device: checks the device (10.3),
+ * builds the global and local RoPE tables on the host and uploads them, and
+ * builds TMA descriptors over the caller's weights (no weight copy).
+ * *out is set to NULL on failure. */
+int laya_enc_create(const laya_enc_config* cfg, const laya_enc_weights* weights,
+                    laya_enc_handle** out);
+
+/* Runs the forward pass on `stream` (a cudaStream_t; NULL is the legacy
+ * default stream).  token_ids: HOST int32 [batch * seq], row-major;
+ * lengths: HOST int32 [batch], each in [1, seq], positions >= length are
+ * padding.  out_hidden: DEVICE BF16 [batch, seq, hidden], caller-owned;
+ * valid positions receive the final hidden states, padded positions receive
+ * finite values of no meaning.  The host arrays are copied into library-owned
+ * pinned memory before the call returns and may be reused at once.  The call
+ * is asynchronous; synchronise `stream` before reading out_hidden.
+ * The first call of a (batch, seq) shape allocates its workspace, runs two
+ * eager warm-up passes and captures a CUDA Graph (unless graphs are off); later
+ * calls replay it.  If `stream` is itself capturing, the kernels are launched
+ * into the caller's capture instead. */
+int laya_enc_run(laya_enc_handle* h, const int32_t* token_ids,
+                 const int32_t* lengths, int batch, int seq, void* out_hidden,
+                 void* stream);
+
+/* As laya_enc_run, with token_ids and lengths in DEVICE memory (int32, same
+ * layouts).  Ids cannot be checked on the host: an out-of-range id or length
+ * is clamped by the kernels and reported as LAYA_E_DEVICE by laya_enc_check. */
+int laya_enc_run_device(laya_enc_handle* h, const int32_t* token_ids_dev,
+                        const int32_t* lengths_dev, int batch, int seq,
+                        void* out_hidden, void* stream);
+
+/* Synchronises `stream` and reads the device error word.  Returns 0, or
+ * LAYA_E_DEVICE (and poisons the handle) if a kernel flagged an error. */
+int laya_enc_check(laya_enc_handle* h, void* stream);
+
+/* 1: use CUDA Graphs (default, unless env LAYA_EAGER=1); 0: eager launches. */
+int laya_enc_set_graphs(laya_enc_handle* h, int enabled);
+
+/* Number of kernel launches one forward pass of this shape makes. */
+int laya_enc_launch_count(const laya_enc_handle* h, int batch, int seq);
+
+/* Bytes of device workspace a (batch, seq) shape uses (activations, split-K
+ * partials, staging). */
+int laya_enc_workspace_bytes(const laya_enc_handle* h, int batch, int seq,
+                             size_t* bytes);
+
+/* Kernel classes reported by the profiling calls below. */
+#define LAYA_PROF_EMBED_NORM 0 /* embedding gather + LayerNorm */
+#define LAYA_PROF_NORM 1       /* LayerNorm (attention, MLP and final norms) */
+#define LAYA_PROF_QKV 2        /* QKV projection */
+#define LAYA_PROF_ROPE 3       /* RoPE */
+#define LAYA_PROF_ATTN 4       /* attention */
+#define LAYA_PROF_OUT 5        /* attention output projection + residual */
+#define LAYA_PROF_UP 6         /* MLP up-projection + GeGLU */
+#define LAYA_PROF_DOWN 7       /* MLP down-projection + residual */
+#define LAYA_PROF_CLASSES 8
+
+/* Measurement aid.  While enabled, laya_enc_run launches eagerly (no graph,
+ * no programmatic dependent launch) and brackets every kernel with CUDA events
+ * on the caller's stream; each run first folds the previous run's event times
+ * into per-class totals (waiting for that run to finish). */
+int laya_enc_set_profiling(laya_enc_handle* h, int enabled);
+
+/* Folds in the last run, then returns and clears the totals: ms[c] (device
+ * time) and launches[c] for classes c < n (n <= LAYA_PROF_CLASSES). */
+int laya_enc_profile_read(laya_enc_handle* h, double* ms, int* launches, int n);
+
+/* Frees the handle and every workspace and graph it owns.  NULL is allowed. */
+int laya_enc_destroy(laya_enc_handle* h);
+
+/* Message of the last error on this handle (or of the last failed create when
+ * h is NULL).  Never NULL; the string lives until the next call. */
+const char* laya_enc_last_error(const laya_enc_handle* h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LAYA_ENC_H_ */

@@ -1,0 +1,107 @@
+/*
+ * laya_ops.h -- C ABI of the single steps of the Laya encoder forward pass.
+ *
+ * These are the kernels laya_enc_run composes, exposed one by one so that each
+ * can be checked against the CPU oracle at the same BF16 storage points.  All
+ * pointers named *_dev or documented as device memory are DEVICE pointers,
+ * 16-byte aligned; BF16 tensors are row-major; `stream` is a cudaStream_t.
+ * Every call returns 0 or a negative LAYA_E_* code (laya_enc.h); on an
+ * argument error nothing is enqueued.  Calls are asynchronous.
+ */
+#ifndef LAYA_OPS_H_
+#define LAYA_OPS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Embedding gather + bias-free LayerNorm:
+ *   x[t] = bf16( LN(emb[ids[t]]) * gamma ),  LN(v) = (v - mean) / sqrt(var + eps)
+ * with mean and variance over the hidden dimension (two passes, fp32).
+ * Sources: "Run Laya encoder and decision layers on CUDA", "H800 comparison"
+ * (token embedding is part of the timed stack); "perf(model): exact Metal
+ * speed-ups of the forward pass - #45" (the encoder has no biases).
+ * emb [vocab, H], gamma [H], ids_dev int32 [M], x [M, H].  H a multiple of 256,
+ * at most 2048.  An id outside [0, vocab) reads row 0 and sets *err_dev to
+ * LAYA_E_DEVICE (err_dev may be NULL). */
+int laya_op_embed_layernorm(const void* emb, const void* gamma,
+                            const int32_t* ids_dev, int M, int H, int vocab,
+                            float eps, void* x, int* err_dev, void* stream);
+
+/* Bias-free LayerNorm of M rows: y[t] = bf16(LN(x[t]) * gamma).  x and y may
+ * be the same buffer.  Same source and limits as above. */
+int laya_op_layernorm(const void* x, const void* gamma, int M, int H, float eps,
+                      void* y, void* stream);
+
+/* Host-side RoPE table, the one laya_enc_create uploads: for position p in
+ * [0, max_seq) and pair i in [0, half): angle = p * theta^(-2i / (2 half)) in
+ * fp64, cos and sin in fp64, rounded to fp32 and, if bf16 != 0, to BF16 values
+ * (kept as fp32).  Layout [max_seq, half] into host arrays.
+ * Sources: "[Performance]: Optimize native Rust/CUDA Laya inference #66",
+ * "Starting evidence" (separate global and local tables); "Laya native CUDA
+ * worker", "Prepare the checkpoint and bundle" (BF16 rounding of the table). */
+int laya_op_rope_table(double theta, int max_seq, int half, int bf16,
+                       float* cos_host, float* sin_host);
+
+/* RoPE in place on the q and k slices of a packed projection qkv [B*S, 3H]
+ * (q at columns [0, H), k at [H, 2H), v untouched), head n at columns n*D.
+ * Pairs (i, i + D/2); position of token (b, s) is s:
+ *   y_i = bf16(x_i c - x_{i+D/2} s),  y_{i+D/2} = bf16(x_{i+D/2} c + x_i s)
+ * with each product and the sum rounded to fp32 separately (no FMA).
+ * cos_dev, sin_dev: fp32 [>= S, D/2] device tables.  One thread per
+ * (pair, head, token) with 32-bit indices.
+ * Sources: "[RFC]: Native Laya inference with Rust and CUDA #14", "Design"
+ * (separate QKV, RoPE and attention launches); "perf(model): exact Metal
+ * speed-ups of the forward pass - #45" (a (half-dim, head, row) grid with
+ * 32-bit indices).  head_dim must be 64. */
+int laya_op_rope(void* qkv, const float* cos_dev, const float* sin_dev, int B,
+                 int S, int heads, int head_dim, void* stream);
+
+/* Softmax attention per (row b, head n):
+ *   ctx_i = sum_j softmax_j(q_i . k_j / sqrt(D)) v_j
+ * over keys j < lengths[b] and, if global == 0, |i - j| <= half_window.
+ * A query with no visible key gets ctx = 0.  Query tiles that lie wholly in
+ * the padding of their row are written as 0 (padded positions carry no
+ * meaning).  qkv [B*S, 3H] as above (after RoPE), lengths_dev int32 [B] with
+ * values in [1, S], ctx [B*S, H] BF16 written as [B, S, heads*D] (no
+ * transpose).  Sources: "perf(model): exact Metal speed-ups of the forward
+ * pass - #45" (one (b,1,1,s) key-padding row broadcast over every query;
+ * output written with (b, s, h, hd) strides); "Run Laya encoder and decision
+ * layers on CUDA", "Test Result" (empty-key padding rows).  head_dim 64. */
+int laya_op_attention(const void* qkv, const int32_t* lengths_dev, int B, int S,
+                      int heads, int head_dim, int global, int half_window,
+                      void* ctx, void* stream);
+
+/* Linear projection on the tensor cores (tcgen05, TMEM accumulators, TMA):
+ *   a = x . w^T  (x [M, K], w [N_w, K] in nn.Linear layout, fp32 accumulate)
+ * kind 0 (plain):    y [M, N] = bf16(a),             N_w = N
+ * kind 1 (residual): y [M, N] = bf16(residual + a),  N_w = N; residual may be y
+ * kind 2 (GeGLU):    y [M, N] = bf16(gelu(a[:, :N]) * a[:, N:]), N_w = 2N,
+ *                    gelu(z) = z/2 (1 + erf(z / sqrt 2))
+ * K a multiple of 64; N a multiple of 8.  splits <= 0 and tile_tokens <= 0
+ * pick the library's plan; positive values force them (tile_tokens a multiple
+ * of 16, at most 256; splits at most 8 and at most K/64).  Split-K partial
+ * sums are reduced in the shared memory of a thread-block cluster, in split
+ * order, so no scratch memory is needed and results do not depend on timing.
+ * Sources: "[Performance]: Optimize native Rust/CUDA Laya inference #66",
+ * "Implementation priorities" (the four encoder GEMMs; small tiles for short
+ * sequences, preserving fp32 accumulation and BF16 rounding); "[RFC]: Native
+ * Laya inference with Rust and CUDA #14" (fused GEMM epilogues). */
+int laya_op_linear(const void* x, int M, int K, const void* w, int N, int kind,
+                   const void* residual, void* y, int splits, int tile_tokens,
+                   void* stream);
+
+/* The plan laya_op_linear picks by default: tokens per tile, split-K factor
+ * and the number of CTAs (feature tiles x token tiles x splits) on a device
+ * with num_sms SMs.  Host-only. */
+int laya_op_linear_plan(int M, int K, int N, int kind, int num_sms,
+                        int* tile_tokens, int* splits, int* ctas);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LAYA_OPS_H_ */

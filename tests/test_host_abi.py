@@ -1,0 +1,104 @@
+"""Host-side checks of the C ABI (CPU only, no compute calls): the library
+loads and exports every symbol the headers declare, configurations are
+validated, the library's RoPE table equals the oracle's bit for bit, and the
+GEMM planner keeps its invariants."""
+import glob
+import os
+import re
+
+import numpy as np
+import pytest
+
+import transformer_encoder_bf16_gb300 as te
+from transformer_encoder_bf16_gb300 import build as tebuild
+from transformer_encoder_bf16_gb300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    tebuild.build()
+    return te.lib()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(laya_\w+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in te._SIGNATURES, f"binding lacks {n}"
+
+
+def test_abi_version(lib):
+    assert te.abi_version() == 1
+
+
+def test_validate_config(lib):
+    assert te.validate_config(synth.FULL) == te.OK
+    assert te.validate_config(synth.REDUCED) == te.OK
+    for field, bad in (("hidden", 1000), ("head_dim", 32), ("heads", 15), ("intermediate", 2600),
+                       ("max_seq", 513), ("max_batch", 17), ("global_every", 0),
+                       ("local_half_window", -1), ("ln_eps", 0.0), ("vocab", 0),
+                       ("n_encoder_layers", 0), ("final_norm", 2)):
+        assert te.validate_config(dict(synth.FULL, **{field: bad})) == te.E_INVAL, field
+
+
+@pytest.mark.parametrize("theta", [10000.0, 160000.0, 777.0])
+@pytest.mark.parametrize("bf16", [True, False])
+def test_rope_table_equals_oracle_bitwise(lib, orc, theta, bf16):
+    c, s = te.rope_table(theta, 512, 32, bf16)
+    oc, os_ = orc.rope_table(theta, 512, 32, bf16)
+    np.testing.assert_array_equal(c.view(np.uint32), oc.view(np.uint32))
+    np.testing.assert_array_equal(s.view(np.uint32), os_.view(np.uint32))
+
+
+@pytest.mark.parametrize("M", [1, 7, 48, 100, 256, 257, 464, 1856, 8192])
+@pytest.mark.parametrize("N,K,kind", [(3072, 1024, 0), (1024, 1024, 1), (2624, 1024, 2),
+                                      (1024, 2624, 1), (768, 256, 0), (640, 256, 2)])
+def test_linear_plan_invariants(lib, M, N, K, kind):
+    for sms in (148, 152):
+        nt, splits, ctas = te.linear_plan(M, K, N, kind, sms)
+        assert nt % 16 == 0 and 16 <= nt <= 256
+        tiles_t = -(-M // nt)
+        assert tiles_t * nt >= M and (tiles_t - 1) * nt < M
+        assert 1 <= splits <= min(8, K // 64)
+        assert ctas == tiles_t * -(-N // 128) * splits
+        if M <= 256 and (kind != 2 or M <= 208):
+            # one tile, no token padding beyond 15 (a GeGLU split-K partial of
+            # more than 208 tokens does not fit in shared memory: two tiles then)
+            assert tiles_t == 1 and nt - M < 16
+        if tiles_t * -(-N // 128) >= sms:
+            assert splits == 1
+
+
+def test_linear_plan_rejects_bad_shapes(lib):
+    with pytest.raises(te.LayaError):
+        te.linear_plan(48, 100, 1024, 0, 148)      # K not a multiple of 64
+    with pytest.raises(te.LayaError):
+        te.linear_plan(0, 1024, 1024, 0, 148)
+
+
+def test_create_reports_errors_without_a_gpu(lib):
+    import ctypes
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("host-only check")
+    cfg = te.Config.from_model(synth.REDUCED)
+    h = ctypes.c_void_p()
+    # null weights: rejected before any CUDA call
+    assert lib.laya_enc_create(ctypes.byref(cfg), None, ctypes.byref(h)) == te.E_INVAL
+    assert not h.value
+    assert lib.laya_enc_last_error(None)
+    assert lib.laya_enc_destroy(None) == te.OK
+    assert lib.laya_enc_run(None, None, None, 1, 1, None, None) == te.E_INVAL

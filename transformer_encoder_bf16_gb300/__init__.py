@@ -1,1 +1,277 @@
-"""Laya BF16 encoder forward pass on one GB300 (sm_103a): Python binding."""
+"""Laya BF16 encoder forward pass on one GB300 (sm_103a): Python binding.
+
+A thin ctypes layer over ``lib/liblaya_enc.so`` (the C ABI declared in
+``include/laya_enc.h`` and ``include/laya_ops.h``).  Functions keep the C
+names without their prefix and only marshal arguments: device tensors are
+passed as raw pointers, streams as ``cudaStream_t`` handles.  PyTorch is used
+by callers for device memory and streams; every step of the forward pass runs
+in the library's CUDA kernels.  There is no CPU fallback: if the library is
+missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import synth  # noqa: F401  (seeded inputs; no arithmetic of the method)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "liblaya_enc.so")
+
+OK, E_INVAL, E_NOMEM, E_CUDA, E_POISONED, E_UNSUPPORTED, E_DEVICE = 0, -1, -2, -3, -4, -5, -6
+ERROR_NAMES = {E_INVAL: "LAYA_E_INVAL", E_NOMEM: "LAYA_E_NOMEM", E_CUDA: "LAYA_E_CUDA",
+               E_POISONED: "LAYA_E_POISONED", E_UNSUPPORTED: "LAYA_E_UNSUPPORTED",
+               E_DEVICE: "LAYA_E_DEVICE"}
+KIND_PLAIN, KIND_RESIDUAL, KIND_GEGLU = 0, 1, 2
+PROFILE_CLASSES = ("embed_norm", "norm", "qkv", "rope", "attention", "out_proj", "up_geglu",
+                   "down")
+
+
+class LayaError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"{ERROR_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+class Config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "hidden", "heads", "head_dim", "intermediate", "vocab", "n_encoder_layers",
+        "n_decision_layers", "global_every", "local_half_window")] + [
+        ("theta_global", ctypes.c_float), ("theta_local", ctypes.c_float),
+        ("ln_eps", ctypes.c_float)] + [(n, ctypes.c_int32) for n in (
+            "max_batch", "max_seq", "rope_table_bf16", "first_attn_norm_identity",
+            "final_norm")]
+
+    @classmethod
+    def from_model(cls, model: dict) -> "Config":
+        c = cls()
+        for name, _ in cls._fields_:
+            setattr(c, name, model[name])
+        return c
+
+
+class LayerWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("attn_norm", "wqkv", "wo", "mlp_norm", "wup", "wdown")]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [("tok_emb", ctypes.c_void_p), ("emb_norm", ctypes.c_void_p),
+                ("final_norm", ctypes.c_void_p), ("n_layers", ctypes.c_int32),
+                ("layers", ctypes.POINTER(LayerWeights))]
+
+
+_lib = None
+_P, _I, _F, _D, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_double, ctypes.c_size_t
+
+# name -> (argtypes, restype)
+_SIGNATURES = {
+    "laya_enc_abi_version": ([], _I),
+    "laya_enc_validate_config": ([ctypes.POINTER(Config)], _I),
+    "laya_enc_create": ([ctypes.POINTER(Config), ctypes.POINTER(Weights), ctypes.POINTER(_P)], _I),
+    "laya_enc_run": ([_P, _P, _P, _I, _I, _P, _P], _I),
+    "laya_enc_run_device": ([_P, _P, _P, _I, _I, _P, _P], _I),
+    "laya_enc_check": ([_P, _P], _I),
+    "laya_enc_set_graphs": ([_P, _I], _I),
+    "laya_enc_launch_count": ([_P, _I, _I], _I),
+    "laya_enc_workspace_bytes": ([_P, _I, _I, ctypes.POINTER(_SZ)], _I),
+    "laya_enc_set_profiling": ([_P, _I], _I),
+    "laya_enc_profile_read": ([_P, ctypes.POINTER(_D), ctypes.POINTER(_I), _I], _I),
+    "laya_enc_destroy": ([_P], _I),
+    "laya_enc_last_error": ([_P], ctypes.c_char_p),
+    "laya_op_embed_layernorm": ([_P, _P, _P, _I, _I, _I, _F, _P, _P, _P], _I),
+    "laya_op_layernorm": ([_P, _P, _I, _I, _F, _P, _P], _I),
+    "laya_op_rope_table": ([_D, _I, _I, _I, _P, _P], _I),
+    "laya_op_rope": ([_P, _P, _P, _I, _I, _I, _I, _P], _I),
+    "laya_op_attention": ([_P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
+    "laya_op_linear": ([_P, _I, _I, _P, _I, _I, _P, _P, _I, _I, _P], _I),
+    "laya_op_linear_plan": ([_I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I),
+                             ctypes.POINTER(_I)], _I),
+}
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -m transformer_encoder_bf16_gb300.build` (there is no CPU fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (argt, rest) in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.argtypes = argt
+            fn.restype = rest
+        _lib = L
+    return _lib
+
+
+def _check(rc, handle=None):
+    if rc != OK:
+        msg = lib().laya_enc_last_error(handle).decode() if handle is not None else "see arguments"
+        raise LayaError(rc, msg)
+    return rc
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream  # torch.cuda.Stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+# ------------------------------------------------------------- full stack ---
+
+def upload_weights(weights: dict, device="cuda"):
+    """Copy the uint16 BF16 bit patterns of synth.make_weights to device
+    tensors (torch.bfloat16).  Returns a dict of the same shape."""
+    import torch
+
+    def up(a):
+        if a is None:
+            return None
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+
+    return {"tok_emb": up(weights["tok_emb"]), "emb_norm": up(weights["emb_norm"]),
+            "final_norm": up(weights["final_norm"]),
+            "layers": [{k: up(v) for k, v in layer.items()} for layer in weights["layers"]]}
+
+
+class Encoder:
+    """Owns a laya_enc_handle over device weights (kept referenced here)."""
+
+    def __init__(self, model: dict, dev_weights: dict):
+        self.model = model
+        self._weights = dev_weights
+        self._cfg = Config.from_model(model)
+        layers = dev_weights["layers"]
+        arr = (LayerWeights * len(layers))()
+        for i, lw in enumerate(layers):
+            for k in ("attn_norm", "wqkv", "wo", "mlp_norm", "wup", "wdown"):
+                setattr(arr[i], k, _ptr(lw[k]))
+        self._layers = arr
+        w = Weights(_ptr(dev_weights["tok_emb"]), _ptr(dev_weights["emb_norm"]),
+                    _ptr(dev_weights["final_norm"]), len(layers),
+                    ctypes.cast(arr, ctypes.POINTER(LayerWeights)))
+        h = ctypes.c_void_p()
+        rc = lib().laya_enc_create(ctypes.byref(self._cfg), ctypes.byref(w), ctypes.byref(h))
+        if rc != OK:
+            raise LayaError(rc, lib().laya_enc_last_error(None).decode())
+        self.handle = h
+
+    def run(self, ids: np.ndarray, lengths: np.ndarray, out, stream=None):
+        """ids int32 [B, S] and lengths int32 [B] in HOST memory; out a device
+        bfloat16 tensor [B, S, hidden]."""
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        lengths = np.ascontiguousarray(lengths, dtype=np.int32)
+        B, S = ids.shape
+        _check(lib().laya_enc_run(self.handle, ids.ctypes.data, lengths.ctypes.data, B, S,
+                                  _ptr(out), _stream_ptr(stream)), self.handle)
+
+    def run_device(self, ids_dev, lengths_dev, out, stream=None):
+        """ids_dev int32 [B, S] and lengths_dev int32 [B] device tensors."""
+        B, S = ids_dev.shape
+        _check(lib().laya_enc_run_device(self.handle, _ptr(ids_dev), _ptr(lengths_dev), B, S,
+                                         _ptr(out), _stream_ptr(stream)), self.handle)
+
+    def check(self, stream=None):
+        return _check(lib().laya_enc_check(self.handle, _stream_ptr(stream)), self.handle)
+
+    def set_graphs(self, enabled: bool):
+        _check(lib().laya_enc_set_graphs(self.handle, 1 if enabled else 0), self.handle)
+
+    def set_profiling(self, enabled: bool):
+        _check(lib().laya_enc_set_profiling(self.handle, 1 if enabled else 0), self.handle)
+
+    def profile_read(self) -> dict:
+        """{class: (total device ms, launches)} since the last read."""
+        n = len(PROFILE_CLASSES)
+        ms = (ctypes.c_double * n)()
+        cnt = (ctypes.c_int * n)()
+        _check(lib().laya_enc_profile_read(self.handle, ms, cnt, n), self.handle)
+        return {PROFILE_CLASSES[i]: (ms[i], cnt[i]) for i in range(n)}
+
+    def launch_count(self, B, S) -> int:
+        return lib().laya_enc_launch_count(self.handle, B, S)
+
+    def workspace_bytes(self, B, S) -> int:
+        n = ctypes.c_size_t()
+        _check(lib().laya_enc_workspace_bytes(self.handle, B, S, ctypes.byref(n)), self.handle)
+        return n.value
+
+    def last_error(self) -> str:
+        return lib().laya_enc_last_error(self.handle).decode()
+
+    def close(self):
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            lib().laya_enc_destroy(self.handle)
+        self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def abi_version() -> int:
+    return lib().laya_enc_abi_version()
+
+
+def validate_config(model: dict) -> int:
+    return lib().laya_enc_validate_config(ctypes.byref(Config.from_model(model)))
+
+
+# ------------------------------------------------------------ single steps ---
+
+def embed_layernorm(emb, gamma, ids_dev, eps, x, err_dev=None, stream=None):
+    M = ids_dev.numel()
+    V, H = emb.shape
+    _check(lib().laya_op_embed_layernorm(_ptr(emb), _ptr(gamma), _ptr(ids_dev), M, H, V, eps,
+                                         _ptr(x), _ptr(err_dev), _stream_ptr(stream)))
+
+
+def layernorm(x, gamma, eps, y, stream=None):
+    M, H = x.shape
+    _check(lib().laya_op_layernorm(_ptr(x), _ptr(gamma), M, H, eps, _ptr(y), _stream_ptr(stream)))
+
+
+def rope_table(theta, max_seq, half, bf16=True):
+    c = np.zeros((max_seq, half), np.float32)
+    s = np.zeros((max_seq, half), np.float32)
+    _check(lib().laya_op_rope_table(float(theta), max_seq, half, 1 if bf16 else 0,
+                                    c.ctypes.data, s.ctypes.data))
+    return c, s
+
+
+def rope(qkv, cos_dev, sin_dev, B, S, heads, head_dim=64, stream=None):
+    _check(lib().laya_op_rope(_ptr(qkv), _ptr(cos_dev), _ptr(sin_dev), B, S, heads, head_dim,
+                              _stream_ptr(stream)))
+
+
+def attention(qkv, lengths_dev, B, S, heads, global_, half_window, ctx, head_dim=64, stream=None):
+    _check(lib().laya_op_attention(_ptr(qkv), _ptr(lengths_dev), B, S, heads, head_dim,
+                                   1 if global_ else 0, half_window, _ptr(ctx),
+                                   _stream_ptr(stream)))
+
+
+def linear(x, w, y, kind=KIND_PLAIN, residual=None, splits=0, tile_tokens=0, stream=None):
+    M, K = x.shape
+    N = y.shape[1]
+    _check(lib().laya_op_linear(_ptr(x), M, K, _ptr(w), N, kind, _ptr(residual), _ptr(y),
+                                splits, tile_tokens, _stream_ptr(stream)))
+
+
+def linear_plan(M, K, N, kind, num_sms):
+    nt, sp, ct = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(lib().laya_op_linear_plan(M, K, N, kind, num_sms, ctypes.byref(nt), ctypes.byref(sp),
+                                     ctypes.byref(ct)))
+    return nt.value, sp.value, ct.value

@@ -1,0 +1,675 @@
+// encoder.cu -- the handle behind laya_enc_*: configuration checks, RoPE
+// tables, TMA descriptors over the caller's weights, per-shape workspaces with
+// CUDA Graph capture and replay, and the layer loop.
+//
+// Layer loop (one forward pass, all on the caller's stream):
+//   x = LN(E[ids])                                       embedding + norm
+//   for each of the n_enc encoder and n_dec decision layers l:
+//     if l == n_enc and final_norm:  x = LN_final(x)
+//     h   = (l == 0 and first_attn_norm_identity) ? x : LN_attn(x)
+//     qkv = h Wqkv^T                  GEMM, plain epilogue
+//     q,k = RoPE(q,k)                 global table iff decision layer or l % global_every == 0
+//     ctx = attention(qkv, lengths)   sliding window on local layers
+//     x   = x + ctx Wo^T              GEMM, residual epilogue (in place)
+//     h   = LN_mlp(x)
+//     g   = gelu(h Wup_in^T) * (h Wup_gate^T)   GEMM, GeGLU epilogue
+//     x   = x + g Wdown^T             GEMM, residual epilogue (last layer: into out)
+// Sources: "Run Laya encoder and decision layers on CUDA" ("Purpose",
+// "H800 comparison"); "[RFC]: Native Laya inference with Rust and CUDA #14"
+// ("Design": separate QKV, RoPE and attention launches; per-shape CUDA Graphs
+// with two warm-ups before a synchronous capture; an LRU cache of four shapes
+// and 512 MiB of workspaces); "[Performance]: Optimize native Rust/CUDA Laya
+// inference #66" ("Implementation priorities": grouped uploads with safe host
+// buffer lifetimes, resolved handles reused).  The norm placement, GeGLU half
+// order and layer-0 identity norm are readings of pages that do not write the
+// layer equations out; the CPU oracle states the same readings.
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/laya_ops.h"
+#include "internal.h"
+
+namespace laya {
+
+namespace {
+
+constexpr int kMaxShapes = 4;
+constexpr size_t kMaxWorkspaceBytes = 512ull << 20;
+
+struct LayerMaps {
+  CUtensorMap wqkv, wo, wup_in, wup_gate, wdown;
+  const bf16* attn_norm;
+  const bf16* mlp_norm;
+};
+
+struct Workspace {
+  int B = 0, S = 0, M = 0;
+  void* block = nullptr;  // one device allocation for every buffer below
+  size_t bytes = 0;
+  bf16 *x = nullptr, *h = nullptr, *qkv = nullptr, *ctx = nullptr, *g = nullptr;
+  int32_t* ids = nullptr;   // device staging [M], followed by
+  int32_t* lens = nullptr;  // device staging [B]
+  int32_t* host = nullptr;  // pinned staging [M + B]
+  cudaEvent_t staged = nullptr;   // the last upload from `host` has been consumed
+  cudaEvent_t done = nullptr;     // the last forward using this workspace has finished
+  GemmPlan p_qkv, p_o, p_up, p_dn;
+  CUtensorMap tm_x, tm_h, tm_ctx, tm_g;
+  cudaGraphExec_t exec = nullptr;
+  void* graph_out = nullptr;
+  uint64_t last_use = 0;
+};
+
+}  // namespace
+}  // namespace laya
+
+struct laya_enc_handle {
+  laya_enc_config cfg;
+  int L = 0;
+  int device = 0;
+  int num_sms = 0;
+  const laya::bf16* tok_emb = nullptr;
+  const laya::bf16* emb_norm = nullptr;
+  const laya::bf16* final_norm = nullptr;
+  std::vector<laya::LayerMaps> layers;
+  float* rope = nullptr;  // device: cos_g, sin_g, cos_l, sin_l, each [max_seq, 32]
+  int* err = nullptr;     // device error word
+  cudaStream_t capture_stream = nullptr;
+  std::vector<laya::Workspace*> cache;
+  uint64_t tick = 0;
+  bool graphs = true;
+  bool pdl = true;
+  bool poisoned = false;
+  std::string last_error;
+  // profiling: event pairs of the last run, per-class totals
+  bool profiling = false;
+  std::vector<cudaEvent_t> prof_events;  // 2 per launch, reused
+  std::vector<int> prof_class;           // class of each recorded launch
+  size_t prof_used = 0;
+  double prof_ms[LAYA_PROF_CLASSES] = {};
+  int prof_count[LAYA_PROF_CLASSES] = {};
+};
+
+namespace laya {
+namespace {
+
+thread_local std::string g_create_error = "no error";
+
+int fail(laya_enc_handle* h, int code, const std::string& msg) {
+  if (h) {
+    h->last_error = msg;
+    if (code == LAYA_E_CUDA || code == LAYA_E_DEVICE) h->poisoned = true;
+  } else {
+    g_create_error = msg;
+  }
+  return code;
+}
+
+int cuda_fail(laya_enc_handle* h, cudaError_t e, const char* what) {
+  return fail(h, LAYA_E_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+bool env_flag(const char* name) {
+  const char* v = std::getenv(name);
+  return v != nullptr && v[0] != '\0' && v[0] != '0';
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+void free_workspace(Workspace* w) {
+  if (!w) return;
+  if (w->done) cudaEventSynchronize(w->done);
+  if (w->exec) cudaGraphExecDestroy(w->exec);
+  if (w->staged) cudaEventDestroy(w->staged);
+  if (w->done) cudaEventDestroy(w->done);
+  if (w->host) cudaFreeHost(w->host);
+  if (w->block) cudaFree(w->block);
+  delete w;
+}
+
+// Activations and staging for one (B, S) shape, and the GEMM plans for it.
+int workspace_layout(const laya_enc_handle* h, int B, int S, Workspace* w, size_t* total) {
+  const laya_enc_config& c = h->cfg;
+  const int M = B * S;
+  const int H = c.hidden, I = c.intermediate;
+  w->B = B;
+  w->S = S;
+  w->M = M;
+  if (!plan_gemm(M, 3 * H, H, kGemmPlain, h->num_sms, 0, 0, &w->p_qkv) ||
+      !plan_gemm(M, H, H, kGemmResidual, h->num_sms, 0, 0, &w->p_o) ||
+      !plan_gemm(M, I, H, kGemmGeglu, h->num_sms, 0, 0, &w->p_up) ||
+      !plan_gemm(M, H, I, kGemmResidual, h->num_sms, 0, 0, &w->p_dn))
+    return LAYA_E_INVAL;
+  size_t off = 0;
+  auto take = [&](size_t n) {
+    const size_t o = off;
+    off = align_up(off + n, 256);
+    return o;
+  };
+  const size_t ox = take(static_cast<size_t>(M) * H * 2);
+  const size_t oh = take(static_cast<size_t>(M) * H * 2);
+  const size_t oq = take(static_cast<size_t>(M) * 3 * H * 2);
+  const size_t oc = take(static_cast<size_t>(M) * H * 2);
+  const size_t og = take(static_cast<size_t>(M) * I * 2);
+  const size_t oi = take(static_cast<size_t>(M + B) * 4);  // ids then lengths, adjacent
+  *total = off;
+  if (w->block) {
+    char* base = static_cast<char*>(w->block);
+    w->x = reinterpret_cast<bf16*>(base + ox);
+    w->h = reinterpret_cast<bf16*>(base + oh);
+    w->qkv = reinterpret_cast<bf16*>(base + oq);
+    w->ctx = reinterpret_cast<bf16*>(base + oc);
+    w->g = reinterpret_cast<bf16*>(base + og);
+    w->ids = reinterpret_cast<int32_t*>(base + oi);
+    w->lens = w->ids + M;
+  }
+  return LAYA_OK;
+}
+
+int kernel_count(const laya_enc_config& c) {
+  const int L = c.n_encoder_layers + c.n_decision_layers;
+  int n = 1 + 8 * L;
+  if (c.first_attn_norm_identity) n -= 1;
+  if (c.final_norm && c.n_decision_layers > 0) n += 1;
+  return n;
+}
+
+// Records an event pair around one launch when profiling.
+struct Prof {
+  laya_enc_handle* h;
+  cudaStream_t s;
+  int cls = 0;
+  cudaError_t begin(int c) {
+    if (!h->profiling) return cudaSuccess;
+    cls = c;
+    const size_t i = 2 * h->prof_used;
+    while (h->prof_events.size() < i + 2) {
+      cudaEvent_t e;
+      cudaError_t r = cudaEventCreate(&e);
+      if (r != cudaSuccess) return r;
+      h->prof_events.push_back(e);
+    }
+    return cudaEventRecord(h->prof_events[i], s);
+  }
+  cudaError_t end(cudaError_t launched) {
+    if (!h->profiling || launched != cudaSuccess) return launched;
+    const size_t i = 2 * h->prof_used;
+    if (h->prof_class.size() <= h->prof_used) h->prof_class.resize(h->prof_used + 1);
+    h->prof_class[h->prof_used] = cls;
+    ++h->prof_used;
+    return cudaEventRecord(h->prof_events[i + 1], s);
+  }
+};
+
+cudaError_t prof_fold(laya_enc_handle* h) {
+  if (h->prof_used == 0) return cudaSuccess;
+  cudaError_t e = cudaEventSynchronize(h->prof_events[2 * h->prof_used - 1]);
+  if (e != cudaSuccess) return e;
+  for (size_t i = 0; i < h->prof_used; ++i) {
+    float ms = 0.f;
+    e = cudaEventElapsedTime(&ms, h->prof_events[2 * i], h->prof_events[2 * i + 1]);
+    if (e != cudaSuccess) return e;
+    h->prof_ms[h->prof_class[i]] += ms;
+    h->prof_count[h->prof_class[i]] += 1;
+  }
+  h->prof_used = 0;
+  return cudaSuccess;
+}
+
+cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, bf16* out, cudaStream_t stream) {
+  const laya_enc_config& c = h->cfg;
+  const int H = c.hidden;
+  const int M = w->M;
+  const bool pdl = h->pdl && !h->profiling;
+  const Launch first{stream, false};
+  const Launch l{stream, pdl};
+  const float* cos_g = h->rope;
+  const float* sin_g = h->rope + static_cast<size_t>(c.max_seq) * 32;
+  const float* cos_l = sin_g + static_cast<size_t>(c.max_seq) * 32;
+  const float* sin_l = cos_l + static_cast<size_t>(c.max_seq) * 32;
+  Prof pr{h, stream};
+  cudaError_t e;
+#define LAYA_LAUNCH(cls, call)              \
+  do {                                      \
+    e = pr.begin(cls);                      \
+    if (e == cudaSuccess) e = pr.end(call); \
+    if (e != cudaSuccess) return e;         \
+  } while (0)
+
+  LAYA_LAUNCH(LAYA_PROF_EMBED_NORM,
+              launch_embed_layernorm(h->tok_emb, h->emb_norm, w->ids, M, H, c.vocab, c.ln_eps,
+                                     w->x, h->err, first));
+  for (int li = 0; li < h->L; ++li) {
+    const LayerMaps& lw = h->layers[li];
+    const bool dec = li >= c.n_encoder_layers;
+    const bool glob = dec || (li % c.global_every == 0);
+    if (li == c.n_encoder_layers && c.final_norm)
+      LAYA_LAUNCH(LAYA_PROF_NORM,
+                  launch_layernorm(w->x, h->final_norm, M, H, c.ln_eps, w->x, l));
+    const CUtensorMap* qkv_in = &w->tm_h;
+    if (li == 0 && c.first_attn_norm_identity) {
+      qkv_in = &w->tm_x;
+    } else {
+      LAYA_LAUNCH(LAYA_PROF_NORM, launch_layernorm(w->x, lw.attn_norm, M, H, c.ln_eps, w->h, l));
+    }
+    GemmOperands o;
+    o.err = h->err;
+    o.w = lw.wqkv;
+    o.w2 = lw.wqkv;
+    o.x = *qkv_in;
+    o.y = w->qkv;
+    LAYA_LAUNCH(LAYA_PROF_QKV, launch_gemm(w->p_qkv, o, l));
+    LAYA_LAUNCH(LAYA_PROF_ROPE, launch_rope(w->qkv, glob ? cos_g : cos_l, glob ? sin_g : sin_l,
+                                            w->B, w->S, c.heads, l));
+    LAYA_LAUNCH(LAYA_PROF_ATTN, launch_attention(w->qkv, w->lens, w->B, w->S, c.heads,
+                                                 glob ? 1 : 0, c.local_half_window, w->ctx,
+                                                 h->err, l));
+    o.w = lw.wo;
+    o.w2 = lw.wo;
+    o.x = w->tm_ctx;
+    o.y = w->x;
+    o.residual = w->x;
+    LAYA_LAUNCH(LAYA_PROF_OUT, launch_gemm(w->p_o, o, l));
+    LAYA_LAUNCH(LAYA_PROF_NORM, launch_layernorm(w->x, lw.mlp_norm, M, H, c.ln_eps, w->h, l));
+    o.w = lw.wup_in;
+    o.w2 = lw.wup_gate;
+    o.x = w->tm_h;
+    o.y = w->g;
+    o.residual = nullptr;
+    LAYA_LAUNCH(LAYA_PROF_UP, launch_gemm(w->p_up, o, l));
+    o.w = lw.wdown;
+    o.w2 = lw.wdown;
+    o.x = w->tm_g;
+    o.y = (li == h->L - 1) ? out : w->x;
+    o.residual = w->x;
+    LAYA_LAUNCH(LAYA_PROF_DOWN, launch_gemm(w->p_dn, o, l));
+  }
+#undef LAYA_LAUNCH
+  return cudaSuccess;
+}
+
+int get_workspace(laya_enc_handle* h, int B, int S, Workspace** out) {
+  for (Workspace* w : h->cache) {
+    if (w->B == B && w->S == S) {
+      w->last_use = ++h->tick;
+      *out = w;
+      return LAYA_OK;
+    }
+  }
+  Workspace* w = new (std::nothrow) Workspace();
+  if (!w) return fail(h, LAYA_E_NOMEM, "workspace: host allocation failed");
+  size_t bytes = 0;
+  if (workspace_layout(h, B, S, w, &bytes) != LAYA_OK) {
+    delete w;
+    return fail(h, LAYA_E_INVAL, "no GEMM plan for this shape");
+  }
+  // evict least-recently-used shapes beyond four or 512 MiB
+  auto used = [&]() {
+    size_t s = 0;
+    for (Workspace* x : h->cache) s += x->bytes;
+    return s;
+  };
+  while (!h->cache.empty() && (h->cache.size() >= static_cast<size_t>(kMaxShapes) ||
+                               used() + bytes > kMaxWorkspaceBytes)) {
+    auto it = std::min_element(h->cache.begin(), h->cache.end(),
+                               [](Workspace* a, Workspace* b) { return a->last_use < b->last_use; });
+    free_workspace(*it);
+    h->cache.erase(it);
+  }
+  cudaError_t e = cudaMalloc(&w->block, bytes);
+  if (e != cudaSuccess) {
+    delete w;
+    return fail(h, LAYA_E_NOMEM, std::string("workspace: ") + cudaGetErrorString(e));
+  }
+  w->bytes = bytes;
+  workspace_layout(h, B, S, w, &bytes);
+  e = cudaHostAlloc(reinterpret_cast<void**>(&w->host), sizeof(int32_t) * (w->M + B),
+                    cudaHostAllocDefault);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&w->staged, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&w->done, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaMemset(w->block, 0, w->bytes);
+  if (e != cudaSuccess) {
+    free_workspace(w);
+    return fail(h, LAYA_E_NOMEM, std::string("workspace: ") + cudaGetErrorString(e));
+  }
+  const laya_enc_config& c = h->cfg;
+  const int M = w->M;
+  const uint32_t nt = static_cast<uint32_t>(w->p_qkv.nt);
+  bool ok = make_tmap_bf16_2d(&w->tm_x, w->x, M, c.hidden, c.hidden * 2ull, nt) &&
+            make_tmap_bf16_2d(&w->tm_h, w->h, M, c.hidden, c.hidden * 2ull, nt) &&
+            make_tmap_bf16_2d(&w->tm_ctx, w->ctx, M, c.hidden, c.hidden * 2ull, nt) &&
+            make_tmap_bf16_2d(&w->tm_g, w->g, M, c.intermediate, c.intermediate * 2ull, nt);
+  if (!ok) {
+    free_workspace(w);
+    return fail(h, LAYA_E_CUDA, "workspace: tensor map encoding failed");
+  }
+  w->last_use = ++h->tick;
+  h->cache.push_back(w);
+  *out = w;
+  return LAYA_OK;
+}
+
+int run_common(laya_enc_handle* h, Workspace* w, void* out, cudaStream_t stream) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamIsCapturing");
+  if (h->profiling && cap == cudaStreamCaptureStatusNone) {
+    e = prof_fold(h);
+    if (e != cudaSuccess) return cuda_fail(h, e, "profiling events");
+  }
+  if (!h->graphs || h->profiling || cap != cudaStreamCaptureStatusNone) {
+    e = enqueue_forward(h, w, static_cast<bf16*>(out), stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");
+  } else {
+    if (w->exec == nullptr || w->graph_out != out) {
+      if (w->exec == nullptr) {
+        // two eager warm-up passes before the first capture of a shape
+        for (int i = 0; i < 2; ++i) {
+          e = enqueue_forward(h, w, static_cast<bf16*>(out), stream);
+          if (e != cudaSuccess) return cuda_fail(h, e, "warm-up launch");
+        }
+      }
+      e = cudaStreamSynchronize(stream);
+      if (e != cudaSuccess) return cuda_fail(h, e, "warm-up");
+      cudaGraph_t graph = nullptr;
+      e = cudaStreamBeginCapture(h->capture_stream, cudaStreamCaptureModeThreadLocal);
+      if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamBeginCapture");
+      cudaError_t el = enqueue_forward(h, w, static_cast<bf16*>(out), h->capture_stream);
+      e = cudaStreamEndCapture(h->capture_stream, &graph);
+      if (el != cudaSuccess) {
+        if (graph) cudaGraphDestroy(graph);
+        return cuda_fail(h, el, "launch during capture");
+      }
+      if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamEndCapture");
+      if (w->exec) {
+        cudaGraphExecDestroy(w->exec);
+        w->exec = nullptr;
+      }
+      e = cudaGraphInstantiate(&w->exec, graph, 0);
+      cudaGraphDestroy(graph);
+      if (e != cudaSuccess) return cuda_fail(h, e, "cudaGraphInstantiate");
+      w->graph_out = out;
+    }
+    e = cudaGraphLaunch(w->exec, stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaGraphLaunch");
+  }
+  e = cudaEventRecord(w->done, stream);
+  if (e != cudaSuccess && cap == cudaStreamCaptureStatusNone)
+    return cuda_fail(h, e, "cudaEventRecord");
+  return LAYA_OK;
+}
+
+int check_run_args(laya_enc_handle* h, int B, int S, void* out) {
+  if (!h) return LAYA_E_INVAL;
+  if (h->poisoned) return fail(h, LAYA_E_POISONED, "handle is poisoned by an earlier error");
+  if (B < 1 || B > h->cfg.max_batch)
+    return fail(h, LAYA_E_INVAL, "batch outside [1, max_batch]");
+  if (S < 1 || S > h->cfg.max_seq) return fail(h, LAYA_E_INVAL, "seq outside [1, max_seq]");
+  if (!out || (reinterpret_cast<uintptr_t>(out) & 15u) != 0)
+    return fail(h, LAYA_E_INVAL, "out_hidden must be a 16-byte aligned device pointer");
+  return LAYA_OK;
+}
+
+}  // namespace
+
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+}  // namespace laya
+
+using laya::bf16;
+
+extern "C" {
+
+int laya_enc_abi_version(void) { return LAYA_ENC_ABI_VERSION; }
+
+int laya_enc_validate_config(const laya_enc_config* c) {
+  if (!c) return LAYA_E_INVAL;
+  if (!laya::rowops_supported_hidden(c->hidden)) return LAYA_E_INVAL;
+  if (c->head_dim != 64 || c->heads < 1 || c->heads * c->head_dim != c->hidden) return LAYA_E_INVAL;
+  if (c->intermediate < 64 || c->intermediate % 64 != 0) return LAYA_E_INVAL;
+  if (c->vocab < 1) return LAYA_E_INVAL;
+  if (c->n_encoder_layers < 1 || c->n_decision_layers < 0) return LAYA_E_INVAL;
+  if (c->n_encoder_layers + c->n_decision_layers > 256) return LAYA_E_INVAL;
+  if (c->global_every < 1 || c->local_half_window < 0) return LAYA_E_INVAL;
+  if (!(c->theta_global > 0.f) || !(c->theta_local > 0.f) || !(c->ln_eps > 0.f))
+    return LAYA_E_INVAL;
+  if (c->max_batch < 1 || c->max_batch > 16 || c->max_seq < 1 || c->max_seq > 512)
+    return LAYA_E_INVAL;
+  if ((c->rope_table_bf16 | 1) != 1 || (c->first_attn_norm_identity | 1) != 1 ||
+      (c->final_norm | 1) != 1)
+    return LAYA_E_INVAL;
+  return LAYA_OK;
+}
+
+int laya_enc_create(const laya_enc_config* cfg, const laya_enc_weights* wts,
+                    laya_enc_handle** out) {
+  using namespace laya;
+  if (out) *out = nullptr;
+  if (!out || !cfg || !wts) return fail(nullptr, LAYA_E_INVAL, "null argument");
+  if (laya_enc_validate_config(cfg) != LAYA_OK)
+    return fail(nullptr, LAYA_E_INVAL, "unsupported configuration");
+  const int L = cfg->n_encoder_layers + cfg->n_decision_layers;
+  if (wts->n_layers != L || !wts->layers)
+    return fail(nullptr, LAYA_E_INVAL, "weights.n_layers does not match the configuration");
+  auto aligned = [](const void* p) {
+    return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+  };
+  if (!aligned(wts->tok_emb) || !aligned(wts->emb_norm) ||
+      (cfg->final_norm && !aligned(wts->final_norm)))
+    return fail(nullptr, LAYA_E_INVAL, "embedding or norm weights missing or misaligned");
+  for (int l = 0; l < L; ++l) {
+    const laya_enc_layer_weights& lw = wts->layers[l];
+    const bool need_attn_norm = !(l == 0 && cfg->first_attn_norm_identity);
+    if ((need_attn_norm && !aligned(lw.attn_norm)) || !aligned(lw.wqkv) || !aligned(lw.wo) ||
+        !aligned(lw.mlp_norm) || !aligned(lw.wup) || !aligned(lw.wdown))
+      return fail(nullptr, LAYA_E_INVAL,
+                  "layer " + std::to_string(l) + ": weight missing or not 16-byte aligned");
+  }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(nullptr, LAYA_E_CUDA, cudaGetErrorString(e));
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3)
+    return fail(nullptr, LAYA_E_UNSUPPORTED,
+                "device compute capability " + std::to_string(major) + "." +
+                    std::to_string(minor) + " is not 10.3 (GB300)");
+
+  laya_enc_handle* h = new (std::nothrow) laya_enc_handle();
+  if (!h) return fail(nullptr, LAYA_E_NOMEM, "host allocation failed");
+  h->cfg = *cfg;
+  h->L = L;
+  h->device = dev;
+  h->num_sms = device_sm_count();
+  h->graphs = !env_flag("LAYA_EAGER");
+  h->pdl = !env_flag("LAYA_NO_PDL");
+  h->tok_emb = static_cast<const bf16*>(wts->tok_emb);
+  h->emb_norm = static_cast<const bf16*>(wts->emb_norm);
+  h->final_norm = static_cast<const bf16*>(wts->final_norm);
+  const int H = cfg->hidden, I = cfg->intermediate;
+  h->layers.resize(L);
+  bool ok = true;
+  for (int l = 0; l < L && ok; ++l) {
+    const laya_enc_layer_weights& lw = wts->layers[l];
+    LayerMaps& m = h->layers[l];
+    m.attn_norm = static_cast<const bf16*>(lw.attn_norm);
+    m.mlp_norm = static_cast<const bf16*>(lw.mlp_norm);
+    const char* up = static_cast<const char*>(lw.wup);
+    ok = make_tmap_bf16_2d(&m.wqkv, lw.wqkv, 3ull * H, H, H * 2ull, 128) &&
+         make_tmap_bf16_2d(&m.wo, lw.wo, H, H, H * 2ull, 128) &&
+         make_tmap_bf16_2d(&m.wup_in, up, I, H, H * 2ull, 128) &&
+         make_tmap_bf16_2d(&m.wup_gate, up + static_cast<size_t>(I) * H * 2, I, H, H * 2ull,
+                           128) &&
+         make_tmap_bf16_2d(&m.wdown, lw.wdown, H, I, I * 2ull, 128);
+  }
+  if (!ok) {
+    delete h;
+    return fail(nullptr, LAYA_E_CUDA, "weight tensor map encoding failed");
+  }
+  const size_t tab = static_cast<size_t>(cfg->max_seq) * 32;
+  std::vector<float> host(4 * tab);
+  rope_table_host(cfg->theta_global, cfg->max_seq, 32, cfg->rope_table_bf16, host.data(),
+                  host.data() + tab);
+  rope_table_host(cfg->theta_local, cfg->max_seq, 32, cfg->rope_table_bf16, host.data() + 2 * tab,
+                  host.data() + 3 * tab);
+  e = cudaMalloc(&h->rope, 4 * tab * sizeof(float));
+  if (e == cudaSuccess)
+    e = cudaMemcpy(h->rope, host.data(), 4 * tab * sizeof(float), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMalloc(&h->err, 4 * sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(h->err, 0, 4 * sizeof(int));
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->capture_stream, cudaStreamNonBlocking);
+  if (e != cudaSuccess) {
+    std::string msg = std::string("create: ") + cudaGetErrorString(e);
+    laya_enc_destroy(h);
+    return fail(nullptr, LAYA_E_NOMEM, msg);
+  }
+  h->last_error = "no error";
+  *out = h;
+  return LAYA_OK;
+}
+
+static int run_impl(laya_enc_handle* h, const int32_t* ids, const int32_t* lengths, int B, int S,
+                    void* out, void* stream_v, bool device_inputs) {
+  using namespace laya;
+  int rc = check_run_args(h, B, S, out);
+  if (rc != LAYA_OK) return rc;
+  if (!ids || !lengths) return fail(h, LAYA_E_INVAL, "null token_ids or lengths");
+  if (!device_inputs) {
+    for (int b = 0; b < B; ++b)
+      if (lengths[b] < 1 || lengths[b] > S)
+        return fail(h, LAYA_E_INVAL, "lengths[" + std::to_string(b) + "] outside [1, seq]");
+    const int64_t M = static_cast<int64_t>(B) * S;
+    for (int64_t t = 0; t < M; ++t)
+      if (ids[t] < 0 || ids[t] >= h->cfg.vocab)
+        return fail(h, LAYA_E_INVAL, "token id outside [0, vocab)");
+  }
+  cudaError_t e = cudaSetDevice(h->device);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaSetDevice");
+  Workspace* w = nullptr;
+  rc = get_workspace(h, B, S, &w);
+  if (rc != LAYA_OK) return rc;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  const size_t nid = static_cast<size_t>(w->M) * sizeof(int32_t);
+  const size_t nlen = static_cast<size_t>(B) * sizeof(int32_t);
+  if (device_inputs) {
+    e = cudaMemcpyAsync(w->ids, ids, nid, cudaMemcpyDeviceToDevice, stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(w->lens, lengths, nlen, cudaMemcpyDeviceToDevice, stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "input copy");
+  } else {
+    // the previous upload from the pinned buffer must have been consumed
+    e = cudaEventSynchronize(w->staged);
+    if (e != cudaSuccess) return cuda_fail(h, e, "staging wait");
+    std::memcpy(w->host, ids, nid);
+    std::memcpy(w->host + w->M, lengths, nlen);
+    // ids and lengths are adjacent on both sides: one grouped upload
+    e = cudaMemcpyAsync(w->ids, w->host, nid + nlen, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "input upload");
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing(stream, &cap);
+    if (cap == cudaStreamCaptureStatusNone) {
+      e = cudaEventRecord(w->staged, stream);
+      if (e != cudaSuccess) return cuda_fail(h, e, "cudaEventRecord");
+    }
+  }
+  return run_common(h, w, out, stream);
+}
+
+int laya_enc_run(laya_enc_handle* h, const int32_t* token_ids, const int32_t* lengths, int batch,
+                 int seq, void* out_hidden, void* stream) {
+  return run_impl(h, token_ids, lengths, batch, seq, out_hidden, stream, false);
+}
+
+int laya_enc_run_device(laya_enc_handle* h, const int32_t* token_ids_dev,
+                        const int32_t* lengths_dev, int batch, int seq, void* out_hidden,
+                        void* stream) {
+  return run_impl(h, token_ids_dev, lengths_dev, batch, seq, out_hidden, stream, true);
+}
+
+int laya_enc_check(laya_enc_handle* h, void* stream) {
+  using namespace laya;
+  if (!h) return LAYA_E_INVAL;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamSynchronize");
+  int word = 0;
+  e = cudaMemcpy(&word, h->err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(h, e, "error word read");
+  if (word != 0) return fail(h, LAYA_E_DEVICE, "kernel reported device error " + std::to_string(word));
+  if (h->poisoned) return fail(h, LAYA_E_POISONED, "handle is poisoned by an earlier error");
+  return LAYA_OK;
+}
+
+int laya_enc_set_graphs(laya_enc_handle* h, int enabled) {
+  if (!h) return LAYA_E_INVAL;
+  h->graphs = enabled != 0;
+  return LAYA_OK;
+}
+
+int laya_enc_set_profiling(laya_enc_handle* h, int enabled) {
+  if (!h) return LAYA_E_INVAL;
+  if (!enabled && h->profiling) {
+    cudaError_t e = laya::prof_fold(h);
+    if (e != cudaSuccess) return laya::cuda_fail(h, e, "profiling events");
+  }
+  h->profiling = enabled != 0;
+  return LAYA_OK;
+}
+
+int laya_enc_profile_read(laya_enc_handle* h, double* ms, int* launches, int n) {
+  if (!h || !ms || !launches || n < 1 || n > LAYA_PROF_CLASSES) return LAYA_E_INVAL;
+  cudaError_t e = laya::prof_fold(h);
+  if (e != cudaSuccess) return laya::cuda_fail(h, e, "profiling events");
+  for (int c = 0; c < n; ++c) {
+    ms[c] = h->prof_ms[c];
+    launches[c] = h->prof_count[c];
+  }
+  for (int c = 0; c < LAYA_PROF_CLASSES; ++c) {
+    h->prof_ms[c] = 0.0;
+    h->prof_count[c] = 0;
+  }
+  return LAYA_OK;
+}
+
+int laya_enc_launch_count(const laya_enc_handle* h, int batch, int seq) {
+  (void)batch;
+  (void)seq;
+  if (!h) return LAYA_E_INVAL;
+  return laya::kernel_count(h->cfg);
+}
+
+int laya_enc_workspace_bytes(const laya_enc_handle* h, int batch, int seq, size_t* bytes) {
+  if (!h || !bytes || batch < 1 || batch > h->cfg.max_batch || seq < 1 || seq > h->cfg.max_seq)
+    return LAYA_E_INVAL;
+  laya::Workspace w;
+  size_t b = 0;
+  if (laya::workspace_layout(h, batch, seq, &w, &b) != LAYA_OK) return LAYA_E_INVAL;
+  *bytes = b;
+  return LAYA_OK;
+}
+
+int laya_enc_destroy(laya_enc_handle* h) {
+  if (!h) return LAYA_OK;
+  for (laya::Workspace* w : h->cache) laya::free_workspace(w);
+  h->cache.clear();
+  for (cudaEvent_t e : h->prof_events) cudaEventDestroy(e);
+  if (h->capture_stream) cudaStreamDestroy(h->capture_stream);
+  if (h->rope) cudaFree(h->rope);
+  if (h->err) cudaFree(h->err);
+  delete h;
+  return LAYA_OK;
+}
+
+const char* laya_enc_last_error(const laya_enc_handle* h) {
+  if (!h) return laya::g_create_error.c_str();
+  return h->last_error.c_str();
+}
+
+}  // extern "C"

@@ -1,0 +1,92 @@
+// internal.h -- declarations shared by the translation units of liblaya_enc.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/laya_enc.h"
+
+namespace laya {
+
+using bf16 = __nv_bfloat16;
+
+// Device error word codes (first error wins; the host maps any of them to
+// LAYA_E_DEVICE).
+enum DeviceError : int {
+  kDevOk = 0,
+  kDevWaitFull = 1,     // GEMM: MMA issuer gave up waiting for a TMA stage
+  kDevWaitEmpty = 2,    // GEMM: producer gave up waiting for a free stage
+  kDevWaitAccum = 3,    // GEMM: epilogue gave up waiting for the accumulator
+  kDevBadId = 4,        // embedding: token id outside [0, vocab)
+  kDevBadLength = 5,    // attention: row length outside [1, S]
+};
+
+// Upper bound on any device-side wait, in nanoseconds.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// Launch options shared by every launcher.
+struct Launch {
+  cudaStream_t stream = nullptr;
+  bool pdl = false;  // programmatic dependent launch (overlap with the previous kernel)
+};
+
+// ----------------------------------------------------------- row kernels ---
+cudaError_t launch_embed_layernorm(const bf16* emb, const bf16* gamma, const int32_t* ids, int M,
+                                   int H, int vocab, float eps, bf16* x, int* err, Launch l);
+cudaError_t launch_layernorm(const bf16* x, const bf16* gamma, int M, int H, float eps, bf16* y,
+                             Launch l);
+cudaError_t launch_rope(bf16* qkv, const float* cos_t, const float* sin_t, int B, int S,
+                        int heads, Launch l);
+bool rowops_supported_hidden(int H);
+
+// ------------------------------------------------------------- attention ---
+cudaError_t launch_attention(const bf16* qkv, const int32_t* lengths, int B, int S, int heads,
+                             int global, int half_window, bf16* ctx, int* err, Launch l);
+
+// ------------------------------------------------------------------ GEMM ---
+enum GemmKind : int { kGemmPlain = 0, kGemmResidual = 1, kGemmGeglu = 2 };
+
+struct GemmPlan {
+  int M = 0, N = 0, K = 0, kind = 0;
+  int nt = 0;            // tokens per tile (MMA N)
+  int token_tiles = 0;   // ceil(M / nt)
+  int feat_tiles = 0;    // ceil(N / 128)
+  int splits = 1;        // split-K factor = cluster size along z
+  int stages = 0;        // pipeline depth
+  int k_blocks = 0;      // K / 64
+  uint32_t tmem_cols = 0;
+  size_t smem_bytes = 0;
+  int ctas() const { return feat_tiles * token_tiles * splits; }
+};
+
+// Chooses tile and split for an M x N x K projection; force_* > 0 override.
+// Returns false if the shape is unsupported.
+bool plan_gemm(int M, int N, int K, int kind, int num_sms, int force_splits, int force_nt,
+               GemmPlan* p);
+
+// Tensor-map encoder (driver entry point resolved through the runtime).
+bool make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                       uint64_t row_stride_bytes, uint32_t box_rows);
+
+struct GemmOperands {
+  CUtensorMap w;       // weights [N, K] (GeGLU: the GELU half)
+  CUtensorMap w2;      // GeGLU gate half [N, K]; unused otherwise
+  CUtensorMap x;       // activations [M, K], box rows = plan.nt
+  bf16* y = nullptr;   // output [M, N]
+  const bf16* residual = nullptr;
+  int* err = nullptr;
+};
+
+cudaError_t launch_gemm(const GemmPlan& p, const GemmOperands& o, Launch l);
+
+// Host RoPE table (shared by create() and the op-level entry point).
+void rope_table_host(double theta, int max_seq, int half, int bf16_round, float* cos_t,
+                     float* sin_t);
+
+int device_sm_count();
+
+}  // namespace laya

@@ -1,0 +1,104 @@
+// ops_abi.cu -- the single-step entry points declared in laya_ops.h.  They
+// validate arguments on the host and launch the same kernels laya_enc_run
+// uses; nothing here computes on the CPU.
+#include <cstring>
+
+#include "../../include/laya_ops.h"
+#include "internal.h"
+
+using laya::bf16;
+
+namespace {
+
+bool al16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int rc_of(cudaError_t e) { return e == cudaSuccess ? LAYA_OK : LAYA_E_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int laya_op_embed_layernorm(const void* emb, const void* gamma, const int32_t* ids_dev, int M,
+                            int H, int vocab, float eps, void* x, int* err_dev, void* stream) {
+  if (!al16(emb) || !al16(gamma) || !ids_dev || !al16(x) || M < 1 || vocab < 1 ||
+      !laya::rowops_supported_hidden(H) || !(eps > 0.f))
+    return LAYA_E_INVAL;
+  laya::Launch l{static_cast<cudaStream_t>(stream), false};
+  return rc_of(laya::launch_embed_layernorm(static_cast<const bf16*>(emb),
+                                            static_cast<const bf16*>(gamma), ids_dev, M, H, vocab,
+                                            eps, static_cast<bf16*>(x), err_dev, l));
+}
+
+int laya_op_layernorm(const void* x, const void* gamma, int M, int H, float eps, void* y,
+                      void* stream) {
+  if (!al16(x) || !al16(gamma) || !al16(y) || M < 1 || !laya::rowops_supported_hidden(H) ||
+      !(eps > 0.f))
+    return LAYA_E_INVAL;
+  laya::Launch l{static_cast<cudaStream_t>(stream), false};
+  return rc_of(laya::launch_layernorm(static_cast<const bf16*>(x), static_cast<const bf16*>(gamma),
+                                      M, H, eps, static_cast<bf16*>(y), l));
+}
+
+int laya_op_rope_table(double theta, int max_seq, int half, int bf16_round, float* cos_host,
+                       float* sin_host) {
+  if (!(theta > 0.0) || max_seq < 1 || half < 1 || !cos_host || !sin_host) return LAYA_E_INVAL;
+  laya::rope_table_host(theta, max_seq, half, bf16_round ? 1 : 0, cos_host, sin_host);
+  return LAYA_OK;
+}
+
+int laya_op_rope(void* qkv, const float* cos_dev, const float* sin_dev, int B, int S, int heads,
+                 int head_dim, void* stream) {
+  if (!al16(qkv) || !cos_dev || !sin_dev || B < 1 || S < 1 || heads < 1 || head_dim != 64)
+    return LAYA_E_INVAL;
+  if (static_cast<long long>(B) * S > 65535) return LAYA_E_INVAL;
+  laya::Launch l{static_cast<cudaStream_t>(stream), false};
+  return rc_of(laya::launch_rope(static_cast<bf16*>(qkv), cos_dev, sin_dev, B, S, heads, l));
+}
+
+int laya_op_attention(const void* qkv, const int32_t* lengths_dev, int B, int S, int heads,
+                      int head_dim, int global, int half_window, void* ctx, void* stream) {
+  if (!al16(qkv) || !lengths_dev || !al16(ctx) || B < 1 || S < 1 || heads < 1 ||
+      head_dim != 64 || half_window < 0 || B > 65535 || heads > 65535)
+    return LAYA_E_INVAL;
+  laya::Launch l{static_cast<cudaStream_t>(stream), false};
+  return rc_of(laya::launch_attention(static_cast<const bf16*>(qkv), lengths_dev, B, S, heads,
+                                      global ? 1 : 0, half_window, static_cast<bf16*>(ctx),
+                                      nullptr, l));
+}
+
+int laya_op_linear_plan(int M, int K, int N, int kind, int num_sms, int* tile_tokens,
+                        int* splits, int* ctas) {
+  laya::GemmPlan p;
+  if (!laya::plan_gemm(M, N, K, kind, num_sms, 0, 0, &p)) return LAYA_E_INVAL;
+  if (tile_tokens) *tile_tokens = p.nt;
+  if (splits) *splits = p.splits;
+  if (ctas) *ctas = p.ctas();
+  return LAYA_OK;
+}
+
+int laya_op_linear(const void* x, int M, int K, const void* w, int N, int kind,
+                   const void* residual, void* y, int splits, int tile_tokens, void* stream) {
+  if (!al16(x) || !al16(w) || !al16(y)) return LAYA_E_INVAL;
+  if (kind == laya::kGemmResidual && !al16(residual)) return LAYA_E_INVAL;
+  laya::GemmPlan p;
+  if (!laya::plan_gemm(M, N, K, kind, laya::device_sm_count(), splits, tile_tokens, &p))
+    return LAYA_E_INVAL;
+  laya::GemmOperands o;
+  const uint64_t ldk = static_cast<uint64_t>(K) * 2;
+  bool ok = laya::make_tmap_bf16_2d(&o.w, w, N, K, ldk, 128) &&
+            laya::make_tmap_bf16_2d(&o.x, x, M, K, ldk, static_cast<uint32_t>(p.nt));
+  if (kind == laya::kGemmGeglu) {
+    const char* gate = static_cast<const char*>(w) + static_cast<size_t>(N) * K * 2;
+    ok = ok && laya::make_tmap_bf16_2d(&o.w2, gate, N, K, ldk, 128);
+  } else {
+    o.w2 = o.w;
+  }
+  if (!ok) return LAYA_E_INVAL;
+  o.y = static_cast<bf16*>(y);
+  o.residual = static_cast<const bf16*>(residual);
+  o.err = nullptr;
+  laya::Launch l{static_cast<cudaStream_t>(stream), false};
+  return rc_of(laya::launch_gemm(p, o, l));
+}
+
+}  // extern "C"

@@ -1,0 +1,234 @@
+// rowops.cu -- memory-bound row kernels: embedding gather + LayerNorm,
+// LayerNorm, RoPE; and the host-side RoPE table.
+//
+// LayerNorm: bias-free, y = (x - mean) * (1 / sqrt(var + eps)) * gamma with
+// the mean first and the variance about it second, fp32, one BF16 rounding
+// ("perf(model): exact Metal speed-ups of the forward pass - #45": the encoder
+// has no biases).  One warp per row, 16-byte vector loads: for hidden 1024
+// each lane holds 32 values in registers, so the row is read from HBM once.
+//
+// RoPE: rotate-half pairs (i, i + 32) of every 64-wide q and k head, at the
+// token's index in its padded row, with fp32 tables; each product and the sum
+// are rounded separately (no FMA) and the result once to BF16, so the result
+// is bit-identical to the CPU oracle ("[Performance]: Optimize native
+// Rust/CUDA Laya inference #66", "Starting evidence": bitwise RoPE checks at
+// both tables).  Grid (pair, head, token) with 32-bit indices, the geometry
+// "perf(model): exact Metal speed-ups of the forward pass - #45" found fast.
+#include <cmath>
+#include <cstring>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace laya {
+
+namespace {
+
+__device__ __forceinline__ void unpack8(const uint4& u, float* f) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+__device__ __forceinline__ uint4 pack8(const float* f) {
+  uint4 u;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  return u;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// V = hidden / 256 chunks of 8 BF16 per lane.  ids != nullptr selects the
+// embedding form: row t reads emb[ids[t]].
+template <int V>
+__global__ void __launch_bounds__(128) layernorm_kernel(const bf16* __restrict__ src,
+                                                        const bf16* __restrict__ gamma, int M,
+                                                        float eps, bf16* dst,
+                                                        const int32_t* __restrict__ ids,
+                                                        int vocab, int* err) {
+  ptx::grid_launch_dependents();
+  ptx::grid_dependency_wait();
+  constexpr int H = 256 * V;
+  const int row = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= M) return;
+  const bf16* in;
+  if (ids != nullptr) {
+    int id = ids[row];
+    if (id < 0 || id >= vocab) {
+      if (lane == 0 && err != nullptr) atomicCAS(err, 0, kDevBadId);
+      id = 0;
+    }
+    in = src + static_cast<size_t>(id) * H;
+  } else {
+    in = src + static_cast<size_t>(row) * H;
+  }
+  const uint4* in4 = reinterpret_cast<const uint4*>(in);
+  float v[V][8];
+#pragma unroll
+  for (int c = 0; c < V; ++c) unpack8(in4[lane + 32 * c], v[c]);
+
+  float s = 0.f;
+#pragma unroll
+  for (int c = 0; c < V; ++c)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s += v[c][i];
+  const float mean = warp_sum(s) / static_cast<float>(H);
+  float q = 0.f;
+#pragma unroll
+  for (int c = 0; c < V; ++c)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float d = v[c][i] - mean;
+      q += d * d;
+    }
+  const float var = warp_sum(q) / static_cast<float>(H);
+  const float rstd = 1.0f / sqrtf(var + eps);
+
+  const uint4* g4 = reinterpret_cast<const uint4*>(gamma);
+  uint4* out4 = reinterpret_cast<uint4*>(dst + static_cast<size_t>(row) * H);
+#pragma unroll
+  for (int c = 0; c < V; ++c) {
+    float g[8], y[8];
+    unpack8(g4[lane + 32 * c], g);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] = ((v[c][i] - mean) * rstd) * g[i];
+    out4[lane + 32 * c] = pack8(y);
+  }
+}
+
+// threadIdx.x = pair i in [0, 32), threadIdx.y + 8 * blockIdx.x = head-part
+// (q heads then k heads), blockIdx.y = token.
+__global__ void __launch_bounds__(256) rope_kernel(bf16* qkv, const float* __restrict__ cos_t,
+                                                   const float* __restrict__ sin_t, int S,
+                                                   int heads) {
+  ptx::grid_launch_dependents();
+  ptx::grid_dependency_wait();
+  const uint32_t i = threadIdx.x;
+  const uint32_t hp = blockIdx.x * blockDim.y + threadIdx.y;
+  if (hp >= 2u * static_cast<uint32_t>(heads)) return;
+  const uint32_t t = blockIdx.y;
+  const uint32_t s = t % static_cast<uint32_t>(S);
+  const uint32_t H = static_cast<uint32_t>(heads) * 64u;
+  const uint32_t part = hp / static_cast<uint32_t>(heads);
+  const uint32_t n = hp - part * static_cast<uint32_t>(heads);
+  bf16* p = qkv + t * 3u * H + part * H + n * 64u + i;
+  const float x1 = __bfloat162float(p[0]);
+  const float x2 = __bfloat162float(p[32]);
+  const float c = cos_t[s * 32u + i];
+  const float sn = sin_t[s * 32u + i];
+  const float y1 = __fsub_rn(__fmul_rn(x1, c), __fmul_rn(x2, sn));
+  const float y2 = __fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, sn));
+  p[0] = __float2bfloat16_rn(y1);
+  p[32] = __float2bfloat16_rn(y2);
+}
+
+cudaError_t launch_cfg(const void* fn, dim3 grid, dim3 block, size_t smem, Launch l,
+                       void** args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = l.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = l.pdl ? 1 : 0;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+template <int V>
+cudaError_t launch_ln_v(const bf16* src, const bf16* gamma, int M, float eps, bf16* dst,
+                        const int32_t* ids, int vocab, int* err, Launch l) {
+  const int rows_per_block = 4;
+  dim3 grid((M + rows_per_block - 1) / rows_per_block), block(32 * rows_per_block);
+  void* args[] = {(void*)&src, (void*)&gamma, (void*)&M, (void*)&eps,
+                  (void*)&dst, (void*)&ids,   (void*)&vocab, (void*)&err};
+  return launch_cfg(reinterpret_cast<const void*>(&layernorm_kernel<V>), grid, block, 0, l,
+                    args);
+}
+
+cudaError_t launch_ln(const bf16* src, const bf16* gamma, int M, int H, float eps, bf16* dst,
+                      const int32_t* ids, int vocab, int* err, Launch l) {
+  switch (H / 256) {
+    case 1: return launch_ln_v<1>(src, gamma, M, eps, dst, ids, vocab, err, l);
+    case 2: return launch_ln_v<2>(src, gamma, M, eps, dst, ids, vocab, err, l);
+    case 3: return launch_ln_v<3>(src, gamma, M, eps, dst, ids, vocab, err, l);
+    case 4: return launch_ln_v<4>(src, gamma, M, eps, dst, ids, vocab, err, l);
+    case 5: return launch_ln_v<5>(src, gamma, M, eps, dst, ids, vocab, err, l);
+    case 6: return launch_ln_v<6>(src, gamma, M, eps, dst, ids, vocab, err, l);
+    case 7: return launch_ln_v<7>(src, gamma, M, eps, dst, ids, vocab, err, l);
+    case 8: return launch_ln_v<8>(src, gamma, M, eps, dst, ids, vocab, err, l);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+float bf16_round_host(float x) {
+  uint32_t u;
+  std::memcpy(&u, &x, 4);
+  if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu) != 0u) {
+    u = (u & 0xffff0000u) | 0x00400000u;
+  } else {
+    u += 0x7fffu + ((u >> 16) & 1u);
+    u &= 0xffff0000u;
+  }
+  float y;
+  std::memcpy(&y, &u, 4);
+  return y;
+}
+
+}  // namespace
+
+bool rowops_supported_hidden(int H) { return H >= 256 && H <= 2048 && H % 256 == 0; }
+
+cudaError_t launch_embed_layernorm(const bf16* emb, const bf16* gamma, const int32_t* ids, int M,
+                                   int H, int vocab, float eps, bf16* x, int* err, Launch l) {
+  if (M <= 0 || ids == nullptr) return cudaErrorInvalidValue;
+  return launch_ln(emb, gamma, M, H, eps, x, ids, vocab, err, l);
+}
+
+cudaError_t launch_layernorm(const bf16* x, const bf16* gamma, int M, int H, float eps, bf16* y,
+                             Launch l) {
+  if (M <= 0) return cudaErrorInvalidValue;
+  return launch_ln(x, gamma, M, H, eps, y, nullptr, 0, nullptr, l);
+}
+
+cudaError_t launch_rope(bf16* qkv, const float* cos_t, const float* sin_t, int B, int S,
+                        int heads, Launch l) {
+  const int M = B * S;
+  if (M <= 0 || heads <= 0) return cudaErrorInvalidValue;
+  dim3 block(32, 8), grid((2 * heads + 7) / 8, M);
+  void* args[] = {(void*)&qkv, (void*)&cos_t, (void*)&sin_t, (void*)&S, (void*)&heads};
+  return launch_cfg(reinterpret_cast<const void*>(&rope_kernel), grid, block, 0, l, args);
+}
+
+void rope_table_host(double theta, int max_seq, int half, int bf16_round, float* cos_t,
+                     float* sin_t) {
+  for (int p = 0; p < max_seq; ++p) {
+    for (int i = 0; i < half; ++i) {
+      const double inv_freq = std::pow(theta, -2.0 * i / static_cast<double>(2 * half));
+      const double angle = static_cast<double>(p) * inv_freq;
+      float c = static_cast<float>(std::cos(angle));
+      float s = static_cast<float>(std::sin(angle));
+      if (bf16_round) {
+        c = bf16_round_host(c);
+        s = bf16_round_host(s);
+      }
+      cos_t[static_cast<size_t>(p) * half + i] = c;
+      sin_t[static_cast<size_t>(p) * half + i] = s;
+    }
+  }
+}
+
+}  // namespace laya
