@@ -75,6 +75,16 @@ int laya_op_attention(const void* qkv, const int32_t* lengths_dev, int B, int S,
                       int heads, int head_dim, int global, int half_window,
                       void* ctx, void* stream);
 
+/* RoPE and attention in one kernel: the q and k of each tile are rotated in
+ * shared memory (same arithmetic as laya_op_rope, bit-identical values) and
+ * attended as in laya_op_attention; qkv in memory is not modified.  cos_dev,
+ * sin_dev: fp32 [>= S, 32] device tables.  This is the form laya_enc_run uses.
+ * Sources: as laya_op_rope and laya_op_attention. */
+int laya_op_attention_rope(const void* qkv, const int32_t* lengths_dev,
+                           const float* cos_dev, const float* sin_dev, int B,
+                           int S, int heads, int head_dim, int global,
+                           int half_window, void* ctx, void* stream);
+
 /* Linear projection on the tensor cores (tcgen05, TMEM accumulators, TMA):
  *   a = x . w^T  (x [M, K], w [N_w, K] in nn.Linear layout, fp32 accumulate)
  * kind 0 (plain):    y [M, N] = bf16(a),             N_w = N

@@ -83,7 +83,7 @@ def test_linear_plan_small_shapes_fill_the_gpu():
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     for (N, K, kind) in ((3072, 1024, 0), (1024, 1024, 1), (2624, 1024, 2), (1024, 2624, 1)):
         nt, splits, ctas = te.linear_plan(48, K, N, kind, sms)
-        assert nt == 48 and ctas >= sms // 3, (N, K, nt, splits, ctas)
+        assert nt <= 48 and ctas >= sms // 3, (N, K, nt, splits, ctas)
 
 
 # ------------------------------------------------------------- row steps --
@@ -176,3 +176,39 @@ def _attention_case(B, S, heads, lengths, glob, hw, seed):
 ])
 def test_attention_matches_oracle(B, S, heads, lengths, glob, hw):
     _attention_case(B, S, heads, np.array(lengths, np.int32), glob, hw, seed=B * S + heads)
+
+
+@pytest.mark.parametrize("B,S,heads,lengths,glob,theta", [
+    (1, 48, 16, [48], True, 160000.0),
+    (4, 64, 16, [16, 64, 33, 50], False, 10000.0),
+    (2, 200, 4, [200, 77], False, 10000.0),
+    (3, 130, 2, [130, 1, 65], True, 160000.0),
+    (2, 512, 2, [512, 300], True, 160000.0),
+])
+def test_attention_with_fused_rope_matches_oracle(B, S, heads, lengths, glob, theta):
+    # the fused kernel rotates q and k in shared memory; the oracle applies
+    # RoPE to the packed projection first and then attends
+    torch = require_gpu()
+    rng = np.random.default_rng(B * S + heads + 7)
+    H = heads * 64
+    lengths = np.array(lengths, np.int32)
+    qkv = rnd_bits(rng, (B * S, 3 * H), std=0.7)
+    c, s = te.rope_table(theta, 512, 32)
+    dev = to_dev(qkv)
+    ctx = torch.full((B * S, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    te.attention_rope(dev, i32_dev(lengths), torch.from_numpy(c).cuda(), torch.from_numpy(s).cuda(),
+                      B, S, heads, glob, 64, ctx)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to_bits(dev), qkv)                  # projection not modified
+    rotated = oracle.rope(qkv, B, S, heads, 64, *oracle.rope_table(theta, 512, 32))
+    ref = bf16_bits_to_f32(oracle.attention(rotated, lengths, B, S, heads, 64, glob, 64)).reshape(B, S, H)
+    got = bf16_bits_to_f32(to_bits(ctx)).reshape(B, S, H)
+    v = bf16_bits_to_f32(qkv).reshape(B, S, 3, heads, 64)[:, :, 2]
+    for b in range(B):
+        L = lengths[b]
+        g, r = got[b, :L].astype(np.float64), ref[b, :L].astype(np.float64)
+        vmax = np.abs(v[b, :L]).max(axis=(0, 2))
+        lim = 0.5 * ulp_bf16(r) + 2.0 ** -8 * np.repeat(vmax, 64)[None, :]
+        assert np.all(np.abs(g - r) <= lim), (b, float(np.max(np.abs(g - r) - lim)))
+        assert nrms(g, r) < 3e-3
+    assert np.all(np.isfinite(got))

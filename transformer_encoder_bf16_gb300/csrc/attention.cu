@@ -14,6 +14,12 @@
 //
 // Tensor cores: QK^T and PV run on mma.sync m16n8k16 (BF16 in, fp32 out); P
 // is rounded to BF16 for the PV product.  Softmax in fp32 with exp2.
+//
+// RoPE fused: with tables given, each Q tile and each K tile is rotated in
+// shared memory right after it lands, with exactly the arithmetic of the
+// stand-alone RoPE kernel (fp32 products and sum each rounded, one BF16
+// rounding), so attention sees bit-identical q and k while the packed
+// projection in memory is read once and never rewritten.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -79,11 +85,34 @@ __device__ __forceinline__ void load_tile(uint32_t sdst, const bf16* base, int r
   }
 }
 
+// Rotate pairs (i, i + 32) of a 64 x 64 tile in shared memory whose first row
+// is at position row0; rows at or beyond S (zero-filled) are left alone.
+__device__ __forceinline__ void rope_tile(bf16* tile, int row0, int S,
+                                          const float* __restrict__ cos_t,
+                                          const float* __restrict__ sin_t, int tid) {
+#pragma unroll 4
+  for (int r = 0; r < 16; ++r) {
+    const int idx = tid + 128 * r;
+    const int row = idx >> 5, i = idx & 31;
+    const int pos = row0 + row;
+    if (pos < S) {
+      bf16* p = tile + row * kLd + i;
+      const float x1 = __bfloat162float(p[0]);
+      const float x2 = __bfloat162float(p[32]);
+      const float c = cos_t[pos * 32 + i];
+      const float sn = sin_t[pos * 32 + i];
+      p[0] = __float2bfloat16_rn(__fsub_rn(__fmul_rn(x1, c), __fmul_rn(x2, sn)));
+      p[32] = __float2bfloat16_rn(__fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, sn)));
+    }
+  }
+}
+
 __global__ void __launch_bounds__(128) attention_kernel(const bf16* __restrict__ qkv,
                                                         const int32_t* __restrict__ lengths,
                                                         int S, int heads, int global,
                                                         int half_window, bf16* __restrict__ ctx,
-                                                        int* err) {
+                                                        int* err, const float* __restrict__ cos_t,
+                                                        const float* __restrict__ sin_t) {
   __shared__ __align__(128) bf16 sQ[kQ * kLd];
   __shared__ __align__(128) bf16 sK[2][kKT * kLd];
   __shared__ __align__(128) bf16 sV[2][kKT * kLd];
@@ -160,6 +189,11 @@ __global__ void __launch_bounds__(128) attention_kernel(const bf16* __restrict__
       cp_async_wait<0>();
     }
     __syncthreads();
+    if (cos_t != nullptr) {
+      if (kt == kt0) rope_tile(sQ, q0, S, cos_t, sin_t, tid);
+      rope_tile(buf ? sK[1] : sK[0], kt * kKT, S, cos_t, sin_t, tid);
+      __syncthreads();
+    }
     if (kt == kt0) {
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
@@ -278,7 +312,8 @@ __global__ void __launch_bounds__(128) attention_kernel(const bf16* __restrict__
 }  // namespace
 
 cudaError_t launch_attention(const bf16* qkv, const int32_t* lengths, int B, int S, int heads,
-                             int global, int half_window, bf16* ctx, int* err, Launch l) {
+                             int global, int half_window, bf16* ctx, int* err, Launch l,
+                             const float* cos_t, const float* sin_t) {
   if (B <= 0 || S <= 0 || heads <= 0) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((S + kQ - 1) / kQ, heads, B);
@@ -290,7 +325,7 @@ cudaError_t launch_attention(const bf16* qkv, const int32_t* lengths, int B, int
   cfg.attrs = attr;
   cfg.numAttrs = l.pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, attention_kernel, qkv, lengths, S, heads, global, half_window,
-                            ctx, err);
+                            ctx, err, cos_t, sin_t);
 }
 
 }  // namespace laya

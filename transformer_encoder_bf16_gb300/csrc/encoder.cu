@@ -8,8 +8,9 @@
 //     if l == n_enc and final_norm:  x = LN_final(x)
 //     h   = (l == 0 and first_attn_norm_identity) ? x : LN_attn(x)
 //     qkv = h Wqkv^T                  GEMM, plain epilogue
-//     q,k = RoPE(q,k)                 global table iff decision layer or l % global_every == 0
-//     ctx = attention(qkv, lengths)   sliding window on local layers
+//     ctx = attention(RoPE(q), RoPE(k), v, lengths)   RoPE fused into the attention
+//                                     kernel; global table iff decision layer or
+//                                     l % global_every == 0; sliding window on local layers
 //     x   = x + ctx Wo^T              GEMM, residual epilogue (in place)
 //     h   = LN_mlp(x)
 //     g   = gelu(h Wup_in^T) * (h Wup_gate^T)   GEMM, GeGLU epilogue
@@ -57,7 +58,9 @@ struct Workspace {
   cudaEvent_t staged = nullptr;   // the last upload from `host` has been consumed
   cudaEvent_t done = nullptr;     // the last forward using this workspace has finished
   GemmPlan p_qkv, p_o, p_up, p_dn;
-  CUtensorMap tm_x, tm_h, tm_ctx, tm_g;
+  // activation operand of each GEMM; the TMA box height is that GEMM's own
+  // token tile (plans may differ: a GeGLU split-K partial can force a smaller tile)
+  CUtensorMap tm_x_qkv, tm_h_qkv, tm_ctx_o, tm_h_up, tm_g_dn;
   cudaGraphExec_t exec = nullptr;
   void* graph_out = nullptr;
   uint64_t last_use = 0;
@@ -171,7 +174,7 @@ int workspace_layout(const laya_enc_handle* h, int B, int S, Workspace* w, size_
 
 int kernel_count(const laya_enc_config& c) {
   const int L = c.n_encoder_layers + c.n_decision_layers;
-  int n = 1 + 8 * L;
+  int n = 1 + 7 * L;  // norm, QKV, attention (+RoPE), out-proj, norm, up, down
   if (c.first_attn_norm_identity) n -= 1;
   if (c.final_norm && c.n_decision_layers > 0) n += 1;
   return n;
@@ -249,9 +252,9 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, bf16* out, cudaStr
     if (li == c.n_encoder_layers && c.final_norm)
       LAYA_LAUNCH(LAYA_PROF_NORM,
                   launch_layernorm(w->x, h->final_norm, M, H, c.ln_eps, w->x, l));
-    const CUtensorMap* qkv_in = &w->tm_h;
+    const CUtensorMap* qkv_in = &w->tm_h_qkv;
     if (li == 0 && c.first_attn_norm_identity) {
-      qkv_in = &w->tm_x;
+      qkv_in = &w->tm_x_qkv;
     } else {
       LAYA_LAUNCH(LAYA_PROF_NORM, launch_layernorm(w->x, lw.attn_norm, M, H, c.ln_eps, w->h, l));
     }
@@ -260,29 +263,32 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, bf16* out, cudaStr
     o.w = lw.wqkv;
     o.w2 = lw.wqkv;
     o.x = *qkv_in;
+    o.x_box_rows = w->p_qkv.nt;
     o.y = w->qkv;
     LAYA_LAUNCH(LAYA_PROF_QKV, launch_gemm(w->p_qkv, o, l));
-    LAYA_LAUNCH(LAYA_PROF_ROPE, launch_rope(w->qkv, glob ? cos_g : cos_l, glob ? sin_g : sin_l,
-                                            w->B, w->S, c.heads, l));
     LAYA_LAUNCH(LAYA_PROF_ATTN, launch_attention(w->qkv, w->lens, w->B, w->S, c.heads,
                                                  glob ? 1 : 0, c.local_half_window, w->ctx,
-                                                 h->err, l));
+                                                 h->err, l, glob ? cos_g : cos_l,
+                                                 glob ? sin_g : sin_l));
     o.w = lw.wo;
     o.w2 = lw.wo;
-    o.x = w->tm_ctx;
+    o.x = w->tm_ctx_o;
+    o.x_box_rows = w->p_o.nt;
     o.y = w->x;
     o.residual = w->x;
     LAYA_LAUNCH(LAYA_PROF_OUT, launch_gemm(w->p_o, o, l));
     LAYA_LAUNCH(LAYA_PROF_NORM, launch_layernorm(w->x, lw.mlp_norm, M, H, c.ln_eps, w->h, l));
     o.w = lw.wup_in;
     o.w2 = lw.wup_gate;
-    o.x = w->tm_h;
+    o.x = w->tm_h_up;
+    o.x_box_rows = w->p_up.nt;
     o.y = w->g;
     o.residual = nullptr;
     LAYA_LAUNCH(LAYA_PROF_UP, launch_gemm(w->p_up, o, l));
     o.w = lw.wdown;
     o.w2 = lw.wdown;
-    o.x = w->tm_g;
+    o.x = w->tm_g_dn;
+    o.x_box_rows = w->p_dn.nt;
     o.y = (li == h->L - 1) ? out : w->x;
     o.residual = w->x;
     LAYA_LAUNCH(LAYA_PROF_DOWN, launch_gemm(w->p_dn, o, l));
@@ -337,11 +343,13 @@ int get_workspace(laya_enc_handle* h, int B, int S, Workspace** out) {
   }
   const laya_enc_config& c = h->cfg;
   const int M = w->M;
-  const uint32_t nt = static_cast<uint32_t>(w->p_qkv.nt);
-  bool ok = make_tmap_bf16_2d(&w->tm_x, w->x, M, c.hidden, c.hidden * 2ull, nt) &&
-            make_tmap_bf16_2d(&w->tm_h, w->h, M, c.hidden, c.hidden * 2ull, nt) &&
-            make_tmap_bf16_2d(&w->tm_ctx, w->ctx, M, c.hidden, c.hidden * 2ull, nt) &&
-            make_tmap_bf16_2d(&w->tm_g, w->g, M, c.intermediate, c.intermediate * 2ull, nt);
+  auto box = [](const GemmPlan& p) { return static_cast<uint32_t>(p.nt); };
+  const uint64_t ldh = c.hidden * 2ull, ldi = c.intermediate * 2ull;
+  bool ok = make_tmap_bf16_2d(&w->tm_x_qkv, w->x, M, c.hidden, ldh, box(w->p_qkv)) &&
+            make_tmap_bf16_2d(&w->tm_h_qkv, w->h, M, c.hidden, ldh, box(w->p_qkv)) &&
+            make_tmap_bf16_2d(&w->tm_ctx_o, w->ctx, M, c.hidden, ldh, box(w->p_o)) &&
+            make_tmap_bf16_2d(&w->tm_h_up, w->h, M, c.hidden, ldh, box(w->p_up)) &&
+            make_tmap_bf16_2d(&w->tm_g_dn, w->g, M, c.intermediate, ldi, box(w->p_dn));
   if (!ok) {
     free_workspace(w);
     return fail(h, LAYA_E_CUDA, "workspace: tensor map encoding failed");

@@ -35,7 +35,9 @@
 // overlaps the tail of the kernel before it; activations are loaded after.
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -51,6 +53,7 @@ constexpr uint32_t kATileBytes = kBM * kBK * 2;
 constexpr int kMaxSplits = 8;            // portable cluster size
 constexpr size_t kSmemLimit = 227 * 1024;
 constexpr size_t kCtrlBytes = 256;
+constexpr int kEpiBatch = 4;             // epilogue units whose loads are issued together
 
 struct GemmArgs {
   int M, N, k_blocks, nt, splits, stages;
@@ -63,18 +66,6 @@ struct GemmArgs {
 
 __device__ __forceinline__ float gelu_erf(float z) {
   return (0.5f * z) * (1.0f + erff(z * 0.70710678118654752f));
-}
-
-template <int KIND>
-__device__ __forceinline__ void store_out(const GemmArgs& a, int t, int f, float v, float g) {
-  const size_t o = static_cast<size_t>(t) * a.N + f;
-  if (KIND == kGemmPlain) {
-    a.y[o] = __float2bfloat16_rn(v);
-  } else if (KIND == kGemmResidual) {
-    a.y[o] = __float2bfloat16_rn(__bfloat162float(a.residual[o]) + v);
-  } else {
-    a.y[o] = __float2bfloat16_rn(gelu_erf(v) * g);
-  }
 }
 
 template <int KIND>
@@ -126,6 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   ptx::grid_launch_dependents();
   const uint32_t tmem = *tmem_slot;
+  bool epi_ok = false;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -195,81 +187,146 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mma_commit(accum_bar);
     }
   } else {
-    // -------------------------------------------------------------- epilogue
+    // ------------------------------------------- epilogue phase 1: drain TMEM
+    // fp32 tile staged token-major in shared memory: stg[c * 128 + row] for
+    // token column c and feature row (the pipeline stages are free by now).
+    // Split-K parks the raw partial (GeGLU: both halves); otherwise the
+    // GeGLU product is formed here.
     const int q = warp & 3;
     const int row = q * 32 + lane;
-    const int f = f_tile * kBM + row;
-    const int t_base = t_tile * a.nt;
     const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    const bool ok = ptx::mbar_wait(accum_bar, 0, abort_flag, a.err, kDevWaitAccum, kWaitLimitNs);
+    epi_ok = ptx::mbar_wait(accum_bar, 0, abort_flag, a.err, kDevWaitAccum, kWaitLimitNs);
     ptx::tc_fence_after();
-    if (ok) {
-      if (a.splits == 1) {
-        ptx::grid_dependency_wait();  // residual / output of earlier kernels
-        for (int c0 = 0; c0 < a.nt; c0 += 16) {
-          float v[16], g[16];
-          ptx::tmem_ld16(tq + c0, v);
-          if (NA == 2) ptx::tmem_ld16(tq + a.nt + c0, g);
-          if (f < a.N) {
+    if (epi_ok) {
+      float* stg = reinterpret_cast<float*>(smem);
+      for (int c0 = 0; c0 < a.nt; c0 += 16) {
+        float v[16];
+        ptx::tmem_ld16(tq + c0, v);
+        if (NA == 2) {
+          float g[16];
+          ptx::tmem_ld16(tq + a.nt + c0, g);
+          if (a.splits == 1) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int t = t_base + c0 + j;
-              if (t < a.M) store_out<KIND>(a, t, f, v[j], NA == 2 ? g[j] : 0.f);
-            }
+            for (int j = 0; j < 16; ++j) v[j] = gelu_erf(v[j]) * g[j];
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) stg[(a.nt + c0 + j) * kBM + row] = g[j];
           }
         }
-      } else {
-        // park the partial tile: part[(c * 128) + row], c = token column
-        float* part = reinterpret_cast<float*>(smem);
-        for (int c0 = 0; c0 < a.nt; c0 += 16) {
-          float v[16];
-          ptx::tmem_ld16(tq + c0, v);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) part[(c0 + j) * kBM + row] = v[j];
-          if (NA == 2) {
-            ptx::tmem_ld16(tq + a.nt + c0, v);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) part[(a.nt + c0 + j) * kBM + row] = v[j];
-          }
-        }
+        for (int j = 0; j < 16; ++j) stg[(c0 + j) * kBM + row] = v[j];
       }
     }
+    if (a.splits == 1) ptx::named_barrier_sync(1, kThreads - 64);
   }
 
   if (a.splits > 1) {
     __syncwarp();
     ptx::cluster_sync();  // every partial of the cluster is parked
-    if (warp >= 2) {
-      ptx::grid_dependency_wait();
-      const uint32_t S = static_cast<uint32_t>(a.splits);
+  }
+
+  if (warp >= 2 && epi_ok) {
+    // ------------------------------- epilogue phase 2: 16-byte vector stores
+    // unit = 8 consecutive features of one token; consecutive threads take
+    // consecutive units of a token row, so loads and stores are coalesced.
+    // Split-K: this CTA finishes the feature groups [g0, g1) of the tile,
+    // summing the partials of every CTA of the cluster in rank order.
+    int g0 = 0, g1 = kBM / 8;
+    uint32_t remote[kMaxSplits];
+    if (a.splits > 1) {
       const uint32_t rank = ptx::cluster_ctarank();
-      const int r0 = static_cast<int>(rank * kBM / S);
-      const int r1 = static_cast<int>((rank + 1) * kBM / S);
-      const int nrows = r1 - r0;
-      const int total = nrows * a.nt;
-      const int t_base = t_tile * a.nt;
-      uint32_t remote[kMaxSplits];
+      g0 = static_cast<int>(rank * (kBM / 8) / a.splits);
+      g1 = static_cast<int>((rank + 1) * (kBM / 8) / a.splits);
 #pragma unroll
       for (int s = 0; s < kMaxSplits; ++s) remote[s] = s < a.splits ? ptx::mapa(sbase, s) : 0u;
-      for (int e = threadIdx.x - 64; e < total; e += kThreads - 64) {
-        const int rr = e % nrows;
-        const int c = e / nrows;
-        const int row = r0 + rr;
-        const int f = f_tile * kBM + row;
-        const int t = t_base + c;
-        const uint32_t off = static_cast<uint32_t>(c * kBM + row) * 4u;
-        const uint32_t off2 = static_cast<uint32_t>((a.nt + c) * kBM + row) * 4u;
-        float v = 0.f, g = 0.f;
+    }
+    const int ng = g1 - g0;
+    const int units = ng * a.nt;
+    const int t_base = t_tile * a.nt;
+    const int tid_e = threadIdx.x - 64;
+    const float* stg = reinterpret_cast<const float*>(smem);
+    ptx::grid_dependency_wait();  // residual written by earlier kernels
+    for (int u0 = tid_e; u0 < units; u0 += (kThreads - 64) * kEpiBatch) {
+      float v[kEpiBatch][8], gt[kEpiBatch][8];
+      uint4 res[kEpiBatch];
+      int tok[kEpiBatch], fea[kEpiBatch];
+      // loads first (the output may alias the residual: keep every load of
+      // the batch ahead of its stores)
 #pragma unroll
-        for (int s = 0; s < kMaxSplits; ++s) {
-          if (s < a.splits) {
-            v += ptx::ld_dsmem_f32(remote[s] + off);
-            if (NA == 2) g += ptx::ld_dsmem_f32(remote[s] + off2);
+      for (int b = 0; b < kEpiBatch; ++b) {
+        const int u = u0 + (kThreads - 64) * b;
+        tok[b] = -1;
+        if (u < units) {
+          const int c = u / ng;
+          const int grp = g0 + u % ng;
+          const uint32_t off = static_cast<uint32_t>(c * kBM + grp * 8) * 4u;
+          if (a.splits > 1) {
+            const uint32_t off2 = off + static_cast<uint32_t>(a.nt * kBM) * 4u;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              v[b][i] = 0.f;
+              gt[b][i] = 0.f;
+            }
+#pragma unroll
+            for (int s = 0; s < kMaxSplits; ++s) {
+              if (s < a.splits) {
+                float t8[8];
+                ptx::ld_dsmem_f32x8(remote[s] + off, t8);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[b][i] += t8[i];
+                if (NA == 2) {
+                  ptx::ld_dsmem_f32x8(remote[s] + off2, t8);
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) gt[b][i] += t8[i];
+                }
+              }
+            }
+            if (NA == 2) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) v[b][i] = gelu_erf(v[b][i]) * gt[b][i];
+            }
+          } else {
+            const float4* p4 = reinterpret_cast<const float4*>(stg + off / 4u);
+            const float4 lo = p4[0], hi = p4[1];
+            v[b][0] = lo.x; v[b][1] = lo.y; v[b][2] = lo.z; v[b][3] = lo.w;
+            v[b][4] = hi.x; v[b][5] = hi.y; v[b][6] = hi.z; v[b][7] = hi.w;
+          }
+          const int t = t_base + c;
+          const int f = f_tile * kBM + grp * 8;
+          if (t < a.M && f < a.N) {
+            tok[b] = t;
+            fea[b] = f;
+            if (KIND == kGemmResidual)
+              res[b] = *reinterpret_cast<const uint4*>(a.residual + static_cast<size_t>(t) * a.N + f);
           }
         }
-        if (f < a.N && t < a.M) store_out<KIND>(a, t, f, v, g);
+      }
+#pragma unroll
+      for (int b = 0; b < kEpiBatch; ++b) {
+        if (tok[b] < 0) continue;
+        float o[8];
+        if (KIND == kGemmResidual) {
+          const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&res[b]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 rf = __bfloat1622float2(r2[i]);
+            o[2 * i] = rf.x + v[b][2 * i];
+            o[2 * i + 1] = rf.y + v[b][2 * i + 1];
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) o[i] = v[b][i];
+        }
+        uint4 packed;
+        __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&packed);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) p2[i] = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+        *reinterpret_cast<uint4*>(a.y + static_cast<size_t>(tok[b]) * a.N + fea[b]) = packed;
       }
     }
+  }
+
+  if (a.splits > 1) {
     __syncwarp();
     ptx::cluster_sync();  // nobody leaves while its partial may still be read
   }
@@ -301,6 +358,8 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
+cudaError_t configure_kernels();
+
 uint32_t pow2_cols(uint32_t n) {
   uint32_t c = 32;
   while (c < n) c <<= 1;
@@ -309,18 +368,8 @@ uint32_t pow2_cols(uint32_t n) {
 
 template <int KIND>
 cudaError_t launch_kind(const GemmPlan& p, const GemmOperands& o, Launch l) {
-  static bool configured = false;
-  static std::mutex mu;
-  {
-    std::lock_guard<std::mutex> g(mu);
-    if (!configured) {
-      cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<KIND>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(kSmemLimit));
-      if (e != cudaSuccess) return e;
-      configured = true;
-    }
-  }
+  cudaError_t ce = configure_kernels();
+  if (ce != cudaSuccess) return ce;
   GemmArgs a;
   a.M = p.M;
   a.N = p.N;
@@ -332,7 +381,7 @@ cudaError_t launch_kind(const GemmPlan& p, const GemmOperands& o, Launch l) {
   const int na = KIND == kGemmGeglu ? 2 : 1;
   const size_t stage_bytes = static_cast<size_t>(na) * kATileBytes + static_cast<size_t>(p.nt) * 128;
   size_t data = stage_bytes * p.stages;
-  const size_t part = p.splits > 1 ? static_cast<size_t>(na) * p.nt * kBM * 4 : 0;
+  const size_t part = static_cast<size_t>(p.splits > 1 ? na : 1) * p.nt * kBM * 4;
   if (part > data) data = part;
   a.ctrl_offset = static_cast<uint32_t>(data);
   a.y = o.y;
@@ -365,6 +414,64 @@ cudaError_t launch_kind(const GemmPlan& p, const GemmOperands& o, Launch l) {
 
 namespace {
 
+const void* kernel_ptr(int kind) {
+  switch (kind) {
+    case kGemmPlain: return reinterpret_cast<const void*>(&gemm_tc_kernel<kGemmPlain>);
+    case kGemmResidual: return reinterpret_cast<const void*>(&gemm_tc_kernel<kGemmResidual>);
+    default: return reinterpret_cast<const void*>(&gemm_tc_kernel<kGemmGeglu>);
+  }
+}
+
+// Opt every kernel variant into the full dynamic shared memory once.
+cudaError_t configure_kernels() {
+  static cudaError_t status = cudaErrorNotReady;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    status = cudaSuccess;
+    for (int k = kGemmPlain; k <= kGemmGeglu && status == cudaSuccess; ++k)
+      status = cudaFuncSetAttribute(kernel_ptr(k), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(kSmemLimit));
+  });
+  return status;
+}
+
+// How many clusters of `splits` CTAs with this shared memory can be resident
+// at once on the current device; -1 when there is no device to ask.
+int max_active_clusters(int kind, size_t smem, int splits) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, size_t, int>, int> cache;
+  const auto key = std::make_tuple(kind, smem, splits);
+  {
+    std::lock_guard<std::mutex> g(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  int n = -1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && configure_kernels() == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, splits);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = splits;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel_ptr(kind), &cfg) != cudaSuccess) n = -1;
+  }
+  cudaGetLastError();  // a failed query must not leave a sticky-looking error behind
+  std::lock_guard<std::mutex> g(mu);
+  cache[key] = n;
+  return n;
+}
+
+}  // namespace
+
+namespace {
+
 // Fills everything that follows from (M, N, K, kind, nt, splits); false if the
 // tile does not fit in shared memory or TMEM.
 bool finish_plan(GemmPlan* r) {
@@ -378,7 +485,8 @@ bool finish_plan(GemmPlan* r) {
   if (stages < 1) return false;
   r->stages = stages;
   size_t data = stage_bytes * stages;
-  const size_t part = r->splits > 1 ? static_cast<size_t>(na) * r->nt * kBM * 4 : 0;
+  // fp32 staging tile of the epilogue (split-K: one per half of a GeGLU)
+  const size_t part = static_cast<size_t>(r->splits > 1 ? na : 1) * r->nt * kBM * 4;
   if (part > budget) return false;
   if (part > data) data = part;
   r->smem_bytes = data + kCtrlBytes + 1024;
@@ -402,10 +510,20 @@ bool plan_gemm(int M, int N, int K, int kind, int num_sms, int force_splits, int
   if (M <= 0 || N <= 0 || K <= 0 || K % kBK != 0 || N % 8 != 0) return false;
   if (kind < kGemmPlain || kind > kGemmGeglu) return false;
   if (force_nt > 0 && (force_nt % 16 != 0 || force_nt > 256)) return false;
+  if (force_splits > 0 && (force_splits > kMaxSplits || force_splits > K / kBK)) return false;
   if (num_sms <= 0) num_sms = 148;
-  // token tiling: the fewest tiles of at most 256 tokens, evened out; one more
-  // tile at a time while a split-K partial would not fit in shared memory
-  for (int tt = (M + 255) / 256; tt <= (M + 15) / 16; ++tt) {
+  const int na = kind == kGemmGeglu ? 2 : 1;
+  // Candidates: token tilings (the fewest tiles of at most 256 tokens, evened
+  // out, and up to three finer ones) x split-K factors.  Cost model: waves x
+  // per-CTA time, a wave being as many clusters as the device can hold at
+  // once and the per-CTA time the bytes one CTA streams (in 16 KB weight-tile
+  // units) plus a fixed overhead of two units for set-up, epilogue and the
+  // cluster reduction.
+  GemmPlan best;
+  double best_cost = 0.0;
+  bool found = false;
+  const int tt_min = (M + 255) / 256;
+  for (int tt = tt_min; tt <= tt_min + 3; ++tt) {
     GemmPlan r;
     r.M = M;
     r.N = N;
@@ -413,34 +531,39 @@ bool plan_gemm(int M, int N, int K, int kind, int num_sms, int force_splits, int
     r.kind = kind;
     r.k_blocks = K / kBK;
     if (force_nt > 0) {
+      if (tt > tt_min) break;
       r.nt = force_nt;
     } else {
       const int per = (M + tt - 1) / tt;
       r.nt = (per + 15) / 16 * 16;
+      if (tt > tt_min && r.nt < 32) break;
     }
     r.token_tiles = (M + r.nt - 1) / r.nt;
     r.feat_tiles = (N + kBM - 1) / kBM;
     const int tiles = r.token_tiles * r.feat_tiles;
-    int splits;
-    if (force_splits > 0) {
-      splits = force_splits;
-    } else {
-      splits = tiles >= num_sms ? 1 : num_sms / tiles;
-      // keep at least two K blocks per CTA so that each split still pipelines
-      if (splits > r.k_blocks / 2) splits = r.k_blocks / 2;
+    const int s_lo = force_splits > 0 ? force_splits : 1;
+    const int s_hi = force_splits > 0 ? force_splits : (tiles >= num_sms ? 1 : kMaxSplits);
+    for (int S = s_lo; S <= s_hi && S <= r.k_blocks; ++S) {
+      GemmPlan c = r;
+      c.splits = S;
+      if (!finish_plan(&c)) continue;
+      int mac = max_active_clusters(kind, c.smem_bytes, S);
+      if (mac <= 0) mac = num_sms / S;  // no device to ask: one CTA per SM
+      if (mac <= 0) continue;
+      const int waves = (tiles + mac - 1) / mac;
+      const int kb_per = (c.k_blocks + S - 1) / S;
+      const double unit = (na * kATileBytes + static_cast<double>(c.nt) * 128.0) / kATileBytes;
+      const double cost = waves * (kb_per * unit + 2.0);
+      if (!found || cost < best_cost - 1e-9) {
+        best = c;
+        best_cost = cost;
+        found = true;
+      }
     }
-    if (splits < 1) splits = 1;
-    if (splits > kMaxSplits) splits = kMaxSplits;
-    if (splits > r.k_blocks) splits = r.k_blocks;
-    if (force_splits > 0 && splits != force_splits) return false;
-    r.splits = splits;
-    if (finish_plan(&r)) {
-      *p = r;
-      return true;
-    }
-    if (force_nt > 0) return false;
   }
-  return false;
+  if (!found) return false;
+  *p = best;
+  return true;
 }
 
 bool make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
@@ -461,6 +584,8 @@ bool make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t
 }
 
 cudaError_t launch_gemm(const GemmPlan& p, const GemmOperands& o, Launch l) {
+  // the TMA box must match the shared-memory stage the plan reserves for it
+  if (o.x_box_rows != p.nt) return cudaErrorInvalidValue;
   switch (p.kind) {
     case kGemmPlain: return launch_kind<kGemmPlain>(p, o, l);
     case kGemmResidual: return launch_kind<kGemmResidual>(p, o, l);

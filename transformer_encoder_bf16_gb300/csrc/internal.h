@@ -44,8 +44,10 @@ cudaError_t launch_rope(bf16* qkv, const float* cos_t, const float* sin_t, int B
 bool rowops_supported_hidden(int H);
 
 // ------------------------------------------------------------- attention ---
+// cos_t/sin_t non-null: RoPE is applied to q and k inside the kernel.
 cudaError_t launch_attention(const bf16* qkv, const int32_t* lengths, int B, int S, int heads,
-                             int global, int half_window, bf16* ctx, int* err, Launch l);
+                             int global, int half_window, bf16* ctx, int* err, Launch l,
+                             const float* cos_t = nullptr, const float* sin_t = nullptr);
 
 // ------------------------------------------------------------------ GEMM ---
 enum GemmKind : int { kGemmPlain = 0, kGemmResidual = 1, kGemmGeglu = 2 };
@@ -76,6 +78,7 @@ struct GemmOperands {
   CUtensorMap w;       // weights [N, K] (GeGLU: the GELU half)
   CUtensorMap w2;      // GeGLU gate half [N, K]; unused otherwise
   CUtensorMap x;       // activations [M, K], box rows = plan.nt
+  int x_box_rows = 0;  // the box height x was encoded with; launch_gemm checks it
   bf16* y = nullptr;   // output [M, N]
   const bf16* residual = nullptr;
   int* err = nullptr;

@@ -66,6 +66,18 @@ int laya_op_attention(const void* qkv, const int32_t* lengths_dev, int B, int S,
                                       nullptr, l));
 }
 
+int laya_op_attention_rope(const void* qkv, const int32_t* lengths_dev, const float* cos_dev,
+                           const float* sin_dev, int B, int S, int heads, int head_dim, int global,
+                           int half_window, void* ctx, void* stream) {
+  if (!al16(qkv) || !lengths_dev || !cos_dev || !sin_dev || !al16(ctx) || B < 1 || S < 1 ||
+      heads < 1 || head_dim != 64 || half_window < 0 || B > 65535 || heads > 65535)
+    return LAYA_E_INVAL;
+  laya::Launch l{static_cast<cudaStream_t>(stream), false};
+  return rc_of(laya::launch_attention(static_cast<const bf16*>(qkv), lengths_dev, B, S, heads,
+                                      global ? 1 : 0, half_window, static_cast<bf16*>(ctx),
+                                      nullptr, l, cos_dev, sin_dev));
+}
+
 int laya_op_linear_plan(int M, int K, int N, int kind, int num_sms, int* tile_tokens,
                         int* splits, int* ctas) {
   laya::GemmPlan p;
@@ -94,6 +106,7 @@ int laya_op_linear(const void* x, int M, int K, const void* w, int N, int kind,
     o.w2 = o.w;
   }
   if (!ok) return LAYA_E_INVAL;
+  o.x_box_rows = p.nt;
   o.y = static_cast<bf16*>(y);
   o.residual = static_cast<const bf16*>(residual);
   o.err = nullptr;

@@ -205,6 +205,18 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
   return v;
 }
 
+// Eight consecutive fp32 values (32 bytes, 16-byte aligned) of a cluster peer.
+__device__ __forceinline__ void ld_dsmem_f32x8(uint32_t addr, float (&v)[8]) {
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3])
+               : "r"(addr)
+               : "memory");
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7])
+               : "r"(addr + 16u)
+               : "memory");
+}
+
 // ------------------------------------------- programmatic dependent launch ---
 
 // Wait until the preceding kernel in the stream has finished and its writes
