@@ -68,6 +68,34 @@ def barrier(world: int):
         dist.barrier()
 
 
+def csrc_sha16():
+    """Hash of the kernel sources, to tell whether recorded ncu counters still apply."""
+    import glob
+    import hashlib
+    d = os.path.join(ROOT, "transformer_encoder_bf16_gb300", "csrc")
+    h = hashlib.sha256()
+    for pat in ("*.cu", "*.cuh", "*.h"):
+        for f in sorted(glob.glob(os.path.join(d, pat))):
+            with open(f, "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload, kernel_class):
+    """DRAM bytes per launch from the committed ncu capture, or None when the
+    kernels changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        if d.get("csrc_sha16") != csrc_sha16():
+            return None
+        v = d.get(workload, {}).get(kernel_class)
+        return float(v) if v is not None else None
+    except Exception:
+        return None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -340,7 +368,7 @@ def main():
     else:
         roof = {"bound": "hbm", "achieved": nbytes / avg_s / 1e9, "peak": hbm_peak, "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = recorded_traffic(args.workload, cls)
     roof["kernel"] = cls
     roof["avg_launch_us"] = avg_s * 1e6
     roof["launches"] = n

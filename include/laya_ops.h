@@ -104,6 +104,31 @@ int laya_op_linear(const void* x, int M, int K, const void* w, int N, int kind,
                    const void* residual, void* y, int splits, int tile_tokens,
                    void* stream);
 
+/* A projection whose input is LayerNorm'd on load: the GEMM reads rows of
+ * x_raw [M, K] and computes h = bf16(LN(x_raw) * gamma) in shared memory with
+ * exactly the arithmetic of laya_op_layernorm, so y equals laya_op_layernorm
+ * followed by laya_op_linear bit for bit; kinds as laya_op_linear.  The
+ * split-K kernel is used (short sequences: laya_enc_run folds the attention
+ * and MLP norms this way when its plan for the shape is split-K).  K a
+ * multiple of 256, at most 2048.  Sources: as laya_op_layernorm and
+ * laya_op_linear. */
+int laya_op_linear_ln(const void* x_raw, const void* gamma, float eps, int M,
+                      int K, const void* w, int N, int kind,
+                      const void* residual, void* y, int splits,
+                      int tile_tokens, void* stream);
+
+/* The QKV projection as laya_enc_run runs it: kind 0 (plain) with RoPE
+ * applied in the epilogue to output columns [0, rope_cols) (the q and k heads
+ * of 64): each value is rounded to BF16 as the plain projection stores it,
+ * then rotated with exactly the arithmetic of laya_op_rope at position
+ * token % S, so y equals laya_op_linear followed by laya_op_rope bit for bit.
+ * rope_cols a multiple of 128 and at most N; cos_dev, sin_dev fp32 [>= S, 32].
+ * Sources: as laya_op_linear and laya_op_rope. */
+int laya_op_linear_rope(const void* x, int M, int K, const void* w, int N,
+                        const float* cos_dev, const float* sin_dev, int S,
+                        int rope_cols, void* y, int splits, int tile_tokens,
+                        void* stream);
+
 /* The plan laya_op_linear picks by default: tokens per tile, split-K factor
  * and the number of CTAs (feature tiles x token tiles x splits) on a device
  * with num_sms SMs.  Host-only. */

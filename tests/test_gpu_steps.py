@@ -24,7 +24,9 @@ def rnd_bits(rng, shape, std=1.0, mean=0.0):
 
 @pytest.mark.parametrize("M,N,K,splits,nt", [
     (48, 256, 128, 1, 0), (48, 384, 1024, 4, 0), (7, 128, 256, 2, 16), (300, 520, 192, 3, 0),
-    (513, 136, 64, 1, 256), (100, 1024, 2624, 8, 0)])
+    (513, 136, 64, 1, 256), (100, 1024, 2624, 8, 0),
+    # persistent kernel: several tiles per CTA, both TMEM accumulators, ragged edges
+    (2000, 1024, 128, 1, 32), (3000, 520, 256, 1, 48), (1111, 3072, 1024, 1, 0)])
 def test_linear_exact_integers(M, N, K, splits, nt):
     # small integers: every partial sum is exact in fp32, so any layout,
     # swizzle, transpose or split-K error shows up as a wrong value
@@ -43,7 +45,8 @@ def test_linear_exact_integers(M, N, K, splits, nt):
 @pytest.mark.parametrize("kind", [te.KIND_PLAIN, te.KIND_RESIDUAL, te.KIND_GEGLU])
 @pytest.mark.parametrize("M,N,K,splits,nt", [
     (48, 3072, 1024, 0, 0), (48, 1024, 2624, 0, 0), (1, 2624, 1024, 0, 0), (256, 1024, 1024, 0, 0),
-    (464, 1024, 1024, 3, 0), (600, 640, 256, 1, 128), (130, 2624, 1024, 2, 48)])
+    (464, 1024, 1024, 3, 0), (600, 640, 256, 1, 128), (130, 2624, 1024, 2, 48),
+    (1200, 3072, 1024, 1, 0), (1000, 1024, 2624, 1, 112)])
 def test_linear_matches_oracle(kind, M, N, K, splits, nt):
     torch = require_gpu()
     rng = np.random.default_rng(1000 + M + N + K + kind)
@@ -212,3 +215,57 @@ def test_attention_with_fused_rope_matches_oracle(B, S, heads, lengths, glob, th
         assert np.all(np.abs(g - r) <= lim), (b, float(np.max(np.abs(g - r) - lim)))
         assert nrms(g, r) < 3e-3
     assert np.all(np.isfinite(got))
+
+
+@pytest.mark.parametrize("B,S,splits,nt,theta", [
+    (1, 48, 0, 0, 160000.0),        # library plan (split-K clusters at 48 tokens)
+    (4, 64, 4, 64, 10000.0),        # forced split-K
+    (2, 300, 1, 112, 10000.0),      # persistent kernel, several tiles per CTA
+    (16, 512, 0, 0, 160000.0),      # library plan at 8192 tokens
+])
+def test_qkv_with_rope_epilogue_bit_exact(B, S, splits, nt, theta):
+    # RoPE applied in the QKV epilogue must equal the plain projection followed
+    # by the stand-alone RoPE kernel, byte for byte (q and k rotated, v as is)
+    torch = require_gpu()
+    rng = np.random.default_rng(B * S + splits)
+    H, M = 1024, B * S
+    xb, wb = rnd_bits(rng, (M, H)), rnd_bits(rng, (3 * H, H), std=0.02)
+    c, s = te.rope_table(theta, 512, 32)
+    cd, sd = torch.from_numpy(c).cuda(), torch.from_numpy(s).cuda()
+    x, w = to_dev(xb), to_dev(wb)
+    fused = torch.empty((M, 3 * H), dtype=torch.bfloat16, device="cuda")
+    te.linear_rope(x, w, fused, cd, sd, S, 2 * H, splits=splits, tile_tokens=nt)
+    plain = torch.empty_like(fused)
+    te.linear(x, w, plain, te.KIND_PLAIN, splits=splits, tile_tokens=nt)
+    two_step = plain.clone()
+    te.rope(two_step, cd, sd, B, S, 16)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to_bits(fused), to_bits(two_step))
+    np.testing.assert_array_equal(to_bits(fused)[:, 2 * H:], to_bits(plain)[:, 2 * H:])
+
+
+@pytest.mark.parametrize("kind", [te.KIND_PLAIN, te.KIND_GEGLU])
+@pytest.mark.parametrize("M,N,splits,nt", [(48, 3072, 4, 48), (48, 2624, 6, 48), (256, 1024, 2, 128),
+                                           (100, 640, 3, 112), (48, 1024, 1, 48)])
+def test_linear_with_layernorm_on_load_bit_exact(kind, M, N, splits, nt):
+    # the GEMM normalising its input tiles on load equals the LayerNorm kernel
+    # followed by the same GEMM plan, byte for byte
+    torch = require_gpu()
+    rng = np.random.default_rng(M + N + splits + kind)
+    K = 1024
+    Nw = 2 * N if kind == te.KIND_GEGLU else N
+    xb = rnd_bits(rng, (M, K), std=1.5, mean=0.2)
+    gb = rnd_bits(rng, (K,), std=0.02, mean=1.0)
+    wb = rnd_bits(rng, (Nw, K), std=0.02)
+    x, g, w = to_dev(xb), to_dev(gb), to_dev(wb)
+    fused = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    te.linear_ln(x, g, 1e-5, w, fused, kind, splits=splits, tile_tokens=nt)
+    h = torch.empty_like(x)
+    te.layernorm(x, g, 1e-5, h)
+    two_step = torch.empty_like(fused)
+    te.linear(h, w, two_step, kind, splits=splits, tile_tokens=nt)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to_bits(fused), to_bits(two_step))
+    ref = oracle.linear(oracle.layernorm(xb, gb, 1e-5), wb, kind)
+    ok, msg = bf16_close(to_bits(fused), ref, ulps=1.0, min_exact=0.9)
+    assert ok, msg

@@ -73,10 +73,11 @@ def test_linear_plan_invariants(lib, M, N, K, kind):
         tiles_t = -(-M // nt)
         assert tiles_t * nt >= M and (tiles_t - 1) * nt < M
         assert 1 <= splits <= min(8, K // 64)
-        assert ctas == tiles_t * -(-N // 128) * splits
-        assert tiles_t <= -(-M // 256) + 3            # at most three tiles finer than needed
-        if tiles_t * -(-N // 128) >= sms:
-            assert splits == 1
+        tiles = tiles_t * -(-N // 128)
+        if splits == 1:
+            assert ctas == min(tiles, sms)             # persistent: one CTA per SM walks the tiles
+        else:
+            assert ctas == tiles * splits              # one CTA per (tile, split), clusters of `splits`
         if M <= 512 and K >= 1024:
             assert ctas >= sms // 3                    # short sequences keep the GPU busy
 

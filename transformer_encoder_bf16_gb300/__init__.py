@@ -88,6 +88,8 @@ _SIGNATURES = {
     "laya_op_attention": ([_P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "laya_op_attention_rope": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "laya_op_linear": ([_P, _I, _I, _P, _I, _I, _P, _P, _I, _I, _P], _I),
+    "laya_op_linear_ln": ([_P, _P, _F, _I, _I, _P, _I, _I, _P, _P, _I, _I, _P], _I),
+    "laya_op_linear_rope": ([_P, _I, _I, _P, _I, _P, _P, _I, _I, _P, _I, _I, _P], _I),
     "laya_op_linear_plan": ([_I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I),
                              ctypes.POINTER(_I)], _I),
 }
@@ -276,6 +278,22 @@ def linear(x, w, y, kind=KIND_PLAIN, residual=None, splits=0, tile_tokens=0, str
     N = y.shape[1]
     _check(lib().laya_op_linear(_ptr(x), M, K, _ptr(w), N, kind, _ptr(residual), _ptr(y),
                                 splits, tile_tokens, _stream_ptr(stream)))
+
+
+def linear_ln(x_raw, gamma, eps, w, y, kind=KIND_PLAIN, residual=None, splits=0, tile_tokens=0,
+              stream=None):
+    M, K = x_raw.shape
+    N = y.shape[1]
+    _check(lib().laya_op_linear_ln(_ptr(x_raw), _ptr(gamma), eps, M, K, _ptr(w), N, kind,
+                                   _ptr(residual), _ptr(y), splits, tile_tokens,
+                                   _stream_ptr(stream)))
+
+
+def linear_rope(x, w, y, cos_dev, sin_dev, S, rope_cols, splits=0, tile_tokens=0, stream=None):
+    M, K = x.shape
+    N = y.shape[1]
+    _check(lib().laya_op_linear_rope(_ptr(x), M, K, _ptr(w), N, _ptr(cos_dev), _ptr(sin_dev), S,
+                                     rope_cols, _ptr(y), splits, tile_tokens, _stream_ptr(stream)))
 
 
 def linear_plan(M, K, N, kind, num_sms):

@@ -7,12 +7,13 @@
 //   for each of the n_enc encoder and n_dec decision layers l:
 //     if l == n_enc and final_norm:  x = LN_final(x)
 //     h   = (l == 0 and first_attn_norm_identity) ? x : LN_attn(x)
-//     qkv = h Wqkv^T                  GEMM, plain epilogue
-//     ctx = attention(RoPE(q), RoPE(k), v, lengths)   RoPE fused into the attention
-//                                     kernel; global table iff decision layer or
-//                                     l % global_every == 0; sliding window on local layers
+//           (short sequences: the QKV GEMM normalises x on load instead)
+//     qkv = RoPE(h Wqkv^T)            GEMM, plain epilogue with RoPE on q and k
+//                                     (RoPE of q and k in the same epilogue: global table
+//                                     iff decision layer or l % global_every == 0)
+//     ctx = attention(qkv, lengths)   sliding window on local layers
 //     x   = x + ctx Wo^T              GEMM, residual epilogue (in place)
-//     h   = LN_mlp(x)
+//     h   = LN_mlp(x)                  (short sequences: folded into the up GEMM)
 //     g   = gelu(h Wup_in^T) * (h Wup_gate^T)   GEMM, GeGLU epilogue
 //     x   = x + g Wdown^T             GEMM, residual epilogue (last layer: into out)
 // Sources: "Run Laya encoder and decision layers on CUDA" ("Purpose",
@@ -60,7 +61,10 @@ struct Workspace {
   GemmPlan p_qkv, p_o, p_up, p_dn;
   // activation operand of each GEMM; the TMA box height is that GEMM's own
   // token tile (plans may differ: a GeGLU split-K partial can force a smaller tile)
-  CUtensorMap tm_x_qkv, tm_h_qkv, tm_ctx_o, tm_h_up, tm_g_dn;
+  CUtensorMap tm_x_qkv, tm_h_qkv, tm_ctx_o, tm_h_up, tm_x_up, tm_g_dn;
+  // LayerNorm folded into the QKV / up GEMM (their plans are split-K): the
+  // GEMM normalises x on load and the LN kernel is not launched
+  bool ln_qkv = false, ln_up = false;
   cudaGraphExec_t exec = nullptr;
   void* graph_out = nullptr;
   uint64_t last_use = 0;
@@ -146,6 +150,11 @@ int workspace_layout(const laya_enc_handle* h, int B, int S, Workspace* w, size_
       !plan_gemm(M, I, H, kGemmGeglu, h->num_sms, 0, 0, &w->p_up) ||
       !plan_gemm(M, H, I, kGemmResidual, h->num_sms, 0, 0, &w->p_dn))
     return LAYA_E_INVAL;
+  // LayerNorm on load (laya_op_linear_ln) is not used here: measured on the
+  // GB300 it made 48- and 256-token requests slower (every split-K CTA
+  // recomputes the statistics of all its rows) than the LN kernel it replaces.
+  w->ln_qkv = false;
+  w->ln_up = false;
   size_t off = 0;
   auto take = [&](size_t n) {
     const size_t o = off;
@@ -172,10 +181,12 @@ int workspace_layout(const laya_enc_handle* h, int B, int S, Workspace* w, size_
   return LAYA_OK;
 }
 
-int kernel_count(const laya_enc_config& c) {
+int kernel_count(const laya_enc_config& c, const Workspace& w) {
   const int L = c.n_encoder_layers + c.n_decision_layers;
-  int n = 1 + 7 * L;  // norm, QKV, attention (+RoPE), out-proj, norm, up, down
-  if (c.first_attn_norm_identity) n -= 1;
+  // per layer: QKV, attention, out-proj, up, down, and the two norms unless folded
+  int n = 1 + 5 * L;
+  if (!w.ln_qkv) n += L - (c.first_attn_norm_identity ? 1 : 0);
+  if (!w.ln_up) n += L;
   if (c.final_norm && c.n_decision_layers > 0) n += 1;
   return n;
 }
@@ -252,24 +263,35 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, bf16* out, cudaStr
     if (li == c.n_encoder_layers && c.final_norm)
       LAYA_LAUNCH(LAYA_PROF_NORM,
                   launch_layernorm(w->x, h->final_norm, M, H, c.ln_eps, w->x, l));
+    GemmOperands o;
+    o.err = h->err;
     const CUtensorMap* qkv_in = &w->tm_h_qkv;
     if (li == 0 && c.first_attn_norm_identity) {
       qkv_in = &w->tm_x_qkv;
+    } else if (w->ln_qkv) {
+      qkv_in = &w->tm_x_qkv;  // normalised on load
+      o.ln_x = w->x;
+      o.ln_gamma = lw.attn_norm;
+      o.ln_eps = c.ln_eps;
     } else {
       LAYA_LAUNCH(LAYA_PROF_NORM, launch_layernorm(w->x, lw.attn_norm, M, H, c.ln_eps, w->h, l));
     }
-    GemmOperands o;
-    o.err = h->err;
     o.w = lw.wqkv;
     o.w2 = lw.wqkv;
     o.x = *qkv_in;
     o.x_box_rows = w->p_qkv.nt;
     o.y = w->qkv;
+    // RoPE in the QKV epilogue: q and k columns [0, 2H) leave the GEMM rotated
+    o.rope_cos = glob ? cos_g : cos_l;
+    o.rope_sin = glob ? sin_g : sin_l;
+    o.rope_S = w->S;
+    o.rope_cols = 2 * H;
     LAYA_LAUNCH(LAYA_PROF_QKV, launch_gemm(w->p_qkv, o, l));
+    o.rope_cos = o.rope_sin = nullptr;
+    o.ln_x = o.ln_gamma = nullptr;
     LAYA_LAUNCH(LAYA_PROF_ATTN, launch_attention(w->qkv, w->lens, w->B, w->S, c.heads,
                                                  glob ? 1 : 0, c.local_half_window, w->ctx,
-                                                 h->err, l, glob ? cos_g : cos_l,
-                                                 glob ? sin_g : sin_l));
+                                                 h->err, l));
     o.w = lw.wo;
     o.w2 = lw.wo;
     o.x = w->tm_ctx_o;
@@ -277,14 +299,22 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, bf16* out, cudaStr
     o.y = w->x;
     o.residual = w->x;
     LAYA_LAUNCH(LAYA_PROF_OUT, launch_gemm(w->p_o, o, l));
-    LAYA_LAUNCH(LAYA_PROF_NORM, launch_layernorm(w->x, lw.mlp_norm, M, H, c.ln_eps, w->h, l));
     o.w = lw.wup_in;
     o.w2 = lw.wup_gate;
-    o.x = w->tm_h_up;
     o.x_box_rows = w->p_up.nt;
     o.y = w->g;
     o.residual = nullptr;
+    if (w->ln_up) {
+      o.x = w->tm_x_up;  // normalised on load
+      o.ln_x = w->x;
+      o.ln_gamma = lw.mlp_norm;
+      o.ln_eps = c.ln_eps;
+    } else {
+      LAYA_LAUNCH(LAYA_PROF_NORM, launch_layernorm(w->x, lw.mlp_norm, M, H, c.ln_eps, w->h, l));
+      o.x = w->tm_h_up;
+    }
     LAYA_LAUNCH(LAYA_PROF_UP, launch_gemm(w->p_up, o, l));
+    o.ln_x = o.ln_gamma = nullptr;
     o.w = lw.wdown;
     o.w2 = lw.wdown;
     o.x = w->tm_g_dn;
@@ -349,6 +379,7 @@ int get_workspace(laya_enc_handle* h, int B, int S, Workspace** out) {
             make_tmap_bf16_2d(&w->tm_h_qkv, w->h, M, c.hidden, ldh, box(w->p_qkv)) &&
             make_tmap_bf16_2d(&w->tm_ctx_o, w->ctx, M, c.hidden, ldh, box(w->p_o)) &&
             make_tmap_bf16_2d(&w->tm_h_up, w->h, M, c.hidden, ldh, box(w->p_up)) &&
+            make_tmap_bf16_2d(&w->tm_x_up, w->x, M, c.hidden, ldh, box(w->p_up)) &&
             make_tmap_bf16_2d(&w->tm_g_dn, w->g, M, c.intermediate, ldi, box(w->p_dn));
   if (!ok) {
     free_workspace(w);
@@ -647,10 +678,12 @@ int laya_enc_profile_read(laya_enc_handle* h, double* ms, int* launches, int n) 
 }
 
 int laya_enc_launch_count(const laya_enc_handle* h, int batch, int seq) {
-  (void)batch;
-  (void)seq;
-  if (!h) return LAYA_E_INVAL;
-  return laya::kernel_count(h->cfg);
+  if (!h || batch < 1 || batch > h->cfg.max_batch || seq < 1 || seq > h->cfg.max_seq)
+    return LAYA_E_INVAL;
+  laya::Workspace w;
+  size_t b = 0;
+  if (laya::workspace_layout(h, batch, seq, &w, &b) != LAYA_OK) return LAYA_E_INVAL;
+  return laya::kernel_count(h->cfg, w);
 }
 
 int laya_enc_workspace_bytes(const laya_enc_handle* h, int batch, int seq, size_t* bytes) {

@@ -41,6 +41,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "rowstats.cuh"
 
 namespace laya {
 
@@ -53,19 +54,92 @@ constexpr uint32_t kATileBytes = kBM * kBK * 2;
 constexpr int kMaxSplits = 8;            // portable cluster size
 constexpr size_t kSmemLimit = 227 * 1024;
 constexpr size_t kCtrlBytes = 256;
+constexpr size_t kLnStatsBytes = 256 * 8;  // [nt <= 256][mean, rstd] for LayerNorm on load
 constexpr int kEpiBatch = 4;             // epilogue units whose loads are issued together
+constexpr int kChunk = 32;               // persistent epilogue: token columns per drain step
+constexpr size_t kStagingBytes = 2ull * kChunk * kBM * 4;  // double-buffered fp32 staging
 
 struct GemmArgs {
   int M, N, k_blocks, nt, splits, stages;
+  int feat_tiles, token_tiles;  // persistent kernel: tile = f + feat_tiles * t
   uint32_t tmem_cols;
   uint32_t ctrl_offset;  // bytes from the aligned smem base to barriers
   bf16* y;
   const bf16* residual;
   int* err;
+  // RoPE in the epilogue (plain kind): output features below rope_cols are
+  // q|k heads of 64, rotated with the [pos, 32] tables at pos = token % rope_S
+  const float* rope_cos;
+  const float* rope_sin;
+  int rope_S, rope_cols;
+  // LayerNorm on load (split kernel): the activation tiles TMA brings in are
+  // rows of ln_x, normalised in shared memory before the MMA reads them
+  const bf16* ln_x;
+  const bf16* ln_gamma;
+  float ln_eps;
 };
 
 __device__ __forceinline__ float gelu_erf(float z) {
   return (0.5f * z) * (1.0f + erff(z * 0.70710678118654752f));
+}
+
+__device__ __forceinline__ void load8_smem(const float* p, float (&v)[8]) {
+  const float4 lo = reinterpret_cast<const float4*>(p)[0];
+  const float4 hi = reinterpret_cast<const float4*>(p)[1];
+  v[0] = lo.x; v[1] = lo.y; v[2] = lo.z; v[3] = lo.w;
+  v[4] = hi.x; v[5] = hi.y; v[6] = hi.z; v[7] = hi.w;
+}
+
+// Round to BF16 (the value the projection stores), then rotate the pair
+// (x1, x2) = (feature i, feature i + 32) of a head exactly as the RoPE kernel
+// does: fp32 products and sum each rounded, one BF16 rounding of the result.
+// f1 is the output column of the first member of eight consecutive pairs.
+__device__ __forceinline__ void rope_store16(const GemmArgs& a, int t, int f1, const float (&v1)[8],
+                                             const float (&v2)[8]) {
+  const int pos = t % a.rope_S;
+  const int i0 = f1 & 31;  // pair index within the head of the first element
+  // eight consecutive table entries: 32-byte aligned (i0 is a multiple of 8)
+  const float4* ct = reinterpret_cast<const float4*>(a.rope_cos + static_cast<size_t>(pos) * 32 + i0);
+  const float4* st = reinterpret_cast<const float4*>(a.rope_sin + static_cast<size_t>(pos) * 32 + i0);
+  const float4 c0 = __ldg(ct), c1 = __ldg(ct + 1), s0 = __ldg(st), s1 = __ldg(st + 1);
+  const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+  uint4 o1, o2;
+  __nv_bfloat16* p1 = reinterpret_cast<__nv_bfloat16*>(&o1);
+  __nv_bfloat16* p2 = reinterpret_cast<__nv_bfloat16*>(&o2);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float x1 = __bfloat162float(__float2bfloat16_rn(v1[i]));
+    const float x2 = __bfloat162float(__float2bfloat16_rn(v2[i]));
+    const float c = cv[i], sn = sv[i];
+    p1[i] = __float2bfloat16_rn(__fsub_rn(__fmul_rn(x1, c), __fmul_rn(x2, sn)));
+    p2[i] = __float2bfloat16_rn(__fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, sn)));
+  }
+  bf16* row = a.y + static_cast<size_t>(t) * a.N;
+  *reinterpret_cast<uint4*>(row + f1) = o1;
+  *reinterpret_cast<uint4*>(row + f1 + 32) = o2;
+}
+
+// mean and rstd of row t of ln_x (K = 256 * V values), one warp.
+template <int V>
+__device__ __forceinline__ void ln_row(const GemmArgs& a, int t, int lane, float& mean, float& rstd) {
+  float v[V][8];
+  row_stats<V>(reinterpret_cast<const uint4*>(a.ln_x + static_cast<size_t>(t) * (256 * V)), lane,
+               a.ln_eps, v, mean, rstd);
+}
+
+__device__ __forceinline__ void ln_row_any(const GemmArgs& a, int t, int lane, float& mean,
+                                           float& rstd) {
+  switch (a.k_blocks / 4) {
+    case 1: ln_row<1>(a, t, lane, mean, rstd); break;
+    case 2: ln_row<2>(a, t, lane, mean, rstd); break;
+    case 3: ln_row<3>(a, t, lane, mean, rstd); break;
+    case 4: ln_row<4>(a, t, lane, mean, rstd); break;
+    case 5: ln_row<5>(a, t, lane, mean, rstd); break;
+    case 6: ln_row<6>(a, t, lane, mean, rstd); break;
+    case 7: ln_row<7>(a, t, lane, mean, rstd); break;
+    default: ln_row<8>(a, t, lane, mean, rstd); break;
+  }
 }
 
 template <int KIND>
@@ -84,8 +158,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t full0 = ptx::smem_u32(bars);
   const uint32_t empty0 = full0 + 8u * a.stages;
   const uint32_t accum_bar = empty0 + 8u * a.stages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * a.stages + 1);
+  const uint32_t xform0 = accum_bar + 8u;  // LayerNorm on load: stage normalised
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * a.stages + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const bool ln = a.ln_x != nullptr;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -98,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < a.stages; ++i) {
       ptx::mbar_init(full0 + 8u * i, 1);
       ptx::mbar_init(empty0 + 8u * i, 1);
+      ptx::mbar_init(xform0 + 8u * i, kThreads - 64);
     }
     ptx::mbar_init(accum_bar, 1);
     *abort_flag = 0;
@@ -168,7 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < nkb; ++i) {
         const int s = i % a.stages;
         const uint32_t ph = static_cast<uint32_t>(i / a.stages) & 1u;
-        if (!ptx::mbar_wait(full0 + 8u * s, ph, abort_flag, a.err, kDevWaitFull, kWaitLimitNs))
+        if (!ptx::mbar_wait((ln ? xform0 : full0) + 8u * s, ph, abort_flag, a.err, kDevWaitFull,
+                            kWaitLimitNs))
           break;
         ptx::tc_fence_after();
         const uint32_t st = sbase + s * stage_bytes;
@@ -195,6 +273,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    if (ln) {
+      // ---- LayerNorm on load: row statistics, then normalise each stage
+      const int tid_e = threadIdx.x - 64;
+      float* stats = reinterpret_cast<float*>(smem + a.ctrl_offset + kCtrlBytes);
+      ptx::grid_dependency_wait();  // ln_x written by the previous kernel
+      for (int r = warp - 2; r < a.nt; r += 4) {
+        const int t = t_tile * a.nt + r;
+        float mean = 0.f, rstd = 0.f;
+        if (t < a.M) ln_row_any(a, t, lane, mean, rstd);
+        if (lane == 0) {
+          stats[2 * r] = mean;
+          stats[2 * r + 1] = rstd;
+        }
+      }
+      ptx::named_barrier_sync(1, kThreads - 64);
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % a.stages;
+        const uint32_t ph = static_cast<uint32_t>(i / a.stages) & 1u;
+        if (!ptx::mbar_wait(full0 + 8u * s, ph, abort_flag, a.err, kDevWaitFull, kWaitLimitNs))
+          break;
+        // B tile: nt rows of 128 bytes; 16-byte chunk j of row r sits at j ^ (r % 8)
+        uint8_t* bt = smem + static_cast<size_t>(s) * stage_bytes + NA * kATileBytes;
+        const int kc = (kb0 + i) * kBK;
+        for (int u = tid_e; u < a.nt * 8; u += kThreads - 64) {
+          const int r = u >> 3, pc = u & 7, j = pc ^ (r & 7);
+          uint4* p = reinterpret_cast<uint4*>(bt + r * 128 + pc * 16);
+          float xv[8], g[8];
+          bf16x8_to_f32(*p, xv);
+          bf16x8_to_f32(*reinterpret_cast<const uint4*>(a.ln_gamma + kc + 8 * j), g);
+          const float mean = stats[2 * r], rstd = stats[2 * r + 1];
+          uint4 o;
+          __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            o2[e] = __floats2bfloat162_rn(ln_apply(xv[2 * e], mean, rstd, g[2 * e]),
+                                          ln_apply(xv[2 * e + 1], mean, rstd, g[2 * e + 1]));
+          *p = o;
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(xform0 + 8u * s);
+      }
+    }
     epi_ok = ptx::mbar_wait(accum_bar, 0, abort_flag, a.err, kDevWaitAccum, kWaitLimitNs);
     ptx::tc_fence_after();
     if (epi_ok) {
@@ -231,12 +351,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // consecutive units of a token row, so loads and stores are coalesced.
     // Split-K: this CTA finishes the feature groups [g0, g1) of the tile,
     // summing the partials of every CTA of the cluster in rank order.
-    int g0 = 0, g1 = kBM / 8;
+    const bool rope_tile = KIND == kGemmPlain && a.rope_cos != nullptr && f_tile * kBM < a.rope_cols;
+    const int ngroups = rope_tile ? kBM / 16 : kBM / 8;  // RoPE: pairs of groups (f, f + 32)
+    int g0 = 0, g1 = ngroups;
     uint32_t remote[kMaxSplits];
     if (a.splits > 1) {
       const uint32_t rank = ptx::cluster_ctarank();
-      g0 = static_cast<int>(rank * (kBM / 8) / a.splits);
-      g1 = static_cast<int>((rank + 1) * (kBM / 8) / a.splits);
+      g0 = static_cast<int>(rank * ngroups / a.splits);
+      g1 = static_cast<int>((rank + 1) * ngroups / a.splits);
 #pragma unroll
       for (int s = 0; s < kMaxSplits; ++s) remote[s] = s < a.splits ? ptx::mapa(sbase, s) : 0u;
     }
@@ -246,6 +368,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid_e = threadIdx.x - 64;
     const float* stg = reinterpret_cast<const float*>(smem);
     ptx::grid_dependency_wait();  // residual written by earlier kernels
+    if (rope_tile) {
+      // unit = token column c, pair group p: features (fo, fo + 32), fo = 64 (p / 4) + 8 (p % 4)
+      for (int u = tid_e; u < units; u += kThreads - 64) {
+        const int c = u / ng;
+        const int pg = g0 + u % ng;
+        const int fo = 64 * (pg >> 2) + 8 * (pg & 3);
+        const int t = t_base + c;
+        float v1[8], v2[8];
+        const uint32_t off1 = static_cast<uint32_t>(c * kBM + fo) * 4u;
+        const uint32_t off2 = off1 + 32u * 4u;
+        if (a.splits > 1) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v1[i] = v2[i] = 0.f;
+#pragma unroll
+          for (int s = 0; s < kMaxSplits; ++s) {
+            if (s < a.splits) {
+              float t8[8];
+              ptx::ld_dsmem_f32x8(remote[s] + off1, t8);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) v1[i] += t8[i];
+              ptx::ld_dsmem_f32x8(remote[s] + off2, t8);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) v2[i] += t8[i];
+            }
+          }
+        } else {
+          load8_smem(stg + off1 / 4u, v1);
+          load8_smem(stg + off2 / 4u, v2);
+        }
+        if (t < a.M) rope_store16(a, t, f_tile * kBM + fo, v1, v2);
+      }
+    } else
     for (int u0 = tid_e; u0 < units; u0 += (kThreads - 64) * kEpiBatch) {
       float v[kEpiBatch][8], gt[kEpiBatch][8];
       uint4 res[kEpiBatch];
@@ -358,6 +512,269 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
+// Persistent variant for splits == 1: one CTA per SM walks the output tiles
+// (tile = feature tile + feat_tiles * token tile, strided by gridDim.x).  Two
+// TMEM accumulators alternate, so the epilogue of one tile (drained 32 token
+// columns at a time through a double-buffered fp32 staging area) overlaps the
+// main loop of the next; the TMA ring runs continuously across tiles.
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_persistent_kernel(const __grid_constant__ CUtensorMap tm_w,
+                           const __grid_constant__ CUtensorMap tm_w2,
+                           const __grid_constant__ CUtensorMap tm_x, const GemmArgs a) {
+  constexpr int NA = (KIND == kGemmGeglu) ? 2 : 1;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_u32(smem);
+  const uint32_t b_bytes = static_cast<uint32_t>(a.nt) * kBK * 2;
+  const uint32_t stage_bytes = NA * kATileBytes + b_bytes;
+  float* staging = reinterpret_cast<float*>(smem + static_cast<size_t>(a.stages) * stage_bytes);
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + a.ctrl_offset);
+  const uint32_t full0 = ptx::smem_u32(bars);
+  const uint32_t empty0 = full0 + 8u * a.stages;
+  const uint32_t accf0 = empty0 + 8u * a.stages;  // accumulator b ready: accf0 + 8b
+  const uint32_t acce0 = accf0 + 16u;             // accumulator b drained: acce0 + 8b
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * a.stages + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int tiles = a.feat_tiles * a.token_tiles;
+  const int KB = a.k_blocks;
+  const uint32_t acc_cols = static_cast<uint32_t>(NA * a.nt);  // one accumulator's columns
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < a.stages; ++i) {
+      ptx::mbar_init(full0 + 8u * i, 1);
+      ptx::mbar_init(empty0 + 8u * i, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(accf0 + 8u * b, 1);
+      ptx::mbar_init(acce0 + 8u * b, kThreads - 64);
+    }
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tm_w);
+    if (NA == 2) ptx::prefetch_tmap(&tm_w2);
+    ptx::prefetch_tmap(&tm_x);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), a.tmem_cols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  ptx::grid_launch_dependents();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      const uint64_t pol_w = ptx::policy_evict_first();
+      const uint64_t pol_x = ptx::policy_evict_last();
+      int issued = 0;
+      const int first = blockIdx.x;
+      if (first < tiles) {
+        // weights of the first stages of the first tile before the dependency wait
+        const int pre = KB < a.stages ? KB : a.stages;
+        const int f0 = first % a.feat_tiles;
+        for (int i = 0; i < pre; ++i) {
+          const uint32_t st = sbase + i * stage_bytes;
+          ptx::mbar_arrive_expect_tx(full0 + 8u * i, stage_bytes);
+          ptx::tma_load_2d(st, &tm_w, full0 + 8u * i, i * kBK, f0 * kBM, pol_w);
+          if (NA == 2) ptx::tma_load_2d(st + kATileBytes, &tm_w2, full0 + 8u * i, i * kBK, f0 * kBM, pol_w);
+        }
+        ptx::grid_dependency_wait();
+        const int t0 = first / a.feat_tiles;
+        for (int i = 0; i < pre; ++i)
+          ptx::tma_load_2d(sbase + i * stage_bytes + NA * kATileBytes, &tm_x, full0 + 8u * i,
+                           i * kBK, t0 * a.nt, pol_x);
+        issued = pre;
+        int it = 0;
+        bool stop = false;
+        for (int tile = first; tile < tiles && !stop; tile += gridDim.x) {
+          const int ft = tile % a.feat_tiles, tt = tile / a.feat_tiles;
+          for (int kb = 0; kb < KB; ++kb, ++it) {
+            if (it < pre) continue;  // issued above
+            const int s = it % a.stages;
+            const uint32_t ph = static_cast<uint32_t>(it / a.stages) & 1u;
+            if (!ptx::mbar_wait(empty0 + 8u * s, ph ^ 1u, abort_flag, a.err, kDevWaitEmpty,
+                                kWaitLimitNs)) {
+              stop = true;
+              break;
+            }
+            const uint32_t st = sbase + s * stage_bytes;
+            const uint32_t fb = full0 + 8u * s;
+            ptx::mbar_arrive_expect_tx(fb, stage_bytes);
+            ptx::tma_load_2d(st, &tm_w, fb, kb * kBK, ft * kBM, pol_w);
+            if (NA == 2) ptx::tma_load_2d(st + kATileBytes, &tm_w2, fb, kb * kBK, ft * kBM, pol_w);
+            ptx::tma_load_2d(st + NA * kATileBytes, &tm_x, fb, kb * kBK, tt * a.nt, pol_x);
+            issued = it + 1;
+          }
+        }
+      }
+      for (int i = (issued > a.stages ? issued - a.stages : 0); i < issued; ++i)
+        ptx::mbar_wait(full0 + 8u * (i % a.stages), static_cast<uint32_t>(i / a.stages) & 1u,
+                       abort_flag, a.err, kDevWaitFull, kWaitLimitNs);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      const uint32_t idesc = ptx::idesc_bf16(kBM, a.nt);
+      int it = 0, lt = 0;
+      bool stop = false;
+      for (int tile = blockIdx.x; tile < tiles && !stop; tile += gridDim.x, ++lt) {
+        const int b = lt & 1;
+        const int use = lt >> 1;
+        if (lt >= 2 && !ptx::mbar_wait(acce0 + 8u * b, static_cast<uint32_t>(use - 1) & 1u,
+                                       abort_flag, a.err, kDevWaitAccum, kWaitLimitNs))
+          break;
+        ptx::tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(b) * acc_cols;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % a.stages;
+          const uint32_t ph = static_cast<uint32_t>(it / a.stages) & 1u;
+          if (!ptx::mbar_wait(full0 + 8u * s, ph, abort_flag, a.err, kDevWaitFull, kWaitLimitNs)) {
+            stop = true;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t st = sbase + s * stage_bytes;
+          const uint32_t sb = st + NA * kATileBytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t bdesc = ptx::sdesc_sw128(sb + kk * 32);
+            const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+            ptx::mma_bf16(d, ptx::sdesc_sw128(st + kk * 32), bdesc, idesc, acc);
+            if (NA == 2)
+              ptx::mma_bf16(d + static_cast<uint32_t>(a.nt),
+                            ptx::sdesc_sw128(st + kATileBytes + kk * 32), bdesc, idesc, acc);
+          }
+          ptx::mma_commit(empty0 + 8u * s);
+        }
+        ptx::mma_commit(accf0 + 8u * b);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const int tid_e = threadIdx.x - 64;
+    ptx::grid_dependency_wait();  // residual written by earlier kernels
+    int lt = 0, cc = 0;
+    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++lt) {
+      const int b = lt & 1;
+      const int use = lt >> 1;
+      ptx::mbar_wait(accf0 + 8u * b, static_cast<uint32_t>(use) & 1u, abort_flag, a.err,
+                     kDevWaitAccum, kWaitLimitNs);
+      // all epilogue threads leave together: whoever gave up raised the flag
+      // before this barrier, so everyone reads the same value after it
+      ptx::named_barrier_sync(1, kThreads - 64);
+      if (*abort_flag) break;
+      ptx::tc_fence_after();
+      const int ft = tile % a.feat_tiles, tt = tile / a.feat_tiles;
+      const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b) * acc_cols;
+      for (int c0 = 0; c0 < a.nt; c0 += kChunk, ++cc) {
+        float* buf = staging + (cc & 1) * (kChunk * kBM);
+        const int ncols = a.nt - c0 < kChunk ? a.nt - c0 : kChunk;
+        for (int j0 = 0; j0 < ncols; j0 += 16) {
+          float v[16];
+          ptx::tmem_ld16(tq + c0 + j0, v);
+          if (NA == 2) {
+            float g[16];
+            ptx::tmem_ld16(tq + a.nt + c0 + j0, g);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = gelu_erf(v[j]) * g[j];
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) buf[(j0 + j) * kBM + row] = v[j];
+        }
+        if (c0 + kChunk >= a.nt) {
+          // every TMEM read of this tile is complete: hand the accumulator back
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(acce0 + 8u * b);
+        }
+        ptx::named_barrier_sync(1, kThreads - 64);
+        // 16-byte vector stores: 8 features of one token per unit
+        const bool rope_tile =
+            KIND == kGemmPlain && a.rope_cos != nullptr && ft * kBM < a.rope_cols;
+        if (rope_tile) {
+          for (int u = tid_e; u < ncols * (kBM / 16); u += kThreads - 64) {
+            const int c = u / (kBM / 16), pg = u % (kBM / 16);
+            const int fo = 64 * (pg >> 2) + 8 * (pg & 3);
+            const int t = tt * a.nt + c0 + c;
+            float v1[8], v2[8];
+            load8_smem(buf + c * kBM + fo, v1);
+            load8_smem(buf + c * kBM + fo + 32, v2);
+            if (t < a.M) rope_store16(a, t, ft * kBM + fo, v1, v2);
+          }
+          continue;
+        }
+        const int units = ncols * (kBM / 8);
+        for (int u0 = tid_e; u0 < units; u0 += (kThreads - 64) * kEpiBatch) {
+          float v[kEpiBatch][8];
+          uint4 res[kEpiBatch];
+          int tok[kEpiBatch], fea[kEpiBatch];
+#pragma unroll
+          for (int bb = 0; bb < kEpiBatch; ++bb) {
+            const int u = u0 + (kThreads - 64) * bb;
+            tok[bb] = -1;
+            if (u < units) {
+              const int c = u / (kBM / 8), grp = u % (kBM / 8);
+              const float4* p4 = reinterpret_cast<const float4*>(buf + c * kBM + grp * 8);
+              const float4 lo = p4[0], hi = p4[1];
+              v[bb][0] = lo.x; v[bb][1] = lo.y; v[bb][2] = lo.z; v[bb][3] = lo.w;
+              v[bb][4] = hi.x; v[bb][5] = hi.y; v[bb][6] = hi.z; v[bb][7] = hi.w;
+              const int t = tt * a.nt + c0 + c;
+              const int f = ft * kBM + grp * 8;
+              if (t < a.M && f < a.N) {
+                tok[bb] = t;
+                fea[bb] = f;
+                if (KIND == kGemmResidual)
+                  res[bb] = *reinterpret_cast<const uint4*>(a.residual + static_cast<size_t>(t) * a.N + f);
+              }
+            }
+          }
+#pragma unroll
+          for (int bb = 0; bb < kEpiBatch; ++bb) {
+            if (tok[bb] < 0) continue;
+            float o[8];
+            if (KIND == kGemmResidual) {
+              const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&res[bb]);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float2 rf = __bfloat1622float2(r2[i]);
+                o[2 * i] = rf.x + v[bb][2 * i];
+                o[2 * i + 1] = rf.y + v[bb][2 * i + 1];
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) o[i] = v[bb][i];
+            }
+            uint4 packed;
+            __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&packed);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) p2[i] = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+            *reinterpret_cast<uint4*>(a.y + static_cast<size_t>(tok[bb]) * a.N + fea[bb]) = packed;
+          }
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, a.tmem_cols);
+  }
+}
+
 cudaError_t configure_kernels();
 
 uint32_t pow2_cols(uint32_t n) {
@@ -377,29 +794,46 @@ cudaError_t launch_kind(const GemmPlan& p, const GemmOperands& o, Launch l) {
   a.nt = p.nt;
   a.splits = p.splits;
   a.stages = p.stages;
+  a.feat_tiles = p.feat_tiles;
+  a.token_tiles = p.token_tiles;
   a.tmem_cols = p.tmem_cols;
   const int na = KIND == kGemmGeglu ? 2 : 1;
   const size_t stage_bytes = static_cast<size_t>(na) * kATileBytes + static_cast<size_t>(p.nt) * 128;
   size_t data = stage_bytes * p.stages;
-  const size_t part = static_cast<size_t>(p.splits > 1 ? na : 1) * p.nt * kBM * 4;
-  if (part > data) data = part;
+  if (p.persistent) {
+    data += kStagingBytes;
+  } else {
+    const size_t part = static_cast<size_t>(p.splits > 1 ? na : 1) * p.nt * kBM * 4;
+    if (part > data) data = part;
+  }
   a.ctrl_offset = static_cast<uint32_t>(data);
   a.y = o.y;
   a.residual = o.residual;
   a.err = o.err;
+  a.rope_cos = o.rope_cos;
+  a.rope_sin = o.rope_sin;
+  a.rope_S = o.rope_S;
+  a.rope_cols = o.rope_cols;
+  a.ln_x = o.ln_x;
+  a.ln_gamma = o.ln_gamma;
+  a.ln_eps = o.ln_eps;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.feat_tiles, p.token_tiles, p.splits);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = p.smem_bytes;
   cfg.stream = l.stream;
   cudaLaunchAttribute attr[2];
   int n = 0;
-  attr[n].id = cudaLaunchAttributeClusterDimension;
-  attr[n].val.clusterDim.x = 1;
-  attr[n].val.clusterDim.y = 1;
-  attr[n].val.clusterDim.z = p.splits;
-  ++n;
+  if (p.persistent) {
+    cfg.gridDim = dim3(p.grid_ctas, 1, 1);
+  } else {
+    cfg.gridDim = dim3(p.feat_tiles, p.token_tiles, p.splits);
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 1;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = p.splits;
+    ++n;
+  }
   if (l.pdl) {
     attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[n].val.programmaticStreamSerializationAllowed = 1;
@@ -407,6 +841,8 @@ cudaError_t launch_kind(const GemmPlan& p, const GemmOperands& o, Launch l) {
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
+  if (p.persistent)
+    return cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<KIND>, o.w, o.w2, o.x, a);
   return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<KIND>, o.w, o.w2, o.x, a);
 }
 
@@ -428,9 +864,16 @@ cudaError_t configure_kernels() {
   static std::once_flag once;
   std::call_once(once, [] {
     status = cudaSuccess;
-    for (int k = kGemmPlain; k <= kGemmGeglu && status == cudaSuccess; ++k)
+    const void* persistent[3] = {reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmPlain>),
+                                 reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmResidual>),
+                                 reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmGeglu>)};
+    for (int k = kGemmPlain; k <= kGemmGeglu && status == cudaSuccess; ++k) {
       status = cudaFuncSetAttribute(kernel_ptr(k), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(kSmemLimit));
+      if (status == cudaSuccess)
+        status = cudaFuncSetAttribute(persistent[k], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(kSmemLimit));
+    }
   });
   return status;
 }
@@ -477,8 +920,21 @@ namespace {
 bool finish_plan(GemmPlan* r) {
   const int na = r->kind == kGemmGeglu ? 2 : 1;
   const size_t stage_bytes = static_cast<size_t>(na) * kATileBytes + static_cast<size_t>(r->nt) * 128;
+  const size_t budget = kSmemLimit - kCtrlBytes - kLnStatsBytes - 1024;
+  if (r->persistent) {
+    // ring of stages + double-buffered staging; two accumulators in TMEM
+    const size_t avail = budget - kStagingBytes;
+    int stages = static_cast<int>(avail / stage_bytes);
+    if (stages > 8) stages = 8;
+    if (stages > r->k_blocks) stages = r->k_blocks;
+    if (stages < 2 && r->k_blocks >= 2) return false;
+    if (stages < 1) return false;
+    r->stages = stages;
+    r->smem_bytes = stage_bytes * stages + kStagingBytes + kCtrlBytes + 1024;
+    r->tmem_cols = pow2_cols(static_cast<uint32_t>(2 * na * r->nt));
+    return r->tmem_cols <= 512 && r->smem_bytes <= kSmemLimit;
+  }
   const int max_kb = (r->k_blocks + r->splits - 1) / r->splits;  // K blocks of the largest split
-  const size_t budget = kSmemLimit - kCtrlBytes - 1024;
   int stages = static_cast<int>(budget / stage_bytes);
   if (stages > 8) stages = 8;
   if (stages > max_kb) stages = max_kb;
@@ -489,7 +945,7 @@ bool finish_plan(GemmPlan* r) {
   const size_t part = static_cast<size_t>(r->splits > 1 ? na : 1) * r->nt * kBM * 4;
   if (part > budget) return false;
   if (part > data) data = part;
-  r->smem_bytes = data + kCtrlBytes + 1024;
+  r->smem_bytes = data + kCtrlBytes + kLnStatsBytes + 1024;
   r->tmem_cols = pow2_cols(static_cast<uint32_t>(na * r->nt));
   if (r->tmem_cols > 512) return false;
   // Never let more CTAs share an SM than its 512 TMEM columns can hold: a CTA
@@ -506,54 +962,58 @@ bool finish_plan(GemmPlan* r) {
 }  // namespace
 
 bool plan_gemm(int M, int N, int K, int kind, int num_sms, int force_splits, int force_nt,
-               GemmPlan* p) {
+               GemmPlan* p, bool allow_persistent) {
   if (M <= 0 || N <= 0 || K <= 0 || K % kBK != 0 || N % 8 != 0) return false;
   if (kind < kGemmPlain || kind > kGemmGeglu) return false;
   if (force_nt > 0 && (force_nt % 16 != 0 || force_nt > 256)) return false;
   if (force_splits > 0 && (force_splits > kMaxSplits || force_splits > K / kBK)) return false;
   if (num_sms <= 0) num_sms = 148;
   const int na = kind == kGemmGeglu ? 2 : 1;
-  // Candidates: token tilings (the fewest tiles of at most 256 tokens, evened
-  // out, and up to three finer ones) x split-K factors.  Cost model: waves x
-  // per-CTA time, a wave being as many clusters as the device can hold at
-  // once and the per-CTA time the bytes one CTA streams (in 16 KB weight-tile
-  // units) plus a fixed overhead of two units for set-up, epilogue and the
-  // cluster reduction.
+  // Candidates: every token tile nt (a multiple of 16 up to 256) x split-K
+  // factor.  Split 1 runs the persistent kernel (one CTA per SM walking the
+  // tiles, epilogue overlapped with the next tile's main loop); splits > 1
+  // run one CTA per (tile, split) in clusters.  Cost in units of one 16 KB
+  // weight tile streamed by one CTA:
+  //   persistent: ceil(tiles / CTAs) x (K blocks x unit + 0.3) + 2
+  //   split:      waves x (K blocks per split x unit + 2),
+  // a wave being as many clusters as the device can hold at once.
   GemmPlan best;
   double best_cost = 0.0;
   bool found = false;
-  const int tt_min = (M + 255) / 256;
-  for (int tt = tt_min; tt <= tt_min + 3; ++tt) {
+  const int nt_max = ((M + 15) / 16) * 16 < 256 ? ((M + 15) / 16) * 16 : 256;
+  for (int nt = 16; nt <= nt_max; nt += 16) {
+    if (force_nt > 0 && nt != force_nt) continue;
     GemmPlan r;
     r.M = M;
     r.N = N;
     r.K = K;
     r.kind = kind;
     r.k_blocks = K / kBK;
-    if (force_nt > 0) {
-      if (tt > tt_min) break;
-      r.nt = force_nt;
-    } else {
-      const int per = (M + tt - 1) / tt;
-      r.nt = (per + 15) / 16 * 16;
-      if (tt > tt_min && r.nt < 32) break;
-    }
-    r.token_tiles = (M + r.nt - 1) / r.nt;
+    r.nt = nt;
+    r.token_tiles = (M + nt - 1) / nt;
     r.feat_tiles = (N + kBM - 1) / kBM;
     const int tiles = r.token_tiles * r.feat_tiles;
+    const double unit = (na * kATileBytes + static_cast<double>(nt) * 128.0) / kATileBytes;
     const int s_lo = force_splits > 0 ? force_splits : 1;
     const int s_hi = force_splits > 0 ? force_splits : (tiles >= num_sms ? 1 : kMaxSplits);
     for (int S = s_lo; S <= s_hi && S <= r.k_blocks; ++S) {
       GemmPlan c = r;
       c.splits = S;
+      c.persistent = (S == 1) && allow_persistent;
       if (!finish_plan(&c)) continue;
-      int mac = max_active_clusters(kind, c.smem_bytes, S);
-      if (mac <= 0) mac = num_sms / S;  // no device to ask: one CTA per SM
-      if (mac <= 0) continue;
-      const int waves = (tiles + mac - 1) / mac;
-      const int kb_per = (c.k_blocks + S - 1) / S;
-      const double unit = (na * kATileBytes + static_cast<double>(c.nt) * 128.0) / kATileBytes;
-      const double cost = waves * (kb_per * unit + 2.0);
+      double cost;
+      if (c.persistent) {
+        c.grid_ctas = tiles < num_sms ? tiles : num_sms;
+        const int per_cta = (tiles + c.grid_ctas - 1) / c.grid_ctas;
+        cost = per_cta * (c.k_blocks * unit + 0.3) + 2.0;
+      } else {
+        int mac = max_active_clusters(kind, c.smem_bytes, S);
+        if (mac <= 0) mac = num_sms / S;  // no device to ask: one CTA per SM
+        if (mac <= 0) continue;
+        const int waves = (tiles + mac - 1) / mac;
+        const int kb_per = (c.k_blocks + S - 1) / S;
+        cost = waves * (kb_per * unit + 2.0);
+      }
       if (!found || cost < best_cost - 1e-9) {
         best = c;
         best_cost = cost;
@@ -586,6 +1046,14 @@ bool make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t
 cudaError_t launch_gemm(const GemmPlan& p, const GemmOperands& o, Launch l) {
   // the TMA box must match the shared-memory stage the plan reserves for it
   if (o.x_box_rows != p.nt) return cudaErrorInvalidValue;
+  // LayerNorm on load: split kernel only, K a multiple of 256 up to 2048
+  if (o.ln_x != nullptr &&
+      (p.persistent || o.ln_gamma == nullptr || p.K % 256 != 0 || p.K > 2048))
+    return cudaErrorInvalidValue;
+  // RoPE in the epilogue: plain kind, whole 64-wide heads in whole 128-feature tiles
+  if (o.rope_cos != nullptr &&
+      (p.kind != kGemmPlain || o.rope_sin == nullptr || o.rope_S < 1 || o.rope_cols % kBM != 0))
+    return cudaErrorInvalidValue;
   switch (p.kind) {
     case kGemmPlain: return launch_kind<kGemmPlain>(p, o, l);
     case kGemmResidual: return launch_kind<kGemmResidual>(p, o, l);

@@ -59,16 +59,18 @@ struct GemmPlan {
   int feat_tiles = 0;    // ceil(N / 128)
   int splits = 1;        // split-K factor = cluster size along z
   int stages = 0;        // pipeline depth
+  bool persistent = false;  // one CTA per SM walks the tiles (splits == 1)
+  int grid_ctas = 0;     // persistent: CTAs launched
   int k_blocks = 0;      // K / 64
   uint32_t tmem_cols = 0;
   size_t smem_bytes = 0;
-  int ctas() const { return feat_tiles * token_tiles * splits; }
+  int ctas() const { return persistent ? grid_ctas : feat_tiles * token_tiles * splits; }
 };
 
 // Chooses tile and split for an M x N x K projection; force_* > 0 override.
 // Returns false if the shape is unsupported.
 bool plan_gemm(int M, int N, int K, int kind, int num_sms, int force_splits, int force_nt,
-               GemmPlan* p);
+               GemmPlan* p, bool allow_persistent = true);
 
 // Tensor-map encoder (driver entry point resolved through the runtime).
 bool make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
@@ -82,6 +84,16 @@ struct GemmOperands {
   bf16* y = nullptr;   // output [M, N]
   const bf16* residual = nullptr;
   int* err = nullptr;
+  // plain kind only: rotate output columns [0, rope_cols) as q|k heads of 64
+  const float* rope_cos = nullptr;  // [>= rope_S, 32]
+  const float* rope_sin = nullptr;
+  int rope_S = 0;     // position of token t is t % rope_S
+  int rope_cols = 0;  // a multiple of 128
+  // LayerNorm on load (non-persistent plans): x maps ln_x, the GEMM computes
+  // bf16(LN(ln_x) * ln_gamma) in shared memory, bit-identical to the LN kernel
+  const bf16* ln_x = nullptr;
+  const bf16* ln_gamma = nullptr;
+  float ln_eps = 0.f;
 };
 
 cudaError_t launch_gemm(const GemmPlan& p, const GemmOperands& o, Launch l);

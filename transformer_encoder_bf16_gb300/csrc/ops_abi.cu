@@ -114,4 +114,61 @@ int laya_op_linear(const void* x, int M, int K, const void* w, int N, int kind,
   return rc_of(laya::launch_gemm(p, o, l));
 }
 
+int laya_op_linear_ln(const void* x_raw, const void* gamma, float eps, int M, int K, const void* w,
+                      int N, int kind, const void* residual, void* y, int splits, int tile_tokens,
+                      void* stream) {
+  if (!al16(x_raw) || !al16(gamma) || !al16(w) || !al16(y) || !(eps > 0.f) || K % 256 != 0 ||
+      K > 2048)
+    return LAYA_E_INVAL;
+  if (kind == laya::kGemmResidual && !al16(residual)) return LAYA_E_INVAL;
+  laya::GemmPlan p;
+  if (!laya::plan_gemm(M, N, K, kind, laya::device_sm_count(), splits, tile_tokens, &p, false))
+    return LAYA_E_INVAL;
+  laya::GemmOperands o;
+  const uint64_t ldk = static_cast<uint64_t>(K) * 2;
+  bool ok = laya::make_tmap_bf16_2d(&o.w, w, N, K, ldk, 128) &&
+            laya::make_tmap_bf16_2d(&o.x, x_raw, M, K, ldk, static_cast<uint32_t>(p.nt));
+  if (kind == laya::kGemmGeglu) {
+    const char* gate = static_cast<const char*>(w) + static_cast<size_t>(N) * K * 2;
+    ok = ok && laya::make_tmap_bf16_2d(&o.w2, gate, N, K, ldk, 128);
+  } else {
+    o.w2 = o.w;
+  }
+  if (!ok) return LAYA_E_INVAL;
+  o.x_box_rows = p.nt;
+  o.y = static_cast<bf16*>(y);
+  o.residual = static_cast<const bf16*>(residual);
+  o.ln_x = static_cast<const bf16*>(x_raw);
+  o.ln_gamma = static_cast<const bf16*>(gamma);
+  o.ln_eps = eps;
+  laya::Launch l{static_cast<cudaStream_t>(stream), false};
+  return rc_of(laya::launch_gemm(p, o, l));
+}
+
+int laya_op_linear_rope(const void* x, int M, int K, const void* w, int N, const float* cos_dev,
+                        const float* sin_dev, int S, int rope_cols, void* y, int splits,
+                        int tile_tokens, void* stream) {
+  if (!al16(x) || !al16(w) || !al16(y) || !cos_dev || !sin_dev || S < 1 || S > 65535 ||
+      rope_cols < 0 || rope_cols % 128 != 0 || rope_cols > N)
+    return LAYA_E_INVAL;
+  laya::GemmPlan p;
+  if (!laya::plan_gemm(M, N, K, laya::kGemmPlain, laya::device_sm_count(), splits, tile_tokens,
+                       &p))
+    return LAYA_E_INVAL;
+  laya::GemmOperands o;
+  const uint64_t ldk = static_cast<uint64_t>(K) * 2;
+  if (!laya::make_tmap_bf16_2d(&o.w, w, N, K, ldk, 128) ||
+      !laya::make_tmap_bf16_2d(&o.x, x, M, K, ldk, static_cast<uint32_t>(p.nt)))
+    return LAYA_E_INVAL;
+  o.w2 = o.w;
+  o.x_box_rows = p.nt;
+  o.y = static_cast<bf16*>(y);
+  o.rope_cos = cos_dev;
+  o.rope_sin = sin_dev;
+  o.rope_S = S;
+  o.rope_cols = rope_cols;
+  laya::Launch l{static_cast<cudaStream_t>(stream), false};
+  return rc_of(laya::launch_gemm(p, o, l));
+}
+
 }  // extern "C"

@@ -19,6 +19,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "rowstats.cuh"
 
 namespace laya {
 
@@ -42,16 +43,10 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
   return u;
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
 // V = hidden / 256 chunks of 8 BF16 per lane.  ids != nullptr selects the
 // embedding form: row t reads emb[ids[t]].
 template <int V>
-__global__ void __launch_bounds__(128) layernorm_kernel(const bf16* __restrict__ src,
+__global__ void __launch_bounds__(128) layernorm_kernel(const bf16* src,
                                                         const bf16* __restrict__ gamma, int M,
                                                         float eps, bf16* dst,
                                                         const int32_t* __restrict__ ids,
@@ -73,27 +68,9 @@ __global__ void __launch_bounds__(128) layernorm_kernel(const bf16* __restrict__
   } else {
     in = src + static_cast<size_t>(row) * H;
   }
-  const uint4* in4 = reinterpret_cast<const uint4*>(in);
   float v[V][8];
-#pragma unroll
-  for (int c = 0; c < V; ++c) unpack8(in4[lane + 32 * c], v[c]);
-
-  float s = 0.f;
-#pragma unroll
-  for (int c = 0; c < V; ++c)
-#pragma unroll
-    for (int i = 0; i < 8; ++i) s += v[c][i];
-  const float mean = warp_sum(s) / static_cast<float>(H);
-  float q = 0.f;
-#pragma unroll
-  for (int c = 0; c < V; ++c)
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float d = v[c][i] - mean;
-      q += d * d;
-    }
-  const float var = warp_sum(q) / static_cast<float>(H);
-  const float rstd = 1.0f / sqrtf(var + eps);
+  float mean, rstd;
+  row_stats<V>(reinterpret_cast<const uint4*>(in), lane, eps, v, mean, rstd);
 
   const uint4* g4 = reinterpret_cast<const uint4*>(gamma);
   uint4* out4 = reinterpret_cast<uint4*>(dst + static_cast<size_t>(row) * H);
@@ -102,7 +79,7 @@ __global__ void __launch_bounds__(128) layernorm_kernel(const bf16* __restrict__
     float g[8], y[8];
     unpack8(g4[lane + 32 * c], g);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) y[i] = ((v[c][i] - mean) * rstd) * g[i];
+    for (int i = 0; i < 8; ++i) y[i] = ln_apply(v[c][i], mean, rstd, g[i]);
     out4[lane + 32 * c] = pack8(y);
   }
 }
