@@ -93,16 +93,25 @@ int laya_op_attention_rope(const void* qkv, const int32_t* lengths_dev,
  *                    gelu(z) = z/2 (1 + erf(z / sqrt 2))
  * K a multiple of 64; N a multiple of 8.  splits <= 0 and tile_tokens <= 0
  * pick the library's plan; positive values force them (tile_tokens a multiple
- * of 16, at most 256; splits at most 8 and at most K/64).  Split-K partial
- * sums are reduced in the shared memory of a thread-block cluster, in split
- * order, so no scratch memory is needed and results do not depend on timing.
+ * of 16, at most 256; splits at most 8 and at most K/64).  workspace: device
+ * scratch of at least laya_op_linear_workspace_size() bytes, 16-byte aligned,
+ * caller-owned (NULL allowed when that size is 0): split-K writes its fp32
+ * partial tiles there and the CTAs of each cluster sum them in split order,
+ * so results do not depend on timing.  The contents need no initialisation
+ * and are garbage afterwards; concurrent calls must not share it.
  * Sources: "[Performance]: Optimize native Rust/CUDA Laya inference #66",
  * "Implementation priorities" (the four encoder GEMMs; small tiles for short
  * sequences, preserving fp32 accumulation and BF16 rounding); "[RFC]: Native
  * Laya inference with Rust and CUDA #14" (fused GEMM epilogues). */
 int laya_op_linear(const void* x, int M, int K, const void* w, int N, int kind,
-                   const void* residual, void* y, int splits, int tile_tokens,
+                   const void* residual, void* y, void* workspace,
+                   size_t workspace_bytes, int splits, int tile_tokens,
                    void* stream);
+
+/* Workspace bytes laya_op_linear (and the _ln / _rope forms) need for this
+ * shape and plan; 0 when the plan does not split K. */
+int laya_op_linear_workspace_size(int M, int K, int N, int kind, int splits,
+                                  int tile_tokens, size_t* bytes);
 
 /* A projection whose input is LayerNorm'd on load: the GEMM reads rows of
  * x_raw [M, K] and computes h = bf16(LN(x_raw) * gamma) in shared memory with
@@ -114,8 +123,9 @@ int laya_op_linear(const void* x, int M, int K, const void* w, int N, int kind,
  * laya_op_linear. */
 int laya_op_linear_ln(const void* x_raw, const void* gamma, float eps, int M,
                       int K, const void* w, int N, int kind,
-                      const void* residual, void* y, int splits,
-                      int tile_tokens, void* stream);
+                      const void* residual, void* y, void* workspace,
+                      size_t workspace_bytes, int splits, int tile_tokens,
+                      void* stream);
 
 /* The QKV projection as laya_enc_run runs it: kind 0 (plain) with RoPE
  * applied in the epilogue to output columns [0, rope_cols) (the q and k heads
@@ -126,7 +136,8 @@ int laya_op_linear_ln(const void* x_raw, const void* gamma, float eps, int M,
  * Sources: as laya_op_linear and laya_op_rope. */
 int laya_op_linear_rope(const void* x, int M, int K, const void* w, int N,
                         const float* cos_dev, const float* sin_dev, int S,
-                        int rope_cols, void* y, int splits, int tile_tokens,
+                        int rope_cols, void* y, void* workspace,
+                        size_t workspace_bytes, int splits, int tile_tokens,
                         void* stream);
 
 /* The plan laya_op_linear picks by default: tokens per tile, split-K factor

@@ -87,9 +87,10 @@ _SIGNATURES = {
     "laya_op_rope": ([_P, _P, _P, _I, _I, _I, _I, _P], _I),
     "laya_op_attention": ([_P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "laya_op_attention_rope": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
-    "laya_op_linear": ([_P, _I, _I, _P, _I, _I, _P, _P, _I, _I, _P], _I),
-    "laya_op_linear_ln": ([_P, _P, _F, _I, _I, _P, _I, _I, _P, _P, _I, _I, _P], _I),
-    "laya_op_linear_rope": ([_P, _I, _I, _P, _I, _P, _P, _I, _I, _P, _I, _I, _P], _I),
+    "laya_op_linear": ([_P, _I, _I, _P, _I, _I, _P, _P, _P, _SZ, _I, _I, _P], _I),
+    "laya_op_linear_workspace_size": ([_I, _I, _I, _I, _I, _I, ctypes.POINTER(_SZ)], _I),
+    "laya_op_linear_ln": ([_P, _P, _F, _I, _I, _P, _I, _I, _P, _P, _P, _SZ, _I, _I, _P], _I),
+    "laya_op_linear_rope": ([_P, _I, _I, _P, _I, _P, _P, _I, _I, _P, _P, _SZ, _I, _I, _P], _I),
     "laya_op_linear_plan": ([_I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I),
                              ctypes.POINTER(_I)], _I),
 }
@@ -273,27 +274,50 @@ def attention_rope(qkv, lengths_dev, cos_dev, sin_dev, B, S, heads, global_, hal
                                         _ptr(ctx), _stream_ptr(stream)))
 
 
-def linear(x, w, y, kind=KIND_PLAIN, residual=None, splits=0, tile_tokens=0, stream=None):
+def linear(x, w, y, kind=KIND_PLAIN, residual=None, splits=0, tile_tokens=0, stream=None,
+           workspace=None):
+    """workspace: a device tensor of at least linear_workspace_size() bytes; a
+    fresh one is allocated when None (pass one when capturing a graph)."""
     M, K = x.shape
     N = y.shape[1]
-    _check(lib().laya_op_linear(_ptr(x), M, K, _ptr(w), N, kind, _ptr(residual), _ptr(y),
-                                splits, tile_tokens, _stream_ptr(stream)))
+    ws = workspace if workspace is not None else _workspace(M, K, N, kind, splits, tile_tokens, y.device)
+    _check(lib().laya_op_linear(_ptr(x), M, K, _ptr(w), N, kind, _ptr(residual), _ptr(y), _ptr(ws),
+                                ws.numel() if ws is not None else 0, splits, tile_tokens,
+                                _stream_ptr(stream)))
+
+
+def linear_workspace_size(M, K, N, kind, splits=0, tile_tokens=0) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().laya_op_linear_workspace_size(M, K, N, kind, splits, tile_tokens, ctypes.byref(n)))
+    return n.value
+
+
+def _workspace(M, K, N, kind, splits, tile_tokens, device):
+    """A device scratch tensor of the size the plan needs (None when it needs none)."""
+    import torch
+    n = linear_workspace_size(M, K, N, kind, splits, tile_tokens)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device) if n else None
 
 
 def linear_ln(x_raw, gamma, eps, w, y, kind=KIND_PLAIN, residual=None, splits=0, tile_tokens=0,
-              stream=None):
+              stream=None, workspace=None):
     M, K = x_raw.shape
     N = y.shape[1]
+    ws = workspace if workspace is not None else _workspace(M, K, N, kind, splits, tile_tokens, y.device)
     _check(lib().laya_op_linear_ln(_ptr(x_raw), _ptr(gamma), eps, M, K, _ptr(w), N, kind,
-                                   _ptr(residual), _ptr(y), splits, tile_tokens,
-                                   _stream_ptr(stream)))
+                                   _ptr(residual), _ptr(y), _ptr(ws), ws.numel() if ws is not None else 0,
+                                   splits, tile_tokens, _stream_ptr(stream)))
 
 
-def linear_rope(x, w, y, cos_dev, sin_dev, S, rope_cols, splits=0, tile_tokens=0, stream=None):
+def linear_rope(x, w, y, cos_dev, sin_dev, S, rope_cols, splits=0, tile_tokens=0, stream=None,
+                workspace=None):
     M, K = x.shape
     N = y.shape[1]
+    ws = workspace if workspace is not None else _workspace(M, K, N, KIND_PLAIN, splits, tile_tokens,
+                                                             y.device)
     _check(lib().laya_op_linear_rope(_ptr(x), M, K, _ptr(w), N, _ptr(cos_dev), _ptr(sin_dev), S,
-                                     rope_cols, _ptr(y), splits, tile_tokens, _stream_ptr(stream)))
+                                     rope_cols, _ptr(y), _ptr(ws), ws.numel() if ws is not None else 0,
+                                     splits, tile_tokens, _stream_ptr(stream)))
 
 
 def linear_plan(M, K, N, kind, num_sms):

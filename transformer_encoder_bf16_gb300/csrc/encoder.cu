@@ -56,6 +56,8 @@ struct Workspace {
   int32_t* ids = nullptr;   // device staging [M], followed by
   int32_t* lens = nullptr;  // device staging [B]
   int32_t* host = nullptr;  // pinned staging [M + B]
+  float* partials = nullptr;  // split-K workspace shared by the four GEMMs (stream-ordered)
+  size_t partials_bytes = 0;
   cudaEvent_t staged = nullptr;   // the last upload from `host` has been consumed
   cudaEvent_t done = nullptr;     // the last forward using this workspace has finished
   GemmPlan p_qkv, p_o, p_up, p_dn;
@@ -137,7 +139,8 @@ void free_workspace(Workspace* w) {
   delete w;
 }
 
-// Activations and staging for one (B, S) shape, and the GEMM plans for it.
+// Activations, staging and split-K workspace for one (B, S) shape, and the
+// GEMM plans for it.
 int workspace_layout(const laya_enc_handle* h, int B, int S, Workspace* w, size_t* total) {
   const laya_enc_config& c = h->cfg;
   const int M = B * S;
@@ -167,6 +170,9 @@ int workspace_layout(const laya_enc_handle* h, int B, int S, Workspace* w, size_
   const size_t oc = take(static_cast<size_t>(M) * H * 2);
   const size_t og = take(static_cast<size_t>(M) * I * 2);
   const size_t oi = take(static_cast<size_t>(M + B) * 4);  // ids then lengths, adjacent
+  const size_t pbytes = std::max(std::max(w->p_qkv.workspace_bytes, w->p_o.workspace_bytes),
+                                 std::max(w->p_up.workspace_bytes, w->p_dn.workspace_bytes));
+  const size_t op = take(pbytes);
   *total = off;
   if (w->block) {
     char* base = static_cast<char*>(w->block);
@@ -177,6 +183,8 @@ int workspace_layout(const laya_enc_handle* h, int B, int S, Workspace* w, size_
     w->g = reinterpret_cast<bf16*>(base + og);
     w->ids = reinterpret_cast<int32_t*>(base + oi);
     w->lens = w->ids + M;
+    w->partials = pbytes ? reinterpret_cast<float*>(base + op) : nullptr;
+    w->partials_bytes = pbytes;
   }
   return LAYA_OK;
 }
@@ -265,6 +273,8 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, bf16* out, cudaStr
                   launch_layernorm(w->x, h->final_norm, M, H, c.ln_eps, w->x, l));
     GemmOperands o;
     o.err = h->err;
+    o.partials = w->partials;
+    o.partials_bytes = w->partials_bytes;
     const CUtensorMap* qkv_in = &w->tm_h_qkv;
     if (li == 0 && c.first_attn_norm_identity) {
       qkv_in = &w->tm_x_qkv;

@@ -21,10 +21,12 @@
 // Split-K for short sequences, where the weights are the traffic and too few
 // tiles exist to occupy every SM ("Implementation priorities": smaller tiles
 // for the short shapes): the K blocks are divided among the CTAs of a thread-
-// block cluster along z.  Each CTA parks its fp32 partial tile in its own
-// shared memory; after a cluster barrier every CTA sums one slice of rows over
-// all partials in rank order (deterministic) through distributed shared
-// memory and runs the epilogue for it.  No global scratch, no atomics.
+// block cluster along z.  Each CTA writes its fp32 partial tile to a global
+// workspace (coalesced, L2-resident); after a cluster barrier (release /
+// acquire) every CTA sums one slice of the tile over all partials in rank
+// order (deterministic, no atomics) and runs the epilogue for it.  (Parking
+// the partials in shared memory and reducing through DSMEM was measured: the
+// distributed-shared-memory reads were the slowest part of the kernel.)
 //
 // Roles (192 threads): warp 0 lane 0 issues TMA, warp 1 owns TMEM and its lane
 // 0 issues the MMAs, warps 2-5 drain TMEM (warp w reads TMEM lanes
@@ -57,7 +59,11 @@ constexpr size_t kCtrlBytes = 256;
 constexpr size_t kLnStatsBytes = 256 * 8;  // [nt <= 256][mean, rstd] for LayerNorm on load
 constexpr int kEpiBatch = 4;             // epilogue units whose loads are issued together
 constexpr int kChunk = 32;               // persistent epilogue: token columns per drain step
-constexpr size_t kStagingBytes = 2ull * kChunk * kBM * 4;  // double-buffered fp32 staging
+// fp32 staging tiles are token-major with a padded row of kSld floats: the
+// padding spreads the rows of consecutive tokens over different banks for
+// the 16-byte reads of the vector phase (and the DSMEM reads of split-K).
+constexpr int kSld = kBM + 4;
+constexpr size_t kStagingBytes = 2ull * kChunk * kSld * 4;  // double-buffered fp32 staging
 
 struct GemmArgs {
   int M, N, k_blocks, nt, splits, stages;
@@ -67,6 +73,7 @@ struct GemmArgs {
   bf16* y;
   const bf16* residual;
   int* err;
+  float* partials;  // split-K workspace: [tile][split][half][nt][kBM] fp32
   // RoPE in the epilogue (plain kind): output features below rope_cols are
   // q|k heads of 64, rotated with the [pos, 32] tables at pos = token % rope_S
   const float* rope_cos;
@@ -88,6 +95,48 @@ __device__ __forceinline__ void load8_smem(const float* p, float (&v)[8]) {
   const float4 hi = reinterpret_cast<const float4*>(p)[1];
   v[0] = lo.x; v[1] = lo.y; v[2] = lo.z; v[3] = lo.w;
   v[4] = hi.x; v[5] = hi.y; v[6] = hi.z; v[7] = hi.w;
+}
+
+// Sums, in split order, of the 8 consecutive fp32 values at float offset off
+// (and, for TWO, at off2) of every split's partial tile; `base` is the first
+// split's tile and `stride` the distance between splits, in floats.  All
+// loads are issued before the first add; .cg loads read L2 (the partials were
+// written by other SMs of the cluster).
+template <bool TWO>
+__device__ __forceinline__ void split_sum8(const float* base, size_t stride, int splits,
+                                           uint32_t off, uint32_t off2, float (&v)[8],
+                                           float (&w)[8]) {
+  float4 t[kMaxSplits][2], u[kMaxSplits][2];
+#pragma unroll
+  for (int s = 0; s < kMaxSplits; ++s) {
+    if (s < splits) {
+      const float4* p = reinterpret_cast<const float4*>(base + s * stride + off);
+      t[s][0] = __ldcg(p);
+      t[s][1] = __ldcg(p + 1);
+      if (TWO) {
+        const float4* q = reinterpret_cast<const float4*>(base + s * stride + off2);
+        u[s][0] = __ldcg(q);
+        u[s][1] = __ldcg(q + 1);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = w[i] = 0.f;
+#pragma unroll
+  for (int s = 0; s < kMaxSplits; ++s) {
+    if (s < splits) {
+      const float a8[8] = {t[s][0].x, t[s][0].y, t[s][0].z, t[s][0].w,
+                           t[s][1].x, t[s][1].y, t[s][1].z, t[s][1].w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] += a8[i];
+      if (TWO) {
+        const float b8[8] = {u[s][0].x, u[s][0].y, u[s][0].z, u[s][0].w,
+                             u[s][1].x, u[s][1].y, u[s][1].z, u[s][1].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] += b8[i];
+      }
+    }
+  }
 }
 
 // Round to BF16 (the value the projection stores), then rotate the pair
@@ -266,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------- epilogue phase 1: drain TMEM
-    // fp32 tile staged token-major in shared memory: stg[c * 128 + row] for
+    // fp32 tile staged token-major in shared memory: stg[c * kSld + row] for
     // token column c and feature row (the pipeline stages are free by now).
     // Split-K parks the raw partial (GeGLU: both halves); otherwise the
     // GeGLU product is formed here.
@@ -317,7 +366,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     epi_ok = ptx::mbar_wait(accum_bar, 0, abort_flag, a.err, kDevWaitAccum, kWaitLimitNs);
     ptx::tc_fence_after();
-    if (epi_ok) {
+    if (epi_ok && a.splits > 1) {
+      // partial tile to the workspace: part[(c * kBM) + row], GeGLU gate half after it
+      const int tile = t_tile * gridDim.x + f_tile;
+      float* part = a.partials + (static_cast<size_t>(tile) * a.splits + split) * NA * a.nt * kBM;
+      for (int c0 = 0; c0 < a.nt; c0 += 16) {
+        float v[16];
+        ptx::tmem_ld16(tq + c0, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) part[(c0 + j) * kBM + row] = v[j];
+        if (NA == 2) {
+          ptx::tmem_ld16(tq + a.nt + c0, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) part[(a.nt + c0 + j) * kBM + row] = v[j];
+        }
+      }
+    } else if (epi_ok) {
       float* stg = reinterpret_cast<float*>(smem);
       for (int c0 = 0; c0 < a.nt; c0 += 16) {
         float v[16];
@@ -325,16 +389,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (NA == 2) {
           float g[16];
           ptx::tmem_ld16(tq + a.nt + c0, g);
-          if (a.splits == 1) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = gelu_erf(v[j]) * g[j];
-          } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) stg[(a.nt + c0 + j) * kBM + row] = g[j];
-          }
+          for (int j = 0; j < 16; ++j) v[j] = gelu_erf(v[j]) * g[j];
         }
 #pragma unroll
-        for (int j = 0; j < 16; ++j) stg[(c0 + j) * kBM + row] = v[j];
+        for (int j = 0; j < 16; ++j) stg[(c0 + j) * kSld + row] = v[j];
       }
     }
     if (a.splits == 1) ptx::named_barrier_sync(1, kThreads - 64);
@@ -342,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (a.splits > 1) {
     __syncwarp();
-    ptx::cluster_sync();  // every partial of the cluster is parked
+    ptx::cluster_sync();  // every partial of the cluster is in the workspace (release/acquire)
   }
 
   if (warp >= 2 && epi_ok) {
@@ -354,13 +413,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool rope_tile = KIND == kGemmPlain && a.rope_cos != nullptr && f_tile * kBM < a.rope_cols;
     const int ngroups = rope_tile ? kBM / 16 : kBM / 8;  // RoPE: pairs of groups (f, f + 32)
     int g0 = 0, g1 = ngroups;
-    uint32_t remote[kMaxSplits];
+    const size_t pstride = static_cast<size_t>(NA) * a.nt * kBM;  // floats between splits
+    const float* pbase = nullptr;
     if (a.splits > 1) {
       const uint32_t rank = ptx::cluster_ctarank();
       g0 = static_cast<int>(rank * ngroups / a.splits);
       g1 = static_cast<int>((rank + 1) * ngroups / a.splits);
-#pragma unroll
-      for (int s = 0; s < kMaxSplits; ++s) remote[s] = s < a.splits ? ptx::mapa(sbase, s) : 0u;
+      pbase = a.partials + static_cast<size_t>(t_tile * gridDim.x + f_tile) * a.splits * pstride;
     }
     const int ng = g1 - g0;
     const int units = ng * a.nt;
@@ -376,26 +435,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int fo = 64 * (pg >> 2) + 8 * (pg & 3);
         const int t = t_base + c;
         float v1[8], v2[8];
-        const uint32_t off1 = static_cast<uint32_t>(c * kBM + fo) * 4u;
-        const uint32_t off2 = off1 + 32u * 4u;
         if (a.splits > 1) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) v1[i] = v2[i] = 0.f;
-#pragma unroll
-          for (int s = 0; s < kMaxSplits; ++s) {
-            if (s < a.splits) {
-              float t8[8];
-              ptx::ld_dsmem_f32x8(remote[s] + off1, t8);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) v1[i] += t8[i];
-              ptx::ld_dsmem_f32x8(remote[s] + off2, t8);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) v2[i] += t8[i];
-            }
-          }
+          const uint32_t off1 = static_cast<uint32_t>(c * kBM + fo);
+          split_sum8<true>(pbase, pstride, a.splits, off1, off1 + 32u, v1, v2);
         } else {
-          load8_smem(stg + off1 / 4u, v1);
-          load8_smem(stg + off2 / 4u, v2);
+          load8_smem(stg + c * kSld + fo, v1);
+          load8_smem(stg + c * kSld + fo + 32, v2);
         }
         if (t < a.M) rope_store16(a, t, f_tile * kBM + fo, v1, v2);
       }
@@ -413,34 +458,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (u < units) {
           const int c = u / ng;
           const int grp = g0 + u % ng;
-          const uint32_t off = static_cast<uint32_t>(c * kBM + grp * 8) * 4u;
           if (a.splits > 1) {
-            const uint32_t off2 = off + static_cast<uint32_t>(a.nt * kBM) * 4u;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              v[b][i] = 0.f;
-              gt[b][i] = 0.f;
-            }
-#pragma unroll
-            for (int s = 0; s < kMaxSplits; ++s) {
-              if (s < a.splits) {
-                float t8[8];
-                ptx::ld_dsmem_f32x8(remote[s] + off, t8);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) v[b][i] += t8[i];
-                if (NA == 2) {
-                  ptx::ld_dsmem_f32x8(remote[s] + off2, t8);
-#pragma unroll
-                  for (int i = 0; i < 8; ++i) gt[b][i] += t8[i];
-                }
-              }
-            }
+            const uint32_t off = static_cast<uint32_t>(c * kBM + grp * 8);
+            split_sum8<NA == 2>(pbase, pstride, a.splits, off, off + static_cast<uint32_t>(a.nt * kBM),
+                                v[b], gt[b]);
             if (NA == 2) {
 #pragma unroll
               for (int i = 0; i < 8; ++i) v[b][i] = gelu_erf(v[b][i]) * gt[b][i];
             }
           } else {
-            const float4* p4 = reinterpret_cast<const float4*>(stg + off / 4u);
+            const float4* p4 = reinterpret_cast<const float4*>(stg + c * kSld + grp * 8);
             const float4 lo = p4[0], hi = p4[1];
             v[b][0] = lo.x; v[b][1] = lo.y; v[b][2] = lo.z; v[b][3] = lo.w;
             v[b][4] = hi.x; v[b][5] = hi.y; v[b][6] = hi.z; v[b][7] = hi.w;
@@ -478,11 +505,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint4*>(a.y + static_cast<size_t>(tok[b]) * a.N + fea[b]) = packed;
       }
     }
-  }
-
-  if (a.splits > 1) {
-    __syncwarp();
-    ptx::cluster_sync();  // nobody leaves while its partial may still be read
   }
 
   ptx::tc_fence_before();
@@ -680,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ft = tile % a.feat_tiles, tt = tile / a.feat_tiles;
       const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b) * acc_cols;
       for (int c0 = 0; c0 < a.nt; c0 += kChunk, ++cc) {
-        float* buf = staging + (cc & 1) * (kChunk * kBM);
+        float* buf = staging + (cc & 1) * (kChunk * kSld);
         const int ncols = a.nt - c0 < kChunk ? a.nt - c0 : kChunk;
         for (int j0 = 0; j0 < ncols; j0 += 16) {
           float v[16];
@@ -692,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < 16; ++j) v[j] = gelu_erf(v[j]) * g[j];
           }
 #pragma unroll
-          for (int j = 0; j < 16; ++j) buf[(j0 + j) * kBM + row] = v[j];
+          for (int j = 0; j < 16; ++j) buf[(j0 + j) * kSld + row] = v[j];
         }
         if (c0 + kChunk >= a.nt) {
           // every TMEM read of this tile is complete: hand the accumulator back
@@ -709,8 +731,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int fo = 64 * (pg >> 2) + 8 * (pg & 3);
             const int t = tt * a.nt + c0 + c;
             float v1[8], v2[8];
-            load8_smem(buf + c * kBM + fo, v1);
-            load8_smem(buf + c * kBM + fo + 32, v2);
+            load8_smem(buf + c * kSld + fo, v1);
+            load8_smem(buf + c * kSld + fo + 32, v2);
             if (t < a.M) rope_store16(a, t, ft * kBM + fo, v1, v2);
           }
           continue;
@@ -726,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tok[bb] = -1;
             if (u < units) {
               const int c = u / (kBM / 8), grp = u % (kBM / 8);
-              const float4* p4 = reinterpret_cast<const float4*>(buf + c * kBM + grp * 8);
+              const float4* p4 = reinterpret_cast<const float4*>(buf + c * kSld + grp * 8);
               const float4 lo = p4[0], hi = p4[1];
               v[bb][0] = lo.x; v[bb][1] = lo.y; v[bb][2] = lo.z; v[bb][3] = lo.w;
               v[bb][4] = hi.x; v[bb][5] = hi.y; v[bb][6] = hi.z; v[bb][7] = hi.w;
@@ -802,14 +824,15 @@ cudaError_t launch_kind(const GemmPlan& p, const GemmOperands& o, Launch l) {
   size_t data = stage_bytes * p.stages;
   if (p.persistent) {
     data += kStagingBytes;
-  } else {
-    const size_t part = static_cast<size_t>(p.splits > 1 ? na : 1) * p.nt * kBM * 4;
+  } else if (p.splits == 1) {
+    const size_t part = static_cast<size_t>(p.nt) * kSld * 4;
     if (part > data) data = part;
   }
   a.ctrl_offset = static_cast<uint32_t>(data);
   a.y = o.y;
   a.residual = o.residual;
   a.err = o.err;
+  a.partials = o.partials;
   a.rope_cos = o.rope_cos;
   a.rope_sin = o.rope_sin;
   a.rope_S = o.rope_S;
@@ -941,10 +964,13 @@ bool finish_plan(GemmPlan* r) {
   if (stages < 1) return false;
   r->stages = stages;
   size_t data = stage_bytes * stages;
-  // fp32 staging tile of the epilogue (split-K: one per half of a GeGLU)
-  const size_t part = static_cast<size_t>(r->splits > 1 ? na : 1) * r->nt * kBM * 4;
+  // fp32 staging tile of the epilogue (split-K partials go to the workspace)
+  const size_t part = r->splits > 1 ? 0 : static_cast<size_t>(r->nt) * kSld * 4;
   if (part > budget) return false;
   if (part > data) data = part;
+  r->workspace_bytes = r->splits > 1 ? static_cast<size_t>(r->feat_tiles) * r->token_tiles *
+                                           r->splits * na * r->nt * kBM * 4
+                                     : 0;
   r->smem_bytes = data + kCtrlBytes + kLnStatsBytes + 1024;
   r->tmem_cols = pow2_cols(static_cast<uint32_t>(na * r->nt));
   if (r->tmem_cols > 512) return false;
@@ -975,7 +1001,7 @@ bool plan_gemm(int M, int N, int K, int kind, int num_sms, int force_splits, int
   // run one CTA per (tile, split) in clusters.  Cost in units of one 16 KB
   // weight tile streamed by one CTA:
   //   persistent: ceil(tiles / CTAs) x (K blocks x unit + 0.3) + 2
-  //   split:      waves x (K blocks per split x unit + 2),
+  //   split:      waves x (K blocks per split x unit + 2 + partial round trip),
   // a wave being as many clusters as the device can hold at once.
   GemmPlan best;
   double best_cost = 0.0;
@@ -1012,7 +1038,10 @@ bool plan_gemm(int M, int N, int K, int kind, int num_sms, int force_splits, int
         if (mac <= 0) continue;
         const int waves = (tiles + mac - 1) / mac;
         const int kb_per = (c.k_blocks + S - 1) / S;
-        cost = waves * (kb_per * unit + 2.0);
+        // + the partial tile written to and read back from L2 (about half the
+        //   cost of streaming the same bytes from HBM)
+        const double partial = 0.5 * na * c.nt * kBM * 4.0 / kATileBytes;
+        cost = waves * (kb_per * unit + 2.0 + partial);
       }
       if (!found || cost < best_cost - 1e-9) {
         best = c;
@@ -1046,6 +1075,10 @@ bool make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t
 cudaError_t launch_gemm(const GemmPlan& p, const GemmOperands& o, Launch l) {
   // the TMA box must match the shared-memory stage the plan reserves for it
   if (o.x_box_rows != p.nt) return cudaErrorInvalidValue;
+  // split-K needs its workspace, 16-byte aligned
+  if (p.splits > 1 && (o.partials == nullptr || o.partials_bytes < p.workspace_bytes ||
+                       (reinterpret_cast<uintptr_t>(o.partials) & 15u) != 0))
+    return cudaErrorInvalidValue;
   // LayerNorm on load: split kernel only, K a multiple of 256 up to 2048
   if (o.ln_x != nullptr &&
       (p.persistent || o.ln_gamma == nullptr || p.K % 256 != 0 || p.K > 2048))

@@ -61,6 +61,7 @@ struct GemmPlan {
   int stages = 0;        // pipeline depth
   bool persistent = false;  // one CTA per SM walks the tiles (splits == 1)
   int grid_ctas = 0;     // persistent: CTAs launched
+  size_t workspace_bytes = 0;  // split-K partial tiles (0 when splits == 1)
   int k_blocks = 0;      // K / 64
   uint32_t tmem_cols = 0;
   size_t smem_bytes = 0;
@@ -84,6 +85,8 @@ struct GemmOperands {
   bf16* y = nullptr;   // output [M, N]
   const bf16* residual = nullptr;
   int* err = nullptr;
+  float* partials = nullptr;   // split-K workspace (plan.workspace_bytes, 16-byte aligned)
+  size_t partials_bytes = 0;
   // plain kind only: rotate output columns [0, rope_cols) as q|k heads of 64
   const float* rope_cos = nullptr;  // [>= rope_S, 32]
   const float* rope_sin = nullptr;

@@ -88,8 +88,18 @@ int laya_op_linear_plan(int M, int K, int N, int kind, int num_sms, int* tile_to
   return LAYA_OK;
 }
 
+int laya_op_linear_workspace_size(int M, int K, int N, int kind, int splits, int tile_tokens,
+                                  size_t* bytes) {
+  laya::GemmPlan p;
+  if (!bytes || !laya::plan_gemm(M, N, K, kind, laya::device_sm_count(), splits, tile_tokens, &p))
+    return LAYA_E_INVAL;
+  *bytes = p.workspace_bytes;
+  return LAYA_OK;
+}
+
 int laya_op_linear(const void* x, int M, int K, const void* w, int N, int kind,
-                   const void* residual, void* y, int splits, int tile_tokens, void* stream) {
+                   const void* residual, void* y, void* workspace, size_t workspace_bytes,
+                   int splits, int tile_tokens, void* stream) {
   if (!al16(x) || !al16(w) || !al16(y)) return LAYA_E_INVAL;
   if (kind == laya::kGemmResidual && !al16(residual)) return LAYA_E_INVAL;
   laya::GemmPlan p;
@@ -110,13 +120,17 @@ int laya_op_linear(const void* x, int M, int K, const void* w, int N, int kind,
   o.y = static_cast<bf16*>(y);
   o.residual = static_cast<const bf16*>(residual);
   o.err = nullptr;
+  if (p.workspace_bytes > workspace_bytes || (p.workspace_bytes && !al16(workspace)))
+    return LAYA_E_INVAL;
+  o.partials = static_cast<float*>(workspace);
+  o.partials_bytes = workspace_bytes;
   laya::Launch l{static_cast<cudaStream_t>(stream), false};
   return rc_of(laya::launch_gemm(p, o, l));
 }
 
 int laya_op_linear_ln(const void* x_raw, const void* gamma, float eps, int M, int K, const void* w,
-                      int N, int kind, const void* residual, void* y, int splits, int tile_tokens,
-                      void* stream) {
+                      int N, int kind, const void* residual, void* y, void* workspace,
+                      size_t workspace_bytes, int splits, int tile_tokens, void* stream) {
   if (!al16(x_raw) || !al16(gamma) || !al16(w) || !al16(y) || !(eps > 0.f) || K % 256 != 0 ||
       K > 2048)
     return LAYA_E_INVAL;
@@ -141,13 +155,17 @@ int laya_op_linear_ln(const void* x_raw, const void* gamma, float eps, int M, in
   o.ln_x = static_cast<const bf16*>(x_raw);
   o.ln_gamma = static_cast<const bf16*>(gamma);
   o.ln_eps = eps;
+  if (p.workspace_bytes > workspace_bytes || (p.workspace_bytes && !al16(workspace)))
+    return LAYA_E_INVAL;
+  o.partials = static_cast<float*>(workspace);
+  o.partials_bytes = workspace_bytes;
   laya::Launch l{static_cast<cudaStream_t>(stream), false};
   return rc_of(laya::launch_gemm(p, o, l));
 }
 
 int laya_op_linear_rope(const void* x, int M, int K, const void* w, int N, const float* cos_dev,
-                        const float* sin_dev, int S, int rope_cols, void* y, int splits,
-                        int tile_tokens, void* stream) {
+                        const float* sin_dev, int S, int rope_cols, void* y, void* workspace,
+                        size_t workspace_bytes, int splits, int tile_tokens, void* stream) {
   if (!al16(x) || !al16(w) || !al16(y) || !cos_dev || !sin_dev || S < 1 || S > 65535 ||
       rope_cols < 0 || rope_cols % 128 != 0 || rope_cols > N)
     return LAYA_E_INVAL;
@@ -167,6 +185,10 @@ int laya_op_linear_rope(const void* x, int M, int K, const void* w, int N, const
   o.rope_sin = sin_dev;
   o.rope_S = S;
   o.rope_cols = rope_cols;
+  if (p.workspace_bytes > workspace_bytes || (p.workspace_bytes && !al16(workspace)))
+    return LAYA_E_INVAL;
+  o.partials = static_cast<float*>(workspace);
+  o.partials_bytes = workspace_bytes;
   laya::Launch l{static_cast<cudaStream_t>(stream), false};
   return rc_of(laya::launch_gemm(p, o, l));
 }
