@@ -140,6 +140,24 @@ int laya_op_linear_rope(const void* x, int M, int K, const void* w, int N,
                         size_t workspace_bytes, int splits, int tile_tokens,
                         void* stream);
 
+/* laya_op_linear for callers that cannot allocate device memory.  The pages
+ * have no counterpart: this entry point exists for library users who must not
+ * call cudaMalloc (code under a device-memory budget owned by a host
+ * framework, or latency-critical loops where an allocation could synchronise
+ * the device) and cannot keep a workspace of their own.  Same arguments and
+ * results as laya_op_linear, minus the workspace: split-K partial tiles go to
+ * a fixed 16 MiB device array inside the library (every GPU that loads the
+ * library holds it until the process exits).  A plan needing more than that
+ * (laya_op_linear_workspace_size > 16 MiB) is rejected with LAYA_E_INVAL and
+ * nothing is enqueued.  The first call on a device looks the array's address
+ * up (cudaGetSymbolAddress) and keeps it: make that first call before any
+ * stream capture.  All calls share the array and it keeps the last call's
+ * contents (nothing in it needs to start at zero); calls whose kernels
+ * overlap on the GPU race.  Allocates nothing: no cudaMalloc or cudaFree. */
+int laya_op_linear_noalloc(const void* x, int M, int K, const void* w, int N,
+                           int kind, const void* residual, void* y, int splits,
+                           int tile_tokens, void* stream);
+
 /* The plan laya_op_linear picks by default: tokens per tile, split-K factor
  * and the number of CTAs (feature tiles x token tiles x splits) on a device
  * with num_sms SMs.  Host-only. */

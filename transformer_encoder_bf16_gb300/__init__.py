@@ -88,6 +88,7 @@ _SIGNATURES = {
     "laya_op_attention": ([_P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "laya_op_attention_rope": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "laya_op_linear": ([_P, _I, _I, _P, _I, _I, _P, _P, _P, _SZ, _I, _I, _P], _I),
+    "laya_op_linear_noalloc": ([_P, _I, _I, _P, _I, _I, _P, _P, _I, _I, _P], _I),
     "laya_op_linear_workspace_size": ([_I, _I, _I, _I, _I, _I, ctypes.POINTER(_SZ)], _I),
     "laya_op_linear_ln": ([_P, _P, _F, _I, _I, _P, _I, _I, _P, _P, _P, _SZ, _I, _I, _P], _I),
     "laya_op_linear_rope": ([_P, _I, _I, _P, _I, _P, _P, _I, _I, _P, _P, _SZ, _I, _I, _P], _I),
@@ -284,6 +285,15 @@ def linear(x, w, y, kind=KIND_PLAIN, residual=None, splits=0, tile_tokens=0, str
     _check(lib().laya_op_linear(_ptr(x), M, K, _ptr(w), N, kind, _ptr(residual), _ptr(y), _ptr(ws),
                                 ws.numel() if ws is not None else 0, splits, tile_tokens,
                                 _stream_ptr(stream)))
+
+
+def linear_noalloc(x, w, y, kind=KIND_PLAIN, residual=None, splits=0, tile_tokens=0, stream=None):
+    """linear() without a workspace argument: the library's fixed 16 MiB device
+    array holds the split-K partials (for callers that cannot allocate)."""
+    M, K = x.shape
+    N = y.shape[1]
+    _check(lib().laya_op_linear_noalloc(_ptr(x), M, K, _ptr(w), N, kind, _ptr(residual), _ptr(y),
+                                        splits, tile_tokens, _stream_ptr(stream)))
 
 
 def linear_workspace_size(M, K, N, kind, splits=0, tile_tokens=0) -> int:
