@@ -75,6 +75,18 @@ int laya_op_attention(const void* qkv, const int32_t* lengths_dev, int B, int S,
                       int heads, int head_dim, int global, int half_window,
                       void* ctx, void* stream);
 
+/* laya_op_attention on the 5th-generation tensor cores: S = Q K^T and O = P V
+ * by tcgen05.mma with fp32 accumulators in tensor memory, one CTA per 128
+ * queries of one head and row, Q/K/V tiles brought in by TMA.  Same arguments,
+ * layouts, mask and results contract as laya_op_attention; P is rounded to
+ * BF16 for the P V product (the row sums are not).  qkv must be 16-byte
+ * aligned with B*S rows of 3*heads*64 BF16 values.  Returns LAYA_E_INVAL for
+ * bad arguments, LAYA_E_CUDA when the launch fails.
+ * Sources: as laya_op_attention. */
+int laya_op_attention_tc(const void* qkv, const int32_t* lengths_dev, int B, int S,
+                         int heads, int head_dim, int global, int half_window,
+                         void* ctx, void* stream);
+
 /* RoPE and attention in one kernel: the q and k of each tile are rotated in
  * shared memory (same arithmetic as laya_op_rope, bit-identical values) and
  * attended as in laya_op_attention; qkv in memory is not modified.  cos_dev,

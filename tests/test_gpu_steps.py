@@ -146,13 +146,14 @@ def test_rope_bit_exact(theta, B, S, heads):
     np.testing.assert_array_equal(got[:, 2 * H:], qkv[:, 2 * H:])   # V bytes preserved
 
 
-def _attention_case(B, S, heads, lengths, glob, hw, seed):
+def _attention_case(B, S, heads, lengths, glob, hw, seed, impl="mma"):
     torch = require_gpu()
     rng = np.random.default_rng(seed)
     H = heads * 64
     qkv = rnd_bits(rng, (B * S, 3 * H), std=0.7)
     ctx = torch.full((B * S, H), float("nan"), dtype=torch.bfloat16, device="cuda")
-    te.attention(to_dev(qkv), i32_dev(lengths), B, S, heads, glob, hw, ctx)
+    fn = te.attention if impl == "mma" else te.attention_tc
+    fn(to_dev(qkv), i32_dev(lengths), B, S, heads, glob, hw, ctx)
     torch.cuda.synchronize()
     got = bf16_bits_to_f32(to_bits(ctx)).reshape(B, S, H)
     ref = bf16_bits_to_f32(oracle.attention(qkv, lengths, B, S, heads, 64, glob, hw)).reshape(B, S, H)
@@ -176,9 +177,11 @@ def _attention_case(B, S, heads, lengths, glob, hw, seed):
     (3, 130, 2, [130, 1, 65], False, 64),
     (3, 130, 2, [130, 1, 65], True, 64),
     (2, 300, 2, [300, 129], False, 3),
+    (2, 464, 4, [464, 300], False, 128),
 ])
-def test_attention_matches_oracle(B, S, heads, lengths, glob, hw):
-    _attention_case(B, S, heads, np.array(lengths, np.int32), glob, hw, seed=B * S + heads)
+@pytest.mark.parametrize("impl", ["mma", "tc"])
+def test_attention_matches_oracle(B, S, heads, lengths, glob, hw, impl):
+    _attention_case(B, S, heads, np.array(lengths, np.int32), glob, hw, seed=B * S + heads, impl=impl)
 
 
 @pytest.mark.parametrize("B,S,heads,lengths,glob,theta", [

@@ -86,6 +86,7 @@ _SIGNATURES = {
     "laya_op_rope_table": ([_D, _I, _I, _I, _P, _P], _I),
     "laya_op_rope": ([_P, _P, _P, _I, _I, _I, _I, _P], _I),
     "laya_op_attention": ([_P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
+    "laya_op_attention_tc": ([_P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "laya_op_attention_rope": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "laya_op_linear": ([_P, _I, _I, _P, _I, _I, _P, _P, _P, _SZ, _I, _I, _P], _I),
     "laya_op_linear_noalloc": ([_P, _I, _I, _P, _I, _I, _P, _P, _I, _I, _P], _I),
@@ -266,6 +267,13 @@ def attention(qkv, lengths_dev, B, S, heads, global_, half_window, ctx, head_dim
     _check(lib().laya_op_attention(_ptr(qkv), _ptr(lengths_dev), B, S, heads, head_dim,
                                    1 if global_ else 0, half_window, _ptr(ctx),
                                    _stream_ptr(stream)))
+
+
+def attention_tc(qkv, lengths_dev, B, S, heads, global_, half_window, ctx, head_dim=64, stream=None):
+    """attention() on the tcgen05 kernel (TMEM accumulators, TMA tiles)."""
+    _check(lib().laya_op_attention_tc(_ptr(qkv), _ptr(lengths_dev), B, S, heads, head_dim,
+                                      1 if global_ else 0, half_window, _ptr(ctx),
+                                      _stream_ptr(stream)))
 
 
 def attention_rope(qkv, lengths_dev, cos_dev, sin_dev, B, S, heads, global_, half_window, ctx,

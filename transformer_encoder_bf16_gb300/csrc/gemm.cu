@@ -106,34 +106,40 @@ template <bool TWO>
 __device__ __forceinline__ void split_sum8(const float* base, size_t stride, int splits,
                                            uint32_t off, uint32_t off2, float (&v)[8],
                                            float (&w)[8]) {
-  float4 t[kMaxSplits][2], u[kMaxSplits][2];
-#pragma unroll
-  for (int s = 0; s < kMaxSplits; ++s) {
-    if (s < splits) {
-      const float4* p = reinterpret_cast<const float4*>(base + s * stride + off);
-      t[s][0] = __ldcg(p);
-      t[s][1] = __ldcg(p + 1);
-      if (TWO) {
-        const float4* q = reinterpret_cast<const float4*>(base + s * stride + off2);
-        u[s][0] = __ldcg(q);
-        u[s][1] = __ldcg(q + 1);
-      }
-    }
-  }
 #pragma unroll
   for (int i = 0; i < 8; ++i) v[i] = w[i] = 0.f;
+  // groups of four splits: the loads of a group are in flight together, and
+  // the sum still runs in split order (0, 1, 2, ...)
 #pragma unroll
-  for (int s = 0; s < kMaxSplits; ++s) {
-    if (s < splits) {
-      const float a8[8] = {t[s][0].x, t[s][0].y, t[s][0].z, t[s][0].w,
-                           t[s][1].x, t[s][1].y, t[s][1].z, t[s][1].w};
+  for (int s0 = 0; s0 < kMaxSplits; s0 += 4) {
+    if (s0 >= splits) break;
+    float4 t[4][2], u[4][2];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] += a8[i];
-      if (TWO) {
-        const float b8[8] = {u[s][0].x, u[s][0].y, u[s][0].z, u[s][0].w,
-                             u[s][1].x, u[s][1].y, u[s][1].z, u[s][1].w};
+    for (int j = 0; j < 4; ++j) {
+      if (s0 + j < splits) {
+        const float4* p = reinterpret_cast<const float4*>(base + (s0 + j) * stride + off);
+        t[j][0] = __ldcg(p);
+        t[j][1] = __ldcg(p + 1);
+        if (TWO) {
+          const float4* q = reinterpret_cast<const float4*>(base + (s0 + j) * stride + off2);
+          u[j][0] = __ldcg(q);
+          u[j][1] = __ldcg(q + 1);
+        }
+      }
+    }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) w[i] += b8[i];
+    for (int j = 0; j < 4; ++j) {
+      if (s0 + j < splits) {
+        const float a8[8] = {t[j][0].x, t[j][0].y, t[j][0].z, t[j][0].w,
+                             t[j][1].x, t[j][1].y, t[j][1].z, t[j][1].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] += a8[i];
+        if (TWO) {
+          const float b8[8] = {u[j][0].x, u[j][0].y, u[j][0].z, u[j][0].w,
+                               u[j][1].x, u[j][1].y, u[j][1].z, u[j][1].w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w[i] += b8[i];
+        }
       }
     }
   }
@@ -191,8 +197,11 @@ __device__ __forceinline__ void ln_row_any(const GemmArgs& a, int t, int lane, f
   }
 }
 
+// (launch bounds: two CTAs per SM, so that with programmatic dependent
+// launch the next projection's CTAs fit beside this one's and stream their
+// weights while it finishes)
 template <int KIND>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_w2,
                    const __grid_constant__ CUtensorMap tm_x, const GemmArgs a) {
   constexpr int NA = (KIND == kGemmGeglu) ? 2 : 1;
@@ -958,7 +967,10 @@ bool finish_plan(GemmPlan* r) {
     return r->tmem_cols <= 512 && r->smem_bytes <= kSmemLimit;
   }
   const int max_kb = (r->k_blocks + r->splits - 1) / r->splits;  // K blocks of the largest split
-  int stages = static_cast<int>(budget / stage_bytes);
+  // at most ~110 KB of stages, so that two CTAs (this projection's and the
+  // next one's, under programmatic dependent launch) share an SM
+  const size_t split_budget = 110 * 1024;
+  int stages = static_cast<int>((budget < split_budget ? budget : split_budget) / stage_bytes);
   if (stages > 8) stages = 8;
   if (stages > max_kb) stages = max_kb;
   if (stages < 1) return false;

@@ -49,6 +49,12 @@ cudaError_t launch_attention(const bf16* qkv, const int32_t* lengths, int B, int
                              int global, int half_window, bf16* ctx, int* err, Launch l,
                              const float* cos_t = nullptr, const float* sin_t = nullptr);
 
+// tcgen05 attention: tm_qkv maps the packed projection [B*S, 3H] with a box of
+// 128 rows x 64 columns (make_tmap_bf16_2d(..., box_rows = 128)).
+cudaError_t launch_attention_tc(const CUtensorMap& tm_qkv, const int32_t* lengths, int B, int S,
+                                int heads, int global, int half_window, bf16* ctx, int* err,
+                                Launch l);
+
 // ------------------------------------------------------------------ GEMM ---
 enum GemmKind : int { kGemmPlain = 0, kGemmResidual = 1, kGemmGeglu = 2 };
 

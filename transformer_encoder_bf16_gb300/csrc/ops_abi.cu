@@ -66,6 +66,20 @@ int laya_op_attention(const void* qkv, const int32_t* lengths_dev, int B, int S,
                                       nullptr, l));
 }
 
+int laya_op_attention_tc(const void* qkv, const int32_t* lengths_dev, int B, int S, int heads,
+                         int head_dim, int global, int half_window, void* ctx, void* stream) {
+  if (!al16(qkv) || !lengths_dev || !al16(ctx) || B < 1 || S < 1 || heads < 1 ||
+      head_dim != 64 || half_window < 0 || B > 65535 || heads > 65535)
+    return LAYA_E_INVAL;
+  CUtensorMap tm;
+  const uint64_t cols = 3ull * heads * 64;
+  if (!laya::make_tmap_bf16_2d(&tm, qkv, static_cast<uint64_t>(B) * S, cols, cols * 2, 128))
+    return LAYA_E_INVAL;
+  laya::Launch l{static_cast<cudaStream_t>(stream), false};
+  return rc_of(laya::launch_attention_tc(tm, lengths_dev, B, S, heads, global ? 1 : 0, half_window,
+                                         static_cast<bf16*>(ctx), nullptr, l));
+}
+
 int laya_op_attention_rope(const void* qkv, const int32_t* lengths_dev, const float* cos_dev,
                            const float* sin_dev, int B, int S, int heads, int head_dim, int global,
                            int half_window, void* ctx, void* stream) {
