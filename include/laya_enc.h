@@ -143,6 +143,19 @@ int laya_enc_check(laya_enc_handle* h, void* stream);
 /* 1: use CUDA Graphs (default, unless env LAYA_EAGER=1); 0: eager launches. */
 int laya_enc_set_graphs(laya_enc_handle* h, int enabled);
 
+/* 1: a request of at most 128 tokens (batch * seq <= 128) runs as ONE
+ * persistent kernel, launched cooperatively in clusters of four CTAs (one per
+ * SM), that streams every layer's weights by TMA while earlier phases run;
+ * split-K projections on tcgen05 reduced through distributed shared memory,
+ * LayerNorm applied as activation tiles are loaded, attention on mma.sync.
+ * Same layer equations and result contract as the layer-by-layer path;
+ * launched eagerly (no graph) and not used while `stream` is capturing.
+ * 0 (default, unless env LAYA_FUSED=1): the layer-by-layer kernels.
+ * Sources: "[Performance]: Optimize native Rust/CUDA Laya inference #66"
+ * ("Implementation priorities": the short shapes are weight-streaming
+ * bound). */
+int laya_enc_set_fused(laya_enc_handle* h, int enabled);
+
 /* Number of kernel launches one forward pass of this shape makes. */
 int laya_enc_launch_count(const laya_enc_handle* h, int batch, int seq);
 
@@ -160,7 +173,8 @@ int laya_enc_workspace_bytes(const laya_enc_handle* h, int batch, int seq,
 #define LAYA_PROF_OUT 5        /* attention output projection + residual */
 #define LAYA_PROF_UP 6         /* MLP up-projection + GeGLU */
 #define LAYA_PROF_DOWN 7       /* MLP down-projection + residual */
-#define LAYA_PROF_CLASSES 8
+#define LAYA_PROF_FUSED 8      /* the whole forward as one kernel (short requests) */
+#define LAYA_PROF_CLASSES 9
 
 /* Measurement aid.  While enabled, laya_enc_run launches eagerly (no graph,
  * no programmatic dependent launch) and brackets every kernel with CUDA events

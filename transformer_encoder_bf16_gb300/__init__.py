@@ -26,7 +26,7 @@ ERROR_NAMES = {E_INVAL: "LAYA_E_INVAL", E_NOMEM: "LAYA_E_NOMEM", E_CUDA: "LAYA_E
                E_DEVICE: "LAYA_E_DEVICE"}
 KIND_PLAIN, KIND_RESIDUAL, KIND_GEGLU = 0, 1, 2
 PROFILE_CLASSES = ("embed_norm", "norm", "qkv", "rope", "attention", "out_proj", "up_geglu",
-                   "down")
+                   "down", "fused")
 
 
 class LayaError(RuntimeError):
@@ -75,6 +75,7 @@ _SIGNATURES = {
     "laya_enc_run_device": ([_P, _P, _P, _I, _I, _P, _P], _I),
     "laya_enc_check": ([_P, _P], _I),
     "laya_enc_set_graphs": ([_P, _I], _I),
+    "laya_enc_set_fused": ([_P, _I], _I),
     "laya_enc_launch_count": ([_P, _I, _I], _I),
     "laya_enc_workspace_bytes": ([_P, _I, _I, ctypes.POINTER(_SZ)], _I),
     "laya_enc_set_profiling": ([_P, _I], _I),
@@ -193,6 +194,10 @@ class Encoder:
 
     def set_graphs(self, enabled: bool):
         _check(lib().laya_enc_set_graphs(self.handle, 1 if enabled else 0), self.handle)
+
+    def set_fused(self, enabled: bool):
+        """Short requests (batch * seq <= 128) as one persistent kernel (default off)."""
+        _check(lib().laya_enc_set_fused(self.handle, 1 if enabled else 0), self.handle)
 
     def set_profiling(self, enabled: bool):
         _check(lib().laya_enc_set_profiling(self.handle, 1 if enabled else 0), self.handle)

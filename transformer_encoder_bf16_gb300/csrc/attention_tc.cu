@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 64);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 72);
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int q0 = blockIdx.x * kAQ;
   const int n = blockIdx.y;
   const int b = blockIdx.z;

@@ -67,6 +67,14 @@ struct Workspace {
   // LayerNorm folded into the QKV / up GEMM (their plans are split-K): the
   // GEMM normalises x on load and the LN kernel is not launched
   bool ln_qkv = false, ln_up = false;
+  // fused short forward (batch * seq <= 128): plan, slice statistics and the
+  // counters of its phase program (zeroed with the block, only ever grow)
+  bool fused_ok = false;
+  bool fused_now = false;  // this enqueue uses the fused kernel
+  FusedPlanOut fp;
+  CUtensorMap fm_x, fm_ctx, fm_g, fm_qkv;  // activation maps of the fused kernel
+  float* stats = nullptr;
+  uint32_t* counters = nullptr;
   cudaGraphExec_t exec = nullptr;
   void* graph_out = nullptr;
   uint64_t last_use = 0;
@@ -91,6 +99,9 @@ struct laya_enc_handle {
   uint64_t tick = 0;
   bool graphs = true;
   bool pdl = true;
+  bool fused = false;
+  int fused_clusters = 0;                    // clusters of the fused kernel (0: unavailable)
+  laya::FusedLayer* fused_layers = nullptr;  // device [L]
   bool poisoned = false;
   std::string last_error;
   // profiling: event pairs of the last run, per-class totals
@@ -139,6 +150,13 @@ void free_workspace(Workspace* w) {
   delete w;
 }
 
+// Counters of the fused kernel: one per phase, then generation / finished
+// CTAs / abort word.
+size_t fused_counter_words(const laya_enc_handle* h) {
+  const laya_enc_config& c = h->cfg;
+  return fused_phase_count(h->L, c.n_encoder_layers, c.final_norm != 0) + 4;
+}
+
 // Activations, staging and split-K workspace for one (B, S) shape, and the
 // GEMM plans for it.
 int workspace_layout(const laya_enc_handle* h, int B, int S, Workspace* w, size_t* total) {
@@ -172,6 +190,12 @@ int workspace_layout(const laya_enc_handle* h, int B, int S, Workspace* w, size_
   const size_t oi = take(static_cast<size_t>(M + B) * 4);  // ids then lengths, adjacent
   const size_t pbytes = std::max(std::max(w->p_qkv.workspace_bytes, w->p_o.workspace_bytes),
                                  std::max(w->p_up.workspace_bytes, w->p_dn.workspace_bytes));
+  w->fused_ok = h->fused_clusters > 0 && plan_fused(M, H, I, c.heads, h->fused_clusters, &w->fp);
+  size_t ost = 0, octr = 0;
+  if (w->fused_ok) {
+    ost = take(static_cast<size_t>(M) * (H / 128) * 2 * sizeof(float));
+    octr = take(fused_counter_words(h) * sizeof(uint32_t));
+  }
   const size_t op = take(pbytes);
   *total = off;
   if (w->block) {
@@ -185,11 +209,16 @@ int workspace_layout(const laya_enc_handle* h, int B, int S, Workspace* w, size_
     w->lens = w->ids + M;
     w->partials = pbytes ? reinterpret_cast<float*>(base + op) : nullptr;
     w->partials_bytes = pbytes;
+    if (w->fused_ok) {
+      w->stats = reinterpret_cast<float*>(base + ost);
+      w->counters = reinterpret_cast<uint32_t*>(base + octr);
+    }
   }
   return LAYA_OK;
 }
 
 int kernel_count(const laya_enc_config& c, const Workspace& w) {
+  if (w.fused_now) return 1;
   const int L = c.n_encoder_layers + c.n_decision_layers;
   // per layer: QKV, attention, out-proj, up, down, and the two norms unless folded
   int n = 1 + 5 * L;
@@ -261,6 +290,47 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, bf16* out, cudaStr
     if (e != cudaSuccess) return e;         \
   } while (0)
 
+  if (w->fused_now) {
+    FusedArgs a{};
+    a.tm_x = w->fm_x;
+    a.tm_ctx = w->fm_ctx;
+    a.tm_g = w->fm_g;
+    a.tm_qkv = w->fm_qkv;
+    a.M = M;
+    a.B = w->B;
+    a.S = w->S;
+    a.nt = w->fp.nt;
+    a.L = h->L;
+    a.n_enc = c.n_encoder_layers;
+    a.heads = c.heads;
+    a.H = H;
+    a.I = c.intermediate;
+    a.vocab = c.vocab;
+    a.half_window = c.local_half_window;
+    a.global_every = c.global_every;
+    a.max_seq = c.max_seq;
+    a.eps = c.ln_eps;
+    for (int i = 0; i < 4; ++i) a.plan[i] = w->fp.plan[i];
+    std::memcpy(a.cluster_tile, w->fp.cluster_tile, sizeof(a.cluster_tile));
+    a.layers = h->fused_layers;
+    a.ids = w->ids;
+    a.lens = w->lens;
+    a.emb = h->tok_emb;
+    a.emb_gamma = h->emb_norm;
+    a.final_gamma = c.final_norm ? h->final_norm : nullptr;
+    a.rope = h->rope;
+    a.x = w->x;
+    a.qkv = w->qkv;
+    a.ctx = w->ctx;
+    a.g = w->g;
+    a.out = out;
+    a.stats = w->stats;
+    a.ready = w->counters;
+    a.sync = a.ready + fused_phase_count(h->L, c.n_encoder_layers, c.final_norm != 0);
+    a.err = h->err;
+    LAYA_LAUNCH(LAYA_PROF_FUSED, launch_fused(a, w->fp.n_clusters, stream));
+    return cudaSuccess;
+  }
   LAYA_LAUNCH(LAYA_PROF_EMBED_NORM,
               launch_embed_layernorm(h->tok_emb, h->emb_norm, w->ids, M, H, c.vocab, c.ln_eps,
                                      w->x, h->err, first));
@@ -391,6 +461,13 @@ int get_workspace(laya_enc_handle* h, int B, int S, Workspace** out) {
             make_tmap_bf16_2d(&w->tm_h_up, w->h, M, c.hidden, ldh, box(w->p_up)) &&
             make_tmap_bf16_2d(&w->tm_x_up, w->x, M, c.hidden, ldh, box(w->p_up)) &&
             make_tmap_bf16_2d(&w->tm_g_dn, w->g, M, c.intermediate, ldi, box(w->p_dn));
+  if (ok && w->fused_ok) {
+    const uint32_t nt = static_cast<uint32_t>(w->fp.nt);
+    ok = make_tmap_bf16_2d(&w->fm_x, w->x, M, c.hidden, ldh, nt) &&
+         make_tmap_bf16_2d(&w->fm_ctx, w->ctx, M, c.hidden, ldh, nt) &&
+         make_tmap_bf16_2d(&w->fm_g, w->g, M, c.intermediate, ldi, nt) &&
+         make_tmap_bf16_2d(&w->fm_qkv, w->qkv, M, 3ull * c.hidden, 3 * ldh, 128);
+  }
   if (!ok) {
     free_workspace(w);
     return fail(h, LAYA_E_CUDA, "workspace: tensor map encoding failed");
@@ -409,7 +486,9 @@ int run_common(laya_enc_handle* h, Workspace* w, void* out, cudaStream_t stream)
     e = prof_fold(h);
     if (e != cudaSuccess) return cuda_fail(h, e, "profiling events");
   }
-  if (!h->graphs || h->profiling || cap != cudaStreamCaptureStatusNone) {
+  // the fused kernel (a cooperative launch) runs eagerly, never inside a capture
+  w->fused_now = h->fused && w->fused_ok && cap == cudaStreamCaptureStatusNone;
+  if (!h->graphs || h->profiling || cap != cudaStreamCaptureStatusNone || w->fused_now) {
     e = enqueue_forward(h, w, static_cast<bf16*>(out), stream);
     if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");
   } else {
@@ -564,6 +643,8 @@ int laya_enc_create(const laya_enc_config* cfg, const laya_enc_weights* wts,
     delete h;
     return fail(nullptr, LAYA_E_CUDA, "weight tensor map encoding failed");
   }
+  h->fused = env_flag("LAYA_FUSED");
+  h->fused_clusters = fused_max_clusters();
   const size_t tab = static_cast<size_t>(cfg->max_seq) * 32;
   std::vector<float> host(4 * tab);
   rope_table_host(cfg->theta_global, cfg->max_seq, 32, cfg->rope_table_bf16, host.data(),
@@ -576,6 +657,23 @@ int laya_enc_create(const laya_enc_config* cfg, const laya_enc_weights* wts,
   if (e == cudaSuccess) e = cudaMalloc(&h->err, 4 * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(h->err, 0, 4 * sizeof(int));
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->capture_stream, cudaStreamNonBlocking);
+  if (e == cudaSuccess && h->fused_clusters > 0) {
+    // the fused kernel reads every layer's tensor maps from device memory
+    std::vector<FusedLayer> fl(L);
+    for (int l = 0; l < L; ++l) {
+      const LayerMaps& m = h->layers[l];
+      fl[l].maps[0] = m.wqkv;
+      fl[l].maps[1] = m.wo;
+      fl[l].maps[2] = m.wup_in;
+      fl[l].maps[3] = m.wup_gate;
+      fl[l].maps[4] = m.wdown;
+      fl[l].attn_norm = (l == 0 && cfg->first_attn_norm_identity) ? nullptr : m.attn_norm;
+      fl[l].mlp_norm = m.mlp_norm;
+    }
+    e = cudaMalloc(&h->fused_layers, sizeof(FusedLayer) * L);
+    if (e == cudaSuccess)
+      e = cudaMemcpy(h->fused_layers, fl.data(), sizeof(FusedLayer) * L, cudaMemcpyHostToDevice);
+  }
   if (e != cudaSuccess) {
     std::string msg = std::string("create: ") + cudaGetErrorString(e);
     laya_enc_destroy(h);
@@ -662,6 +760,12 @@ int laya_enc_set_graphs(laya_enc_handle* h, int enabled) {
   return LAYA_OK;
 }
 
+int laya_enc_set_fused(laya_enc_handle* h, int enabled) {
+  if (!h) return LAYA_E_INVAL;
+  h->fused = enabled != 0;
+  return LAYA_OK;
+}
+
 int laya_enc_set_profiling(laya_enc_handle* h, int enabled) {
   if (!h) return LAYA_E_INVAL;
   if (!enabled && h->profiling) {
@@ -693,6 +797,7 @@ int laya_enc_launch_count(const laya_enc_handle* h, int batch, int seq) {
   laya::Workspace w;
   size_t b = 0;
   if (laya::workspace_layout(h, batch, seq, &w, &b) != LAYA_OK) return LAYA_E_INVAL;
+  w.fused_now = h->fused && w.fused_ok;
   return laya::kernel_count(h->cfg, w);
 }
 
@@ -714,6 +819,7 @@ int laya_enc_destroy(laya_enc_handle* h) {
   if (h->capture_stream) cudaStreamDestroy(h->capture_stream);
   if (h->rope) cudaFree(h->rope);
   if (h->err) cudaFree(h->err);
+  if (h->fused_layers) cudaFree(h->fused_layers);
   delete h;
   return LAYA_OK;
 }

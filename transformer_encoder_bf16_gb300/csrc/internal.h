@@ -107,6 +107,66 @@ struct GemmOperands {
 
 cudaError_t launch_gemm(const GemmPlan& p, const GemmOperands& o, Launch l);
 
+// ------------------------------------------------ fused short forward ---
+// The whole forward of a request of at most 128 tokens as one persistent,
+// cooperatively launched kernel (fused.cu).
+
+// Weights of one layer as the fused kernel reads them (device memory).
+struct FusedLayer {
+  CUtensorMap maps[5];      // wqkv, wo, wup (GELU half), wup (gate half), wdown; boxes 64 x 128
+  const bf16* attn_norm;    // null: identity (encoder layer 0)
+  const bf16* mlp_norm;
+};
+
+struct FusedGemmPlan {
+  int tiles;  // 128-feature tiles
+  int kb;     // 64-wide k-blocks (split among the four CTAs of a cluster)
+};
+
+constexpr int kFusedMaxClusters = 64;
+
+struct FusedPlanOut {
+  int nt = 0;                  // token columns of the MMA (M rounded up to 16)
+  int n_clusters = 0;          // clusters of four CTAs launched
+  FusedGemmPlan plan[4] = {};  // QKV, out-projection, up (GeGLU), down
+  // tile of each projection each cluster computes (255: none)
+  uint8_t cluster_tile[4][kFusedMaxClusters] = {};
+};
+
+struct FusedArgs {
+  // activation tiles (boxes nt rows x 64) and the projection rows attention
+  // reads (boxes 128 rows x 64), over the workspace buffers
+  CUtensorMap tm_x, tm_ctx, tm_g, tm_qkv;
+  int M, B, S, nt;
+  int L, n_enc, heads, H, I, vocab, half_window, global_every, max_seq;
+  float eps;
+  FusedGemmPlan plan[4];
+  uint8_t cluster_tile[4][kFusedMaxClusters];
+  const FusedLayer* layers;    // [L]
+  const int32_t* ids;          // [M]
+  const int32_t* lens;         // [B]
+  const bf16* emb;             // [vocab, H]
+  const bf16* emb_gamma;
+  const bf16* final_gamma;     // null: no final norm before the decision layers
+  const float* rope;           // cos_g, sin_g, cos_l, sin_l, each [max_seq, 32]
+  bf16 *x, *qkv, *ctx, *g, *out;
+  float* stats;                // [M][H / 128] (mean, sum of squared deviations)
+  uint32_t* ready;             // [phases], zero-initialised, only grow
+  uint32_t* sync;              // [0] generation, [1] finished CTAs, [2] abort word
+  int* err;
+};
+
+// Number of ready counters the program of a configuration uses.
+inline int fused_phase_count(int L, int n_enc, bool final_norm) {
+  return 1 + 5 * L + ((final_norm && L > n_enc) ? 1 : 0);
+}
+
+bool plan_fused(int M, int H, int I, int heads, int n_clusters, FusedPlanOut* out);
+// Clusters of four CTAs (one per SM) that can be resident at once (at most
+// kFusedMaxClusters), 0 if the kernel cannot be launched.
+int fused_max_clusters();
+cudaError_t launch_fused(const FusedArgs& a, int n_clusters, cudaStream_t stream);
+
 // Host RoPE table (shared by create() and the op-level entry point).
 void rope_table_host(double theta, int max_seq, int half, int bf16_round, float* cos_t,
                      float* sin_t);
