@@ -21,6 +21,7 @@
 // rounding), so attention sees bit-identical q and k while the packed
 // projection in memory is read once and never rewritten.
 #include "internal.h"
+#include "packing.cuh"
 #include "ptx.cuh"
 
 namespace laya {
@@ -112,7 +113,8 @@ __global__ void __launch_bounds__(128) attention_kernel(const bf16* __restrict__
                                                         int S, int heads, int global,
                                                         int half_window, bf16* __restrict__ ctx,
                                                         int* err, const float* __restrict__ cos_t,
-                                                        const float* __restrict__ sin_t) {
+                                                        const float* __restrict__ sin_t,
+                                                        int packed) {
   __shared__ __align__(128) bf16 sQ[kQ * kLd];
   __shared__ __align__(128) bf16 sK[2][kKT * kLd];
   __shared__ __align__(128) bf16 sV[2][kKT * kLd];
@@ -131,10 +133,18 @@ __global__ void __launch_bounds__(128) attention_kernel(const bf16* __restrict__
     if (tid == 0 && err != nullptr) atomicCAS(err, 0, kDevBadLength);
     len = len < 1 ? 1 : S;
   }
-  const bf16* rowbase = qkv + static_cast<size_t>(b) * S * ld;
-  bf16* out = ctx + static_cast<size_t>(b) * S * H + static_cast<size_t>(n) * 64;
+  // padded rows: row b starts at token b S and rows up to S exist (padding
+  // tokens are read as keys, masked); packed rows (packing.cuh): row b starts
+  // at cu(b) and only its len tokens are read or written (the next row
+  // follows), so tiles are cut at len
+  const size_t r0 = packed ? static_cast<size_t>(packed_start(lengths, b, S))
+                           : static_cast<size_t>(b) * S;
+  const int rows = packed ? len : S;
+  const bf16* rowbase = qkv + r0 * ld;
+  bf16* out = ctx + r0 * H + static_cast<size_t>(n) * 64;
 
   if (q0 >= len) {
+    if (packed) return;  // no such tokens
     // the whole tile is padding: defined zeros
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
@@ -160,9 +170,9 @@ __global__ void __launch_bounds__(128) attention_kernel(const bf16* __restrict__
   const uint32_t sk0 = ptx::smem_u32(sK[0]), sk1 = ptx::smem_u32(sK[1]);
   const uint32_t sv0 = ptx::smem_u32(sV[0]), sv1 = ptx::smem_u32(sV[1]);
 
-  load_tile(sq, rowbase + n * 64, q0, S, ld, tid);
-  load_tile(sk0, rowbase + H + n * 64, kt0 * kKT, S, ld, tid);
-  load_tile(sv0, rowbase + 2 * H + n * 64, kt0 * kKT, S, ld, tid);
+  load_tile(sq, rowbase + n * 64, q0, rows, ld, tid);
+  load_tile(sk0, rowbase + H + n * 64, kt0 * kKT, rows, ld, tid);
+  load_tile(sv0, rowbase + 2 * H + n * 64, kt0 * kKT, rows, ld, tid);
   cp_async_commit();
 
   const int g = lane >> 2, c4 = lane & 3;
@@ -181,8 +191,8 @@ __global__ void __launch_bounds__(128) attention_kernel(const bf16* __restrict__
     const int buf = (kt - kt0) & 1;
     const bool prefetch = kt + 1 < kt1;
     if (prefetch) {
-      load_tile(buf ? sk0 : sk1, rowbase + H + n * 64, (kt + 1) * kKT, S, ld, tid);
-      load_tile(buf ? sv0 : sv1, rowbase + 2 * H + n * 64, (kt + 1) * kKT, S, ld, tid);
+      load_tile(buf ? sk0 : sk1, rowbase + H + n * 64, (kt + 1) * kKT, rows, ld, tid);
+      load_tile(buf ? sv0 : sv1, rowbase + 2 * H + n * 64, (kt + 1) * kKT, rows, ld, tid);
       cp_async_commit();
       cp_async_wait<1>();
     } else {
@@ -190,8 +200,8 @@ __global__ void __launch_bounds__(128) attention_kernel(const bf16* __restrict__
     }
     __syncthreads();
     if (cos_t != nullptr) {
-      if (kt == kt0) rope_tile(sQ, q0, S, cos_t, sin_t, tid);
-      rope_tile(buf ? sK[1] : sK[0], kt * kKT, S, cos_t, sin_t, tid);
+      if (kt == kt0) rope_tile(sQ, q0, rows, cos_t, sin_t, tid);
+      rope_tile(buf ? sK[1] : sK[0], kt * kKT, rows, cos_t, sin_t, tid);
       __syncthreads();
     }
     if (kt == kt0) {
@@ -300,10 +310,10 @@ __global__ void __launch_bounds__(128) attention_kernel(const bf16* __restrict__
 #pragma unroll
   for (int jd = 0; jd < 8; ++jd) {
     const int d = jd * 8 + 2 * c4;
-    if (qi0 < S)
+    if (qi0 < rows)
       *reinterpret_cast<uint32_t*>(out + static_cast<size_t>(qi0) * H + d) =
           pack_bf16(o[jd][0] * inv0, o[jd][1] * inv0);
-    if (qi0 + 8 < S)
+    if (qi0 + 8 < rows)
       *reinterpret_cast<uint32_t*>(out + static_cast<size_t>(qi0 + 8) * H + d) =
           pack_bf16(o[jd][2] * inv1, o[jd][3] * inv1);
   }
@@ -313,7 +323,7 @@ __global__ void __launch_bounds__(128) attention_kernel(const bf16* __restrict__
 
 cudaError_t launch_attention(const bf16* qkv, const int32_t* lengths, int B, int S, int heads,
                              int global, int half_window, bf16* ctx, int* err, Launch l,
-                             const float* cos_t, const float* sin_t) {
+                             const float* cos_t, const float* sin_t, bool packed) {
   if (B <= 0 || S <= 0 || heads <= 0) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((S + kQ - 1) / kQ, heads, B);
@@ -325,7 +335,7 @@ cudaError_t launch_attention(const bf16* qkv, const int32_t* lengths, int B, int
   cfg.attrs = attr;
   cfg.numAttrs = l.pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, attention_kernel, qkv, lengths, S, heads, global, half_window,
-                            ctx, err, cos_t, sin_t);
+                            ctx, err, cos_t, sin_t, packed ? 1 : 0);
 }
 
 }  // namespace laya

@@ -67,6 +67,9 @@ struct Workspace {
   // LayerNorm folded into the QKV / up GEMM (their plans are split-K): the
   // GEMM normalises x on load and the LN kernel is not launched
   bool ln_qkv = false, ln_up = false;
+  // packed tokens (packing.cuh) for batches of several rows: the kernels skip
+  // the padding and a last kernel writes the padded output
+  bool packed = false;
   // fused short forward (batch * seq <= 128): plan, slice statistics and the
   // counters of its phase program (zeroed with the block, only ever grow)
   bool fused_ok = false;
@@ -166,6 +169,7 @@ int workspace_layout(const laya_enc_handle* h, int B, int S, Workspace* w, size_
   w->B = B;
   w->S = S;
   w->M = M;
+  w->packed = B > 1;
   if (!plan_gemm(M, 3 * H, H, kGemmPlain, h->num_sms, 0, 0, &w->p_qkv) ||
       !plan_gemm(M, H, H, kGemmResidual, h->num_sms, 0, 0, &w->p_o) ||
       !plan_gemm(M, I, H, kGemmGeglu, h->num_sms, 0, 0, &w->p_up) ||
@@ -225,6 +229,7 @@ int kernel_count(const laya_enc_config& c, const Workspace& w) {
   if (!w.ln_qkv) n += L - (c.first_attn_norm_identity ? 1 : 0);
   if (!w.ln_up) n += L;
   if (c.final_norm && c.n_decision_layers > 0) n += 1;
+  if (w.packed) n += 1;  // the padded output
   return n;
 }
 
@@ -331,20 +336,29 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, bf16* out, cudaStr
     LAYA_LAUNCH(LAYA_PROF_FUSED, launch_fused(a, w->fp.n_clusters, stream));
     return cudaSuccess;
   }
+  Packing pk;
+  if (w->packed) {
+    pk.lens = w->lens;
+    pk.B = w->B;
+    pk.S = w->S;
+  }
   LAYA_LAUNCH(LAYA_PROF_EMBED_NORM,
               launch_embed_layernorm(h->tok_emb, h->emb_norm, w->ids, M, H, c.vocab, c.ln_eps,
-                                     w->x, h->err, first));
+                                     w->x, h->err, first, pk));
   for (int li = 0; li < h->L; ++li) {
     const LayerMaps& lw = h->layers[li];
     const bool dec = li >= c.n_encoder_layers;
     const bool glob = dec || (li % c.global_every == 0);
     if (li == c.n_encoder_layers && c.final_norm)
       LAYA_LAUNCH(LAYA_PROF_NORM,
-                  launch_layernorm(w->x, h->final_norm, M, H, c.ln_eps, w->x, l));
+                  launch_layernorm(w->x, h->final_norm, M, H, c.ln_eps, w->x, l, pk));
     GemmOperands o;
     o.err = h->err;
     o.partials = w->partials;
     o.partials_bytes = w->partials_bytes;
+    o.lens = pk.lens;
+    o.lens_B = pk.B;
+    o.lens_S = pk.S;
     const CUtensorMap* qkv_in = &w->tm_h_qkv;
     if (li == 0 && c.first_attn_norm_identity) {
       qkv_in = &w->tm_x_qkv;
@@ -354,7 +368,8 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, bf16* out, cudaStr
       o.ln_gamma = lw.attn_norm;
       o.ln_eps = c.ln_eps;
     } else {
-      LAYA_LAUNCH(LAYA_PROF_NORM, launch_layernorm(w->x, lw.attn_norm, M, H, c.ln_eps, w->h, l));
+      LAYA_LAUNCH(LAYA_PROF_NORM,
+                  launch_layernorm(w->x, lw.attn_norm, M, H, c.ln_eps, w->h, l, pk));
     }
     o.w = lw.wqkv;
     o.w2 = lw.wqkv;
@@ -371,7 +386,7 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, bf16* out, cudaStr
     o.ln_x = o.ln_gamma = nullptr;
     LAYA_LAUNCH(LAYA_PROF_ATTN, launch_attention(w->qkv, w->lens, w->B, w->S, c.heads,
                                                  glob ? 1 : 0, c.local_half_window, w->ctx,
-                                                 h->err, l));
+                                                 h->err, l, nullptr, nullptr, w->packed));
     o.w = lw.wo;
     o.w2 = lw.wo;
     o.x = w->tm_ctx_o;
@@ -390,7 +405,8 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, bf16* out, cudaStr
       o.ln_gamma = lw.mlp_norm;
       o.ln_eps = c.ln_eps;
     } else {
-      LAYA_LAUNCH(LAYA_PROF_NORM, launch_layernorm(w->x, lw.mlp_norm, M, H, c.ln_eps, w->h, l));
+      LAYA_LAUNCH(LAYA_PROF_NORM,
+                  launch_layernorm(w->x, lw.mlp_norm, M, H, c.ln_eps, w->h, l, pk));
       o.x = w->tm_h_up;
     }
     LAYA_LAUNCH(LAYA_PROF_UP, launch_gemm(w->p_up, o, l));
@@ -399,10 +415,13 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, bf16* out, cudaStr
     o.w2 = lw.wdown;
     o.x = w->tm_g_dn;
     o.x_box_rows = w->p_dn.nt;
-    o.y = (li == h->L - 1) ? out : w->x;
+    o.y = (li == h->L - 1 && !w->packed) ? out : w->x;
     o.residual = w->x;
     LAYA_LAUNCH(LAYA_PROF_DOWN, launch_gemm(w->p_dn, o, l));
   }
+  if (w->packed)
+    LAYA_LAUNCH(LAYA_PROF_EMBED_NORM,
+                launch_unpack_rows(w->x, w->lens, w->B, w->S, H, out, l));
 #undef LAYA_LAUNCH
   return cudaSuccess;
 }

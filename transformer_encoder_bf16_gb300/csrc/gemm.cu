@@ -42,6 +42,7 @@
 #include <tuple>
 
 #include "internal.h"
+#include "packing.cuh"
 #include "ptx.cuh"
 #include "rowstats.cuh"
 
@@ -76,9 +77,14 @@ struct GemmArgs {
   float* partials;  // split-K workspace: [tile][split][half][nt][kBM] fp32
   // RoPE in the epilogue (plain kind): output features below rope_cols are
   // q|k heads of 64, rotated with the [pos, 32] tables at pos = token % rope_S
+  // (packed tokens: pos = index of the token in its row)
   const float* rope_cos;
   const float* rope_sin;
   int rope_S, rope_cols;
+  // packed tokens (packing.cuh): the valid token count sum(len) replaces M,
+  // token tiles past it do nothing; null: all M rows
+  const int32_t* lens;
+  int lens_B, lens_S;
   // LayerNorm on load (split kernel): the activation tiles TMA brings in are
   // rows of ln_x, normalised in shared memory before the MMA reads them
   const bf16* ln_x;
@@ -151,7 +157,7 @@ __device__ __forceinline__ void split_sum8(const float* base, size_t stride, int
 // f1 is the output column of the first member of eight consecutive pairs.
 __device__ __forceinline__ void rope_store16(const GemmArgs& a, int t, int f1, const float (&v1)[8],
                                              const float (&v2)[8]) {
-  const int pos = t % a.rope_S;
+  const int pos = a.lens != nullptr ? packed_pos(a.lens, a.lens_B, a.lens_S, t) : t % a.rope_S;
   const int i0 = f1 & 31;  // pair index within the head of the first element
   // eight consecutive table entries: 32-byte aligned (i0 is a multiple of 8)
   const float4* ct = reinterpret_cast<const float4*>(a.rope_cos + static_cast<size_t>(pos) * 32 + i0);
@@ -224,6 +230,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int f_tile = blockIdx.x, t_tile = blockIdx.y, split = blockIdx.z;
+  // tokens this launch covers (packed: the valid ones); a token tile past
+  // them has nothing to do (its whole cluster shares the tile and leaves)
+  const int Meff = a.lens != nullptr ? packed_total(a.lens, a.lens_B, a.lens_S) : a.M;
+  if (t_tile * a.nt >= Meff) return;
   const int kb0 = split * a.k_blocks / a.splits;
   const int kb1 = (split + 1) * a.k_blocks / a.splits;
   const int nkb = kb1 - kb0;
@@ -339,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int r = warp - 2; r < a.nt; r += 4) {
         const int t = t_tile * a.nt + r;
         float mean = 0.f, rstd = 0.f;
-        if (t < a.M) ln_row_any(a, t, lane, mean, rstd);
+        if (t < Meff) ln_row_any(a, t, lane, mean, rstd);
         if (lane == 0) {
           stats[2 * r] = mean;
           stats[2 * r + 1] = rstd;
@@ -451,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           load8_smem(stg + c * kSld + fo, v1);
           load8_smem(stg + c * kSld + fo + 32, v2);
         }
-        if (t < a.M) rope_store16(a, t, f_tile * kBM + fo, v1, v2);
+        if (t < Meff) rope_store16(a, t, f_tile * kBM + fo, v1, v2);
       }
     } else
     for (int u0 = tid_e; u0 < units; u0 += (kThreads - 64) * kEpiBatch) {
@@ -483,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
           const int t = t_base + c;
           const int f = f_tile * kBM + grp * 8;
-          if (t < a.M && f < a.N) {
+          if (t < Meff && f < a.N) {
             tok[b] = t;
             fea[b] = f;
             if (KIND == kGemmResidual)
@@ -572,7 +582,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int tiles = a.feat_tiles * a.token_tiles;
+  // tokens this launch covers (packed: the valid ones) and their tiles
+  const int Meff = a.lens != nullptr ? packed_total(a.lens, a.lens_B, a.lens_S) : a.M;
+  const int tiles = a.feat_tiles * ((Meff + a.nt - 1) / a.nt);
   const int KB = a.k_blocks;
   const uint32_t acc_cols = static_cast<uint32_t>(NA * a.nt);  // one accumulator's columns
 
@@ -742,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float v1[8], v2[8];
             load8_smem(buf + c * kSld + fo, v1);
             load8_smem(buf + c * kSld + fo + 32, v2);
-            if (t < a.M) rope_store16(a, t, ft * kBM + fo, v1, v2);
+            if (t < Meff) rope_store16(a, t, ft * kBM + fo, v1, v2);
           }
           continue;
         }
@@ -763,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               v[bb][4] = hi.x; v[bb][5] = hi.y; v[bb][6] = hi.z; v[bb][7] = hi.w;
               const int t = tt * a.nt + c0 + c;
               const int f = ft * kBM + grp * 8;
-              if (t < a.M && f < a.N) {
+              if (t < Meff && f < a.N) {
                 tok[bb] = t;
                 fea[bb] = f;
                 if (KIND == kGemmResidual)
@@ -846,6 +858,9 @@ cudaError_t launch_kind(const GemmPlan& p, const GemmOperands& o, Launch l) {
   a.rope_sin = o.rope_sin;
   a.rope_S = o.rope_S;
   a.rope_cols = o.rope_cols;
+  a.lens = o.lens;
+  a.lens_B = o.lens_B;
+  a.lens_S = o.lens_S;
   a.ln_x = o.ln_x;
   a.ln_gamma = o.ln_gamma;
   a.ln_eps = o.ln_eps;

@@ -34,20 +34,32 @@ struct Launch {
   bool pdl = false;  // programmatic dependent launch (overlap with the previous kernel)
 };
 
+// Packed tokens (packing.cuh): lens non-null selects them for B rows of S.
+struct Packing {
+  const int32_t* lens = nullptr;
+  int B = 0, S = 0;
+};
+
 // ----------------------------------------------------------- row kernels ---
 cudaError_t launch_embed_layernorm(const bf16* emb, const bf16* gamma, const int32_t* ids, int M,
-                                   int H, int vocab, float eps, bf16* x, int* err, Launch l);
+                                   int H, int vocab, float eps, bf16* x, int* err, Launch l,
+                                   const Packing& pk = Packing());
 cudaError_t launch_layernorm(const bf16* x, const bf16* gamma, int M, int H, float eps, bf16* y,
-                             Launch l);
+                             Launch l, const Packing& pk = Packing());
+// out [B*S, H] (padded) from packed rows x.
+cudaError_t launch_unpack_rows(const bf16* x, const int32_t* lens, int B, int S, int H, bf16* out,
+                               Launch l);
 cudaError_t launch_rope(bf16* qkv, const float* cos_t, const float* sin_t, int B, int S,
                         int heads, Launch l);
 bool rowops_supported_hidden(int H);
 
 // ------------------------------------------------------------- attention ---
 // cos_t/sin_t non-null: RoPE is applied to q and k inside the kernel.
+// packed: qkv and ctx hold packed tokens (packing.cuh) instead of B rows of S.
 cudaError_t launch_attention(const bf16* qkv, const int32_t* lengths, int B, int S, int heads,
                              int global, int half_window, bf16* ctx, int* err, Launch l,
-                             const float* cos_t = nullptr, const float* sin_t = nullptr);
+                             const float* cos_t = nullptr, const float* sin_t = nullptr,
+                             bool packed = false);
 
 // tcgen05 attention: tm_qkv maps the packed projection [B*S, 3H] with a box of
 // 128 rows x 64 columns (make_tmap_bf16_2d(..., box_rows = 128)).
@@ -103,6 +115,10 @@ struct GemmOperands {
   const bf16* ln_x = nullptr;
   const bf16* ln_gamma = nullptr;
   float ln_eps = 0.f;
+  // packed tokens (packing.cuh): rows [0, sum(len)) of x and y hold the valid
+  // tokens of lens_B rows of lens_S; token tiles past them are skipped
+  const int32_t* lens = nullptr;
+  int lens_B = 0, lens_S = 0;
 };
 
 cudaError_t launch_gemm(const GemmPlan& p, const GemmOperands& o, Launch l);

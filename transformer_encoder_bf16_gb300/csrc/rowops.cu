@@ -18,6 +18,7 @@
 #include <cstring>
 
 #include "internal.h"
+#include "packing.cuh"
 #include "ptx.cuh"
 #include "rowstats.cuh"
 
@@ -44,19 +45,34 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
 }
 
 // V = hidden / 256 chunks of 8 BF16 per lane.  ids != nullptr selects the
-// embedding form: row t reads emb[ids[t]].
+// embedding form: row t reads emb[ids[t]].  lens != nullptr selects packed
+// tokens (packing.cuh): the embedding form reads padded row t = b * S + s and
+// writes packed row cu(b) + s (s < len(b) only); the plain form covers the
+// sum(len) packed rows.
 template <int V>
 __global__ void __launch_bounds__(128) layernorm_kernel(const bf16* src,
                                                         const bf16* __restrict__ gamma, int M,
                                                         float eps, bf16* dst,
                                                         const int32_t* __restrict__ ids,
-                                                        int vocab, int* err) {
+                                                        int vocab, int* err,
+                                                        const int32_t* __restrict__ lens, int B,
+                                                        int S) {
   ptx::grid_launch_dependents();
   ptx::grid_dependency_wait();
   constexpr int H = 256 * V;
   const int row = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= M) return;
+  int orow = row;  // output row
+  if (lens != nullptr) {
+    if (ids != nullptr) {
+      const int b = row / S, s = row - b * S;
+      if (s >= packed_len(lens, b, S)) return;  // padding: not kept
+      orow = packed_start(lens, b, S) + s;
+    } else if (row >= packed_total(lens, B, S)) {
+      return;
+    }
+  }
   const bf16* in;
   if (ids != nullptr) {
     int id = ids[row];
@@ -73,7 +89,7 @@ __global__ void __launch_bounds__(128) layernorm_kernel(const bf16* src,
   row_stats<V>(reinterpret_cast<const uint4*>(in), lane, eps, v, mean, rstd);
 
   const uint4* g4 = reinterpret_cast<const uint4*>(gamma);
-  uint4* out4 = reinterpret_cast<uint4*>(dst + static_cast<size_t>(row) * H);
+  uint4* out4 = reinterpret_cast<uint4*>(dst + static_cast<size_t>(orow) * H);
 #pragma unroll
   for (int c = 0; c < V; ++c) {
     float g[8], y[8];
@@ -110,6 +126,28 @@ __global__ void __launch_bounds__(256) rope_kernel(bf16* qkv, const float* __res
   p[32] = __float2bfloat16_rn(y2);
 }
 
+// Padded output from packed rows: out[b * S + s] = x[cu(b) + s] for s < len(b),
+// 0 for the padding.  One warp per padded row, 16-byte copies.
+__global__ void __launch_bounds__(128) unpack_rows_kernel(const bf16* __restrict__ x,
+                                                          const int32_t* __restrict__ lens, int B,
+                                                          int S, int H, bf16* __restrict__ out) {
+  ptx::grid_launch_dependents();
+  ptx::grid_dependency_wait();
+  const int row = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= B * S) return;
+  const int b = row / S, s = row - b * S;
+  uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(row) * H);
+  const int chunks = H / 8;
+  if (s < packed_len(lens, b, S)) {
+    const uint4* src =
+        reinterpret_cast<const uint4*>(x + static_cast<size_t>(packed_start(lens, b, S) + s) * H);
+    for (int c = lane; c < chunks; c += 32) dst[c] = src[c];
+  } else {
+    for (int c = lane; c < chunks; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
+  }
+}
+
 cudaError_t launch_cfg(const void* fn, dim3 grid, dim3 block, size_t smem, Launch l,
                        void** args) {
   cudaLaunchConfig_t cfg = {};
@@ -127,26 +165,29 @@ cudaError_t launch_cfg(const void* fn, dim3 grid, dim3 block, size_t smem, Launc
 
 template <int V>
 cudaError_t launch_ln_v(const bf16* src, const bf16* gamma, int M, float eps, bf16* dst,
-                        const int32_t* ids, int vocab, int* err, Launch l) {
+                        const int32_t* ids, int vocab, int* err, const Packing& pk, Launch l) {
   const int rows_per_block = 4;
   dim3 grid((M + rows_per_block - 1) / rows_per_block), block(32 * rows_per_block);
-  void* args[] = {(void*)&src, (void*)&gamma, (void*)&M, (void*)&eps,
-                  (void*)&dst, (void*)&ids,   (void*)&vocab, (void*)&err};
+  const int32_t* lens = pk.lens;
+  int B = pk.B, S = pk.S;
+  void* args[] = {(void*)&src, (void*)&gamma, (void*)&M,    (void*)&eps, (void*)&dst,
+                  (void*)&ids, (void*)&vocab, (void*)&err,  (void*)&lens, (void*)&B,
+                  (void*)&S};
   return launch_cfg(reinterpret_cast<const void*>(&layernorm_kernel<V>), grid, block, 0, l,
                     args);
 }
 
 cudaError_t launch_ln(const bf16* src, const bf16* gamma, int M, int H, float eps, bf16* dst,
-                      const int32_t* ids, int vocab, int* err, Launch l) {
+                      const int32_t* ids, int vocab, int* err, const Packing& pk, Launch l) {
   switch (H / 256) {
-    case 1: return launch_ln_v<1>(src, gamma, M, eps, dst, ids, vocab, err, l);
-    case 2: return launch_ln_v<2>(src, gamma, M, eps, dst, ids, vocab, err, l);
-    case 3: return launch_ln_v<3>(src, gamma, M, eps, dst, ids, vocab, err, l);
-    case 4: return launch_ln_v<4>(src, gamma, M, eps, dst, ids, vocab, err, l);
-    case 5: return launch_ln_v<5>(src, gamma, M, eps, dst, ids, vocab, err, l);
-    case 6: return launch_ln_v<6>(src, gamma, M, eps, dst, ids, vocab, err, l);
-    case 7: return launch_ln_v<7>(src, gamma, M, eps, dst, ids, vocab, err, l);
-    case 8: return launch_ln_v<8>(src, gamma, M, eps, dst, ids, vocab, err, l);
+    case 1: return launch_ln_v<1>(src, gamma, M, eps, dst, ids, vocab, err, pk, l);
+    case 2: return launch_ln_v<2>(src, gamma, M, eps, dst, ids, vocab, err, pk, l);
+    case 3: return launch_ln_v<3>(src, gamma, M, eps, dst, ids, vocab, err, pk, l);
+    case 4: return launch_ln_v<4>(src, gamma, M, eps, dst, ids, vocab, err, pk, l);
+    case 5: return launch_ln_v<5>(src, gamma, M, eps, dst, ids, vocab, err, pk, l);
+    case 6: return launch_ln_v<6>(src, gamma, M, eps, dst, ids, vocab, err, pk, l);
+    case 7: return launch_ln_v<7>(src, gamma, M, eps, dst, ids, vocab, err, pk, l);
+    case 8: return launch_ln_v<8>(src, gamma, M, eps, dst, ids, vocab, err, pk, l);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -170,15 +211,25 @@ float bf16_round_host(float x) {
 bool rowops_supported_hidden(int H) { return H >= 256 && H <= 2048 && H % 256 == 0; }
 
 cudaError_t launch_embed_layernorm(const bf16* emb, const bf16* gamma, const int32_t* ids, int M,
-                                   int H, int vocab, float eps, bf16* x, int* err, Launch l) {
+                                   int H, int vocab, float eps, bf16* x, int* err, Launch l,
+                                   const Packing& pk) {
   if (M <= 0 || ids == nullptr) return cudaErrorInvalidValue;
-  return launch_ln(emb, gamma, M, H, eps, x, ids, vocab, err, l);
+  return launch_ln(emb, gamma, M, H, eps, x, ids, vocab, err, pk, l);
 }
 
 cudaError_t launch_layernorm(const bf16* x, const bf16* gamma, int M, int H, float eps, bf16* y,
-                             Launch l) {
+                             Launch l, const Packing& pk) {
   if (M <= 0) return cudaErrorInvalidValue;
-  return launch_ln(x, gamma, M, H, eps, y, nullptr, 0, nullptr, l);
+  return launch_ln(x, gamma, M, H, eps, y, nullptr, 0, nullptr, pk, l);
+}
+
+cudaError_t launch_unpack_rows(const bf16* x, const int32_t* lens, int B, int S, int H, bf16* out,
+                               Launch l) {
+  if (B <= 0 || S <= 0 || lens == nullptr || H % 8 != 0) return cudaErrorInvalidValue;
+  const int rows_per_block = 4;
+  dim3 grid((B * S + rows_per_block - 1) / rows_per_block), block(32 * rows_per_block);
+  void* args[] = {(void*)&x, (void*)&lens, (void*)&B, (void*)&S, (void*)&H, (void*)&out};
+  return launch_cfg(reinterpret_cast<const void*>(&unpack_rows_kernel), grid, block, 0, l, args);
 }
 
 cudaError_t launch_rope(bf16* qkv, const float* cos_t, const float* sin_t, int B, int S,
