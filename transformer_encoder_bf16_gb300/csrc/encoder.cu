@@ -55,6 +55,7 @@ struct Workspace {
   bf16 *x = nullptr, *h = nullptr, *qkv = nullptr, *ctx = nullptr, *g = nullptr;
   int32_t* ids = nullptr;   // device staging [M], followed by
   int32_t* lens = nullptr;  // device staging [B]
+  int32_t* pos = nullptr;   // packed tokens: each token's index in its row [M]
   int32_t* host = nullptr;  // pinned staging [M + B]
   float* partials = nullptr;  // split-K workspace shared by the four GEMMs (stream-ordered)
   size_t partials_bytes = 0;
@@ -192,6 +193,7 @@ int workspace_layout(const laya_enc_handle* h, int B, int S, Workspace* w, size_
   const size_t oc = take(static_cast<size_t>(M) * H * 2);
   const size_t og = take(static_cast<size_t>(M) * I * 2);
   const size_t oi = take(static_cast<size_t>(M + B) * 4);  // ids then lengths, adjacent
+  const size_t opos = take(static_cast<size_t>(M) * 4);
   const size_t pbytes = std::max(std::max(w->p_qkv.workspace_bytes, w->p_o.workspace_bytes),
                                  std::max(w->p_up.workspace_bytes, w->p_dn.workspace_bytes));
   w->fused_ok = h->fused_clusters > 0 && plan_fused(M, H, I, c.heads, h->fused_clusters, &w->fp);
@@ -211,6 +213,7 @@ int workspace_layout(const laya_enc_handle* h, int B, int S, Workspace* w, size_
     w->g = reinterpret_cast<bf16*>(base + og);
     w->ids = reinterpret_cast<int32_t*>(base + oi);
     w->lens = w->ids + M;
+    w->pos = reinterpret_cast<int32_t*>(base + opos);
     w->partials = pbytes ? reinterpret_cast<float*>(base + op) : nullptr;
     w->partials_bytes = pbytes;
     if (w->fused_ok) {
@@ -341,6 +344,7 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, bf16* out, cudaStr
     pk.lens = w->lens;
     pk.B = w->B;
     pk.S = w->S;
+    pk.pos = w->pos;
   }
   LAYA_LAUNCH(LAYA_PROF_EMBED_NORM,
               launch_embed_layernorm(h->tok_emb, h->emb_norm, w->ids, M, H, c.vocab, c.ln_eps,
@@ -359,6 +363,7 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, bf16* out, cudaStr
     o.lens = pk.lens;
     o.lens_B = pk.B;
     o.lens_S = pk.S;
+    o.rope_pos = pk.pos;  // read by the RoPE epilogue only
     const CUtensorMap* qkv_in = &w->tm_h_qkv;
     if (li == 0 && c.first_attn_norm_identity) {
       qkv_in = &w->tm_x_qkv;

@@ -77,10 +77,11 @@ struct GemmArgs {
   float* partials;  // split-K workspace: [tile][split][half][nt][kBM] fp32
   // RoPE in the epilogue (plain kind): output features below rope_cols are
   // q|k heads of 64, rotated with the [pos, 32] tables at pos = token % rope_S
-  // (packed tokens: pos = index of the token in its row)
+  // (packed tokens: pos = rope_pos[token], the index of the token in its row)
   const float* rope_cos;
   const float* rope_sin;
   int rope_S, rope_cols;
+  const int32_t* rope_pos;  // packed tokens: position of each token (else t % rope_S)
   // packed tokens (packing.cuh): the valid token count sum(len) replaces M,
   // token tiles past it do nothing; null: all M rows
   const int32_t* lens;
@@ -157,7 +158,7 @@ __device__ __forceinline__ void split_sum8(const float* base, size_t stride, int
 // f1 is the output column of the first member of eight consecutive pairs.
 __device__ __forceinline__ void rope_store16(const GemmArgs& a, int t, int f1, const float (&v1)[8],
                                              const float (&v2)[8]) {
-  const int pos = a.lens != nullptr ? packed_pos(a.lens, a.lens_B, a.lens_S, t) : t % a.rope_S;
+  const int pos = a.rope_pos != nullptr ? a.rope_pos[t] : t % a.rope_S;
   const int i0 = f1 & 31;  // pair index within the head of the first element
   // eight consecutive table entries: 32-byte aligned (i0 is a multiple of 8)
   const float4* ct = reinterpret_cast<const float4*>(a.rope_cos + static_cast<size_t>(pos) * 32 + i0);
@@ -861,6 +862,7 @@ cudaError_t launch_kind(const GemmPlan& p, const GemmOperands& o, Launch l) {
   a.lens = o.lens;
   a.lens_B = o.lens_B;
   a.lens_S = o.lens_S;
+  a.rope_pos = o.rope_pos;
   a.ln_x = o.ln_x;
   a.ln_gamma = o.ln_gamma;
   a.ln_eps = o.ln_eps;

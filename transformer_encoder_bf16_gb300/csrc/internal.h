@@ -38,6 +38,7 @@ struct Launch {
 struct Packing {
   const int32_t* lens = nullptr;
   int B = 0, S = 0;
+  int32_t* pos = nullptr;  // written by the packed embedding: each token's index in its row
 };
 
 // ----------------------------------------------------------- row kernels ---
@@ -119,6 +120,7 @@ struct GemmOperands {
   // tokens of lens_B rows of lens_S; token tiles past them are skipped
   const int32_t* lens = nullptr;
   int lens_B = 0, lens_S = 0;
+  const int32_t* rope_pos = nullptr;  // packed tokens: RoPE position of each token
 };
 
 cudaError_t launch_gemm(const GemmPlan& p, const GemmOperands& o, Launch l);

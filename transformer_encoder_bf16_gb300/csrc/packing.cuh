@@ -6,7 +6,8 @@
 // so the projections, norms and attention skip the padding entirely (the
 // pages leave padded positions without meaning; "Run Laya encoder and
 // decision layers on CUDA", "Test Result").  A token's position for RoPE and
-// for the attention window is still its index s in its row.  Every kernel
+// for the attention window is still its index s in its row (the embedding
+// kernel records it per packed token for the RoPE epilogue).  Every kernel
 // recomputes cu from the device lengths (B <= 16 additions), so no kernel
 // depends on another for the layout.  Lengths outside [1, S] are clamped
 // exactly as the attention kernel clamps them.
@@ -31,17 +32,6 @@ __device__ __forceinline__ int packed_start(const int32_t* lens, int b, int S) {
 // Number of valid tokens of the batch.
 __device__ __forceinline__ int packed_total(const int32_t* lens, int B, int S) {
   return packed_start(lens, B, S);
-}
-
-// Position (index in its row) of packed token t; -1 past the last token.
-__device__ __forceinline__ int packed_pos(const int32_t* lens, int B, int S, int t) {
-  int c = 0;
-  for (int b = 0; b < B; ++b) {
-    const int l = packed_len(lens, b, S);
-    if (t < c + l) return t - c;
-    c += l;
-  }
-  return -1;
 }
 
 }  // namespace laya

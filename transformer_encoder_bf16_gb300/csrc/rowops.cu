@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(128) layernorm_kernel(const bf16* src,
                                                         const int32_t* __restrict__ ids,
                                                         int vocab, int* err,
                                                         const int32_t* __restrict__ lens, int B,
-                                                        int S) {
+                                                        int S, int32_t* __restrict__ pos) {
   ptx::grid_launch_dependents();
   ptx::grid_dependency_wait();
   constexpr int H = 256 * V;
@@ -69,6 +69,7 @@ __global__ void __launch_bounds__(128) layernorm_kernel(const bf16* src,
       const int b = row / S, s = row - b * S;
       if (s >= packed_len(lens, b, S)) return;  // padding: not kept
       orow = packed_start(lens, b, S) + s;
+      if (pos != nullptr && lane == 0) pos[orow] = s;
     } else if (row >= packed_total(lens, B, S)) {
       return;
     }
@@ -170,9 +171,10 @@ cudaError_t launch_ln_v(const bf16* src, const bf16* gamma, int M, float eps, bf
   dim3 grid((M + rows_per_block - 1) / rows_per_block), block(32 * rows_per_block);
   const int32_t* lens = pk.lens;
   int B = pk.B, S = pk.S;
+  int32_t* pos = pk.pos;
   void* args[] = {(void*)&src, (void*)&gamma, (void*)&M,    (void*)&eps, (void*)&dst,
                   (void*)&ids, (void*)&vocab, (void*)&err,  (void*)&lens, (void*)&B,
-                  (void*)&S};
+                  (void*)&S,   (void*)&pos};
   return launch_cfg(reinterpret_cast<const void*>(&layernorm_kernel<V>), grid, block, 0, l,
                     args);
 }
