@@ -70,6 +70,7 @@ constexpr int kWSlots = 8;                  // weight ring
 constexpr int kASlotsMax = 4;               // activation ring slots (see Ctl::nas)
 constexpr uint32_t kWSlotBytes = kFBM * kFBK * 2;   // 16 KB
 constexpr uint32_t kARingBytes = 64 * 1024;          // activation ring
+constexpr uint32_t kASlotBytes = kARingBytes / kASlotsMax;  // up to 128 token rows
 constexpr uint32_t kAttnBytes = 2 * 128 * 128;      // K and V of one head, <= 128 keys
 constexpr uint32_t kOffW = 0;
 constexpr uint32_t kOffA = kOffW + kWSlots * kWSlotBytes;
@@ -105,7 +106,6 @@ struct Phase {
 };
 
 struct Ctl {
-  uint32_t nas, asb;  // activation ring: slots and bytes per slot (nt rows, 1024-aligned)
   uint32_t wfull, wempty, afull, aempty, accfull, accempty, mma_done;
   uint32_t aload;      // activation tile landed (TMA), per ring slot
   uint32_t kvbar;      // attention Q, K and V tiles landed
@@ -753,6 +753,7 @@ __device__ void role_weights(const FusedArgs& a, const Ctl& c, uint32_t sbase) {
 __device__ void role_mma(const FusedArgs& a, const Ctl& c, uint32_t sbase, uint32_t tmem) {
   uint32_t wi = 0, ai = 0, ui = 0;
   const uint32_t idesc = ptx::idesc_bf16(kFBM, a.nt);
+  const uint64_t dA0 = ptx::sdesc_sw128(sbase + kOffA), dW0 = ptx::sdesc_sw128(sbase + kOffW);
   walk(a, [&](const Phase& ph) -> bool {
     if (ph.gemm < 0) return true;
     int k0, k1;
@@ -763,21 +764,21 @@ __device__ void role_mma(const FusedArgs& a, const Ctl& c, uint32_t sbase, uint3
     ptx::tc_fence_after();
     const uint32_t d = tmem + buf * 256u;
     for (int kb = k0; kb < k1; ++kb) {
-      const uint32_t as = ai % c.nas;
-      if (!fwait(a, c, c.afull + 8u * as, (ai / c.nas) & 1u, kFErrMma)) return false;
+      const uint32_t as = ai % kASlotsMax;
+      if (!fwait(a, c, c.afull + 8u * as, (ai / kASlotsMax) & 1u, kFErrMma)) return false;
       for (int h = 0; h < na; ++h)
         if (!fwait(a, c, c.wfull + 8u * ((wi + h) % kWSlots), ((wi + h) / kWSlots) & 1u, kFErrMma))
           return false;
       ptx::tc_fence_after();
-      const uint32_t sa = sbase + kOffA + as * c.asb;
-      const uint32_t sw0 = sbase + kOffW + (wi % kWSlots) * kWSlotBytes;
-      const uint32_t sw1 = sbase + kOffW + ((wi + 1) % kWSlots) * kWSlotBytes;
+      // descriptors: the start-address field advances by 16-byte units
+      const uint64_t da = dA0 + static_cast<uint64_t>(as) * (kASlotBytes >> 4);
+      const uint64_t dw0 = dW0 + static_cast<uint64_t>(wi % kWSlots) * (kWSlotBytes >> 4);
+      const uint64_t dw1 = dW0 + static_cast<uint64_t>((wi + 1) % kWSlots) * (kWSlotBytes >> 4);
 #pragma unroll
       for (int kk = 0; kk < kFBK / 16; ++kk) {
-        const uint64_t bdesc = ptx::sdesc_sw128(sa + kk * 32);
         const uint32_t acc = (kb > k0 || kk > 0) ? 1u : 0u;
-        ptx::mma_bf16(d, ptx::sdesc_sw128(sw0 + kk * 32), bdesc, idesc, acc);
-        if (na == 2) ptx::mma_bf16(d + 128u, ptx::sdesc_sw128(sw1 + kk * 32), bdesc, idesc, acc);
+        ptx::mma_bf16(d, dw0 + 2 * kk, da + 2 * kk, idesc, acc);
+        if (na == 2) ptx::mma_bf16(d + 128u, dw1 + 2 * kk, da + 2 * kk, idesc, acc);
       }
       // the slots are free once these MMAs have read them
       for (int h = 0; h < na; ++h) ptx::mma_commit(c.wempty + 8u * ((wi + h) % kWSlots));
@@ -830,11 +831,11 @@ __device__ void role_loader(const FusedArgs& a, const Ctl& c, uint32_t sbase, ui
       // every k-block's raw tile requested at once (as ring slots allow)
       if (ltid == 0) {
         uint32_t ti = ai;
-        for (int kb = k0; kb < k1 && kb - k0 < static_cast<int>(c.nas); ++kb, ++ti) {
-          const uint32_t as = ti % c.nas;
-          if (!fwait(a, c, c.aempty + 8u * as, ((ti / c.nas) & 1u) ^ 1u, kFErrAct)) break;
+        for (int kb = k0; kb < k1 && kb - k0 < kASlotsMax; ++kb, ++ti) {
+          const uint32_t as = ti % kASlotsMax;
+          if (!fwait(a, c, c.aempty + 8u * as, ((ti / kASlotsMax) & 1u) ^ 1u, kFErrAct)) break;
           ptx::mbar_arrive_expect_tx(c.aload + 8u * as, tile_bytes);
-          ptx::tma_load_2d(sbase + kOffA + as * c.asb, tm, c.aload + 8u * as, kb * kFBK, 0,
+          ptx::tma_load_2d(sbase + kOffA + as * kASlotBytes, tm, c.aload + 8u * as, kb * kFBK, 0,
                            pol);
         }
       }
@@ -863,19 +864,19 @@ __device__ void role_loader(const FusedArgs& a, const Ctl& c, uint32_t sbase, ui
         ptx::named_barrier_sync(2, 64);
       }
       for (int kb = k0; kb < k1; ++kb, ++ai) {
-        const uint32_t as = ai % c.nas;
-        if (ltid == 0 && kb - k0 >= static_cast<int>(c.nas)) {
+        const uint32_t as = ai % kASlotsMax;
+        if (ltid == 0 && kb - k0 >= kASlotsMax) {
           // beyond the ring: request this tile once its slot is free
-          if (!fwait(a, c, c.aempty + 8u * as, ((ai / c.nas) & 1u) ^ 1u, kFErrAct)) return false;
+          if (!fwait(a, c, c.aempty + 8u * as, ((ai / kASlotsMax) & 1u) ^ 1u, kFErrAct)) return false;
           ptx::mbar_arrive_expect_tx(c.aload + 8u * as, tile_bytes);
-          ptx::tma_load_2d(sbase + kOffA + as * c.asb, tm, c.aload + 8u * as, kb * kFBK, 0,
+          ptx::tma_load_2d(sbase + kOffA + as * kASlotBytes, tm, c.aload + 8u * as, kb * kFBK, 0,
                            pol);
         }
-        if (!fwait(a, c, c.aload + 8u * as, (ai / c.nas) & 1u, kFErrAct)) return false;
+        if (!fwait(a, c, c.aload + 8u * as, (ai / kASlotsMax) & 1u, kFErrAct)) return false;
         if (gamma != nullptr) {
           // LayerNorm in place: thread ltid takes 16-byte chunk j = ltid % 8 of
           // token rows ltid / 8 + 8 i (row r's chunk j sits at j ^ (r % 8))
-          const uint32_t slot = sbase + kOffA + as * c.asb;
+          const uint32_t slot = sbase + kOffA + as * kASlotBytes;
           float gm[8];
           uint4 graw;
 #pragma unroll
@@ -1071,9 +1072,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
   c.red_ready = c.kvbar + 8u;
   c.red_done = c.red_ready + 8u;
   c.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kWSlots + 3 * kASlotsMax + 8);
-  // activation ring: four slots of up to 128 token rows
-  c.asb = kARingBytes / 4;
-  c.nas = 4;
+
   c.cta_abort = reinterpret_cast<volatile int*>(c.tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 

@@ -93,6 +93,25 @@ struct GemmArgs {
   float ln_eps;
 };
 
+// Position in a ring of n stages, advanced without division (the stage
+// count is a runtime value, and a division in the single-thread producer and
+// MMA loops costs more issue slots than the loop's real work).
+struct RingPos {
+  int s = 0;
+  uint32_t ph = 0;
+  int n;
+  __device__ explicit RingPos(int stages, int start = 0) : n(stages) {
+    s = start % n;
+    ph = static_cast<uint32_t>(start / n) & 1u;
+  }
+  __device__ __forceinline__ void next() {
+    if (++s == n) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+};
+
 __device__ __forceinline__ float gelu_erf(float z) {
   return (0.5f * z) * (1.0f + erff(z * 0.70710678118654752f));
 }
@@ -287,10 +306,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                          t_tile * a.nt, pol_x);
       }
       int issued = pre;
-      for (int i = pre; i < nkb; ++i) {
-        const int s = i % a.stages;
-        const uint32_t ph = static_cast<uint32_t>(i / a.stages) & 1u;
-        if (!ptx::mbar_wait(empty0 + 8u * s, ph ^ 1u, abort_flag, a.err, kDevWaitEmpty,
+      RingPos rp(a.stages, pre);
+      for (int i = pre; i < nkb; ++i, rp.next()) {
+        const int s = rp.s;
+        if (!ptx::mbar_wait(empty0 + 8u * s, rp.ph ^ 1u, abort_flag, a.err, kDevWaitEmpty,
                             kWaitLimitNs))
           break;
         const uint32_t st = sbase + s * stage_bytes;
@@ -311,23 +330,27 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (lane == 0) {
       // ---------------------------------------------------------- MMA issuer
       const uint32_t idesc = ptx::idesc_bf16(kBM, a.nt);
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % a.stages;
-        const uint32_t ph = static_cast<uint32_t>(i / a.stages) & 1u;
-        if (!ptx::mbar_wait((ln ? xform0 : full0) + 8u * s, ph, abort_flag, a.err, kDevWaitFull,
+      // descriptors of stage 0; stage s and K step kk add s * stage_bytes and
+      // kk * 32 bytes to the start-address field (in 16-byte units)
+      const uint64_t da0 = ptx::sdesc_sw128(sbase);
+      const uint64_t db0 = ptx::sdesc_sw128(sbase + NA * kATileBytes);
+      const uint64_t stage_units = stage_bytes >> 4;
+      RingPos rp(a.stages);
+      for (int i = 0; i < nkb; ++i, rp.next()) {
+        const int s = rp.s;
+        if (!ptx::mbar_wait((ln ? xform0 : full0) + 8u * s, rp.ph, abort_flag, a.err, kDevWaitFull,
                             kWaitLimitNs))
           break;
         ptx::tc_fence_after();
-        const uint32_t st = sbase + s * stage_bytes;
-        const uint32_t sb = st + NA * kATileBytes;
+        const uint64_t da = da0 + static_cast<uint64_t>(s) * stage_units;
+        const uint64_t db = db0 + static_cast<uint64_t>(s) * stage_units;
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk) {
-          const uint64_t bdesc = ptx::sdesc_sw128(sb + kk * 32);
           const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-          ptx::mma_bf16(tmem, ptx::sdesc_sw128(st + kk * 32), bdesc, idesc, acc);
+          ptx::mma_bf16(tmem, da + 2 * kk, db + 2 * kk, idesc, acc);
           if (NA == 2)
-            ptx::mma_bf16(tmem + static_cast<uint32_t>(a.nt),
-                          ptx::sdesc_sw128(st + kATileBytes + kk * 32), bdesc, idesc, acc);
+            ptx::mma_bf16(tmem + static_cast<uint32_t>(a.nt), da + (kATileBytes >> 4) + 2 * kk,
+                          db + 2 * kk, idesc, acc);
         }
         ptx::mma_commit(empty0 + 8u * s);
       }
@@ -357,10 +380,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
       ptx::named_barrier_sync(1, kThreads - 64);
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % a.stages;
-        const uint32_t ph = static_cast<uint32_t>(i / a.stages) & 1u;
-        if (!ptx::mbar_wait(full0 + 8u * s, ph, abort_flag, a.err, kDevWaitFull, kWaitLimitNs))
+      RingPos rp(a.stages);
+      for (int i = 0; i < nkb; ++i, rp.next()) {
+        const int s = rp.s;
+        if (!ptx::mbar_wait(full0 + 8u * s, rp.ph, abort_flag, a.err, kDevWaitFull, kWaitLimitNs))
           break;
         // B tile: nt rows of 128 bytes; 16-byte chunk j of row r sits at j ^ (r % 8)
         uint8_t* bt = smem + static_cast<size_t>(s) * stage_bytes + NA * kATileBytes;
@@ -641,13 +664,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         issued = pre;
         int it = 0;
         bool stop = false;
+        RingPos rp(a.stages);
         for (int tile = first; tile < tiles && !stop; tile += gridDim.x) {
           const int ft = tile % a.feat_tiles, tt = tile / a.feat_tiles;
-          for (int kb = 0; kb < KB; ++kb, ++it) {
+          for (int kb = 0; kb < KB; ++kb, ++it, rp.next()) {
             if (it < pre) continue;  // issued above
-            const int s = it % a.stages;
-            const uint32_t ph = static_cast<uint32_t>(it / a.stages) & 1u;
-            if (!ptx::mbar_wait(empty0 + 8u * s, ph ^ 1u, abort_flag, a.err, kDevWaitEmpty,
+            const int s = rp.s;
+            if (!ptx::mbar_wait(empty0 + 8u * s, rp.ph ^ 1u, abort_flag, a.err, kDevWaitEmpty,
                                 kWaitLimitNs)) {
               stop = true;
               break;
@@ -670,6 +693,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // ---------------------------------------------------------- MMA issuer
       const uint32_t idesc = ptx::idesc_bf16(kBM, a.nt);
+      const uint64_t da0 = ptx::sdesc_sw128(sbase);
+      const uint64_t db0 = ptx::sdesc_sw128(sbase + NA * kATileBytes);
+      const uint64_t stage_units = stage_bytes >> 4;
+      RingPos rp(a.stages);
       int it = 0, lt = 0;
       bool stop = false;
       for (int tile = blockIdx.x; tile < tiles && !stop; tile += gridDim.x, ++lt) {
@@ -680,24 +707,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         ptx::tc_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>(b) * acc_cols;
-        for (int kb = 0; kb < KB; ++kb, ++it) {
-          const int s = it % a.stages;
-          const uint32_t ph = static_cast<uint32_t>(it / a.stages) & 1u;
-          if (!ptx::mbar_wait(full0 + 8u * s, ph, abort_flag, a.err, kDevWaitFull, kWaitLimitNs)) {
+        for (int kb = 0; kb < KB; ++kb, ++it, rp.next()) {
+          const int s = rp.s;
+          if (!ptx::mbar_wait(full0 + 8u * s, rp.ph, abort_flag, a.err, kDevWaitFull, kWaitLimitNs)) {
             stop = true;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t st = sbase + s * stage_bytes;
-          const uint32_t sb = st + NA * kATileBytes;
+          const uint64_t da = da0 + static_cast<uint64_t>(s) * stage_units;
+          const uint64_t db = db0 + static_cast<uint64_t>(s) * stage_units;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t bdesc = ptx::sdesc_sw128(sb + kk * 32);
             const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-            ptx::mma_bf16(d, ptx::sdesc_sw128(st + kk * 32), bdesc, idesc, acc);
+            ptx::mma_bf16(d, da + 2 * kk, db + 2 * kk, idesc, acc);
             if (NA == 2)
-              ptx::mma_bf16(d + static_cast<uint32_t>(a.nt),
-                            ptx::sdesc_sw128(st + kATileBytes + kk * 32), bdesc, idesc, acc);
+              ptx::mma_bf16(d + static_cast<uint32_t>(a.nt), da + (kATileBytes >> 4) + 2 * kk,
+                            db + 2 * kk, idesc, acc);
           }
           ptx::mma_commit(empty0 + 8u * s);
         }
