@@ -60,6 +60,8 @@ constexpr size_t kCtrlBytes = 256;
 constexpr size_t kLnStatsBytes = 256 * 8;  // [nt <= 256][mean, rstd] for LayerNorm on load
 constexpr int kEpiBatch = 4;             // epilogue units whose loads are issued together
 constexpr int kChunk = 32;               // persistent epilogue: token columns per drain step
+// RoPE units (token, 8 pairs) of a chunk per epilogue thread: kChunk * 8 / 128
+constexpr int kRopeUnits = kChunk * 8 / 128;
 // fp32 staging tiles are token-major with a padded row of kSld floats: the
 // padding spreads the rows of consecutive tokens over different banks for
 // the 16-byte reads of the vector phase (and the DSMEM reads of split-K).
@@ -171,20 +173,27 @@ __device__ __forceinline__ void split_sum8(const float* base, size_t stride, int
   }
 }
 
+// The eight consecutive table entries (cos, sin) a RoPE unit of token t and
+// pair index i0 (a multiple of 8) needs: 32-byte aligned.
+struct RopeRow {
+  float4 c0, c1, s0, s1;
+};
+
+__device__ __forceinline__ RopeRow rope_row(const GemmArgs& a, int t, int i0) {
+  const int pos = a.rope_pos != nullptr ? a.rope_pos[t] : t % a.rope_S;
+  const float4* ct = reinterpret_cast<const float4*>(a.rope_cos + static_cast<size_t>(pos) * 32 + i0);
+  const float4* st = reinterpret_cast<const float4*>(a.rope_sin + static_cast<size_t>(pos) * 32 + i0);
+  return RopeRow{__ldg(ct), __ldg(ct + 1), __ldg(st), __ldg(st + 1)};
+}
+
 // Round to BF16 (the value the projection stores), then rotate the pair
 // (x1, x2) = (feature i, feature i + 32) of a head exactly as the RoPE kernel
 // does: fp32 products and sum each rounded, one BF16 rounding of the result.
 // f1 is the output column of the first member of eight consecutive pairs.
-__device__ __forceinline__ void rope_store16(const GemmArgs& a, int t, int f1, const float (&v1)[8],
-                                             const float (&v2)[8]) {
-  const int pos = a.rope_pos != nullptr ? a.rope_pos[t] : t % a.rope_S;
-  const int i0 = f1 & 31;  // pair index within the head of the first element
-  // eight consecutive table entries: 32-byte aligned (i0 is a multiple of 8)
-  const float4* ct = reinterpret_cast<const float4*>(a.rope_cos + static_cast<size_t>(pos) * 32 + i0);
-  const float4* st = reinterpret_cast<const float4*>(a.rope_sin + static_cast<size_t>(pos) * 32 + i0);
-  const float4 c0 = __ldg(ct), c1 = __ldg(ct + 1), s0 = __ldg(st), s1 = __ldg(st + 1);
-  const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-  const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+__device__ __forceinline__ void rope_apply_store16(const GemmArgs& a, int t, int f1, const RopeRow& r,
+                                                   const float (&v1)[8], const float (&v2)[8]) {
+  const float cv[8] = {r.c0.x, r.c0.y, r.c0.z, r.c0.w, r.c1.x, r.c1.y, r.c1.z, r.c1.w};
+  const float sv[8] = {r.s0.x, r.s0.y, r.s0.z, r.s0.w, r.s1.x, r.s1.y, r.s1.z, r.s1.w};
   uint4 o1, o2;
   __nv_bfloat16* p1 = reinterpret_cast<__nv_bfloat16*>(&o1);
   __nv_bfloat16* p2 = reinterpret_cast<__nv_bfloat16*>(&o2);
@@ -199,6 +208,11 @@ __device__ __forceinline__ void rope_store16(const GemmArgs& a, int t, int f1, c
   bf16* row = a.y + static_cast<size_t>(t) * a.N;
   *reinterpret_cast<uint4*>(row + f1) = o1;
   *reinterpret_cast<uint4*>(row + f1 + 32) = o2;
+}
+
+__device__ __forceinline__ void rope_store16(const GemmArgs& a, int t, int f1, const float (&v1)[8],
+                                             const float (&v2)[8]) {
+  rope_apply_store16(a, t, f1, rope_row(a, t, f1 & 31), v1, v2);
 }
 
 // mean and rstd of row t of ln_x (K = 256 * V values), one warp.
@@ -748,9 +762,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       const int ft = tile % a.feat_tiles, tt = tile / a.feat_tiles;
       const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b) * acc_cols;
+      const bool rope_tile =
+          KIND == kGemmPlain && a.rope_cos != nullptr && ft * kBM < a.rope_cols;
       for (int c0 = 0; c0 < a.nt; c0 += kChunk, ++cc) {
         float* buf = staging + (cc & 1) * (kChunk * kSld);
         const int ncols = a.nt - c0 < kChunk ? a.nt - c0 : kChunk;
+        // RoPE tables of this chunk's units (two per thread), requested before
+        // the drain so that their L2 latency overlaps it
+        RopeRow rr[kRopeUnits];
+        if (rope_tile) {
+#pragma unroll
+          for (int k = 0; k < kRopeUnits; ++k) {
+            const int u = tid_e + (kThreads - 64) * k;
+            const int c = u / (kBM / 16), pg = u % (kBM / 16);
+            const int t = tt * a.nt + c0 + c;
+            if (u < ncols * (kBM / 16) && t < Meff) rr[k] = rope_row(a, t, 8 * (pg & 3));
+          }
+        }
         for (int j0 = 0; j0 < ncols; j0 += 16) {
           float v[16];
           ptx::tmem_ld16(tq + c0 + j0, v);
@@ -770,17 +798,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::named_barrier_sync(1, kThreads - 64);
         // 16-byte vector stores: 8 features of one token per unit
-        const bool rope_tile =
-            KIND == kGemmPlain && a.rope_cos != nullptr && ft * kBM < a.rope_cols;
         if (rope_tile) {
-          for (int u = tid_e; u < ncols * (kBM / 16); u += kThreads - 64) {
+#pragma unroll
+          for (int k = 0; k < kRopeUnits; ++k) {
+            const int u = tid_e + (kThreads - 64) * k;
             const int c = u / (kBM / 16), pg = u % (kBM / 16);
             const int fo = 64 * (pg >> 2) + 8 * (pg & 3);
             const int t = tt * a.nt + c0 + c;
-            float v1[8], v2[8];
-            load8_smem(buf + c * kSld + fo, v1);
-            load8_smem(buf + c * kSld + fo + 32, v2);
-            if (t < Meff) rope_store16(a, t, ft * kBM + fo, v1, v2);
+            if (u < ncols * (kBM / 16) && t < Meff) {
+              float v1[8], v2[8];
+              load8_smem(buf + c * kSld + fo, v1);
+              load8_smem(buf + c * kSld + fo + 32, v2);
+              rope_apply_store16(a, t, ft * kBM + fo, rr[k], v1, v2);
+            }
           }
           continue;
         }
