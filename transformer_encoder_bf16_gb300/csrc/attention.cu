@@ -108,7 +108,7 @@ __device__ __forceinline__ void rope_tile(bf16* tile, int row0, int S,
   }
 }
 
-__global__ void __launch_bounds__(128) attention_kernel(const bf16* __restrict__ qkv,
+__global__ void __launch_bounds__(128, 4) attention_kernel(const bf16* __restrict__ qkv,
                                                         const int32_t* __restrict__ lengths,
                                                         int S, int heads, int global,
                                                         int half_window, bf16* __restrict__ ctx,
