@@ -56,7 +56,7 @@ class OrcConfig(ctypes.Structure):
         ("theta_global", ctypes.c_float), ("theta_local", ctypes.c_float),
         ("ln_eps", ctypes.c_float)] + [(n, ctypes.c_int32) for n in (
             "max_seq", "rope_table_bf16", "first_attn_norm_identity",
-            "final_norm", "accum_f64")]
+            "final_norm", "accum_f64", "out_fp32")]
 
 
 _P = ctypes.c_void_p
@@ -118,13 +118,14 @@ def gelu(z: float) -> float:
     return lib().orc_gelu(float(z))
 
 
-def make_config(model: dict, accum_f64: bool = False) -> OrcConfig:
+def make_config(model: dict, accum_f64: bool = False, out_fp32: bool = False) -> OrcConfig:
     c = OrcConfig()
     for name, _ in OrcConfig._fields_:
-        if name == "accum_f64":
+        if name in ("accum_f64", "out_fp32"):
             continue
         setattr(c, name, model[name])
     c.accum_f64 = 1 if accum_f64 else 0
+    c.out_fp32 = 1 if out_fp32 else 0
     return c
 
 
@@ -214,14 +215,15 @@ LAYER_KEYS = ("attn_norm", "wqkv", "wo", "mlp_norm", "wup", "wdown")
 
 
 def forward(model: dict, weights: dict, ids, lengths, accum_f64=False,
-            capture_layer=-1):
+            capture_layer=-1, out_fp32=False):
     """Full stack.  ids [B, S] int32, lengths [B] int32.  Returns fp32 [B, S, H]
-    (BF16 values), or (out, captured) when capture_layer >= 0."""
+    (BF16 values; with out_fp32, the last residual sum before its BF16
+    rounding), or (out, captured) when capture_layer >= 0."""
     ids = np.ascontiguousarray(ids, dtype=np.int32)
     lengths = np.ascontiguousarray(lengths, dtype=np.int32)
     B, S = ids.shape
     H = model["hidden"]
-    cfg = make_config(model, accum_f64)
+    cfg = make_config(model, accum_f64, out_fp32)
     keep = []
     ptrs = []
     for layer in weights["layers"]:

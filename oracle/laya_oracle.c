@@ -39,7 +39,10 @@
  * even) exactly where the GPU path stores BF16.  Dot products are sequential
  * fp32 sums over k ascending (or fp64 when cfg.accum_f64 is set: a diagnostic
  * used to size the rounding floor).  Build with -ffp-contract=off so that no
- * multiply-add is fused.
+ * multiply-add is fused.  With cfg.out_fp32 set, the last residual sum of the
+ * last decision layer is returned as its fp32 value instead of being rounded
+ * to BF16 (a parity mode: the tolerance on hidden states is then read on the
+ * sum before its final rounding); every earlier storage point is unchanged.
  *
  * Parity status: every step function below is pinned by the CPU tests in
  * tests/test_oracle_*.py (closed forms, exact integer cases, invariants, fp64
@@ -55,7 +58,7 @@
 #include <omp.h>
 #endif
 
-#define ORC_ABI 1
+#define ORC_ABI 2
 
 typedef struct {
   int32_t hidden, heads, head_dim, intermediate, vocab;
@@ -66,6 +69,7 @@ typedef struct {
   int32_t rope_table_bf16;
   int32_t first_attn_norm_identity, final_norm;
   int32_t accum_f64;
+  int32_t out_fp32;
 } orc_config;
 
 int orc_abi(void) { return ORC_ABI; }
@@ -389,7 +393,8 @@ void orc_step_embed_layernorm(const uint16_t* emb, const uint16_t* gamma,
  *     is on), 1 wqkv [3H, H], 2 wo [H, H], 3 mlp_norm [H], 4 wup [2I, H],
  *   5 wdown [H, I].
  * Output: out[B*S*H] fp32 holding BF16 values, the residual stream after the
- * last decision layer.  If capture_layer >= 0, the residual stream after that
+ * last decision layer (with cfg->out_fp32, that layer's last residual sum
+ * unrounded).  If capture_layer >= 0, the residual stream after that
  * layer (0-based over encoder then decision layers, before the final norm) is
  * copied to capture.  Returns 0, or -1 on a bad argument. */
 int orc_forward(const orc_config* cfg, const uint16_t* tok_emb,
@@ -487,7 +492,10 @@ int orc_forward(const orc_config* cfg, const uint16_t* tok_emb,
         g[t * I + j] = orc_bf16_round(orc_gelu(acc[t * 2 * I + j]) * acc[t * 2 * I + I + j]);
     bits_to_f32(w[5], (size_t)H * I, wbuf);
     linear_rows(g, (int)M, I, wbuf, H, acc, cfg->accum_f64);
-    for (size_t e = 0; e < M * H; ++e) x[e] = orc_bf16_round(x[e] + acc[e]);
+    if (l == L - 1 && cfg->out_fp32)
+      for (size_t e = 0; e < M * H; ++e) x[e] = x[e] + acc[e];
+    else
+      for (size_t e = 0; e < M * H; ++e) x[e] = orc_bf16_round(x[e] + acc[e]);
 
     if (l == capture_layer && capture) memcpy(capture, x, sizeof(float) * M * H);
   }

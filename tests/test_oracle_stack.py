@@ -219,6 +219,35 @@ def test_capture_and_rounding_floor(orc, reduced):
     assert np.all(bf16_bits_to_f32(f32_to_bf16_bits(a)) == a)     # BF16-valued output
 
 
+def test_fp32_output_is_the_last_sum_before_rounding(orc, reduced):
+    # Parity mode of the tolerance reading on hidden states: the last residual
+    # sum comes back unrounded.  Rounding it to BF16 must give the default
+    # output bit for bit, it must sit within half a BF16 step of it, and most
+    # values must be off the BF16 grid (the rounding really is skipped).
+    m, w = reduced
+    ids, lengths = synth.make_inputs(m, 2, 40, 6, (9, 40))
+    a = orc.forward(m, w, ids, lengths)
+    f = orc.forward(m, w, ids, lengths, out_fp32=True)
+    np.testing.assert_array_equal(bf16_bits_to_f32(f32_to_bf16_bits(f)), a)
+    step = np.exp2(np.floor(np.log2(np.maximum(np.abs(a), 2.0 ** -120))) - 7)
+    assert np.all(np.abs(f - a) <= 0.5 * step)
+    assert np.mean(f != a) > 0.5
+    # the layers before the last keep their BF16 storage points
+    a2, c2 = orc.forward(m, w, ids, lengths, capture_layer=0)
+    f2, d2 = orc.forward(m, w, ids, lengths, capture_layer=0, out_fp32=True)
+    np.testing.assert_array_equal(c2, d2)
+
+
+def test_fp32_output_with_zero_projections_is_the_norms(orc):
+    # every projection zero: the last sum adds exactly 0 to a BF16 residual
+    # stream, so the fp32 output equals the BF16 one
+    m = tiny_model(n_encoder_layers=2, n_decision_layers=1, final_norm=1)
+    w = zero_weights(m, np.random.default_rng(5), emb_scale=3.0)
+    ids = np.array([[1, 4, 9, 2]], np.int32)
+    np.testing.assert_array_equal(orc.forward(m, w, ids, [4], out_fp32=True),
+                                  orc.forward(m, w, ids, [4]))
+
+
 def test_rejects_bad_arguments(orc, reduced):
     m, w = reduced
     ids, _ = synth.make_inputs(m, 1, 8, 0)
