@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define LAYA_ENC_ABI_VERSION 1
+#define LAYA_ENC_ABI_VERSION 2
 
 /* Error codes (negative). */
 #define LAYA_OK 0
@@ -59,7 +59,7 @@ extern "C" {
  * vocab 50368, 28 encoder + 2 decision layers, global_every 3,
  * local_half_window 64, theta_global 160000, theta_local 10000, ln_eps 1e-5,
  * max_batch 16, max_seq 512, rope_table_bf16 1, first_attn_norm_identity 1,
- * final_norm 1.
+ * final_norm 1, out_fp32 0.
  * Supported: hidden a multiple of 256 and at most 2048, head_dim 64,
  * heads * head_dim == hidden, intermediate a multiple of 64,
  * max_seq <= 512, max_batch <= 16. */
@@ -74,6 +74,15 @@ typedef struct {
   int32_t rope_table_bf16;          /* 1: RoPE table values rounded to BF16 (kept fp32) */
   int32_t first_attn_norm_identity; /* 1: encoder layer 0 projects x without LayerNorm */
   int32_t final_norm;               /* 1: LayerNorm after the last encoder layer */
+  int32_t out_fp32; /* 0: out_hidden is BF16.  1 (parity mode): out_hidden is
+                       fp32 and receives the last residual sum of the last
+                       layer before its BF16 rounding (every earlier storage
+                       point unchanged), so that tolerances on the final hidden
+                       states ("[Performance]: Optimize native Rust/CUDA Laya
+                       inference #66", "Starting evidence") can be read
+                       without that last rounding.  Rounding this output to
+                       BF16 gives the out_fp32 = 0 result bit for bit.  The
+                       fused short-request kernel is not used in this mode. */
 } laya_enc_config;
 
 /* Per-layer weights: device pointers to BF16 data in nn.Linear layout
@@ -116,7 +125,8 @@ int laya_enc_create(const laya_enc_config* cfg, const laya_enc_weights* weights,
 /* Runs the forward pass on `stream` (a cudaStream_t; NULL is the legacy
  * default stream).  token_ids: HOST int32 [batch * seq], row-major;
  * lengths: HOST int32 [batch], each in [1, seq], positions >= length are
- * padding.  out_hidden: DEVICE BF16 [batch, seq, hidden], caller-owned;
+ * padding.  out_hidden: DEVICE BF16 [batch, seq, hidden] (fp32 when
+ * cfg.out_fp32), caller-owned;
  * valid positions receive the final hidden states, padded positions receive
  * finite values of no meaning.  The host arrays are copied into library-owned
  * pinned memory before the call returns and may be reused at once.  The call

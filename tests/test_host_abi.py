@@ -41,16 +41,18 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version(lib):
-    assert te.abi_version() == 1
+    assert te.abi_version() == 2
 
 
 def test_validate_config(lib):
     assert te.validate_config(synth.FULL) == te.OK
     assert te.validate_config(synth.REDUCED) == te.OK
+    assert te.validate_config(dict(synth.FULL, out_fp32=1)) == te.OK
     for field, bad in (("hidden", 1000), ("head_dim", 32), ("heads", 15), ("intermediate", 2600),
                        ("max_seq", 513), ("max_batch", 17), ("global_every", 0),
                        ("local_half_window", -1), ("ln_eps", 0.0), ("vocab", 0),
-                       ("n_encoder_layers", 0), ("final_norm", 2)):
+                       ("n_encoder_layers", 0), ("final_norm", 2),
+                       ("out_fp32", 2)):
         assert te.validate_config(dict(synth.FULL, **{field: bad})) == te.E_INVAL, field
 
 

@@ -42,13 +42,14 @@ class Config(ctypes.Structure):
         ("theta_global", ctypes.c_float), ("theta_local", ctypes.c_float),
         ("ln_eps", ctypes.c_float)] + [(n, ctypes.c_int32) for n in (
             "max_batch", "max_seq", "rope_table_bf16", "first_attn_norm_identity",
-            "final_norm")]
+            "final_norm", "out_fp32")]
 
     @classmethod
     def from_model(cls, model: dict) -> "Config":
+        """Every field from the model dict; out_fp32 defaults to 0 (BF16 output)."""
         c = cls()
         for name, _ in cls._fields_:
-            setattr(c, name, model[name])
+            setattr(c, name, model.get(name, 0) if name == "out_fp32" else model[name])
         return c
 
 
@@ -176,18 +177,28 @@ class Encoder:
 
     def run(self, ids: np.ndarray, lengths: np.ndarray, out, stream=None):
         """ids int32 [B, S] and lengths int32 [B] in HOST memory; out a device
-        bfloat16 tensor [B, S, hidden]."""
+        tensor [B, S, hidden], bfloat16 (float32 when the model sets out_fp32)."""
         ids = np.ascontiguousarray(ids, dtype=np.int32)
         lengths = np.ascontiguousarray(lengths, dtype=np.int32)
         B, S = ids.shape
+        self._check_out(out, B, S)
         _check(lib().laya_enc_run(self.handle, ids.ctypes.data, lengths.ctypes.data, B, S,
                                   _ptr(out), _stream_ptr(stream)), self.handle)
 
     def run_device(self, ids_dev, lengths_dev, out, stream=None):
         """ids_dev int32 [B, S] and lengths_dev int32 [B] device tensors."""
         B, S = ids_dev.shape
+        self._check_out(out, B, S)
         _check(lib().laya_enc_run_device(self.handle, _ptr(ids_dev), _ptr(lengths_dev), B, S,
                                          _ptr(out), _stream_ptr(stream)), self.handle)
+
+    def _check_out(self, out, B, S):
+        # the C ABI takes a bare pointer: the element type and size are checked here
+        import torch
+        want = torch.float32 if self._cfg.out_fp32 else torch.bfloat16
+        if out.dtype != want or not out.is_contiguous() or out.numel() < B * S * self._cfg.hidden:
+            raise LayaError(E_INVAL, f"out must be a contiguous {want} tensor of at least "
+                                     f"{B}x{S}x{self._cfg.hidden} elements")
 
     def check(self, stream=None):
         return _check(lib().laya_enc_check(self.handle, _stream_ptr(stream)), self.handle)

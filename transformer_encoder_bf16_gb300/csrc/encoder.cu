@@ -196,7 +196,9 @@ int workspace_layout(const laya_enc_handle* h, int B, int S, Workspace* w, size_
   const size_t opos = take(static_cast<size_t>(M) * 4);
   const size_t pbytes = std::max(std::max(w->p_qkv.workspace_bytes, w->p_o.workspace_bytes),
                                  std::max(w->p_up.workspace_bytes, w->p_dn.workspace_bytes));
-  w->fused_ok = h->fused_clusters > 0 && plan_fused(M, H, I, c.heads, h->fused_clusters, &w->fp);
+  // the fused kernel writes BF16 output only
+  w->fused_ok = h->fused_clusters > 0 && !c.out_fp32 &&
+                plan_fused(M, H, I, c.heads, h->fused_clusters, &w->fp);
   size_t ost = 0, octr = 0;
   if (w->fused_ok) {
     ost = take(static_cast<size_t>(M) * (H / 128) * 2 * sizeof(float));
@@ -278,7 +280,10 @@ cudaError_t prof_fold(laya_enc_handle* h) {
   return cudaSuccess;
 }
 
-cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, bf16* out, cudaStream_t stream) {
+// out: BF16 [B, S, H], or fp32 when cfg.out_fp32 (written by the last
+// residual sum directly, or through the packed fp32 rows it leaves in the
+// qkv buffer, which that layer's attention no longer needs).
+cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, void* out, cudaStream_t stream) {
   const laya_enc_config& c = h->cfg;
   const int H = c.hidden;
   const int M = w->M;
@@ -331,7 +336,7 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, bf16* out, cudaStr
     a.qkv = w->qkv;
     a.ctx = w->ctx;
     a.g = w->g;
-    a.out = out;
+    a.out = static_cast<bf16*>(out);
     a.stats = w->stats;
     a.ready = w->counters;
     a.sync = a.ready + fused_phase_count(h->L, c.n_encoder_layers, c.final_norm != 0);
@@ -420,13 +425,17 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, bf16* out, cudaStr
     o.w2 = lw.wdown;
     o.x = w->tm_g_dn;
     o.x_box_rows = w->p_dn.nt;
-    o.y = (li == h->L - 1 && !w->packed) ? out : w->x;
+    const bool last = li == h->L - 1;
+    o.y = (last && !w->packed) ? static_cast<bf16*>(out) : w->x;
     o.residual = w->x;
+    if (last && c.out_fp32)
+      o.y_f32 = w->packed ? reinterpret_cast<float*>(w->qkv) : static_cast<float*>(out);
     LAYA_LAUNCH(LAYA_PROF_DOWN, launch_gemm(w->p_dn, o, l));
   }
   if (w->packed)
     LAYA_LAUNCH(LAYA_PROF_EMBED_NORM,
-                launch_unpack_rows(w->x, w->lens, w->B, w->S, H, out, l));
+                launch_unpack_rows(c.out_fp32 ? static_cast<const void*>(w->qkv) : w->x, w->lens,
+                                   w->B, w->S, H * (c.out_fp32 ? 4 : 2), out, l));
 #undef LAYA_LAUNCH
   return cudaSuccess;
 }
@@ -513,14 +522,14 @@ int run_common(laya_enc_handle* h, Workspace* w, void* out, cudaStream_t stream)
   // the fused kernel (a cooperative launch) runs eagerly, never inside a capture
   w->fused_now = h->fused && w->fused_ok && cap == cudaStreamCaptureStatusNone;
   if (!h->graphs || h->profiling || cap != cudaStreamCaptureStatusNone || w->fused_now) {
-    e = enqueue_forward(h, w, static_cast<bf16*>(out), stream);
+    e = enqueue_forward(h, w, out, stream);
     if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");
   } else {
     if (w->exec == nullptr || w->graph_out != out) {
       if (w->exec == nullptr) {
         // two eager warm-up passes before the first capture of a shape
         for (int i = 0; i < 2; ++i) {
-          e = enqueue_forward(h, w, static_cast<bf16*>(out), stream);
+          e = enqueue_forward(h, w, out, stream);
           if (e != cudaSuccess) return cuda_fail(h, e, "warm-up launch");
         }
       }
@@ -529,7 +538,7 @@ int run_common(laya_enc_handle* h, Workspace* w, void* out, cudaStream_t stream)
       cudaGraph_t graph = nullptr;
       e = cudaStreamBeginCapture(h->capture_stream, cudaStreamCaptureModeThreadLocal);
       if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamBeginCapture");
-      cudaError_t el = enqueue_forward(h, w, static_cast<bf16*>(out), h->capture_stream);
+      cudaError_t el = enqueue_forward(h, w, out, h->capture_stream);
       e = cudaStreamEndCapture(h->capture_stream, &graph);
       if (el != cudaSuccess) {
         if (graph) cudaGraphDestroy(graph);
@@ -596,7 +605,7 @@ int laya_enc_validate_config(const laya_enc_config* c) {
   if (c->max_batch < 1 || c->max_batch > 16 || c->max_seq < 1 || c->max_seq > 512)
     return LAYA_E_INVAL;
   if ((c->rope_table_bf16 | 1) != 1 || (c->first_attn_norm_identity | 1) != 1 ||
-      (c->final_norm | 1) != 1)
+      (c->final_norm | 1) != 1 || (c->out_fp32 | 1) != 1)
     return LAYA_E_INVAL;
   return LAYA_OK;
 }

@@ -75,6 +75,7 @@ struct GemmArgs {
   uint32_t ctrl_offset;  // bytes from the aligned smem base to barriers
   bf16* y;
   const bf16* residual;
+  float* y_f32;  // residual kind: if set, the fp32 sums are stored here instead of y
   int* err;
   float* partials;  // split-K workspace: [tile][split][half][nt][kBM] fp32
   // RoPE in the epilogue (plain kind): output features below rope_cols are
@@ -213,6 +214,24 @@ __device__ __forceinline__ void rope_apply_store16(const GemmArgs& a, int t, int
 __device__ __forceinline__ void rope_store16(const GemmArgs& a, int t, int f1, const float (&v1)[8],
                                              const float (&v2)[8]) {
   rope_apply_store16(a, t, f1, rope_row(a, t, f1 & 31), v1, v2);
+}
+
+// Eight consecutive output features of token t: one BF16 rounding each into
+// y, or (residual kind with y_f32 set) the fp32 values themselves.
+template <int KIND>
+__device__ __forceinline__ void store8(const GemmArgs& a, int t, int f, const float (&o)[8]) {
+  const size_t e = static_cast<size_t>(t) * a.N + f;
+  if (KIND == kGemmResidual && a.y_f32 != nullptr) {
+    float4* d = reinterpret_cast<float4*>(a.y_f32 + e);
+    d[0] = make_float4(o[0], o[1], o[2], o[3]);
+    d[1] = make_float4(o[4], o[5], o[6], o[7]);
+    return;
+  }
+  uint4 packed;
+  __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&packed);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) p2[i] = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+  *reinterpret_cast<uint4*>(a.y + e) = packed;
 }
 
 // mean and rstd of row t of ln_x (K = 256 * V values), one warp.
@@ -555,11 +574,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
           for (int i = 0; i < 8; ++i) o[i] = v[b][i];
         }
-        uint4 packed;
-        __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&packed);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) p2[i] = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
-        *reinterpret_cast<uint4*>(a.y + static_cast<size_t>(tok[b]) * a.N + fea[b]) = packed;
+        store8<KIND>(a, tok[b], fea[b], o);
       }
     }
   }
@@ -855,11 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int i = 0; i < 8; ++i) o[i] = v[bb][i];
             }
-            uint4 packed;
-            __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&packed);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) p2[i] = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
-            *reinterpret_cast<uint4*>(a.y + static_cast<size_t>(tok[bb]) * a.N + fea[bb]) = packed;
+            store8<KIND>(a, tok[bb], fea[bb], o);
           }
         }
       }
@@ -908,6 +919,7 @@ cudaError_t launch_kind(const GemmPlan& p, const GemmOperands& o, Launch l) {
   a.ctrl_offset = static_cast<uint32_t>(data);
   a.y = o.y;
   a.residual = o.residual;
+  a.y_f32 = KIND == kGemmResidual ? o.y_f32 : nullptr;
   a.err = o.err;
   a.partials = o.partials;
   a.rope_cos = o.rope_cos;

@@ -47,9 +47,10 @@ cudaError_t launch_embed_layernorm(const bf16* emb, const bf16* gamma, const int
                                    const Packing& pk = Packing());
 cudaError_t launch_layernorm(const bf16* x, const bf16* gamma, int M, int H, float eps, bf16* y,
                              Launch l, const Packing& pk = Packing());
-// out [B*S, H] (padded) from packed rows x.
-cudaError_t launch_unpack_rows(const bf16* x, const int32_t* lens, int B, int S, int H, bf16* out,
-                               Launch l);
+// out [B*S rows of row_bytes] (padded) from packed rows x; row_bytes a
+// multiple of 16.
+cudaError_t launch_unpack_rows(const void* x, const int32_t* lens, int B, int S, int row_bytes,
+                               void* out, Launch l);
 cudaError_t launch_rope(bf16* qkv, const float* cos_t, const float* sin_t, int B, int S,
                         int heads, Launch l);
 bool rowops_supported_hidden(int H);
@@ -103,6 +104,7 @@ struct GemmOperands {
   int x_box_rows = 0;  // the box height x was encoded with; launch_gemm checks it
   bf16* y = nullptr;   // output [M, N]
   const bf16* residual = nullptr;
+  float* y_f32 = nullptr;  // residual kind: fp32 output [M, N] in place of y (16-byte aligned)
   int* err = nullptr;
   float* partials = nullptr;   // split-K workspace (plan.workspace_bytes, 16-byte aligned)
   size_t partials_bytes = 0;

@@ -128,21 +128,21 @@ __global__ void __launch_bounds__(256) rope_kernel(bf16* qkv, const float* __res
 }
 
 // Padded output from packed rows: out[b * S + s] = x[cu(b) + s] for s < len(b),
-// 0 for the padding.  One warp per padded row, 16-byte copies.
-__global__ void __launch_bounds__(128) unpack_rows_kernel(const bf16* __restrict__ x,
+// 0 for the padding.  Rows of `chunks` 16-byte units (BF16 or fp32 values);
+// one warp per padded row, 16-byte copies.
+__global__ void __launch_bounds__(128) unpack_rows_kernel(const uint4* __restrict__ x,
                                                           const int32_t* __restrict__ lens, int B,
-                                                          int S, int H, bf16* __restrict__ out) {
+                                                          int S, int chunks,
+                                                          uint4* __restrict__ out) {
   ptx::grid_launch_dependents();
   ptx::grid_dependency_wait();
   const int row = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= B * S) return;
   const int b = row / S, s = row - b * S;
-  uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(row) * H);
-  const int chunks = H / 8;
+  uint4* dst = out + static_cast<size_t>(row) * chunks;
   if (s < packed_len(lens, b, S)) {
-    const uint4* src =
-        reinterpret_cast<const uint4*>(x + static_cast<size_t>(packed_start(lens, b, S) + s) * H);
+    const uint4* src = x + static_cast<size_t>(packed_start(lens, b, S) + s) * chunks;
     for (int c = lane; c < chunks; c += 32) dst[c] = src[c];
   } else {
     for (int c = lane; c < chunks; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
@@ -225,12 +225,14 @@ cudaError_t launch_layernorm(const bf16* x, const bf16* gamma, int M, int H, flo
   return launch_ln(x, gamma, M, H, eps, y, nullptr, 0, nullptr, pk, l);
 }
 
-cudaError_t launch_unpack_rows(const bf16* x, const int32_t* lens, int B, int S, int H, bf16* out,
-                               Launch l) {
-  if (B <= 0 || S <= 0 || lens == nullptr || H % 8 != 0) return cudaErrorInvalidValue;
+cudaError_t launch_unpack_rows(const void* x, const int32_t* lens, int B, int S, int row_bytes,
+                               void* out, Launch l) {
+  if (B <= 0 || S <= 0 || lens == nullptr || row_bytes <= 0 || row_bytes % 16 != 0)
+    return cudaErrorInvalidValue;
   const int rows_per_block = 4;
+  const int chunks = row_bytes / 16;
   dim3 grid((B * S + rows_per_block - 1) / rows_per_block), block(32 * rows_per_block);
-  void* args[] = {(void*)&x, (void*)&lens, (void*)&B, (void*)&S, (void*)&H, (void*)&out};
+  void* args[] = {(void*)&x, (void*)&lens, (void*)&B, (void*)&S, (void*)&chunks, (void*)&out};
   return launch_cfg(reinterpret_cast<const void*>(&unpack_rows_kernel), grid, block, 0, l, args);
 }
 
