@@ -166,6 +166,31 @@ int laya_enc_set_graphs(laya_enc_handle* h, int enabled);
  * bound). */
 int laya_enc_set_fused(laya_enc_handle* h, int enabled);
 
+/* The per-shape workspace and CUDA Graph cache ("[RFC]: Native Laya inference
+ * with Rust and CUDA #14", "Design": capture per shape, replay, an LRU of at
+ * most four shapes and 512 MiB of workspaces).  The first run of a shape
+ * allocates its workspace (evicting least-recently-used shapes until both
+ * bounds hold, after waiting for their last forward), runs two eager warm-up
+ * passes and captures a graph.  A later run of a captured shape with a
+ * different out_hidden re-points the graph's last launch (the one writing
+ * out_hidden) instead of capturing again.  Counters since create; times are
+ * host wall-clock. */
+typedef struct {
+  int32_t shapes;       /* workspaces resident now (<= max_shapes) */
+  int32_t max_shapes;   /* 4 */
+  uint64_t bytes;       /* device bytes they hold (<= max_bytes) */
+  uint64_t max_bytes;   /* 512 MiB */
+  uint64_t created;     /* workspaces allocated */
+  uint64_t evicted;     /* workspaces freed to make room */
+  uint64_t captures;    /* graphs captured and instantiated */
+  uint64_t retargets;   /* graphs re-pointed at a new out_hidden */
+  double setup_ms;      /* time spent creating workspaces */
+  double capture_ms;    /* time spent in first-run warm-ups, captures and
+                           instantiations */
+} laya_enc_cache_stats;
+
+int laya_enc_get_cache_stats(const laya_enc_handle* h, laya_enc_cache_stats* out);
+
 /* Number of kernel launches one forward pass of this shape makes. */
 int laya_enc_launch_count(const laya_enc_handle* h, int batch, int seq);
 

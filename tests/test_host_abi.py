@@ -2,6 +2,7 @@
 loads and exports every symbol the headers declare, configurations are
 validated, the library's RoPE table equals the oracle's bit for bit, and the
 GEMM planner keeps its invariants."""
+import ctypes
 import glob
 import os
 import re
@@ -38,6 +39,12 @@ def test_every_declared_symbol_is_exported(lib):
     for n in names:
         assert hasattr(lib, n), n
         assert n in te._SIGNATURES, f"binding lacks {n}"
+
+
+def test_cache_stats_rejects_null_handle(lib):
+    st = te.CacheStats()
+    assert lib.laya_enc_get_cache_stats(None, ctypes.byref(st)) == te.E_INVAL
+    assert ctypes.sizeof(te.CacheStats) == 2 * 4 + 6 * 8 + 2 * 8
 
 
 def test_abi_version(lib):

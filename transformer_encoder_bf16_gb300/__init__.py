@@ -53,6 +53,13 @@ class Config(ctypes.Structure):
         return c
 
 
+class CacheStats(ctypes.Structure):
+    _fields_ = [("shapes", ctypes.c_int32), ("max_shapes", ctypes.c_int32)] + [
+        (n, ctypes.c_uint64) for n in ("bytes", "max_bytes", "created", "evicted", "captures",
+                                       "retargets")] + [
+        ("setup_ms", ctypes.c_double), ("capture_ms", ctypes.c_double)]
+
+
 class LayerWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("attn_norm", "wqkv", "wo", "mlp_norm", "wup", "wdown")]
@@ -77,6 +84,7 @@ _SIGNATURES = {
     "laya_enc_check": ([_P, _P], _I),
     "laya_enc_set_graphs": ([_P, _I], _I),
     "laya_enc_set_fused": ([_P, _I], _I),
+    "laya_enc_get_cache_stats": ([_P, _P], _I),
     "laya_enc_launch_count": ([_P, _I, _I], _I),
     "laya_enc_workspace_bytes": ([_P, _I, _I, ctypes.POINTER(_SZ)], _I),
     "laya_enc_set_profiling": ([_P, _I], _I),
@@ -220,6 +228,12 @@ class Encoder:
         cnt = (ctypes.c_int * n)()
         _check(lib().laya_enc_profile_read(self.handle, ms, cnt, n), self.handle)
         return {PROFILE_CLASSES[i]: (ms[i], cnt[i]) for i in range(n)}
+
+    def cache_stats(self) -> dict:
+        """The workspace / graph cache counters (laya_enc_get_cache_stats)."""
+        st = CacheStats()
+        _check(lib().laya_enc_get_cache_stats(self.handle, ctypes.byref(st)), self.handle)
+        return {name: getattr(st, name) for name, _ in CacheStats._fields_}
 
     def launch_count(self, B, S) -> int:
         return lib().laya_enc_launch_count(self.handle, B, S)

@@ -26,6 +26,7 @@
 // order and layer-0 identity norm are readings of pages that do not write the
 // layer equations out; the CPU oracle states the same readings.
 #include <algorithm>
+#include <chrono>
 #include <cstdlib>
 #include <cstring>
 #include <new>
@@ -80,6 +81,8 @@ struct Workspace {
   float* stats = nullptr;
   uint32_t* counters = nullptr;
   cudaGraphExec_t exec = nullptr;
+  cudaGraph_t graph = nullptr;         // the template exec was instantiated from
+  cudaGraphNode_t out_node = nullptr;  // its last launch, the one writing the output
   void* graph_out = nullptr;
   uint64_t last_use = 0;
 };
@@ -101,6 +104,7 @@ struct laya_enc_handle {
   cudaStream_t capture_stream = nullptr;
   std::vector<laya::Workspace*> cache;
   uint64_t tick = 0;
+  laya_enc_cache_stats stats = {};  // counters of the workspace / graph cache
   bool graphs = true;
   bool pdl = true;
   bool fused = false;
@@ -147,6 +151,7 @@ void free_workspace(Workspace* w) {
   if (!w) return;
   if (w->done) cudaEventSynchronize(w->done);
   if (w->exec) cudaGraphExecDestroy(w->exec);
+  if (w->graph) cudaGraphDestroy(w->graph);
   if (w->staged) cudaEventDestroy(w->staged);
   if (w->done) cudaEventDestroy(w->done);
   if (w->host) cudaFreeHost(w->host);
@@ -448,6 +453,7 @@ int get_workspace(laya_enc_handle* h, int B, int S, Workspace** out) {
       return LAYA_OK;
     }
   }
+  const auto t_setup = std::chrono::steady_clock::now();
   Workspace* w = new (std::nothrow) Workspace();
   if (!w) return fail(h, LAYA_E_NOMEM, "workspace: host allocation failed");
   size_t bytes = 0;
@@ -467,6 +473,7 @@ int get_workspace(laya_enc_handle* h, int B, int S, Workspace** out) {
                                [](Workspace* a, Workspace* b) { return a->last_use < b->last_use; });
     free_workspace(*it);
     h->cache.erase(it);
+    ++h->stats.evicted;
   }
   cudaError_t e = cudaMalloc(&w->block, bytes);
   if (e != cudaSuccess) {
@@ -507,6 +514,9 @@ int get_workspace(laya_enc_handle* h, int B, int S, Workspace** out) {
   }
   w->last_use = ++h->tick;
   h->cache.push_back(w);
+  ++h->stats.created;
+  h->stats.setup_ms += std::chrono::duration<double, std::milli>(
+                           std::chrono::steady_clock::now() - t_setup).count();
   *out = w;
   return LAYA_OK;
 }
@@ -525,7 +535,21 @@ int run_common(laya_enc_handle* h, Workspace* w, void* out, cudaStream_t stream)
     e = enqueue_forward(h, w, out, stream);
     if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");
   } else {
+    // a new output buffer for a captured shape: repoint the launch that
+    // writes the output instead of capturing again
+    if (w->exec != nullptr && w->graph_out != out && w->out_node != nullptr) {
+      const cudaError_t er =
+          w->packed ? unpack_node_retarget(w->exec, w->out_node, w->graph_out, out)
+                    : gemm_node_retarget(w->exec, w->out_node, w->graph_out, out);
+      if (er == cudaSuccess) {
+        w->graph_out = out;
+        ++h->stats.retargets;
+      } else {
+        cudaGetLastError();  // not retargetable: capture again below
+      }
+    }
     if (w->exec == nullptr || w->graph_out != out) {
+      const auto t_cap = std::chrono::steady_clock::now();
       if (w->exec == nullptr) {
         // two eager warm-up passes before the first capture of a shape
         for (int i = 0; i < 2; ++i) {
@@ -539,6 +563,19 @@ int run_common(laya_enc_handle* h, Workspace* w, void* out, cudaStream_t stream)
       e = cudaStreamBeginCapture(h->capture_stream, cudaStreamCaptureModeThreadLocal);
       if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamBeginCapture");
       cudaError_t el = enqueue_forward(h, w, out, h->capture_stream);
+      // the capture's single open dependency is the last launch: the output writer
+      cudaGraphNode_t sink = nullptr;
+      if (el == cudaSuccess) {
+        cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+        const cudaGraphNode_t* deps = nullptr;
+        size_t nd = 0;
+        if (cudaStreamGetCaptureInfo(h->capture_stream, &st, nullptr, nullptr, &deps, nullptr,
+                                     &nd) == cudaSuccess &&
+            nd == 1)
+          sink = deps[0];
+        else
+          cudaGetLastError();
+      }
       e = cudaStreamEndCapture(h->capture_stream, &graph);
       if (el != cudaSuccess) {
         if (graph) cudaGraphDestroy(graph);
@@ -549,10 +586,22 @@ int run_common(laya_enc_handle* h, Workspace* w, void* out, cudaStream_t stream)
         cudaGraphExecDestroy(w->exec);
         w->exec = nullptr;
       }
+      if (w->graph) {
+        cudaGraphDestroy(w->graph);
+        w->graph = nullptr;
+        w->out_node = nullptr;
+      }
       e = cudaGraphInstantiate(&w->exec, graph, 0);
-      cudaGraphDestroy(graph);
-      if (e != cudaSuccess) return cuda_fail(h, e, "cudaGraphInstantiate");
+      if (e != cudaSuccess) {
+        cudaGraphDestroy(graph);
+        return cuda_fail(h, e, "cudaGraphInstantiate");
+      }
+      w->graph = graph;
+      w->out_node = sink;
       w->graph_out = out;
+      ++h->stats.captures;
+      h->stats.capture_ms += std::chrono::duration<double, std::milli>(
+                                 std::chrono::steady_clock::now() - t_cap).count();
     }
     e = cudaGraphLaunch(w->exec, stream);
     if (e != cudaSuccess) return cuda_fail(h, e, "cudaGraphLaunch");
@@ -790,6 +839,17 @@ int laya_enc_check(laya_enc_handle* h, void* stream) {
 int laya_enc_set_graphs(laya_enc_handle* h, int enabled) {
   if (!h) return LAYA_E_INVAL;
   h->graphs = enabled != 0;
+  return LAYA_OK;
+}
+
+int laya_enc_get_cache_stats(const laya_enc_handle* h, laya_enc_cache_stats* out) {
+  if (!h || !out) return LAYA_E_INVAL;
+  *out = h->stats;
+  out->shapes = static_cast<int32_t>(h->cache.size());
+  out->max_shapes = laya::kMaxShapes;
+  out->bytes = 0;
+  for (const laya::Workspace* w : h->cache) out->bytes += w->bytes;
+  out->max_bytes = laya::kMaxWorkspaceBytes;
   return LAYA_OK;
 }
 

@@ -1191,4 +1191,33 @@ cudaError_t launch_gemm(const GemmPlan& p, const GemmOperands& o, Launch l) {
   }
 }
 
+cudaError_t gemm_node_retarget(cudaGraphExec_t exec, cudaGraphNode_t node, const void* old_y,
+                               void* new_y) {
+  cudaKernelNodeParams p = {};
+  cudaError_t e = cudaGraphKernelNodeGetParams(node, &p);
+  if (e != cudaSuccess) return e;
+  const void* split = reinterpret_cast<const void*>(&gemm_tc_kernel<kGemmResidual>);
+  const void* pers = reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmResidual>);
+  if ((p.func != split && p.func != pers) || p.kernelParams == nullptr)
+    return cudaErrorInvalidValue;
+  // arguments: weight map, gate map, activation map, GemmArgs
+  GemmArgs a = *static_cast<const GemmArgs*>(p.kernelParams[3]);
+  bool hit = false;
+  if (a.y == old_y) {
+    a.y = static_cast<bf16*>(new_y);
+    hit = true;
+  }
+  if (a.y_f32 != nullptr && a.y_f32 == old_y) {
+    a.y_f32 = static_cast<float*>(new_y);
+    hit = true;
+  }
+  if (!hit) return cudaErrorInvalidValue;
+  void* args[4] = {p.kernelParams[0], p.kernelParams[1], p.kernelParams[2], &a};
+  p.kernelParams = args;
+  p.extra = nullptr;
+  e = cudaGraphExecKernelNodeSetParams(exec, node, &p);
+  if (e == cudaSuccess) e = cudaGraphKernelNodeSetParams(node, &p);  // keep the template in step
+  return e;
+}
+
 }  // namespace laya

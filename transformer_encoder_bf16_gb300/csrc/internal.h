@@ -127,6 +127,16 @@ struct GemmOperands {
 
 cudaError_t launch_gemm(const GemmPlan& p, const GemmOperands& o, Launch l);
 
+// Graph nodes that write the forward's output: point the captured launch
+// (a residual GEMM, or the unpack of packed rows) at new output memory in
+// the instantiated graph and its template, in place of old output memory.
+// cudaErrorInvalidValue if the node is not such a launch or does not write
+// old output memory; the graph is then unchanged.
+cudaError_t gemm_node_retarget(cudaGraphExec_t exec, cudaGraphNode_t node, const void* old_y,
+                               void* new_y);
+cudaError_t unpack_node_retarget(cudaGraphExec_t exec, cudaGraphNode_t node, const void* old_out,
+                                 void* new_out);
+
 // ------------------------------------------------ fused short forward ---
 // The whole forward of a request of at most 128 tokens as one persistent,
 // cooperatively launched kernel (fused.cu).

@@ -236,6 +236,24 @@ cudaError_t launch_unpack_rows(const void* x, const int32_t* lens, int B, int S,
   return launch_cfg(reinterpret_cast<const void*>(&unpack_rows_kernel), grid, block, 0, l, args);
 }
 
+cudaError_t unpack_node_retarget(cudaGraphExec_t exec, cudaGraphNode_t node, const void* old_out,
+                                 void* new_out) {
+  cudaKernelNodeParams p = {};
+  cudaError_t e = cudaGraphKernelNodeGetParams(node, &p);
+  if (e != cudaSuccess) return e;
+  if (p.func != reinterpret_cast<const void*>(&unpack_rows_kernel) || p.kernelParams == nullptr)
+    return cudaErrorInvalidValue;
+  // arguments: x, lens, B, S, chunks, out
+  if (*static_cast<void* const*>(p.kernelParams[5]) != old_out) return cudaErrorInvalidValue;
+  void* args[6] = {p.kernelParams[0], p.kernelParams[1], p.kernelParams[2],
+                   p.kernelParams[3], p.kernelParams[4], &new_out};
+  p.kernelParams = args;
+  p.extra = nullptr;
+  e = cudaGraphExecKernelNodeSetParams(exec, node, &p);
+  if (e == cudaSuccess) e = cudaGraphKernelNodeSetParams(node, &p);  // keep the template in step
+  return e;
+}
+
 cudaError_t launch_rope(bf16* qkv, const float* cos_t, const float* sin_t, int B, int S,
                         int heads, Launch l) {
   const int M = B * S;
