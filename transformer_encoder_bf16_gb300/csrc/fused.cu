@@ -160,13 +160,6 @@ __device__ __forceinline__ void cluster_arrive_wait() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
-// Orders this thread's earlier (acquired) view of global memory before its
-// later async-proxy reads of it (TMA and bulk copies of data that other CTAs
-// wrote with ordinary stores).
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
 __device__ __forceinline__ void sts32f(uint32_t addr, float v) {
   asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
@@ -820,7 +813,7 @@ __device__ void role_loader(const FusedArgs& a, const Ctl& c, uint32_t sbase, ui
     // inputs of this phase: every CTA done with the previous phase
     if (ltid == 0) {
       const bool ok = wait_count(a, c, a.ready + (ph.idx - 1), gen * gridDim.x, kFErrPhase);
-      fence_proxy_async_global();
+      ptx::fence_proxy_async_global();
       *phase_ok = ok ? 1 : 0;
     }
     ptx::named_barrier_sync(2, 64);
@@ -960,7 +953,7 @@ __device__ void role_epilogue(const FusedArgs& a, const Ctl& c, uint32_t sbase, 
       // this phase) and the attention area
       const uint32_t sQ = sbase + kOffA, sK = sbase + kOffAttn, sV = sK + 16384u;
       const int S = a.S, H = a.H;
-      if (etid == 0) fence_proxy_async_global();  // qkv was written by other CTAs
+      if (etid == 0) ptx::fence_proxy_async_global();  // qkv was written by other CTAs
       for (int u = blockIdx.x; u < a.B * a.heads; u += G) {
         const int b = u / a.heads, n = u % a.heads;
         int len = a.lens[b];

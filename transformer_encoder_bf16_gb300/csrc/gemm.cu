@@ -119,6 +119,18 @@ __device__ __forceinline__ float gelu_erf(float z) {
   return (0.5f * z) * (1.0f + erff(z * 0.70710678118654752f));
 }
 
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+  return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+
+// gelu(a) * g over four values, out of line: the split-K epilogue runs once
+// per launch with a cold instruction cache, so it keeps one copy of the erf
+// code instead of one per unrolled element.
+__device__ __noinline__ float4 geglu4(float4 a, float4 g) {
+  return make_float4(gelu_erf(a.x) * g.x, gelu_erf(a.y) * g.y, gelu_erf(a.z) * g.z,
+                     gelu_erf(a.w) * g.w);
+}
+
 __device__ __forceinline__ void load8_smem(const float* p, float (&v)[8]) {
   const float4 lo = reinterpret_cast<const float4*>(p)[0];
   const float4 hi = reinterpret_cast<const float4*>(p)[1];
@@ -126,53 +138,31 @@ __device__ __forceinline__ void load8_smem(const float* p, float (&v)[8]) {
   v[4] = hi.x; v[5] = hi.y; v[6] = hi.z; v[7] = hi.w;
 }
 
-// Sums, in split order, of the 8 consecutive fp32 values at float offset off
-// (and, for TWO, at off2) of every split's partial tile; `base` is the first
-// split's tile and `stride` the distance between splits, in floats.  All
-// loads are issued before the first add; .cg loads read L2 (the partials were
-// written by other SMs of the cluster).
-template <bool TWO>
-__device__ __forceinline__ void split_sum8(const float* base, size_t stride, int splits,
-                                           uint32_t off, uint32_t off2, float (&v)[8],
-                                           float (&w)[8]) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = w[i] = 0.f;
-  // groups of four splits: the loads of a group are in flight together, and
-  // the sum still runs in split order (0, 1, 2, ...)
-#pragma unroll
-  for (int s0 = 0; s0 < kMaxSplits; s0 += 4) {
-    if (s0 >= splits) break;
-    float4 t[4][2], u[4][2];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (s0 + j < splits) {
-        const float4* p = reinterpret_cast<const float4*>(base + (s0 + j) * stride + off);
-        t[j][0] = __ldcg(p);
-        t[j][1] = __ldcg(p + 1);
-        if (TWO) {
-          const float4* q = reinterpret_cast<const float4*>(base + (s0 + j) * stride + off2);
-          u[j][0] = __ldcg(q);
-          u[j][1] = __ldcg(q + 1);
-        }
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (s0 + j < splits) {
-        const float a8[8] = {t[j][0].x, t[j][0].y, t[j][0].z, t[j][0].w,
-                             t[j][1].x, t[j][1].y, t[j][1].z, t[j][1].w};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] += a8[i];
-        if (TWO) {
-          const float b8[8] = {u[j][0].x, u[j][0].y, u[j][0].z, u[j][0].w,
-                               u[j][1].x, u[j][1].y, u[j][1].z, u[j][1].w};
-#pragma unroll
-          for (int i = 0; i < 8; ++i) w[i] += b8[i];
-        }
-      }
-    }
-  }
+// Split-K reduction slices.  The groups of a 128-feature tile (8 features
+// each; a RoPE tile pairs features fo..fo+7 with fo+32..fo+39 into groups of
+// 16, fo = 64 (p / 4) + 8 (p % 4) for pair group p) are divided among the
+// cluster's CTAs: rank r reduces groups [r ng / splits, (r + 1) ng / splits).
+// A CTA's partial tile is laid out slice by slice, so that the part of every
+// split's partial one rank reduces is one contiguous block:
+//   [slice r][half][token column c][feature of the slice],
+// a slice's features in group order (a RoPE slice: the low 8 features of each
+// of its pair groups, then the high 8 of each).
+// Slice r starts at float g0(r) * gw * halves * nt, gw the group width.
+__device__ __forceinline__ int slice_g0(int r, int ngroups, int splits) {
+  return r * ngroups / splits;
 }
+
+// Shared memory the split-K reduction needs: the widest rank's slice of every
+// split's partial (a RoPE tile's 16-wide groups bound the plain 8-wide ones).
+constexpr size_t split_reduce_bytes(int na, int nt, int splits) {
+  return static_cast<size_t>(splits) * na * nt * ((8 + splits - 1) / splits) * 16 * 4;
+}
+
+// The rank whose slice holds group g: the largest r with g0(r) <= g.
+__device__ __forceinline__ int slice_owner(int g, int ngroups, int splits) {
+  return ((g + 1) * splits - 1) / ngroups;
+}
+
 
 // The eight consecutive table entries (cos, sin) a RoPE unit of token t and
 // pair index i0 (a multiple of 8) needs: 32-byte aligned.
@@ -209,11 +199,6 @@ __device__ __forceinline__ void rope_apply_store16(const GemmArgs& a, int t, int
   bf16* row = a.y + static_cast<size_t>(t) * a.N;
   *reinterpret_cast<uint4*>(row + f1) = o1;
   *reinterpret_cast<uint4*>(row + f1 + 32) = o2;
-}
-
-__device__ __forceinline__ void rope_store16(const GemmArgs& a, int t, int f1, const float (&v1)[8],
-                                             const float (&v2)[8]) {
-  rope_apply_store16(a, t, f1, rope_row(a, t, f1 & 31), v1, v2);
 }
 
 // Eight consecutive output features of token t: one BF16 rounding each into
@@ -278,6 +263,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t xform0 = accum_bar + 8u;  // LayerNorm on load: stage normalised
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * a.stages + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t red_bar = full0 + 8u * (3 * a.stages + 2);  // split-K slices landed
   const bool ln = a.ln_x != nullptr;
 
   const int warp = threadIdx.x >> 5;
@@ -298,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       ptx::mbar_init(xform0 + 8u * i, kThreads - 64);
     }
     ptx::mbar_init(accum_bar, 1);
+    ptx::mbar_init(red_bar, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -316,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   ptx::grid_launch_dependents();
   const uint32_t tmem = *tmem_slot;
   bool epi_ok = false;
+  bool red_failed = false;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -398,11 +386,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    // LayerNorm input and residual are written by earlier kernels; waiting
+    // here, while the main loop runs, keeps the wait off the epilogue's path
+    ptx::grid_dependency_wait();
     if (ln) {
       // ---- LayerNorm on load: row statistics, then normalise each stage
       const int tid_e = threadIdx.x - 64;
       float* stats = reinterpret_cast<float*>(smem + a.ctrl_offset + kCtrlBytes);
-      ptx::grid_dependency_wait();  // ln_x written by the previous kernel
       for (int r = warp - 2; r < a.nt; r += 4) {
         const int t = t_tile * a.nt + r;
         float mean = 0.f, rstd = 0.f;
@@ -443,18 +433,32 @@ __global__ void __launch_bounds__(kThreads, 2)
     epi_ok = ptx::mbar_wait(accum_bar, 0, abort_flag, a.err, kDevWaitAccum, kWaitLimitNs);
     ptx::tc_fence_after();
     if (epi_ok && a.splits > 1) {
-      // partial tile to the workspace: part[(c * kBM) + row], GeGLU gate half after it
+      // partial tile to the workspace in slice layout (see slice_g0): this
+      // thread's feature row lands in its owner's slice
+      const bool rope_tile =
+          KIND == kGemmPlain && a.rope_cos != nullptr && f_tile * kBM < a.rope_cols;
+      const int gw = rope_tile ? 16 : 8;
+      const int ngroups = kBM / gw;
+      const int grp = rope_tile ? 4 * (row >> 6) + ((row & 31) >> 3) : row >> 3;
+      const int r = slice_owner(grp, ngroups, a.splits);
+      const int sg0 = slice_g0(r, ngroups, a.splits);
+      const int width = (slice_g0(r + 1, ngroups, a.splits) - sg0) * gw;
+      // feature of the slice: group-major; a RoPE slice holds the low 8 of
+      // each pair group first, then the high 8 (a warp's rows stay contiguous)
+      const int in_slice = rope_tile ? ((row & 32) ? width / 2 : 0) + (grp - sg0) * 8 + (row & 7)
+                                     : (grp - sg0) * 8 + (row & 7);
       const int tile = t_tile * gridDim.x + f_tile;
-      float* part = a.partials + (static_cast<size_t>(tile) * a.splits + split) * NA * a.nt * kBM;
+      float* part = a.partials + (static_cast<size_t>(tile) * a.splits + split) * NA * a.nt * kBM +
+                    static_cast<size_t>(sg0) * gw * NA * a.nt + in_slice;
       for (int c0 = 0; c0 < a.nt; c0 += 16) {
         float v[16];
         ptx::tmem_ld16(tq + c0, v);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) part[(c0 + j) * kBM + row] = v[j];
+        for (int j = 0; j < 16; ++j) part[(c0 + j) * width] = v[j];
         if (NA == 2) {
           ptx::tmem_ld16(tq + a.nt + c0, v);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) part[(a.nt + c0 + j) * kBM + row] = v[j];
+          for (int j = 0; j < 16; ++j) part[(a.nt + c0 + j) * width] = v[j];
         }
       }
     } else if (epi_ok) {
@@ -487,22 +491,43 @@ __global__ void __launch_bounds__(kThreads, 2)
     // Split-K: this CTA finishes the feature groups [g0, g1) of the tile,
     // summing the partials of every CTA of the cluster in rank order.
     const bool rope_tile = KIND == kGemmPlain && a.rope_cos != nullptr && f_tile * kBM < a.rope_cols;
-    const int ngroups = rope_tile ? kBM / 16 : kBM / 8;  // RoPE: pairs of groups (f, f + 32)
+    const int gw = rope_tile ? 16 : 8;
+    const int ngroups = kBM / gw;  // RoPE: pairs of groups (f, f + 32)
     int g0 = 0, g1 = ngroups;
-    const size_t pstride = static_cast<size_t>(NA) * a.nt * kBM;  // floats between splits
-    const float* pbase = nullptr;
+    const int tid_e = threadIdx.x - 64;
+    // split-K: this rank's slice of every split's partial, [split][half][c][width]
+    const float* red = reinterpret_cast<const float*>(smem);
+    int width = 0;
+    size_t sstride = 0;  // floats between splits in `red`
     if (a.splits > 1) {
-      const uint32_t rank = ptx::cluster_ctarank();
-      g0 = static_cast<int>(rank * ngroups / a.splits);
-      g1 = static_cast<int>((rank + 1) * ngroups / a.splits);
-      pbase = a.partials + static_cast<size_t>(t_tile * gridDim.x + f_tile) * a.splits * pstride;
+      const int rank = static_cast<int>(ptx::cluster_ctarank());
+      g0 = slice_g0(rank, ngroups, a.splits);
+      g1 = slice_g0(rank + 1, ngroups, a.splits);
+      width = (g1 - g0) * gw;
+      sstride = static_cast<size_t>(NA) * a.nt * width;
+      const uint32_t bytes = static_cast<uint32_t>(sstride * 4);
+      if (tid_e == 0) {
+        // the partials were written by the other CTAs of the cluster with
+        // ordinary stores (ordered before the cluster barrier above)
+        ptx::fence_proxy_async_global();
+        const size_t pstride = static_cast<size_t>(NA) * a.nt * kBM;  // floats between splits
+        const float* src = a.partials +
+                           static_cast<size_t>(t_tile * gridDim.x + f_tile) * a.splits * pstride +
+                           static_cast<size_t>(g0) * gw * NA * a.nt;
+        ptx::mbar_arrive_expect_tx(red_bar, bytes * static_cast<uint32_t>(a.splits));
+        for (int sp = 0; sp < a.splits; ++sp)
+          ptx::bulk_load(sbase + static_cast<uint32_t>(sp) * bytes, src + sp * pstride, bytes,
+                         red_bar);
+      }
     }
     const int ng = g1 - g0;
     const int units = ng * a.nt;
     const int t_base = t_tile * a.nt;
-    const int tid_e = threadIdx.x - 64;
     const float* stg = reinterpret_cast<const float*>(smem);
-    ptx::grid_dependency_wait();  // residual written by earlier kernels
+    if (a.splits > 1 &&
+        !ptx::mbar_wait(red_bar, 0, abort_flag, a.err, kDevWaitReduce, kWaitLimitNs))
+      red_failed = true;
+    if (!red_failed) {
     if (rope_tile) {
       // unit = token column c, pair group p: features (fo, fo + 32), fo = 64 (p / 4) + 8 (p % 4)
       for (int u = tid_e; u < units; u += kThreads - 64) {
@@ -510,19 +535,78 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int pg = g0 + u % ng;
         const int fo = 64 * (pg >> 2) + 8 * (pg & 3);
         const int t = t_base + c;
+        if (t >= Meff) continue;
+        const RopeRow rr = rope_row(a, t, fo & 31);  // in flight during the sums
         float v1[8], v2[8];
         if (a.splits > 1) {
-          const uint32_t off1 = static_cast<uint32_t>(c * kBM + fo);
-          split_sum8<true>(pbase, pstride, a.splits, off1, off1 + 32u, v1, v2);
+          // split order 0, 1, 2, ... from 0 (as every other path sums)
+          const float4* q = reinterpret_cast<const float4*>(red + c * width + (pg - g0) * 8);
+          const int h4 = width / 8;  // float4s from a low feature to its high partner
+          float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0, s2 = s0, s3 = s0;
+#pragma unroll 1
+          for (int sp = 0; sp < a.splits; ++sp, q += sstride / 4) {
+            s0 = add4(s0, q[0]);
+            s1 = add4(s1, q[1]);
+            s2 = add4(s2, q[h4]);
+            s3 = add4(s3, q[h4 + 1]);
+          }
+          v1[0] = s0.x; v1[1] = s0.y; v1[2] = s0.z; v1[3] = s0.w;
+          v1[4] = s1.x; v1[5] = s1.y; v1[6] = s1.z; v1[7] = s1.w;
+          v2[0] = s2.x; v2[1] = s2.y; v2[2] = s2.z; v2[3] = s2.w;
+          v2[4] = s3.x; v2[5] = s3.y; v2[6] = s3.z; v2[7] = s3.w;
         } else {
           load8_smem(stg + c * kSld + fo, v1);
           load8_smem(stg + c * kSld + fo + 32, v2);
         }
-        if (t < Meff) rope_store16(a, t, f_tile * kBM + fo, v1, v2);
+        rope_apply_store16(a, t, f_tile * kBM + fo, rr, v1, v2);
+      }
+    } else if (a.splits > 1) {
+      // split-K: one unit at a time in compact code (a unit's residual load
+      // is issued before its sums); at the short shapes that run split-K a
+      // thread has one or two units, and the code runs once per launch
+#pragma unroll 1
+      for (int u = tid_e; u < units; u += kThreads - 64) {
+        const int c = u / ng;
+        const int grp = g0 + u % ng;
+        const int t = t_base + c;
+        const int f = f_tile * kBM + grp * 8;
+        if (t >= Meff || f >= a.N) continue;
+        uint4 res = make_uint4(0u, 0u, 0u, 0u);
+        if (KIND == kGemmResidual)
+          res = *reinterpret_cast<const uint4*>(a.residual + static_cast<size_t>(t) * a.N + f);
+        // split order 0, 1, 2, ... from 0; the GeGLU gate half follows each
+        // split's first half
+        const float4* q = reinterpret_cast<const float4*>(red + c * width + (grp - g0) * 8);
+        const size_t hoff4 = static_cast<size_t>(a.nt) * width / 4;
+        float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo, glo = lo, ghi = lo;
+#pragma unroll 1
+        for (int sp = 0; sp < a.splits; ++sp, q += sstride / 4) {
+          lo = add4(lo, q[0]);
+          hi = add4(hi, q[1]);
+          if (NA == 2) {
+            glo = add4(glo, q[hoff4]);
+            ghi = add4(ghi, q[hoff4 + 1]);
+          }
+        }
+        if (NA == 2) {
+          lo = geglu4(lo, glo);
+          hi = geglu4(hi, ghi);
+        }
+        float o[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+        if (KIND == kGemmResidual) {
+          const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&res);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 rf = __bfloat1622float2(r2[i]);
+            o[2 * i] = rf.x + o[2 * i];
+            o[2 * i + 1] = rf.y + o[2 * i + 1];
+          }
+        }
+        store8<KIND>(a, t, f, o);
       }
     } else
     for (int u0 = tid_e; u0 < units; u0 += (kThreads - 64) * kEpiBatch) {
-      float v[kEpiBatch][8], gt[kEpiBatch][8];
+      float v[kEpiBatch][8];
       uint4 res[kEpiBatch];
       int tok[kEpiBatch], fea[kEpiBatch];
       // loads first (the output may alias the residual: keep every load of
@@ -534,15 +618,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (u < units) {
           const int c = u / ng;
           const int grp = g0 + u % ng;
-          if (a.splits > 1) {
-            const uint32_t off = static_cast<uint32_t>(c * kBM + grp * 8);
-            split_sum8<NA == 2>(pbase, pstride, a.splits, off, off + static_cast<uint32_t>(a.nt * kBM),
-                                v[b], gt[b]);
-            if (NA == 2) {
-#pragma unroll
-              for (int i = 0; i < 8; ++i) v[b][i] = gelu_erf(v[b][i]) * gt[b][i];
-            }
-          } else {
+          {
+            // one CTA per tile: the staged tile (GeGLU already applied)
             const float4* p4 = reinterpret_cast<const float4*>(stg + c * kSld + grp * 8);
             const float4 lo = p4[0], hi = p4[1];
             v[b][0] = lo.x; v[b][1] = lo.y; v[b][2] = lo.z; v[b][3] = lo.w;
@@ -575,6 +652,13 @@ __global__ void __launch_bounds__(kThreads, 2)
           for (int i = 0; i < 8; ++i) o[i] = v[b][i];
         }
         store8<KIND>(a, tok[b], fea[b], o);
+      }
+    }
+    }  // !red_failed
+    if (red_failed && a.splits > 1 && threadIdx.x == 64) {
+      // no bulk copy may still be landing in this CTA's shared memory at exit
+      const uint64_t t0 = ptx::globaltimer_ns();
+      while (!ptx::mbar_try_wait(red_bar, 0) && ptx::globaltimer_ns() - t0 < kWaitLimitNs) {
       }
     }
   }
@@ -912,8 +996,9 @@ cudaError_t launch_kind(const GemmPlan& p, const GemmOperands& o, Launch l) {
   size_t data = stage_bytes * p.stages;
   if (p.persistent) {
     data += kStagingBytes;
-  } else if (p.splits == 1) {
-    const size_t part = static_cast<size_t>(p.nt) * kSld * 4;
+  } else {
+    const size_t part = p.splits == 1 ? static_cast<size_t>(p.nt) * kSld * 4
+                                      : split_reduce_bytes(na, p.nt, p.splits);
     if (part > data) data = part;
   }
   a.ctrl_offset = static_cast<uint32_t>(data);
@@ -1060,8 +1145,10 @@ bool finish_plan(GemmPlan* r) {
   if (stages < 1) return false;
   r->stages = stages;
   size_t data = stage_bytes * stages;
-  // fp32 staging tile of the epilogue (split-K partials go to the workspace)
-  const size_t part = r->splits > 1 ? 0 : static_cast<size_t>(r->nt) * kSld * 4;
+  // fp32 staging tile of the epilogue, or (split-K) this rank's slices of the
+  // cluster's partials, both in the idle ring once the accumulator is ready
+  const size_t part = r->splits > 1 ? split_reduce_bytes(na, r->nt, r->splits)
+                                    : static_cast<size_t>(r->nt) * kSld * 4;
   if (part > budget) return false;
   if (part > data) data = part;
   r->workspace_bytes = r->splits > 1 ? static_cast<size_t>(r->feat_tiles) * r->token_tiles *

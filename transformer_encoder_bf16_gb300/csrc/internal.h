@@ -23,6 +23,7 @@ enum DeviceError : int {
   kDevWaitAccum = 3,    // GEMM: epilogue gave up waiting for the accumulator
   kDevBadId = 4,        // embedding: token id outside [0, vocab)
   kDevBadLength = 5,    // attention: row length outside [1, S]
+  kDevWaitReduce = 6,   // GEMM: epilogue gave up waiting for the split-K partial slices
 };
 
 // Upper bound on any device-side wait, in nanoseconds.

@@ -69,6 +69,25 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Orders this thread's (acquired) view of global memory before its later
+// async-proxy reads of it: bulk copies of data other CTAs wrote with ordinary
+// stores.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Untiled bulk copy of `bytes` from global memory into this CTA's shared
+// memory, completing on `bar` (both addresses 16-byte aligned, bytes a
+// multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // Make this thread's generic-proxy writes to shared memory visible to the
 // async proxy (TMA, tensor cores) before it signals them.
 __device__ __forceinline__ void fence_proxy_async_smem() {
