@@ -120,7 +120,6 @@ __global__ void __launch_bounds__(128, 4) attention_kernel(const bf16* __restric
   __shared__ __align__(128) bf16 sV[2][kKT * kLd];
 
   ptx::grid_launch_dependents();
-  ptx::grid_dependency_wait();
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q0 = blockIdx.x * kQ;
@@ -128,11 +127,12 @@ __global__ void __launch_bounds__(128, 4) attention_kernel(const bf16* __restric
   const int b = blockIdx.z;
   const int H = heads * 64;
   const size_t ld = static_cast<size_t>(3) * H;
-  int len = lengths[b];
-  if (len < 1 || len > S) {
-    if (tid == 0 && err != nullptr) atomicCAS(err, 0, kDevBadLength);
-    len = len < 1 ? 1 : S;
-  }
+  // The lengths are an input of the whole forward (uploaded before its first
+  // kernel), not an output of the previous kernel: everything up to the
+  // dependency wait below uses only them.
+  const int len_in = lengths[b];
+  const bool bad_len = len_in < 1 || len_in > S;
+  const int len = len_in < 1 ? 1 : (len_in > S ? S : len_in);
   // padded rows: row b starts at token b S and rows up to S exist (padding
   // tokens are read as keys, masked); packed rows (packing.cuh): row b starts
   // at cu(b) and only its len tokens are read or written (the next row
@@ -142,20 +142,7 @@ __global__ void __launch_bounds__(128, 4) attention_kernel(const bf16* __restric
   const int rows = packed ? len : S;
   const bf16* rowbase = qkv + r0 * ld;
   bf16* out = ctx + r0 * H + static_cast<size_t>(n) * 64;
-
-  if (q0 >= len) {
-    if (packed) return;  // no such tokens
-    // the whole tile is padding: defined zeros
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int c = tid + 128 * r;
-      const int row = c >> 3, ch = c & 7;
-      if (q0 + row < S)
-        *reinterpret_cast<uint4*>(out + static_cast<size_t>(q0 + row) * H + ch * 8) =
-            make_uint4(0, 0, 0, 0);
-    }
-    return;
-  }
+  const bool pad_tile = q0 >= len;
 
   int kbeg = 0, kend = len;
   if (!global) {
@@ -169,15 +156,38 @@ __global__ void __launch_bounds__(128, 4) attention_kernel(const bf16* __restric
   const uint32_t sq = ptx::smem_u32(sQ);
   const uint32_t sk0 = ptx::smem_u32(sK[0]), sk1 = ptx::smem_u32(sK[1]);
   const uint32_t sv0 = ptx::smem_u32(sV[0]), sv1 = ptx::smem_u32(sV[1]);
-
-  load_tile(sq, rowbase + n * 64, q0, rows, ld, tid);
-  load_tile(sk0, rowbase + H + n * 64, kt0 * kKT, rows, ld, tid);
-  load_tile(sv0, rowbase + 2 * H + n * 64, kt0 * kKT, rows, ld, tid);
-  cp_async_commit();
-
   const int g = lane >> 2, c4 = lane & 3;
   const float scale_log2 = 0.125f * 1.4426950408889634f;
   const int qi0 = q0 + warp * 16 + g;  // query of accumulator rows 0 (and +8)
+
+  // Pass 0 runs the tile computation once over whatever shared memory holds,
+  // stores nothing, and reads no output of earlier kernels: it executes,
+  // while the previous kernel finishes (programmatic dependent launch), the
+  // same instructions as the live pass 1, whose instruction fetches then hit.
+#pragma unroll 1
+  for (int pass = pad_tile ? 1 : 0; pass < 2; ++pass) {
+  const bool live = pass == 1;
+  if (live) {
+    ptx::grid_dependency_wait();
+    if (bad_len && tid == 0 && err != nullptr) atomicCAS(err, 0, kDevBadLength);
+    if (pad_tile) {
+      if (packed) return;  // no such tokens
+      // the whole tile is padding: defined zeros
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int c = tid + 128 * r;
+        const int row = c >> 3, ch = c & 7;
+        if (q0 + row < S)
+          *reinterpret_cast<uint4*>(out + static_cast<size_t>(q0 + row) * H + ch * 8) =
+              make_uint4(0, 0, 0, 0);
+      }
+      return;
+    }
+    load_tile(sq, rowbase + n * 64, q0, rows, ld, tid);
+    load_tile(sk0, rowbase + H + n * 64, kt0 * kKT, rows, ld, tid);
+    load_tile(sv0, rowbase + 2 * H + n * 64, kt0 * kKT, rows, ld, tid);
+    cp_async_commit();
+  }
 
   uint32_t qf[4][4];
   float o[8][4];
@@ -187,10 +197,12 @@ __global__ void __launch_bounds__(128, 4) attention_kernel(const bf16* __restric
     for (int e = 0; e < 4; ++e) o[j][e] = 0.f;
   float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
 
-  for (int kt = kt0; kt < kt1; ++kt) {
+  const int kt_end = live ? kt1 : kt0 + 1;
+  for (int kt = kt0; kt < kt_end; ++kt) {
     const int buf = (kt - kt0) & 1;
-    const bool prefetch = kt + 1 < kt1;
-    if (prefetch) {
+    const bool prefetch = kt + 1 < kt_end;
+    if (!live) {
+    } else if (prefetch) {
       load_tile(buf ? sk0 : sk1, rowbase + H + n * 64, (kt + 1) * kKT, rows, ld, tid);
       load_tile(buf ? sv0 : sv1, rowbase + 2 * H + n * 64, (kt + 1) * kKT, rows, ld, tid);
       cp_async_commit();
@@ -310,13 +322,14 @@ __global__ void __launch_bounds__(128, 4) attention_kernel(const bf16* __restric
 #pragma unroll
   for (int jd = 0; jd < 8; ++jd) {
     const int d = jd * 8 + 2 * c4;
-    if (qi0 < rows)
+    if (live && qi0 < rows)
       *reinterpret_cast<uint32_t*>(out + static_cast<size_t>(qi0) * H + d) =
           pack_bf16(o[jd][0] * inv0, o[jd][1] * inv0);
-    if (qi0 + 8 < rows)
+    if (live && qi0 + 8 < rows)
       *reinterpret_cast<uint32_t*>(out + static_cast<size_t>(qi0 + 8) * H + d) =
           pack_bf16(o[jd][2] * inv1, o[jd][3] * inv1);
   }
+  }  // pass
 }
 
 }  // namespace

@@ -164,16 +164,33 @@ __device__ __forceinline__ int slice_owner(int g, int ngroups, int splits) {
 }
 
 
+// What the epilogues write and read besides the accumulator (from GemmArgs).
+struct EpiOut {
+  bf16* y;
+  float* y_f32;
+  const bf16* residual;
+  int N;
+  const float* rope_cos;
+  const float* rope_sin;
+  int rope_S;
+  const int32_t* rope_pos;
+};
+
+__device__ __forceinline__ EpiOut epi_out(const GemmArgs& a) {
+  return EpiOut{a.y, a.y_f32, a.residual, a.N, a.rope_cos, a.rope_sin, a.rope_S, a.rope_pos};
+}
+
 // The eight consecutive table entries (cos, sin) a RoPE unit of token t and
-// pair index i0 (a multiple of 8) needs: 32-byte aligned.
+// pair index i0 (a multiple of 8) needs: 32-byte aligned.  padded: take the
+// position from the padded layout (t % rope_S) even for packed tokens.
 struct RopeRow {
   float4 c0, c1, s0, s1;
 };
 
-__device__ __forceinline__ RopeRow rope_row(const GemmArgs& a, int t, int i0) {
-  const int pos = a.rope_pos != nullptr ? a.rope_pos[t] : t % a.rope_S;
-  const float4* ct = reinterpret_cast<const float4*>(a.rope_cos + static_cast<size_t>(pos) * 32 + i0);
-  const float4* st = reinterpret_cast<const float4*>(a.rope_sin + static_cast<size_t>(pos) * 32 + i0);
+__device__ __forceinline__ RopeRow rope_row(const EpiOut& e, int t, int i0, bool padded = false) {
+  const int pos = (e.rope_pos != nullptr && !padded) ? e.rope_pos[t] : t % e.rope_S;
+  const float4* ct = reinterpret_cast<const float4*>(e.rope_cos + static_cast<size_t>(pos) * 32 + i0);
+  const float4* st = reinterpret_cast<const float4*>(e.rope_sin + static_cast<size_t>(pos) * 32 + i0);
   return RopeRow{__ldg(ct), __ldg(ct + 1), __ldg(st), __ldg(st + 1)};
 }
 
@@ -181,8 +198,9 @@ __device__ __forceinline__ RopeRow rope_row(const GemmArgs& a, int t, int i0) {
 // (x1, x2) = (feature i, feature i + 32) of a head exactly as the RoPE kernel
 // does: fp32 products and sum each rounded, one BF16 rounding of the result.
 // f1 is the output column of the first member of eight consecutive pairs.
-__device__ __forceinline__ void rope_apply_store16(const GemmArgs& a, int t, int f1, const RopeRow& r,
-                                                   const float (&v1)[8], const float (&v2)[8]) {
+__device__ __forceinline__ void rope_apply_store16(const EpiOut& a, int t, int f1, const RopeRow& r,
+                                                   const float (&v1)[8], const float (&v2)[8],
+                                                   bool live = true) {
   const float cv[8] = {r.c0.x, r.c0.y, r.c0.z, r.c0.w, r.c1.x, r.c1.y, r.c1.z, r.c1.w};
   const float sv[8] = {r.s0.x, r.s0.y, r.s0.z, r.s0.w, r.s1.x, r.s1.y, r.s1.z, r.s1.w};
   uint4 o1, o2;
@@ -196,6 +214,7 @@ __device__ __forceinline__ void rope_apply_store16(const GemmArgs& a, int t, int
     p1[i] = __float2bfloat16_rn(__fsub_rn(__fmul_rn(x1, c), __fmul_rn(x2, sn)));
     p2[i] = __float2bfloat16_rn(__fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, sn)));
   }
+  if (!live) return;
   bf16* row = a.y + static_cast<size_t>(t) * a.N;
   *reinterpret_cast<uint4*>(row + f1) = o1;
   *reinterpret_cast<uint4*>(row + f1 + 32) = o2;
@@ -204,7 +223,7 @@ __device__ __forceinline__ void rope_apply_store16(const GemmArgs& a, int t, int
 // Eight consecutive output features of token t: one BF16 rounding each into
 // y, or (residual kind with y_f32 set) the fp32 values themselves.
 template <int KIND>
-__device__ __forceinline__ void store8(const GemmArgs& a, int t, int f, const float (&o)[8]) {
+__device__ __forceinline__ void store8(const EpiOut& a, int t, int f, const float (&o)[8]) {
   const size_t e = static_cast<size_t>(t) * a.N + f;
   if (KIND == kGemmResidual && a.y_f32 != nullptr) {
     float4* d = reinterpret_cast<float4*>(a.y_f32 + e);
@@ -238,6 +257,121 @@ __device__ __forceinline__ void ln_row_any(const GemmArgs& a, int t, int lane, f
     case 6: ln_row<6>(a, t, lane, mean, rstd); break;
     case 7: ln_row<7>(a, t, lane, mean, rstd); break;
     default: ln_row<8>(a, t, lane, mean, rstd); break;
+  }
+}
+
+// Split-K epilogue, step 1: this thread's feature row of the fp32 partial
+// (GeGLU: both halves) from TMEM into its slice of the workspace, `width`
+// floats between token columns.
+//
+// Steps 1 and 2 run once per launch at the short shapes that use split-K, a
+// few microseconds after the instruction cache last held them.  They are out
+// of line so that a dry call (live = false) made while the main loop runs
+// executes the very instructions of the live call and brings them into the
+// instruction cache: a dry call reads TMEM before the accumulator is there,
+// sends its stores to the scratch words `dry` (shared memory nothing else
+// uses then) and reads no output of earlier kernels.
+template <int NA>
+__device__ __noinline__ void split_drain(uint32_t tq, float* part, int width, int nt, float* dry,
+                                         bool live) {
+  float* dst = live ? part : dry;
+  const int w = live ? width : 0;
+#pragma unroll 1
+  for (int c0 = 0; c0 < nt; c0 += 16) {
+    float v[16];
+    ptx::tmem_ld16(tq + c0, v);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) dst[(c0 + j) * w] = v[j];
+    if (NA == 2) {
+      ptx::tmem_ld16(tq + nt + c0, v);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) dst[(nt + c0 + j) * w] = v[j];
+    }
+  }
+}
+
+// Split-K epilogue, step 2: the units of this rank's slice (8 features of one
+// token; a RoPE tile: 8 pairs), summed over the splits in split order from 0
+// out of `red` ([split][half][token column][width], sstride floats between
+// splits), then the kind's epilogue and the store.  A dry call (see
+// split_drain) reads the residual and the RoPE table at padded-layout
+// positions and stores into `dry` (512 bytes) with a zero row stride.
+template <int KIND, int NA>
+__device__ __noinline__ void split_epilogue(EpiOut eo, const float* red, int width, int sstride,
+                                            int splits, int nt, int g0, int ng, int units,
+                                            int t_base, int Meff, int f_base, bool rope_tile,
+                                            int tid_e, float* dry, bool live) {
+  const int N = eo.N;  // row stride of the residual and the output
+  if (!live) {
+    // stores land in `dry`: row stride 0, columns within the tile
+    eo.y = reinterpret_cast<bf16*>(dry);
+    if (eo.y_f32 != nullptr) eo.y_f32 = dry;
+    eo.N = 0;
+  }
+  if (KIND == kGemmPlain && rope_tile) {
+    // unit = token column c, pair group p: features (fo, fo + 32), fo = 64 (p / 4) + 8 (p % 4)
+#pragma unroll 1
+    for (int u = tid_e; u < units; u += kThreads - 64) {
+      const int c = u / ng;
+      const int pg = g0 + u % ng;
+      const int fo = 64 * (pg >> 2) + 8 * (pg & 3);
+      const int t = t_base + c;
+      if (t >= Meff) continue;
+      const RopeRow rr = rope_row(eo, t, fo & 31, !live);  // in flight during the sums
+      const float4* q = reinterpret_cast<const float4*>(red + c * width + (pg - g0) * 8);
+      const int h4 = width / 8;  // float4s from a low feature to its high partner
+      float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0, s2 = s0, s3 = s0;
+#pragma unroll 1
+      for (int sp = 0; sp < splits; ++sp, q += sstride / 4) {
+        s0 = add4(s0, q[0]);
+        s1 = add4(s1, q[1]);
+        s2 = add4(s2, q[h4]);
+        s3 = add4(s3, q[h4 + 1]);
+      }
+      const float v1[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+      const float v2[8] = {s2.x, s2.y, s2.z, s2.w, s3.x, s3.y, s3.z, s3.w};
+      rope_apply_store16(eo, live ? t : 0, (live ? f_base : 0) + fo, rr, v1, v2);
+    }
+    return;
+  }
+#pragma unroll 1
+  for (int u = tid_e; u < units; u += kThreads - 64) {
+    const int c = u / ng;
+    const int grp = g0 + u % ng;
+    const int t = t_base + c;
+    const int f = f_base + grp * 8;
+    if (t >= Meff || f >= N) continue;
+    uint4 res = make_uint4(0u, 0u, 0u, 0u);
+    if (KIND == kGemmResidual)  // issued before the sums
+      res = *reinterpret_cast<const uint4*>(eo.residual + static_cast<size_t>(t) * N + f);
+    // the GeGLU gate half follows each split's first half, nt token columns on
+    const float4* q = reinterpret_cast<const float4*>(red + c * width + (grp - g0) * 8);
+    const int hoff4 = nt * width / 4;
+    float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo, glo = lo, ghi = lo;
+#pragma unroll 1
+    for (int sp = 0; sp < splits; ++sp, q += sstride / 4) {
+      lo = add4(lo, q[0]);
+      hi = add4(hi, q[1]);
+      if (NA == 2) {
+        glo = add4(glo, q[hoff4]);
+        ghi = add4(ghi, q[hoff4 + 1]);
+      }
+    }
+    if (NA == 2) {
+      lo = geglu4(lo, glo);
+      hi = geglu4(hi, ghi);
+    }
+    float o[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    if (KIND == kGemmResidual) {
+      const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&res);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 rf = __bfloat1622float2(r2[i]);
+        o[2 * i] = rf.x + o[2 * i];
+        o[2 * i + 1] = rf.y + o[2 * i + 1];
+      }
+    }
+    store8<KIND>(eo, live ? t : 0, live ? f : grp * 8, o);
   }
 }
 
@@ -304,6 +438,37 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t tmem = *tmem_slot;
   bool epi_ok = false;
   bool red_failed = false;
+
+  // split-K geometry (see slice_g0).  Drain side: the slice this thread's
+  // feature row (TMEM lane) belongs to; reduce side: this rank's slice.
+  const bool rope_tile = KIND == kGemmPlain && a.rope_cos != nullptr && f_tile * kBM < a.rope_cols;
+  const int gw = rope_tile ? 16 : 8;
+  const int ngroups = kBM / gw;  // RoPE: pairs of groups (f, f + 32)
+  const int erow = threadIdx.x & 127;  // epilogue warps: TMEM lane (warp % 4) * 32 + lane
+  const int drain_grp = rope_tile ? 4 * (erow >> 6) + ((erow & 31) >> 3) : erow >> 3;
+  int drain_width = 0, red_g0 = 0, red_g1 = ngroups, red_width = 0;
+  float* drain_part = nullptr;
+  if (a.splits > 1) {
+    const int r = slice_owner(drain_grp, ngroups, a.splits);
+    const int sg0 = slice_g0(r, ngroups, a.splits);
+    drain_width = (slice_g0(r + 1, ngroups, a.splits) - sg0) * gw;
+    // feature of the slice: group-major; a RoPE slice holds the low 8 of each
+    // pair group first, then the high 8 (a warp's rows stay contiguous)
+    const int in_slice = rope_tile ? ((erow & 32) ? drain_width / 2 : 0) +
+                                         (drain_grp - sg0) * 8 + (erow & 7)
+                                   : (drain_grp - sg0) * 8 + (erow & 7);
+    const int tile = t_tile * gridDim.x + f_tile;
+    drain_part = a.partials + (static_cast<size_t>(tile) * a.splits + split) * NA * a.nt * kBM +
+                 static_cast<size_t>(sg0) * gw * NA * a.nt + in_slice;
+    const int rank = static_cast<int>(ptx::cluster_ctarank());
+    red_g0 = slice_g0(rank, ngroups, a.splits);
+    red_g1 = slice_g0(rank + 1, ngroups, a.splits);
+    red_width = (red_g1 - red_g0) * gw;
+  }
+  const int red_units = (red_g1 - red_g0) * a.nt;
+  const int red_sstride = NA * a.nt * red_width;  // floats between splits in the reduce buffer
+  // scratch for dry calls: the LayerNorm-statistics area, unused without LayerNorm on load
+  float* dry = reinterpret_cast<float*>(smem + a.ctrl_offset + kCtrlBytes);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -386,6 +551,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    if (a.splits > 1 && !ln) {
+      // dry calls while the main loop runs (see split_drain)
+      split_drain<NA>(tq, drain_part, drain_width, a.nt, dry, false);
+      split_epilogue<KIND, NA>(epi_out(a), reinterpret_cast<const float*>(smem), red_width,
+                               red_sstride, a.splits, a.nt, red_g0, red_g1 - red_g0, red_units,
+                               t_tile * a.nt, Meff, f_tile * kBM, rope_tile,
+                               static_cast<int>(threadIdx.x) - 64, dry, false);
+    }
     // LayerNorm input and residual are written by earlier kernels; waiting
     // here, while the main loop runs, keeps the wait off the epilogue's path
     ptx::grid_dependency_wait();
@@ -433,34 +606,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     epi_ok = ptx::mbar_wait(accum_bar, 0, abort_flag, a.err, kDevWaitAccum, kWaitLimitNs);
     ptx::tc_fence_after();
     if (epi_ok && a.splits > 1) {
-      // partial tile to the workspace in slice layout (see slice_g0): this
-      // thread's feature row lands in its owner's slice
-      const bool rope_tile =
-          KIND == kGemmPlain && a.rope_cos != nullptr && f_tile * kBM < a.rope_cols;
-      const int gw = rope_tile ? 16 : 8;
-      const int ngroups = kBM / gw;
-      const int grp = rope_tile ? 4 * (row >> 6) + ((row & 31) >> 3) : row >> 3;
-      const int r = slice_owner(grp, ngroups, a.splits);
-      const int sg0 = slice_g0(r, ngroups, a.splits);
-      const int width = (slice_g0(r + 1, ngroups, a.splits) - sg0) * gw;
-      // feature of the slice: group-major; a RoPE slice holds the low 8 of
-      // each pair group first, then the high 8 (a warp's rows stay contiguous)
-      const int in_slice = rope_tile ? ((row & 32) ? width / 2 : 0) + (grp - sg0) * 8 + (row & 7)
-                                     : (grp - sg0) * 8 + (row & 7);
-      const int tile = t_tile * gridDim.x + f_tile;
-      float* part = a.partials + (static_cast<size_t>(tile) * a.splits + split) * NA * a.nt * kBM +
-                    static_cast<size_t>(sg0) * gw * NA * a.nt + in_slice;
-      for (int c0 = 0; c0 < a.nt; c0 += 16) {
-        float v[16];
-        ptx::tmem_ld16(tq + c0, v);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) part[(c0 + j) * width] = v[j];
-        if (NA == 2) {
-          ptx::tmem_ld16(tq + a.nt + c0, v);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) part[(a.nt + c0 + j) * width] = v[j];
-        }
-      }
+      // partial tile to the workspace, this thread's row into its owner's slice
+      split_drain<NA>(tq, drain_part, drain_width, a.nt, dry, true);
     } else if (epi_ok) {
       float* stg = reinterpret_cast<float*>(smem);
       for (int c0 = 0; c0 < a.nt; c0 += 16) {
@@ -488,24 +635,15 @@ __global__ void __launch_bounds__(kThreads, 2)
     // ------------------------------- epilogue phase 2: 16-byte vector stores
     // unit = 8 consecutive features of one token; consecutive threads take
     // consecutive units of a token row, so loads and stores are coalesced.
-    // Split-K: this CTA finishes the feature groups [g0, g1) of the tile,
+    // Split-K: this CTA finishes the feature groups of its slice of the tile,
     // summing the partials of every CTA of the cluster in rank order.
-    const bool rope_tile = KIND == kGemmPlain && a.rope_cos != nullptr && f_tile * kBM < a.rope_cols;
-    const int gw = rope_tile ? 16 : 8;
-    const int ngroups = kBM / gw;  // RoPE: pairs of groups (f, f + 32)
-    int g0 = 0, g1 = ngroups;
     const int tid_e = threadIdx.x - 64;
-    // split-K: this rank's slice of every split's partial, [split][half][c][width]
-    const float* red = reinterpret_cast<const float*>(smem);
-    int width = 0;
-    size_t sstride = 0;  // floats between splits in `red`
+    const int t_base = t_tile * a.nt;
+    const EpiOut eo = epi_out(a);
     if (a.splits > 1) {
-      const int rank = static_cast<int>(ptx::cluster_ctarank());
-      g0 = slice_g0(rank, ngroups, a.splits);
-      g1 = slice_g0(rank + 1, ngroups, a.splits);
-      width = (g1 - g0) * gw;
-      sstride = static_cast<size_t>(NA) * a.nt * width;
-      const uint32_t bytes = static_cast<uint32_t>(sstride * 4);
+      // this rank's slice of every split's partial into the idle ring:
+      // [split][half][token column][width]
+      const uint32_t bytes = static_cast<uint32_t>(red_sstride) * 4u;
       if (tid_e == 0) {
         // the partials were written by the other CTAs of the cluster with
         // ordinary stores (ordered before the cluster barrier above)
@@ -513,96 +651,36 @@ __global__ void __launch_bounds__(kThreads, 2)
         const size_t pstride = static_cast<size_t>(NA) * a.nt * kBM;  // floats between splits
         const float* src = a.partials +
                            static_cast<size_t>(t_tile * gridDim.x + f_tile) * a.splits * pstride +
-                           static_cast<size_t>(g0) * gw * NA * a.nt;
+                           static_cast<size_t>(red_g0) * gw * NA * a.nt;
         ptx::mbar_arrive_expect_tx(red_bar, bytes * static_cast<uint32_t>(a.splits));
         for (int sp = 0; sp < a.splits; ++sp)
           ptx::bulk_load(sbase + static_cast<uint32_t>(sp) * bytes, src + sp * pstride, bytes,
                          red_bar);
       }
-    }
-    const int ng = g1 - g0;
-    const int units = ng * a.nt;
-    const int t_base = t_tile * a.nt;
+      if (!ptx::mbar_wait(red_bar, 0, abort_flag, a.err, kDevWaitReduce, kWaitLimitNs))
+        red_failed = true;
+      else
+        split_epilogue<KIND, NA>(eo, reinterpret_cast<const float*>(smem), red_width, red_sstride,
+                                 a.splits, a.nt, red_g0, red_g1 - red_g0, red_units, t_base, Meff,
+                                 f_tile * kBM, rope_tile, tid_e, dry, true);
+    } else {
+    // one CTA per tile: the fp32 tile staged by phase 1 (GeGLU applied)
+    const int ng = ngroups;
+    const int units = red_units;
     const float* stg = reinterpret_cast<const float*>(smem);
-    if (a.splits > 1 &&
-        !ptx::mbar_wait(red_bar, 0, abort_flag, a.err, kDevWaitReduce, kWaitLimitNs))
-      red_failed = true;
-    if (!red_failed) {
     if (rope_tile) {
       // unit = token column c, pair group p: features (fo, fo + 32), fo = 64 (p / 4) + 8 (p % 4)
       for (int u = tid_e; u < units; u += kThreads - 64) {
         const int c = u / ng;
-        const int pg = g0 + u % ng;
+        const int pg = u % ng;
         const int fo = 64 * (pg >> 2) + 8 * (pg & 3);
         const int t = t_base + c;
         if (t >= Meff) continue;
-        const RopeRow rr = rope_row(a, t, fo & 31);  // in flight during the sums
+        const RopeRow rr = rope_row(eo, t, fo & 31);
         float v1[8], v2[8];
-        if (a.splits > 1) {
-          // split order 0, 1, 2, ... from 0 (as every other path sums)
-          const float4* q = reinterpret_cast<const float4*>(red + c * width + (pg - g0) * 8);
-          const int h4 = width / 8;  // float4s from a low feature to its high partner
-          float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0, s2 = s0, s3 = s0;
-#pragma unroll 1
-          for (int sp = 0; sp < a.splits; ++sp, q += sstride / 4) {
-            s0 = add4(s0, q[0]);
-            s1 = add4(s1, q[1]);
-            s2 = add4(s2, q[h4]);
-            s3 = add4(s3, q[h4 + 1]);
-          }
-          v1[0] = s0.x; v1[1] = s0.y; v1[2] = s0.z; v1[3] = s0.w;
-          v1[4] = s1.x; v1[5] = s1.y; v1[6] = s1.z; v1[7] = s1.w;
-          v2[0] = s2.x; v2[1] = s2.y; v2[2] = s2.z; v2[3] = s2.w;
-          v2[4] = s3.x; v2[5] = s3.y; v2[6] = s3.z; v2[7] = s3.w;
-        } else {
-          load8_smem(stg + c * kSld + fo, v1);
-          load8_smem(stg + c * kSld + fo + 32, v2);
-        }
-        rope_apply_store16(a, t, f_tile * kBM + fo, rr, v1, v2);
-      }
-    } else if (a.splits > 1) {
-      // split-K: one unit at a time in compact code (a unit's residual load
-      // is issued before its sums); at the short shapes that run split-K a
-      // thread has one or two units, and the code runs once per launch
-#pragma unroll 1
-      for (int u = tid_e; u < units; u += kThreads - 64) {
-        const int c = u / ng;
-        const int grp = g0 + u % ng;
-        const int t = t_base + c;
-        const int f = f_tile * kBM + grp * 8;
-        if (t >= Meff || f >= a.N) continue;
-        uint4 res = make_uint4(0u, 0u, 0u, 0u);
-        if (KIND == kGemmResidual)
-          res = *reinterpret_cast<const uint4*>(a.residual + static_cast<size_t>(t) * a.N + f);
-        // split order 0, 1, 2, ... from 0; the GeGLU gate half follows each
-        // split's first half
-        const float4* q = reinterpret_cast<const float4*>(red + c * width + (grp - g0) * 8);
-        const size_t hoff4 = static_cast<size_t>(a.nt) * width / 4;
-        float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo, glo = lo, ghi = lo;
-#pragma unroll 1
-        for (int sp = 0; sp < a.splits; ++sp, q += sstride / 4) {
-          lo = add4(lo, q[0]);
-          hi = add4(hi, q[1]);
-          if (NA == 2) {
-            glo = add4(glo, q[hoff4]);
-            ghi = add4(ghi, q[hoff4 + 1]);
-          }
-        }
-        if (NA == 2) {
-          lo = geglu4(lo, glo);
-          hi = geglu4(hi, ghi);
-        }
-        float o[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-        if (KIND == kGemmResidual) {
-          const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&res);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 rf = __bfloat1622float2(r2[i]);
-            o[2 * i] = rf.x + o[2 * i];
-            o[2 * i + 1] = rf.y + o[2 * i + 1];
-          }
-        }
-        store8<KIND>(a, t, f, o);
+        load8_smem(stg + c * kSld + fo, v1);
+        load8_smem(stg + c * kSld + fo + 32, v2);
+        rope_apply_store16(eo, t, f_tile * kBM + fo, rr, v1, v2);
       }
     } else
     for (int u0 = tid_e; u0 < units; u0 += (kThreads - 64) * kEpiBatch) {
@@ -617,9 +695,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         tok[b] = -1;
         if (u < units) {
           const int c = u / ng;
-          const int grp = g0 + u % ng;
+          const int grp = u % ng;
           {
-            // one CTA per tile: the staged tile (GeGLU already applied)
+            // the staged tile (GeGLU already applied)
             const float4* p4 = reinterpret_cast<const float4*>(stg + c * kSld + grp * 8);
             const float4 lo = p4[0], hi = p4[1];
             v[b][0] = lo.x; v[b][1] = lo.y; v[b][2] = lo.z; v[b][3] = lo.w;
@@ -651,10 +729,10 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
           for (int i = 0; i < 8; ++i) o[i] = v[b][i];
         }
-        store8<KIND>(a, tok[b], fea[b], o);
+        store8<KIND>(eo, tok[b], fea[b], o);
       }
     }
-    }  // !red_failed
+    }  // one CTA per tile
     if (red_failed && a.splits > 1 && threadIdx.x == 64) {
       // no bulk copy may still be landing in this CTA's shared memory at exit
       const uint64_t t0 = ptx::globaltimer_ns();
@@ -847,6 +925,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const int tid_e = threadIdx.x - 64;
+    const EpiOut eo = epi_out(a);
     ptx::grid_dependency_wait();  // residual written by earlier kernels
     int lt = 0, cc = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++lt) {
@@ -875,7 +954,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int u = tid_e + (kThreads - 64) * k;
             const int c = u / (kBM / 16), pg = u % (kBM / 16);
             const int t = tt * a.nt + c0 + c;
-            if (u < ncols * (kBM / 16) && t < Meff) rr[k] = rope_row(a, t, 8 * (pg & 3));
+            if (u < ncols * (kBM / 16) && t < Meff) rr[k] = rope_row(eo, t, 8 * (pg & 3));
           }
         }
         for (int j0 = 0; j0 < ncols; j0 += 16) {
@@ -908,7 +987,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               float v1[8], v2[8];
               load8_smem(buf + c * kSld + fo, v1);
               load8_smem(buf + c * kSld + fo + 32, v2);
-              rope_apply_store16(a, t, ft * kBM + fo, rr[k], v1, v2);
+              rope_apply_store16(eo, t, ft * kBM + fo, rr[k], v1, v2);
             }
           }
           continue;
@@ -954,7 +1033,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int i = 0; i < 8; ++i) o[i] = v[bb][i];
             }
-            store8<KIND>(a, tok[bb], fea[bb], o);
+            store8<KIND>(eo, tok[bb], fea[bb], o);
           }
         }
       }

@@ -58,10 +58,16 @@ __global__ void __launch_bounds__(128) layernorm_kernel(const bf16* src,
                                                         const int32_t* __restrict__ lens, int B,
                                                         int S, int32_t* __restrict__ pos) {
   ptx::grid_launch_dependents();
-  ptx::grid_dependency_wait();
   constexpr int H = 256 * V;
   const int row = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
+  // gamma is a weight, not an output of the previous kernel: its loads are
+  // in flight while that kernel finishes
+  const uint4* g4 = reinterpret_cast<const uint4*>(gamma);
+  uint4 gr[V];
+#pragma unroll
+  for (int c = 0; c < V; ++c) gr[c] = __ldg(g4 + lane + 32 * c);
+  ptx::grid_dependency_wait();
   if (row >= M) return;
   int orow = row;  // output row
   if (lens != nullptr) {
@@ -89,12 +95,11 @@ __global__ void __launch_bounds__(128) layernorm_kernel(const bf16* src,
   float mean, rstd;
   row_stats<V>(reinterpret_cast<const uint4*>(in), lane, eps, v, mean, rstd);
 
-  const uint4* g4 = reinterpret_cast<const uint4*>(gamma);
   uint4* out4 = reinterpret_cast<uint4*>(dst + static_cast<size_t>(orow) * H);
 #pragma unroll
   for (int c = 0; c < V; ++c) {
     float g[8], y[8];
-    unpack8(g4[lane + 32 * c], g);
+    unpack8(gr[c], g);
 #pragma unroll
     for (int i = 0; i < 8; ++i) y[i] = ln_apply(v[c][i], mean, rstd, g[i]);
     out4[lane + 32 * c] = pack8(y);
