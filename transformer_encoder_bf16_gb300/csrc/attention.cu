@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(128, 4) attention_kernel(const bf16* __restric
                                                         int half_window, bf16* __restrict__ ctx,
                                                         int* err, const float* __restrict__ cos_t,
                                                         const float* __restrict__ sin_t,
-                                                        int packed) {
+                                                        int packed, int warm) {
   __shared__ __align__(128) bf16 sQ[kQ * kLd];
   __shared__ __align__(128) bf16 sK[2][kKT * kLd];
   __shared__ __align__(128) bf16 sV[2][kKT * kLd];
@@ -160,12 +160,13 @@ __global__ void __launch_bounds__(128, 4) attention_kernel(const bf16* __restric
   const float scale_log2 = 0.125f * 1.4426950408889634f;
   const int qi0 = q0 + warp * 16 + g;  // query of accumulator rows 0 (and +8)
 
-  // Pass 0 runs the tile computation once over whatever shared memory holds,
-  // stores nothing, and reads no output of earlier kernels: it executes,
-  // while the previous kernel finishes (programmatic dependent launch), the
-  // same instructions as the live pass 1, whose instruction fetches then hit.
+  // Pass 0 (warm launches) runs the tile computation once over whatever
+  // shared memory holds, stores nothing, and reads no output of earlier
+  // kernels: it executes, while the previous kernel finishes (programmatic
+  // dependent launch), the same instructions as the live pass 1, whose
+  // instruction fetches then hit.
 #pragma unroll 1
-  for (int pass = pad_tile ? 1 : 0; pass < 2; ++pass) {
+  for (int pass = (pad_tile || !warm) ? 1 : 0; pass < 2; ++pass) {
   const bool live = pass == 1;
   if (live) {
     ptx::grid_dependency_wait();
@@ -347,8 +348,13 @@ cudaError_t launch_attention(const bf16* qkv, const int32_t* lengths, int B, int
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = l.pdl ? 1 : 0;
+  // the dry pass is free only while the previous kernel runs: with
+  // programmatic dependent launch and a grid that is resident at once (one
+  // wave of four CTAs per SM); a later wave would pay for it
+  const long long ctas = static_cast<long long>(cfg.gridDim.x) * heads * B;
+  const int warm = (l.pdl && ctas <= 4ll * device_sm_count()) ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, attention_kernel, qkv, lengths, S, heads, global, half_window,
-                            ctx, err, cos_t, sin_t, packed ? 1 : 0);
+                            ctx, err, cos_t, sin_t, packed ? 1 : 0, warm);
 }
 
 }  // namespace laya
