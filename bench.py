@@ -421,8 +421,7 @@ def main():
                                 if pub else None),
             "dtype": "bf16", "data": "synthetic",
             "config": {"workload": args.workload, "batch": B, "seq": S, "valid_tokens": valid,
-                       "layers": "28 encoder + 2 decision", "hidden": H,
-                       "l2": "weights 838 MB > L2 (126 MB): streamed from HBM every step, no flush",
+                       "l2": "weights 838 MB > L2 (129 MB): streamed from HBM every step, no flush",
                        "graphs": True, "pdl": os.environ.get("LAYA_NO_PDL", "0") in ("", "0"),
                        "parallelism": f"replicas x{world}"},
             "clocks": clk,
