@@ -73,13 +73,19 @@ GEMM_SOURCES = ("gemm.cu", "internal.h", "packing.cuh", "ptx.cuh", "rowstats.cuh
 
 
 def csrc_sha16():
-    """Hash of the GEMM kernel sources, to tell whether recorded ncu counters still apply."""
+    """Hash of the GEMM kernel sources, to tell whether recorded ncu counters
+    still apply: the code only (line comments and blank lines dropped, so that
+    a comment edit does not void a capture)."""
     import hashlib
+    import re
     d = os.path.join(ROOT, "transformer_encoder_bf16_gb300", "csrc")
     h = hashlib.sha256()
     for name in GEMM_SOURCES:
-        with open(os.path.join(d, name), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(d, name), encoding="utf-8") as fh:
+            for line in fh:
+                code = re.sub(r"//.*$", "", line).strip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

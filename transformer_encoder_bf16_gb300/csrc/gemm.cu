@@ -22,11 +22,12 @@
 // tiles exist to occupy every SM ("Implementation priorities": smaller tiles
 // for the short shapes): the K blocks are divided among the CTAs of a thread-
 // block cluster along z.  Each CTA writes its fp32 partial tile to a global
-// workspace (coalesced, L2-resident); after a cluster barrier (release /
-// acquire) every CTA sums one slice of the tile over all partials in rank
-// order (deterministic, no atomics) and runs the epilogue for it.  (Parking
-// the partials in shared memory and reducing through DSMEM was measured: the
-// distributed-shared-memory reads were the slowest part of the kernel.)
+// workspace (L2-resident) in slice layout (see slice_g0); after a cluster
+// barrier (release / acquire) every CTA fetches its slice of all partials with
+// one bulk copy per split, sums it in rank order (deterministic, no atomics)
+// and runs the epilogue for it.  (Measured slower on this GPU: parking the
+// partials in shared memory and reading them through DSMEM, and pushing the
+// slices into the reducers' shared memory with DSMEM bulk copies.)
 //
 // Roles (192 threads): warp 0 lane 0 issues TMA, warp 1 owns TMEM and its lane
 // 0 issues the MMAs, warps 2-5 drain TMEM (warp w reads TMEM lanes
@@ -77,7 +78,7 @@ struct GemmArgs {
   const bf16* residual;
   float* y_f32;  // residual kind: if set, the fp32 sums are stored here instead of y
   int* err;
-  float* partials;  // split-K workspace: [tile][split][half][nt][kBM] fp32
+  float* partials;  // split-K workspace: [tile][split] fp32 partial tiles in slice layout
   // RoPE in the epilogue (plain kind): output features below rope_cols are
   // q|k heads of 64, rotated with the [pos, 32] tables at pos = token % rope_S
   // (packed tokens: pos = rope_pos[token], the index of the token in its row)
