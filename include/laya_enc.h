@@ -150,6 +150,13 @@ int laya_enc_run_device(laya_enc_handle* h, const int32_t* token_ids_dev,
  * LAYA_E_DEVICE (and poisons the handle) if a kernel flagged an error. */
 int laya_enc_check(laya_enc_handle* h, void* stream);
 
+/* Test hook for the failure path: the next laya_enc_run / laya_enc_run_device
+ * on this handle enqueues nothing and fails with LAYA_E_CUDA as a failed
+ * launch would, poisoning the handle ("Laya native CUDA worker", "Start and
+ * check": a native failure stops the executor); later calls return
+ * LAYA_E_POISONED.  No device fault is involved. */
+int laya_enc_debug_fail_next_run(laya_enc_handle* h);
+
 /* 1: use CUDA Graphs (default, unless env LAYA_EAGER=1); 0: eager launches. */
 int laya_enc_set_graphs(laya_enc_handle* h, int enabled);
 

@@ -188,8 +188,8 @@ def test_invariants_bitwise():
         np.testing.assert_array_equal(a[b, :L], r[B - 1 - b, :L])
 
 
-@pytest.mark.parametrize("B,S", [(1, 1), (1, 16), (1, 63), (1, 65), (2, 127), (2, 128), (1, 129),
-                                 (16, 1), (1, 511), (1, 512), (16, 64)])
+@pytest.mark.parametrize("B,S", [(1, 1), (1, 16), (1, 63), (1, 64), (1, 65), (2, 127), (2, 128),
+                                 (1, 129), (16, 1), (1, 511), (1, 512), (16, 64)])
 def test_shape_boundaries(B, S):
     model = synth.REDUCED
     w, enc = encoder_for(model, 0)
@@ -234,3 +234,58 @@ def test_run_device_matches_run():
     enc.run_device(i32_dev(ids), i32_dev(lengths), out)
     enc.check()
     np.testing.assert_array_equal(a, to_bits(out))
+
+
+def test_encoder_stack_state_before_the_decision_layers():
+    # the hidden state after the last encoder layer (the pages' "encoder27"
+    # comparison point, #66 "Starting evidence"): the 28-layer encoder alone,
+    # no final norm, gated like the full stack on the oracle's own spread
+    model, B, S, seed, lr = synth.WORKLOADS["full_1x48"]
+    n = model["n_encoder_layers"]
+    w, enc = encoder_for(model, seed, n)
+    ids, lengths = synth.make_inputs(model, B, S, seed, lr)
+    got = run_gpu(enc, ids, lengths)
+    check_full_depth("full_1x48 encoder stack", got, prefix_model(model, n), prefix_weights(w, n),
+                     ids, lengths)
+
+
+def test_empty_batch_is_rejected():
+    torch = require_gpu()
+    model = synth.REDUCED
+    _, enc = encoder_for(model, 0)
+    ids = np.zeros((0, 8), np.int32)
+    out = torch.empty((0, 8, model["hidden"]), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(te.LayaError) as ex:
+        enc.run(ids, np.zeros(0, np.int32), out)
+    assert ex.value.code == te.E_INVAL
+    enc.check()
+
+
+def test_failure_poisons_the_handle_and_enqueues_nothing():
+    # a failed launch (injected on the host, no device fault) stops this
+    # handle: the failing call and every later one report it, the output is
+    # untouched ("Laya native CUDA worker", "Start and check")
+    torch = require_gpu()
+    model = synth.REDUCED
+    _, base = encoder_for(model, 0)
+    enc = te.Encoder(base.model, base._weights)
+    ids, lengths = synth.make_inputs(model, 1, 16, 3)
+    out = torch.full((1, 16, model["hidden"]), 7.0, dtype=torch.bfloat16, device="cuda")
+    enc.run(ids, lengths, out)
+    enc.check()
+    out.fill_(7.0)
+    enc.debug_fail_next_run()
+    with pytest.raises(te.LayaError) as ex:
+        enc.run(ids, lengths, out)
+    assert ex.value.code == te.E_CUDA
+    for call in (lambda: enc.run(ids, lengths, out), lambda: enc.check()):
+        with pytest.raises(te.LayaError) as ex:
+            call()
+        assert ex.value.code == te.E_POISONED
+    torch.cuda.synchronize()
+    assert torch.all(out == 7.0)
+    enc.close()
+    fresh = te.Encoder(base.model, base._weights)   # other handles are unaffected
+    fresh.run(ids, lengths, out)
+    fresh.check()
+    fresh.close()

@@ -83,6 +83,7 @@ _SIGNATURES = {
     "laya_enc_run_device": ([_P, _P, _P, _I, _I, _P, _P], _I),
     "laya_enc_check": ([_P, _P], _I),
     "laya_enc_set_graphs": ([_P, _I], _I),
+    "laya_enc_debug_fail_next_run": ([_P], _I),
     "laya_enc_set_fused": ([_P, _I], _I),
     "laya_enc_get_cache_stats": ([_P, _P], _I),
     "laya_enc_launch_count": ([_P, _I, _I], _I),
@@ -210,6 +211,10 @@ class Encoder:
 
     def check(self, stream=None):
         return _check(lib().laya_enc_check(self.handle, _stream_ptr(stream)), self.handle)
+
+    def debug_fail_next_run(self):
+        """Test hook: the next run fails like a CUDA launch failure (poisons the handle)."""
+        _check(lib().laya_enc_debug_fail_next_run(self.handle), self.handle)
 
     def set_graphs(self, enabled: bool):
         _check(lib().laya_enc_set_graphs(self.handle, 1 if enabled else 0), self.handle)

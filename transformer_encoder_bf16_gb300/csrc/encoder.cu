@@ -113,6 +113,7 @@ struct laya_enc_handle {
   bool poisoned = false;
   std::string last_error;
   // profiling: event pairs of the last run, per-class totals
+  bool fail_next_run = false;  // test hook: the next run fails as a CUDA error would
   bool profiling = false;
   std::vector<cudaEvent_t> prof_events;  // 2 per launch, reused
   std::vector<int> prof_class;           // class of each recorded launch
@@ -781,6 +782,10 @@ static int run_impl(laya_enc_handle* h, const int32_t* ids, const int32_t* lengt
       if (ids[t] < 0 || ids[t] >= h->cfg.vocab)
         return fail(h, LAYA_E_INVAL, "token id outside [0, vocab)");
   }
+  if (h->fail_next_run) {
+    h->fail_next_run = false;
+    return cuda_fail(h, cudaErrorLaunchFailure, "injected failure (test hook)");
+  }
   cudaError_t e = cudaSetDevice(h->device);
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaSetDevice");
   Workspace* w = nullptr;
@@ -833,6 +838,12 @@ int laya_enc_check(laya_enc_handle* h, void* stream) {
   if (e != cudaSuccess) return cuda_fail(h, e, "error word read");
   if (word != 0) return fail(h, LAYA_E_DEVICE, "kernel reported device error " + std::to_string(word));
   if (h->poisoned) return fail(h, LAYA_E_POISONED, "handle is poisoned by an earlier error");
+  return LAYA_OK;
+}
+
+int laya_enc_debug_fail_next_run(laya_enc_handle* h) {
+  if (!h) return LAYA_E_INVAL;
+  h->fail_next_run = true;
   return LAYA_OK;
 }
 
