@@ -111,3 +111,16 @@ def test_create_reports_errors_without_a_gpu(lib):
     assert lib.laya_enc_last_error(None)
     assert lib.laya_enc_destroy(None) == te.OK
     assert lib.laya_enc_run(None, None, None, 1, 1, None, None) == te.E_INVAL
+
+
+def test_device_input_checks_reject_wrong_tensors():
+    # host-side marshalling checks before the C ABI sees bare pointers (CPU
+    # tensors stand for any tensor the checks must refuse)
+    import torch
+    ids = torch.zeros((2, 8), dtype=torch.int32)
+    lens = torch.full((2,), 8, dtype=torch.int32)
+    for a, b in ((ids, lens), (ids.long(), lens), (ids, lens.long()), (ids.t(), lens),
+                 (ids, lens[:1]), (ids.reshape(-1), lens)):
+        with pytest.raises(te.LayaError) as ex:
+            te.check_device_inputs(a, b)
+        assert ex.value.code == te.E_INVAL

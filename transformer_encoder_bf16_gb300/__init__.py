@@ -162,6 +162,19 @@ def upload_weights(weights: dict, device="cuda"):
             "layers": [{k: up(v) for k, v in layer.items()} for layer in weights["layers"]]}
 
 
+def check_device_inputs(ids_dev, lengths_dev):
+    """The C ABI reads B * S and B int32 values through bare pointers: check
+    the tensors' element type, layout and agreement here."""
+    import torch
+    ok = (ids_dev.dtype == torch.int32 and lengths_dev.dtype == torch.int32 and
+          ids_dev.dim() == 2 and lengths_dev.dim() == 1 and ids_dev.is_contiguous() and
+          lengths_dev.is_contiguous() and lengths_dev.shape[0] == ids_dev.shape[0] and
+          ids_dev.is_cuda and lengths_dev.is_cuda)
+    if not ok:
+        raise LayaError(E_INVAL, "token ids must be a contiguous int32 [B, S] and lengths a "
+                                 "contiguous int32 [B] tensor on the device")
+
+
 class Encoder:
     """Owns a laya_enc_handle over device weights (kept referenced here)."""
 
@@ -196,6 +209,7 @@ class Encoder:
 
     def run_device(self, ids_dev, lengths_dev, out, stream=None):
         """ids_dev int32 [B, S] and lengths_dev int32 [B] device tensors."""
+        check_device_inputs(ids_dev, lengths_dev)
         B, S = ids_dev.shape
         self._check_out(out, B, S)
         _check(lib().laya_enc_run_device(self.handle, _ptr(ids_dev), _ptr(lengths_dev), B, S,
