@@ -89,6 +89,8 @@ def lib():
             L.orc_forward.argtypes = [ctypes.POINTER(OrcConfig), _P, _P, _P, _P,
                                       _P, _P, _I, _I, _P, _I, _P]
             L.orc_forward.restype = _I
+            L.orc_layer.argtypes = [ctypes.POINTER(OrcConfig), _I, _P, _P, _P, _I, _I, _P, _P]
+            L.orc_layer.restype = _I
             _lib = L
     return _lib
 
@@ -247,3 +249,27 @@ def forward(model: dict, weights: dict, ids, lengths, accum_f64=False,
     if rc != 0:
         raise ValueError(f"oracle forward rejected its arguments (rc={rc})")
     return (out, cap) if capture_layer >= 0 else out
+
+
+def layer(model: dict, weights: dict, l: int, x_in, lengths, accum_f64=False, out_fp32=False):
+    """Layer l alone (0-based over the encoder, then the decision layers) on
+    the residual stream x_in [B, S, H] (fp32 holding BF16 values); the final
+    LayerNorm is applied first when l is the first decision layer.  Returns
+    fp32 [B, S, H].  Chaining it from the embedding output reproduces
+    forward() bit for bit."""
+    x_in = _f32(x_in)
+    lengths = np.ascontiguousarray(lengths, dtype=np.int32)
+    B, S, H = x_in.shape
+    cfg = make_config(model, accum_f64, out_fp32)
+    if not 0 <= l < len(weights["layers"]):
+        raise ValueError(f"oracle layer: no layer {l}")
+    lw = weights["layers"][l]
+    keep = [None if lw.get(k) is None else _u16(lw[k]) for k in LAYER_KEYS]
+    arr = (ctypes.c_void_p * 6)(*[None if a is None else a.ctypes.data for a in keep])
+    fn = _u16(weights["final_norm"]) if weights.get("final_norm") is not None else None
+    out = np.zeros((B, S, H), np.float32)
+    rc = lib().orc_layer(ctypes.byref(cfg), int(l), ctypes.cast(arr, ctypes.c_void_p), _ptr(fn),
+                         _ptr(lengths), B, S, _ptr(x_in), _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle layer rejected its arguments (rc={rc})")
+    return out

@@ -58,7 +58,7 @@
 #include <omp.h>
 #endif
 
-#define ORC_ABI 2
+#define ORC_ABI 3
 
 typedef struct {
   int32_t hidden, heads, head_dim, intermediate, vocab;
@@ -388,6 +388,116 @@ void orc_step_embed_layernorm(const uint16_t* emb, const uint16_t* gamma,
 
 /* --------------------------------------------------------- full stack ---- */
 
+/* Scratch of one layer evaluation over M tokens. */
+typedef struct {
+  float *h, *qkv, *ctx, *acc, *g, *gam, *wbuf;
+  float *cos_g, *sin_g, *cos_l, *sin_l;
+} orc_scratch;
+
+static int scratch_alloc(const orc_config* cfg, size_t M, orc_scratch* s) {
+  const int H = cfg->hidden, I = cfg->intermediate, half = cfg->head_dim / 2;
+  size_t wmax = (size_t)3 * H * H;
+  if ((size_t)2 * I * H > wmax) wmax = (size_t)2 * I * H;
+  const size_t tab = (size_t)cfg->max_seq * half;
+  s->h = (float*)malloc(sizeof(float) * M * H);
+  s->qkv = (float*)malloc(sizeof(float) * M * 3 * H);
+  s->ctx = (float*)malloc(sizeof(float) * M * H);
+  s->acc = (float*)malloc(sizeof(float) * M * (size_t)(2 * I > 3 * H ? 2 * I : 3 * H));
+  s->g = (float*)malloc(sizeof(float) * M * I);
+  s->gam = (float*)malloc(sizeof(float) * (size_t)H);
+  s->wbuf = (float*)malloc(sizeof(float) * wmax);
+  s->cos_g = (float*)malloc(sizeof(float) * tab);
+  s->sin_g = (float*)malloc(sizeof(float) * tab);
+  s->cos_l = (float*)malloc(sizeof(float) * tab);
+  s->sin_l = (float*)malloc(sizeof(float) * tab);
+  if (!s->h || !s->qkv || !s->ctx || !s->acc || !s->g || !s->gam || !s->wbuf || !s->cos_g ||
+      !s->sin_g || !s->cos_l || !s->sin_l)
+    return -1;
+  orc_rope_table(cfg->theta_global, cfg->max_seq, half, cfg->rope_table_bf16, s->cos_g, s->sin_g);
+  orc_rope_table(cfg->theta_local, cfg->max_seq, half, cfg->rope_table_bf16, s->cos_l, s->sin_l);
+  return 0;
+}
+
+static void scratch_free(orc_scratch* s) {
+  free(s->h); free(s->qkv); free(s->ctx); free(s->acc); free(s->g); free(s->gam);
+  free(s->wbuf); free(s->cos_g); free(s->sin_g); free(s->cos_l); free(s->sin_l);
+}
+
+static int check_args(const orc_config* cfg, const int32_t* lengths, int B, int S) {
+  if (B < 1 || S < 1 || S > cfg->max_seq || cfg->heads * cfg->head_dim != cfg->hidden ||
+      (cfg->head_dim % 2) != 0)
+    return -1;
+  for (int b = 0; b < B; ++b)
+    if (lengths[b] < 1 || lengths[b] > S) return -1;
+  return 0;
+}
+
+/* Layer l (0-based over the encoder then the decision layers) applied in place
+ * to the residual stream x [B*S, H] (fp32 holding BF16 values).  When l is the
+ * first decision layer and cfg->final_norm is set, the final LayerNorm is
+ * applied to x first, as the stack does.  w: the layer's six weights in the
+ * order of orc_forward. */
+static void layer_step(const orc_config* cfg, int l, const uint16_t* const* w,
+                       const uint16_t* final_norm, const int32_t* lengths, int B, int S,
+                       float* x, orc_scratch* s) {
+  const int H = cfg->hidden, NH = cfg->heads, D = cfg->head_dim;
+  const int I = cfg->intermediate, half = D / 2;
+  const int L = cfg->n_encoder_layers + cfg->n_decision_layers;
+  const size_t M = (size_t)B * S;
+  const int dec = l >= cfg->n_encoder_layers;
+  const int glob = dec || (l % cfg->global_every == 0);
+
+  if (l == cfg->n_encoder_layers && cfg->final_norm) {
+    bits_to_f32(final_norm, (size_t)H, s->gam);
+    layernorm_rows(x, s->gam, (int)M, H, cfg->ln_eps, s->h);
+    memcpy(x, s->h, sizeof(float) * M * H);
+  }
+
+  /* attention sub-layer: h = LN(x); qkv = h W^T; RoPE; attention; x += ctx Wo^T */
+  if (l == 0 && cfg->first_attn_norm_identity) {
+    memcpy(s->h, x, sizeof(float) * M * H);
+  } else {
+    bits_to_f32(w[0], (size_t)H, s->gam);
+    layernorm_rows(x, s->gam, (int)M, H, cfg->ln_eps, s->h);
+  }
+  bits_to_f32(w[1], (size_t)3 * H * H, s->wbuf);
+  linear_rows(s->h, (int)M, H, s->wbuf, 3 * H, s->qkv, cfg->accum_f64);
+  for (size_t e = 0; e < M * 3 * H; ++e) s->qkv[e] = orc_bf16_round(s->qkv[e]);
+
+  {
+    const float* ct = glob ? s->cos_g : s->cos_l;
+    const float* st = glob ? s->sin_g : s->sin_l;
+    for (int b = 0; b < B; ++b)
+      for (int p = 0; p < S; ++p)
+        for (int part = 0; part < 2; ++part)
+          for (int n = 0; n < NH; ++n)
+            orc_rope_vec(s->qkv + ((size_t)b * S + p) * 3 * H + (size_t)part * H + (size_t)n * D,
+                         ct + (size_t)p * half, st + (size_t)p * half, half);
+  }
+
+  attention_rows(s->qkv, lengths, B, S, H, NH, D, glob, cfg->local_half_window, s->ctx);
+
+  bits_to_f32(w[2], (size_t)H * H, s->wbuf);
+  linear_rows(s->ctx, (int)M, H, s->wbuf, H, s->acc, cfg->accum_f64);
+  for (size_t e = 0; e < M * H; ++e) x[e] = orc_bf16_round(x[e] + s->acc[e]);
+
+  /* MLP sub-layer: h = LN(x); a = h Wup^T; g = gelu(a_in) * a_gate; x += g Wdn^T */
+  bits_to_f32(w[3], (size_t)H, s->gam);
+  layernorm_rows(x, s->gam, (int)M, H, cfg->ln_eps, s->h);
+  bits_to_f32(w[4], (size_t)2 * I * H, s->wbuf);
+  linear_rows(s->h, (int)M, H, s->wbuf, 2 * I, s->acc, cfg->accum_f64);
+  for (size_t t = 0; t < M; ++t)
+    for (int j = 0; j < I; ++j)
+      s->g[t * I + j] =
+          orc_bf16_round(orc_gelu(s->acc[t * 2 * I + j]) * s->acc[t * 2 * I + I + j]);
+  bits_to_f32(w[5], (size_t)H * I, s->wbuf);
+  linear_rows(s->g, (int)M, I, s->wbuf, H, s->acc, cfg->accum_f64);
+  if (l == L - 1 && cfg->out_fp32)
+    for (size_t e = 0; e < M * H; ++e) x[e] = x[e] + s->acc[e];
+  else
+    for (size_t e = 0; e < M * H; ++e) x[e] = orc_bf16_round(x[e] + s->acc[e]);
+}
+
 /* Weights per layer, in this order (all BF16 bit patterns, nn.Linear layout):
  *   0 attn_norm [H] (may be NULL at encoder layer 0 when the identity reading
  *     is on), 1 wqkv [3H, H], 2 wo [H, H], 3 mlp_norm [H], 4 wup [2I, H],
@@ -402,106 +512,58 @@ int orc_forward(const orc_config* cfg, const uint16_t* tok_emb,
                 const uint16_t* const* layer_w, const int32_t* ids,
                 const int32_t* lengths, int B, int S, float* out,
                 int capture_layer, float* capture) {
-  const int H = cfg->hidden, NH = cfg->heads, D = cfg->head_dim;
-  const int I = cfg->intermediate;
+  const int H = cfg->hidden;
   const int L = cfg->n_encoder_layers + cfg->n_decision_layers;
-  if (B < 1 || S < 1 || S > cfg->max_seq || NH * D != H || (D % 2) != 0)
-    return -1;
-  for (int b = 0; b < B; ++b)
-    if (lengths[b] < 1 || lengths[b] > S) return -1;
+  if (check_args(cfg, lengths, B, S) != 0) return -1;
   for (int t = 0; t < B * S; ++t)
     if (ids[t] < 0 || ids[t] >= cfg->vocab) return -1;
 
   const size_t M = (size_t)B * S;
-  const int half = D / 2;
-  float* cos_g = (float*)malloc(sizeof(float) * (size_t)cfg->max_seq * half);
-  float* sin_g = (float*)malloc(sizeof(float) * (size_t)cfg->max_seq * half);
-  float* cos_l = (float*)malloc(sizeof(float) * (size_t)cfg->max_seq * half);
-  float* sin_l = (float*)malloc(sizeof(float) * (size_t)cfg->max_seq * half);
-  orc_rope_table(cfg->theta_global, cfg->max_seq, half, cfg->rope_table_bf16, cos_g, sin_g);
-  orc_rope_table(cfg->theta_local, cfg->max_seq, half, cfg->rope_table_bf16, cos_l, sin_l);
-
+  orc_scratch s;
   float* x = (float*)malloc(sizeof(float) * M * H);
-  float* h = (float*)malloc(sizeof(float) * M * H);
-  float* qkv = (float*)malloc(sizeof(float) * M * 3 * H);
-  float* ctx = (float*)malloc(sizeof(float) * M * H);
-  float* acc = (float*)malloc(sizeof(float) * M * (size_t)(2 * I > 3 * H ? 2 * I : 3 * H));
-  float* g = (float*)malloc(sizeof(float) * M * I);
-  float* gam = (float*)malloc(sizeof(float) * (size_t)H);
-  size_t wmax = (size_t)3 * H * H;
-  if ((size_t)2 * I * H > wmax) wmax = (size_t)2 * I * H;
-  float* wbuf = (float*)malloc(sizeof(float) * wmax);
+  if (!x || scratch_alloc(cfg, M, &s) != 0) return -1;
 
   /* token embedding + embedding LayerNorm */
   {
     float* row = (float*)malloc(sizeof(float) * (size_t)H);
-    bits_to_f32(emb_norm, (size_t)H, gam);
+    bits_to_f32(emb_norm, (size_t)H, s.gam);
     for (size_t t = 0; t < M; ++t) {
       bits_to_f32(tok_emb + (size_t)ids[t] * H, (size_t)H, row);
-      orc_layernorm_row(row, gam, H, cfg->ln_eps, x + t * H);
+      orc_layernorm_row(row, s.gam, H, cfg->ln_eps, x + t * H);
     }
     free(row);
   }
 
   for (int l = 0; l < L; ++l) {
-    const uint16_t* const* w = layer_w + (size_t)6 * l;
-    const int dec = l >= cfg->n_encoder_layers;
-    const int glob = dec || (l % cfg->global_every == 0);
-
-    if (l == cfg->n_encoder_layers && cfg->final_norm) {
-      bits_to_f32(final_norm, (size_t)H, gam);
-      layernorm_rows(x, gam, (int)M, H, cfg->ln_eps, h);
-      memcpy(x, h, sizeof(float) * M * H);
-    }
-
-    /* attention sub-layer: h = LN(x); qkv = h W^T; RoPE; attention; x += ctx Wo^T */
-    if (l == 0 && cfg->first_attn_norm_identity) {
-      memcpy(h, x, sizeof(float) * M * H);
-    } else {
-      bits_to_f32(w[0], (size_t)H, gam);
-      layernorm_rows(x, gam, (int)M, H, cfg->ln_eps, h);
-    }
-    bits_to_f32(w[1], (size_t)3 * H * H, wbuf);
-    linear_rows(h, (int)M, H, wbuf, 3 * H, qkv, cfg->accum_f64);
-    for (size_t e = 0; e < M * 3 * H; ++e) qkv[e] = orc_bf16_round(qkv[e]);
-
-    {
-      const float* ct = glob ? cos_g : cos_l;
-      const float* st = glob ? sin_g : sin_l;
-      for (int b = 0; b < B; ++b)
-        for (int s = 0; s < S; ++s)
-          for (int part = 0; part < 2; ++part)
-            for (int n = 0; n < NH; ++n)
-              orc_rope_vec(qkv + ((size_t)b * S + s) * 3 * H + (size_t)part * H + (size_t)n * D,
-                           ct + (size_t)s * half, st + (size_t)s * half, half);
-    }
-
-    attention_rows(qkv, lengths, B, S, H, NH, D, glob, cfg->local_half_window, ctx);
-
-    bits_to_f32(w[2], (size_t)H * H, wbuf);
-    linear_rows(ctx, (int)M, H, wbuf, H, acc, cfg->accum_f64);
-    for (size_t e = 0; e < M * H; ++e) x[e] = orc_bf16_round(x[e] + acc[e]);
-
-    /* MLP sub-layer: h = LN(x); a = h Wup^T; g = gelu(a_in) * a_gate; x += g Wdn^T */
-    bits_to_f32(w[3], (size_t)H, gam);
-    layernorm_rows(x, gam, (int)M, H, cfg->ln_eps, h);
-    bits_to_f32(w[4], (size_t)2 * I * H, wbuf);
-    linear_rows(h, (int)M, H, wbuf, 2 * I, acc, cfg->accum_f64);
-    for (size_t t = 0; t < M; ++t)
-      for (int j = 0; j < I; ++j)
-        g[t * I + j] = orc_bf16_round(orc_gelu(acc[t * 2 * I + j]) * acc[t * 2 * I + I + j]);
-    bits_to_f32(w[5], (size_t)H * I, wbuf);
-    linear_rows(g, (int)M, I, wbuf, H, acc, cfg->accum_f64);
-    if (l == L - 1 && cfg->out_fp32)
-      for (size_t e = 0; e < M * H; ++e) x[e] = x[e] + acc[e];
-    else
-      for (size_t e = 0; e < M * H; ++e) x[e] = orc_bf16_round(x[e] + acc[e]);
-
+    layer_step(cfg, l, layer_w + (size_t)6 * l, final_norm, lengths, B, S, x, &s);
     if (l == capture_layer && capture) memcpy(capture, x, sizeof(float) * M * H);
   }
 
   memcpy(out, x, sizeof(float) * M * H);
-  free(cos_g); free(sin_g); free(cos_l); free(sin_l);
-  free(x); free(h); free(qkv); free(ctx); free(acc); free(g); free(gam); free(wbuf);
+  scratch_free(&s);
+  free(x);
+  return 0;
+}
+
+/* One layer on a given input state: out = layer l applied to x_in [B*S, H]
+ * (fp32 holding BF16 values), with the final LayerNorm first when l is the
+ * first decision layer (as orc_forward does).  w: the six weights of layer l
+ * (order of orc_forward); final_norm may be NULL unless that norm applies.
+ * Chaining it over l = 0 .. L-1 from the embedding output reproduces
+ * orc_forward bit for bit.  It lets a test feed the GPU's own state after
+ * layer l - 1 and compare one layer at a time.  Returns 0, or -1. */
+int orc_layer(const orc_config* cfg, int l, const uint16_t* const* w,
+              const uint16_t* final_norm, const int32_t* lengths, int B, int S,
+              const float* x_in, float* out) {
+  const int H = cfg->hidden;
+  const int L = cfg->n_encoder_layers + cfg->n_decision_layers;
+  if (l < 0 || l >= L || check_args(cfg, lengths, B, S) != 0) return -1;
+  if (l == cfg->n_encoder_layers && cfg->final_norm && final_norm == NULL) return -1;
+  const size_t M = (size_t)B * S;
+  orc_scratch s;
+  if (scratch_alloc(cfg, M, &s) != 0) return -1;
+  memcpy(out, x_in, sizeof(float) * M * H);
+  layer_step(cfg, l, w, final_norm, lengths, B, S, out, &s);
+  scratch_free(&s);
   return 0;
 }

@@ -259,3 +259,46 @@ def test_rejects_bad_arguments(orc, reduced):
     bad[0, 0] = m["vocab"]
     with pytest.raises(ValueError):
         orc.forward(m, w, bad, [8])                # id out of range
+
+
+def _embedding(orc, m, w, ids):
+    B, S = ids.shape
+    x = orc.embed_layernorm(w["tok_emb"], w["emb_norm"], ids, m["ln_eps"])
+    return bf16_bits_to_f32(x).reshape(B, S, m["hidden"])
+
+
+@pytest.mark.parametrize("accum_f64,out_fp32", [(False, False), (True, False), (False, True)])
+def test_layer_chain_reproduces_forward(orc, reduced, accum_f64, out_fp32):
+    # One layer at a time from the embedding output (the final norm taken
+    # inside the first decision layer) must give the whole stack bit for bit;
+    # a layer that ignored its input, or applied the final norm at the wrong
+    # layer, breaks the chain.
+    m, w = reduced
+    ids, lengths = synth.make_inputs(m, 2, 40, 8, (7, 40))
+    ref = orc.forward(m, w, ids, lengths, accum_f64=accum_f64, out_fp32=out_fp32)
+    x = _embedding(orc, m, w, ids)
+    L = m["n_encoder_layers"] + m["n_decision_layers"]
+    for l in range(L):
+        nxt = orc.layer(m, w, l, x, lengths, accum_f64=accum_f64, out_fp32=out_fp32)
+        assert not np.array_equal(nxt, x)
+        x = nxt
+    np.testing.assert_array_equal(x, ref)
+
+
+def test_layer_matches_the_captured_stream(orc, reduced):
+    m, w = reduced
+    ids, lengths = synth.make_inputs(m, 1, 24, 9)
+    _, c1 = orc.forward(m, w, ids, lengths, capture_layer=1)
+    _, c2 = orc.forward(m, w, ids, lengths, capture_layer=2)
+    np.testing.assert_array_equal(orc.layer(m, w, 2, c1, lengths), c2)
+
+
+def test_layer_rejects_bad_arguments(orc, reduced):
+    m, w = reduced
+    x = np.zeros((1, 8, m["hidden"]), np.float32)
+    with pytest.raises(ValueError):
+        orc.layer(m, w, m["n_encoder_layers"] + m["n_decision_layers"], x, [8])  # no such layer
+    with pytest.raises(ValueError):
+        orc.layer(m, w, 0, x, [9])                                               # length > S
+    with pytest.raises(ValueError):                                              # final norm missing
+        orc.layer(m, dict(w, final_norm=None), m["n_encoder_layers"], x, [8])
