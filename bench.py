@@ -1,20 +1,34 @@
 """Benchmark of the Laya BF16 encoder forward pass (embedding + 28 encoder +
 2 decision layers) on GB300, one JSON line on stdout.
 
-A step is one full forward pass over one batch of the workload (default: the
-full-size stack at 1 x 48 tokens).  `value` is valid tokens per second with
-ids and lengths already resident in device memory (graph replay through
-laya_enc_run_device); `e2e` is the same metric through laya_enc_run with HOST
-ids/lengths (H2D upload inside) plus a device-to-host read of the hidden
-states every step.  Weights (735 MB of projections + 103 MB of embedding) are
-larger than the 126 MB L2, so every step streams them from HBM; no flush.
+A step is one full forward pass over one batch of the workload.  The headline
+workload is the largest single-GPU configuration, the full stack at 16 rows x
+512 tokens with mixed row lengths (uniform in [32, 512], 4117 valid tokens at
+seed 4).  `value` is valid tokens per second with ids and lengths already
+resident in device memory (graph replay through laya_enc_run_device); `e2e`
+is the same metric through laya_enc_run with HOST ids/lengths (H2D upload
+inside the timed region) plus a device-to-host read of the hidden states
+every step.  The weights (735 MB of projections + 103 MB of embedding) are
+larger than the 129 MB L2, so every step streams them from HBM; no flush.
+
+`per_config` repeats the device-resident and end-to-end timings for every
+other workload (each with its own seeded weights), so that one run reports
+every configuration.
+
+Per-kernel device times come from the library's profiling mode: the same
+graph of the same kernels (same plans, same programmatic dependent launch),
+in which each kernel's first CTA records when its dependency wait returned.
+Launch k is charged the time from its release to the release of launch k+1,
+so the classes add up to the forward's device time with the overlap of the
+replay.  `roofline` is the class with the largest share, against the measured
+peaks in MEASURED_PEAKS.json (or the fallback when that file is absent).
 
 Multi-GPU: the forward pass has no exchange step, so N GPUs run N independent
-replicas (one process per GPU under torchrun), `value` counts every rank's
+replicas (one process per GPU under torchrun); `value` counts every rank's
 tokens over the slowest rank's time.
 
 --impl reference times the CPU oracle (the only other implementation there
-is) on the host cores, on the same workload.
+is) on the host cores, on a bounded sample of the same workload.
 """
 from __future__ import annotations
 
@@ -36,10 +50,14 @@ from transformer_encoder_bf16_gb300 import synth  # noqa: E402
 
 METRIC = "encoder fwd p50 ms & tokens/s (28+2 layers, BF16, 1 GB300); % of roofline"
 UNIT = "tokens/s"
-# H800 CUDA-event p50 of the Rust encoder at 1 x 48 (PR #49, run 1), other hardware
+HEADLINE = "full_16x512"
+# H800 CUDA-event p50 of the Rust encoder (PR #49, run 1), other hardware: context only
 PUBLISHED_MS = {"full_1x48": 2.771, "full_4x64": 3.195, "full_1x464": 3.742,
                 "full_4x464": 7.545, "full_16x512": 25.785}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+GEMM_CLASSES = ("qkv", "out_proj", "up_geglu", "down")
+# tokens the oracle samples per reference-arm step (one row of the workload, cut)
+REFERENCE_SAMPLE_TOKENS = 64
 
 
 def log(*a):
@@ -109,19 +127,16 @@ def load_peaks():
     if os.path.exists(p):
         try:
             with open(p) as f:
-                d = json.load(f)
-            return d, "measured"
+                return json.load(f), "measured"
         except Exception:
             pass
     return dict(FALLBACK_PEAKS), "fallback"
 
 
 def peak_value(peaks, key):
-    for k, v in peaks.items():
-        if k == key and isinstance(v, (int, float)):
-            return float(v)
-    # tolerate nested layouts, e.g. {"hbm_gbs": {"value": ...}}
     v = peaks.get(key)
+    if isinstance(v, (int, float)):
+        return float(v)
     if isinstance(v, dict):
         for kk in ("value", "median", "max"):
             if isinstance(v.get(kk), (int, float)):
@@ -190,8 +205,23 @@ def gemm_shapes(model):
             "up_geglu": (2 * I, H, I, False), "down": (H, I, H, True)}
 
 
-def algorithmic(model, cls, M):
-    """(bytes, flops) one launch of a kernel class must move / compute."""
+def attention_pairs(model, lengths, glob):
+    """(query, key) pairs a layer's attention must visit, per head."""
+    w = model["local_half_window"]
+    n = 0
+    for L in np.asarray(lengths, np.int64):
+        if glob:
+            n += int(L) * int(L)
+        else:
+            i = np.arange(L)
+            n += int(np.sum(np.minimum(i + w, L - 1) - np.maximum(i - w, 0) + 1))
+    return n
+
+
+def algorithmic(model, cls, M, lengths=None):
+    """(bytes, flops) one launch of a kernel class must move / compute (M
+    tokens processed; attention flops on the visible pairs, averaged over the
+    layer schedule)."""
     H = model["hidden"]
     g = gemm_shapes(model)
     if cls in g:
@@ -205,34 +235,45 @@ def algorithmic(model, cls, M):
     if cls == "rope":
         return 2 * (2 * 2 * M * H), 0.0
     if cls == "attention":
-        return 2 * (3 * M * H + M * H), 0.0
-    if cls == "fused":
-        # the whole forward: every layer's four projections (weights once)
-        L = model["n_encoder_layers"] + model["n_decision_layers"]
-        b = f = 0.0
-        for k in g:
-            kb, kf = algorithmic(model, k, M)
-            b, f = b + kb, f + kf
-        return L * b, L * f
+        f = 0.0
+        if lengths is not None:
+            L = model["n_encoder_layers"] + model["n_decision_layers"]
+            for l in range(L):
+                glob = l >= model["n_encoder_layers"] or l % model["global_every"] == 0
+                f += 4.0 * model["head_dim"] * model["heads"] * attention_pairs(model, lengths, glob)
+            f /= L
+        return 2 * (3 * M * H + M * H), f
+    if cls == "output":
+        return 2 * 2 * M * H, 0.0
     return 0, 0.0
 
 
-def cpu_baseline(model, weights, ids, lengths, budget_s=12.0):
-    """The oracle as it stands, on the host cores, for about budget_s seconds."""
+def cpu_sample(model, weights, ids, lengths, budget_s, max_tokens=None):
+    """The oracle as it stands, on the host cores: rows of the workload alone
+    (cut to their length, or to max_tokens), in order, until budget_s has
+    passed (at least one row).  Returns (tokens, seconds, rows, cores)."""
     import oracle
     oracle.build()
     cores = oracle.set_threads(0)
-    valid = int(np.sum(lengths))
-    runs, t0 = 0, time.perf_counter()
+    tokens, rows, t0 = 0, 0, time.perf_counter()
+    B = ids.shape[0]
     while True:
-        oracle.forward(model, weights, ids, lengths)
-        runs += 1
+        b = rows % B
+        n = int(lengths[b]) if max_tokens is None else min(int(lengths[b]), max_tokens)
+        oracle.forward(model, weights, ids[b:b + 1, :n], np.array([n], np.int32))
+        tokens += n
+        rows += 1
         el = time.perf_counter() - t0
-        if el >= budget_s or runs >= 50:
-            break
-    return {"value": valid * runs / el, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{runs} full forward pass(es) of the workload ({valid} valid tokens each), "
-                      f"{el:.1f} s, OpenMP over {cores} threads"}
+        if el >= budget_s or rows >= 4 * B:
+            return tokens, el, rows, cores
+
+
+def cpu_baseline(model, weights, ids, lengths, budget_s=15.0):
+    tokens, el, rows, cores = cpu_sample(model, weights, ids, lengths, budget_s)
+    return {"value": tokens / el, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{rows} row(s) of the workload, each alone and cut to its length "
+                      f"({tokens} valid tokens, full 28+2-layer stack), {el:.1f} s, OpenMP "
+                      f"over {cores} threads"}
 
 
 def run_reference(args, model, weights, ids, lengths, world, rank):
@@ -241,30 +282,172 @@ def run_reference(args, model, weights, ids, lengths, world, rank):
     import oracle
     oracle.build()
     cores = oracle.set_threads(0)
-    valid = int(np.sum(lengths))
-    for _ in range(args.warmup):
-        oracle.forward(model, weights, ids, lengths)
-    times = []
+    B = ids.shape[0]
+
+    def sample(i):
+        b = i % B
+        n = min(int(lengths[b]), REFERENCE_SAMPLE_TOKENS)
+        oracle.forward(model, weights, ids[b:b + 1, :n], np.array([n], np.int32))
+        return n
+
+    for i in range(min(args.warmup, 2)):
+        sample(i)
+    times, toks = [], []
     t_all = time.perf_counter()
-    for _ in range(args.steps):
+    for i in range(args.steps):
         t0 = time.perf_counter()
-        oracle.forward(model, weights, ids, lengths)
+        toks.append(sample(i))
         times.append(time.perf_counter() - t0)
         if time.perf_counter() - t_all > args.reference_budget:
             break
     total = sum(times)
-    value = valid * len(times) / total
+    value = sum(toks) / total
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": len(times), "warmup": args.warmup,
             "ms_per_step": 1000 * total / len(times), "p50_ms": 1000 * float(np.median(times)),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": {"workload": args.workload, "batch": int(ids.shape[0]),
-                                            "seq": int(ids.shape[1]), "valid_tokens": valid},
+            "data": "synthetic", "config": {"workload": args.workload, "batch": int(B),
+                                            "seq": int(ids.shape[1]),
+                                            "valid_tokens": int(np.sum(lengths))},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"{len(times)} full forward passes of the workload on the "
-                                       f"host cores (steps capped at {args.reference_budget:.0f} s)"},
+                             "sample": f"each step: one row of the workload (rows in turn), its "
+                                       f"first {REFERENCE_SAMPLE_TOKENS} tokens (or all if "
+                                       f"shorter), full 28+2-layer stack, OpenMP over {cores} "
+                                       f"threads; steps capped at {args.reference_budget:.0f} s"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def measure(te, torch, enc, model, ids, lengths, steps, warmup, stream, world, clocks=None):
+    """Device-resident replay timing, end-to-end timing and the per-class
+    profile of one workload on one encoder handle."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    B, S = ids.shape
+    H = model["hidden"]
+    valid = int(np.sum(lengths))
+    out = torch.empty((B, S, H), dtype=torch.bfloat16, device=dev)
+    ids_dev = torch.from_numpy(ids).to(dev)
+    len_dev = torch.from_numpy(lengths).to(dev)
+
+    # ---- device-resident timing (graph replay) -----------------------------
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            enc.run_device(ids_dev, len_dev, out, stream)
+    enc.check(stream)
+    first_shape = enc.cache_stats()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    if clocks is not None:
+        clocks.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    first = torch.cuda.Event(enable_timing=True)
+    last = torch.cuda.Event(enable_timing=True)
+    first.record(stream)
+    for i in range(steps):
+        starts[i].record(stream)
+        enc.run_device(ids_dev, len_dev, out, stream)
+        ends[i].record(stream)
+    last.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop() if clocks is not None else None
+    enc.check(stream)
+    total_ms = max_over_ranks(first.elapsed_time(last), world)
+    step_ms = np.array([s.elapsed_time(e) for s, e in zip(starts, ends)])
+
+    # ---- end-to-end through the public host API -----------------------------
+    host_out = torch.empty((B, S, H), dtype=torch.bfloat16, pin_memory=True)
+    for _ in range(3):
+        enc.run(ids, lengths, out, stream)
+        host_out.copy_(out, non_blocking=True)
+        stream.synchronize()
+    barrier(world)
+    e2e_times = []
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        ts = time.perf_counter()
+        with torch.cuda.stream(stream):
+            enc.run(ids, lengths, out, stream)
+            host_out.copy_(out, non_blocking=True)
+        stream.synchronize()
+        e2e_times.append(time.perf_counter() - ts)
+    e2e_total = max_over_ranks(time.perf_counter() - t0, world)
+    enc.check(stream)
+
+    # ---- per-class device time: the stamped graph of the same kernels -------
+    enc.set_profiling(True)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            enc.run_device(ids_dev, len_dev, out, stream)
+    enc.profile_read()
+    pstarts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    pends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        pstarts[i].record(stream)
+        enc.run_device(ids_dev, len_dev, out, stream)
+        pends[i].record(stream)
+    prof = enc.profile_read()
+    enc.set_profiling(False)
+    torch.cuda.synchronize()
+    enc.check(stream)
+    prof_step_ms = float(np.median([s.elapsed_time(e) for s, e in zip(pstarts, pends)]))
+    return {"valid": valid, "B": B, "S": S, "total_ms": total_ms, "step_ms": step_ms,
+            "e2e_total_s": e2e_total, "e2e_times": e2e_times, "prof": prof,
+            "prof_step_ms": prof_step_ms, "first_shape": first_shape, "clocks": clk,
+            "launches": enc.launch_count(B, S)}
+
+
+def analyse(model, r, steps, world, peaks):
+    """The figures of one workload's measurement."""
+    B, S, valid = r["B"], r["S"], r["valid"]
+    # tokens the kernels process: batches of several rows are packed (the
+    # padding is skipped), a single row is processed whole
+    M = valid if B > 1 else B * S
+    lengths = r.get("lengths")
+    hbm_peak = peak_value(peaks, "hbm_gbs")
+    tc_peak = peak_value(peaks, "bf16_tflops")
+    tc_sus = peak_value(peaks, "bf16_tflops_sustained")
+    per_step = {k: ms / steps for k, (ms, n) in r["prof"].items() if n}
+    launches = {k: n / steps for k, (ms, n) in r["prof"].items() if n}
+    p50 = float(np.median(r["step_ms"]))
+    fwd_bytes = sum(algorithmic(model, k, M, lengths)[0] * launches[k] for k in launches)
+    fwd_flops = sum(algorithmic(model, k, M, lengths)[1] * launches[k] for k in launches)
+    t_roof = max(fwd_bytes / (hbm_peak * 1e9), fwd_flops / (tc_peak * 1e12))
+    classes = {}
+    for k in per_step:
+        avg_s = per_step[k] / launches[k] / 1000.0
+        nb, nf = algorithmic(model, k, M, lengths)
+        c = {"ms_per_step": per_step[k], "launches_per_step": launches[k],
+             "us_per_launch": avg_s * 1e6, "GB_s": nb / avg_s / 1e9}
+        if nf:
+            c["TFLOP_s"] = nf / avg_s / 1e12
+            c["frac_of_bf16_burst"] = c["TFLOP_s"] / tc_peak
+        c["frac_of_hbm"] = c["GB_s"] / hbm_peak
+        classes[k] = c
+    prof_sum = sum(per_step.values())
+    return {"p50_ms": p50, "p95_ms": float(np.percentile(r["step_ms"], 95)),
+            "ms_per_step": r["total_ms"] / steps,
+            "valid_tokens_per_s": valid * steps * world / (r["total_ms"] / 1000.0),
+            "padded_tokens_per_s": B * S * steps * world / (r["total_ms"] / 1000.0),
+            "e2e_tokens_per_s": valid * steps * world / r["e2e_total_s"],
+            "e2e_p50_ms": 1000 * float(np.median(r["e2e_times"])),
+            "launches_per_forward": r["launches"],
+            "forward_roofline": {"bytes": fwd_bytes, "flops": fwd_flops,
+                                 "t_roof_us": t_roof * 1e6, "frac_of_p50": t_roof / (p50 / 1000),
+                                 "bound": ("tensor" if fwd_flops / (tc_peak * 1e12) >
+                                           fwd_bytes / (hbm_peak * 1e9) else "hbm")},
+            "kernel_classes": classes,
+            "profiled_step_ms": r["prof_step_ms"],
+            "class_sum_ms": prof_sum,
+            "class_sum_over_p50": prof_sum / p50,
+            "gemm_tflops_valid": (sum(algorithmic(model, k, M)[1] * launches[k]
+                                      for k in GEMM_CLASSES if k in launches) /
+                                  (sum(per_step[k] for k in GEMM_CLASSES if k in per_step) / 1000)
+                                  / 1e12) if any(k in per_step for k in GEMM_CLASSES) else None,
+            "tc_peak": tc_peak, "tc_sustained": tc_sus, "hbm_peak": hbm_peak,
+            "M": M}
 
 
 def main():
@@ -273,8 +456,11 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="full_1x48", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time the headline workload only")
+    ap.add_argument("--per-config-steps", type=int, default=50)
     ap.add_argument("--reference-budget", type=float, default=150.0)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
@@ -301,108 +487,60 @@ def main():
         torch.cuda.set_device(0)
     tebuild.build()
     dev = torch.device("cuda", torch.cuda.current_device())
-    enc = te.Encoder(model, te.upload_weights(weights, dev))
-    stream = torch.cuda.Stream(device=dev)
-    H = model["hidden"]
-    out = torch.empty((B, S, H), dtype=torch.bfloat16, device=dev)
-    ids_dev = torch.from_numpy(ids).to(dev)
-    len_dev = torch.from_numpy(lengths).to(dev)
-
-    # ---- device-resident timing (graph replay) -----------------------------
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            enc.run_device(ids_dev, len_dev, out, stream)
-    enc.check(stream)
-    # first run of the shape: workspace allocation, two eager warm-ups, graph
-    # capture and instantiation (host wall time, reported apart from the replays)
-    first_shape = enc.cache_stats()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    clocks = ClockSampler(torch.cuda.current_device() if world == 1 else local_rank)
-    clocks.start()
-    time.sleep(0.3)
-    barrier(world)
-    torch.cuda.synchronize()
-    first = torch.cuda.Event(enable_timing=True)
-    last = torch.cuda.Event(enable_timing=True)
-    first.record(stream)
-    for i in range(args.steps):
-        starts[i].record(stream)
-        enc.run_device(ids_dev, len_dev, out, stream)
-        ends[i].record(stream)
-    last.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    clk = clocks.stop()
-    enc.check(stream)
-    total_ms = first.elapsed_time(last)
-    step_ms = np.array([s.elapsed_time(e) for s, e in zip(starts, ends)])
-    total_ms_max = max_over_ranks(total_ms, world)
-    value = valid * args.steps * world / (total_ms_max / 1000.0)
-
-    # ---- end-to-end through the public host API -----------------------------
-    host_out = torch.empty((B, S, H), dtype=torch.bfloat16, pin_memory=True)
-    for _ in range(3):
-        enc.run(ids, lengths, out, stream)
-        host_out.copy_(out, non_blocking=True)
-        stream.synchronize()
-    barrier(world)
-    t0 = time.perf_counter()
-    e2e_times = []
-    for _ in range(args.steps):
-        ts = time.perf_counter()
-        with torch.cuda.stream(stream):
-            enc.run(ids, lengths, out, stream)
-            host_out.copy_(out, non_blocking=True)
-        stream.synchronize()
-        e2e_times.append(time.perf_counter() - ts)
-    e2e_total = max_over_ranks(time.perf_counter() - t0, world)
-    enc.check(stream)
-
-    # ---- per-kernel device time, eager launches bracketed by events ---------
-    enc.set_profiling(True)
-    enc.profile_read()
-    for _ in range(args.steps):
-        enc.run_device(ids_dev, len_dev, out, stream)
-    prof = enc.profile_read()
-    enc.set_profiling(False)
     peaks, peak_src = load_peaks()
-    # tokens the kernels process: batches of several rows are packed (the
-    # padding is skipped), a single row is processed whole
-    M = valid if B > 1 else B * S
-    best = None
-    for cls, (ms, n) in prof.items():
-        if n == 0:
-            continue
-        if best is None or ms > best[1]:
-            best = (cls, ms, n)
-    cls, ms, n = best
-    avg_s = ms / n / 1000.0
-    nbytes, flops = algorithmic(model, cls, M)
-    hbm_peak = peak_value(peaks, "hbm_gbs")
-    tc_peak = peak_value(peaks, "bf16_tflops")
-    t_mem = nbytes / (hbm_peak * 1e9)
-    t_tc = flops / (tc_peak * 1e12) if flops else 0.0
-    if t_tc > t_mem:
-        roof = {"bound": "tensor", "achieved": flops / avg_s / 1e12, "peak": tc_peak,
-                "unit": "TFLOP/s"}
+    stream = torch.cuda.Stream(device=dev)
+
+    enc = te.Encoder(model, te.upload_weights(weights, dev))
+    clocks = ClockSampler(torch.cuda.current_device() if world == 1 else local_rank)
+    r = measure(te, torch, enc, model, ids, lengths, args.steps, args.warmup, stream, world, clocks)
+    r["lengths"] = lengths
+    enc.close()
+    a = analyse(model, r, args.steps, world, peaks)
+
+    # roofline of the dominant kernel class (largest share of the forward)
+    cls = max(a["kernel_classes"], key=lambda k: a["kernel_classes"][k]["ms_per_step"])
+    c = a["kernel_classes"][cls]
+    nbytes, flops = algorithmic(model, cls, a["M"], lengths)
+    if flops and flops / (a["tc_peak"] * 1e12) > nbytes / (a["hbm_peak"] * 1e9):
+        roof = {"bound": "tensor", "achieved": c["TFLOP_s"], "peak": a["tc_peak"],
+                "unit": "TFLOP/s", "frac_of_sustained": c["TFLOP_s"] / a["tc_sustained"]}
     else:
-        roof = {"bound": "hbm", "achieved": nbytes / avg_s / 1e9, "peak": hbm_peak, "unit": "GB/s"}
+        roof = {"bound": "hbm", "achieved": c["GB_s"], "peak": a["hbm_peak"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = recorded_traffic(args.workload, cls)
-    roof["kernel"] = cls
-    roof["avg_launch_us"] = avg_s * 1e6
-    roof["launches"] = n
-    roof["algorithmic_bytes_per_launch"] = nbytes
-    roof["algorithmic_flops_per_launch"] = flops
-    roof["peak_source"] = f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'fallback'})"
-    kernel_ms_per_step = {k: (v[0] / args.steps) for k, v in prof.items()}
+    roof.update({"kernel": cls, "avg_launch_us": c["us_per_launch"],
+                 "launches_per_step": c["launches_per_step"],
+                 "algorithmic_bytes_per_launch": nbytes, "algorithmic_flops_per_launch": flops,
+                 "timing": "release-to-release stamps in the replayed graph (same kernels, same "
+                           "programmatic dependent launch); classes sum to "
+                           f"{a['class_sum_over_p50']:.3f} x the p50 step",
+                 "peak_source": f"{peak_src} ({'MEASURED_PEAKS.json, burst' if peak_src == 'measured' else 'fallback'})"})
 
-    # whole-forward roofline: weights + activations at HBM peak vs flops at tensor peak
-    fwd_bytes = sum(algorithmic(model, k, M)[0] * (c / args.steps) for k, (_, c) in prof.items())
-    fwd_flops = sum(algorithmic(model, k, M)[1] * (c / args.steps) for k, (_, c) in prof.items())
-    t_roof = max(fwd_bytes / (hbm_peak * 1e9), fwd_flops / (tc_peak * 1e12))
-    p50 = float(np.median(step_ms))
+    per_config = {}
+    if not args.no_per_config:
+        for name in sorted(synth.WORKLOADS):
+            if name == args.workload:
+                continue
+            m2, b2, s2, seed2, lr2 = synth.WORKLOADS[name]
+            w2 = synth.make_weights(m2, seed2)
+            ids2, len2 = synth.make_inputs(m2, b2, s2, seed2, lr2)
+            e2 = te.Encoder(m2, te.upload_weights(w2, dev))
+            del w2
+            r2 = measure(te, torch, e2, m2, ids2, len2, args.per_config_steps, args.warmup,
+                         stream, world)
+            r2["lengths"] = len2
+            e2.close()
+            a2 = analyse(m2, r2, args.per_config_steps, world, peaks)
+            pub = PUBLISHED_MS.get(name)
+            per_config[name] = {
+                "batch": b2, "seq": s2, "valid_tokens": int(np.sum(len2)),
+                "steps": args.per_config_steps, **{k: a2[k] for k in (
+                    "p50_ms", "p95_ms", "ms_per_step", "valid_tokens_per_s", "e2e_tokens_per_s",
+                    "e2e_p50_ms", "launches_per_forward", "forward_roofline", "gemm_tflops_valid",
+                    "class_sum_over_p50")},
+                "kernel_ms_per_step": {k: v["ms_per_step"] for k, v in a2["kernel_classes"].items()},
+                "h800_rust_cuda_event_p50_ms": pub}
+            torch.cuda.empty_cache()
 
     if rank == 0:
         cpu = None
@@ -413,36 +551,38 @@ def main():
                 cpu = {"value": None, "unit": UNIT, "cores": 0, "kind": "oracle",
                        "sample": f"unavailable: {ex}"}
         pub = PUBLISHED_MS.get(args.workload)
+        value = a["valid_tokens_per_s"]
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": total_ms_max / args.steps,
-            "padded_tokens_per_s": B * S * args.steps * world / (total_ms_max / 1000.0),
-            "first_shape_ms": {"workspace_setup": first_shape["setup_ms"],
-                               "warmup_capture_instantiate": first_shape["capture_ms"]},
-            "p50_ms": p50, "p95_ms": float(np.percentile(step_ms, 95)),
+            "ms_per_step": a["ms_per_step"],
+            "p50_ms": a["p50_ms"], "p95_ms": a["p95_ms"],
+            "padded_tokens_per_s": a["padded_tokens_per_s"],
+            "first_shape_ms": {"workspace_setup": r["first_shape"]["setup_ms"],
+                               "warmup_capture_instantiate": r["first_shape"]["capture_ms"]},
             "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": (value / world) / (valid / (pub / 1000.0)) if pub else None,
-            "vs_baseline_ref": (f"H800 CUDA-event p50 {pub} ms (PR #49, Rust, run 1); other hardware"
-                                if pub else None),
+            "vs_baseline": None,
+            "h800_context": (f"H800 CUDA-event p50 {pub} ms (PR #49, Rust, run 1) = "
+                             f"{valid / (pub / 1000.0):.0f} valid tokens/s; other hardware"
+                             if pub else None),
             "dtype": "bf16", "data": "synthetic",
             "config": {"workload": args.workload, "batch": B, "seq": S, "valid_tokens": valid,
                        "l2": "weights 838 MB > L2 (129 MB): streamed from HBM every step, no flush",
                        "graphs": True, "pdl": os.environ.get("LAYA_NO_PDL", "0") in ("", "0"),
                        "parallelism": f"replicas x{world}"},
-            "clocks": clk,
-            "e2e": {"value": valid * args.steps * world / e2e_total, "unit": UNIT,
-                    "p50_ms": 1000 * float(np.median(e2e_times)),
-                    "h2d_bytes_per_step": 4 * (B * S + B), "d2h_bytes_per_step": 2 * B * S * H},
-            "gpu_launches": enc.launch_count(B, S) * args.steps,
+            "clocks": r["clocks"],
+            "e2e": {"value": a["e2e_tokens_per_s"], "unit": UNIT, "p50_ms": a["e2e_p50_ms"],
+                    "h2d_bytes_per_step": 4 * (B * S + B), "d2h_bytes_per_step": 2 * B * S * model["hidden"]},
+            "gpu_launches": a["launches_per_forward"] * args.steps,
             "roofline": roof,
-            "forward_roofline": {"bytes": fwd_bytes, "flops": fwd_flops,
-                                 "t_roof_us": t_roof * 1e6, "frac_of_p50": t_roof / (p50 / 1000)},
-            "kernel_ms_per_step": kernel_ms_per_step,
+            "gemm_tflops_valid": a["gemm_tflops_valid"],
+            "forward_roofline": a["forward_roofline"],
+            "kernel_classes": a["kernel_classes"],
+            "class_sum_over_p50": a["class_sum_over_p50"],
+            "per_config": per_config,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
-    enc.close()
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

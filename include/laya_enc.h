@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define LAYA_ENC_ABI_VERSION 2
+#define LAYA_ENC_ABI_VERSION 3
 
 /* Error codes (negative). */
 #define LAYA_OK 0
@@ -81,8 +81,7 @@ typedef struct {
                        states ("[Performance]: Optimize native Rust/CUDA Laya
                        inference #66", "Starting evidence") can be read
                        without that last rounding.  Rounding this output to
-                       BF16 gives the out_fp32 = 0 result bit for bit.  The
-                       fused short-request kernel is not used in this mode. */
+                       BF16 gives the out_fp32 = 0 result bit for bit. */
 } laya_enc_config;
 
 /* Per-layer weights: device pointers to BF16 data in nn.Linear layout
@@ -139,6 +138,30 @@ int laya_enc_run(laya_enc_handle* h, const int32_t* token_ids,
                  const int32_t* lengths, int batch, int seq, void* out_hidden,
                  void* stream);
 
+/* Most marker slots one laya_enc_run_markers call takes ("Laya native CUDA
+ * worker", "Start and check": at most 2048 markers per request). */
+#define LAYA_ENC_MAX_MARKERS 2048
+
+/* The forward pass with the last layer at marker rows only ("perf(model):
+ * exact Metal speed-ups of the forward pass - #45": only the marker positions
+ * reach the scorer; keys and values need every position, but everything after
+ * them is row-wise and attention is independent per query row, so the last
+ * layer attends from, projects and runs its MLP on the batch * kmax marker
+ * rows alone).  token_ids, lengths: as laya_enc_run (HOST).  marker_pos: HOST
+ * int32 [batch * kmax]; marker_pos[b * kmax + j] is a position in [0,
+ * lengths[b]) of row b, or -1 for an empty slot.  out_markers: DEVICE BF16
+ * [batch * kmax, hidden] (fp32 when cfg.out_fp32), caller-owned; slot
+ * b * kmax + j receives the final hidden state of token (b, marker_pos), the
+ * value laya_enc_run leaves at out_hidden[b, marker_pos] up to the order of
+ * fp32 sums in the last layer's projections; empty slots receive finite values
+ * of no meaning.  batch * kmax <= LAYA_ENC_MAX_MARKERS; a marker on padding
+ * (>= lengths[b]) or below -1 is LAYA_E_INVAL.  The workspace and graph cache
+ * is keyed by (batch, seq, kmax).  Otherwise as laya_enc_run. */
+int laya_enc_run_markers(laya_enc_handle* h, const int32_t* token_ids,
+                         const int32_t* lengths, int batch, int seq,
+                         const int32_t* marker_pos, int kmax, void* out_markers,
+                         void* stream);
+
 /* As laya_enc_run, with token_ids and lengths in DEVICE memory (int32, same
  * layouts).  Ids cannot be checked on the host: an out-of-range id or length
  * is clamped by the kernels and reported as LAYA_E_DEVICE by laya_enc_check. */
@@ -159,19 +182,6 @@ int laya_enc_debug_fail_next_run(laya_enc_handle* h);
 
 /* 1: use CUDA Graphs (default, unless env LAYA_EAGER=1); 0: eager launches. */
 int laya_enc_set_graphs(laya_enc_handle* h, int enabled);
-
-/* 1: a request of at most 128 tokens (batch * seq <= 128) runs as ONE
- * persistent kernel, launched cooperatively in clusters of four CTAs (one per
- * SM), that streams every layer's weights by TMA while earlier phases run;
- * split-K projections on tcgen05 reduced through distributed shared memory,
- * LayerNorm applied as activation tiles are loaded, attention on mma.sync.
- * Same layer equations and result contract as the layer-by-layer path;
- * launched eagerly (no graph) and not used while `stream` is capturing.
- * 0 (default, unless env LAYA_FUSED=1): the layer-by-layer kernels.
- * Sources: "[Performance]: Optimize native Rust/CUDA Laya inference #66"
- * ("Implementation priorities": the short shapes are weight-streaming
- * bound). */
-int laya_enc_set_fused(laya_enc_handle* h, int enabled);
 
 /* The per-shape workspace and CUDA Graph cache ("[RFC]: Native Laya inference
  * with Rust and CUDA #14", "Design": capture per shape, replay, an LRU of at
@@ -209,24 +219,44 @@ int laya_enc_workspace_bytes(const laya_enc_handle* h, int batch, int seq,
 /* Kernel classes reported by the profiling calls below. */
 #define LAYA_PROF_EMBED_NORM 0 /* embedding gather + LayerNorm */
 #define LAYA_PROF_NORM 1       /* LayerNorm (attention, MLP and final norms) */
-#define LAYA_PROF_QKV 2        /* QKV projection */
-#define LAYA_PROF_ROPE 3       /* RoPE */
+#define LAYA_PROF_QKV 2        /* QKV projection (RoPE in its epilogue) */
+#define LAYA_PROF_ROPE 3       /* stand-alone RoPE (not launched by the forward) */
 #define LAYA_PROF_ATTN 4       /* attention */
 #define LAYA_PROF_OUT 5        /* attention output projection + residual */
 #define LAYA_PROF_UP 6         /* MLP up-projection + GeGLU */
 #define LAYA_PROF_DOWN 7       /* MLP down-projection + residual */
-#define LAYA_PROF_FUSED 8      /* the whole forward as one kernel (short requests) */
+#define LAYA_PROF_OUTPUT 8     /* copies into the caller's layout (padded output rows) */
 #define LAYA_PROF_CLASSES 9
 
-/* Measurement aid.  While enabled, laya_enc_run launches eagerly (no graph,
- * no programmatic dependent launch) and brackets every kernel with CUDA events
- * on the caller's stream; each run first folds the previous run's event times
+/* Measurement aid.  While enabled, laya_enc_run / laya_enc_run_device launch
+ * the same kernels as without it (same plans, same programmatic dependent
+ * launch, replayed from a graph of their own when graphs are on), except that
+ * the first CTA of every kernel records the %globaltimer value at which its
+ * dependency wait returned, i.e. when the kernel before it completed, and a
+ * one-thread kernel marks the completion of the last.  Launch k is charged
+ * the time from its own release to the release of launch k + 1, so the
+ * charges of a forward add up to its device time with the overlap of the
+ * graph replay.  Each run first folds the previous profiled run's stamps
  * into per-class totals (waiting for that run to finish). */
 int laya_enc_set_profiling(laya_enc_handle* h, int enabled);
 
 /* Folds in the last run, then returns and clears the totals: ms[c] (device
  * time) and launches[c] for classes c < n (n <= LAYA_PROF_CLASSES). */
 int laya_enc_profile_read(laya_enc_handle* h, double* ms, int* launches, int n);
+
+/* Debug aid for per-layer parity: runs the forward as laya_enc_run does (host
+ * token_ids and lengths, out_hidden written the same way) but eagerly, and
+ * also writes `states`: DEVICE BF16 [L, batch, seq, hidden] (L = encoder +
+ * decision layers), caller-owned, where states[l] is the residual stream
+ * entering layer l in the padded layout (states[0]: the embedding output;
+ * states[n_encoder_layers]: the stream before the final norm).  Padded
+ * positions hold 0.  With out_hidden, this gives the input and the output of
+ * every layer, so that a checker can run one layer at a time on the GPU's own
+ * state.  Same argument errors as laya_enc_run; states must be 16-byte
+ * aligned. */
+int laya_enc_debug_capture(laya_enc_handle* h, const int32_t* token_ids,
+                           const int32_t* lengths, int batch, int seq, void* out_hidden,
+                           void* states, void* stream);
 
 /* Frees the handle and every workspace and graph it owns.  NULL is allowed. */
 int laya_enc_destroy(laya_enc_handle* h);

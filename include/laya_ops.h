@@ -14,6 +14,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "laya_enc.h"
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -74,6 +76,24 @@ int laya_op_rope(void* qkv, const float* cos_dev, const float* sin_dev, int B,
 int laya_op_attention(const void* qkv, const int32_t* lengths_dev, int B, int S,
                       int heads, int head_dim, int global, int half_window,
                       void* ctx, void* stream);
+
+/* laya_op_attention from a subset of query rows ("perf(model): exact Metal
+ * speed-ups of the forward pass - #45": attention over a subset of query rows
+ * gets its own entry point; the marker-row last layer attends from the marker
+ * rows only, with the (b, 1, 1, s) key-padding row of its batch row broadcast
+ * over them).  Slot m = b * kmax + r (r < kmax) is query token q_tok_dev[m] (a
+ * row of qkv, normally b * S + q_pos_dev[m]) at position q_pos_dev[m] of row
+ * b (the window's reference on local layers); keys and values are row b's
+ * tokens below lengths[b].  qkv [B*S, 3H] and lengths_dev as for
+ * laya_op_attention; q_tok_dev, q_pos_dev: DEVICE int32 [B*kmax]; ctx_rows:
+ * DEVICE BF16 [B*kmax, H], slot m's context.  B * kmax <=
+ * LAYA_ENC_MAX_MARKERS.  Same arithmetic as laya_op_attention (mma.sync
+ * tiles, key tiles in the same order), so a slot's context equals that
+ * kernel's context of the same query row bit for bit. */
+int laya_op_attention_rows(const void* qkv, const int32_t* lengths_dev,
+                           const int32_t* q_tok_dev, const int32_t* q_pos_dev, int B,
+                           int S, int kmax, int heads, int head_dim, int global,
+                           int half_window, void* ctx_rows, void* stream);
 
 /* laya_op_attention on the 5th-generation tensor cores: S = Q K^T and O = P V
  * by tcgen05.mma with fp32 accumulators in tensor memory, one CTA per 128

@@ -2,7 +2,7 @@
 patterns and the comparison measures (no arithmetic of the method)."""
 import numpy as np
 
-from transformer_encoder_bf16_gb300.synth import bf16_bits_to_f32
+from transformer_encoder_bf16_gb300.synth import bf16_bits_to_f32, f32_to_bf16_bits
 
 
 def require_gpu():
@@ -57,3 +57,8 @@ def bf16_close(got_bits, ref_bits, ulps=1.0, min_exact=0.95, rel_floor=2.0 ** -1
     exact = float(np.mean(np.asarray(got_bits) == np.asarray(ref_bits))) if d.size else 1.0
     ok = worst <= 1.0 and exact >= min_exact
     return ok, f"worst {worst:.3f} of the allowed step, exact fraction {exact:.5f}"
+
+
+def rnd_bits(rng, shape, std=1.0, mean=0.0):
+    """Seeded normal draws rounded to BF16 bit patterns (test inputs)."""
+    return f32_to_bf16_bits(rng.standard_normal(shape).astype(np.float32) * std + mean)

@@ -14,8 +14,11 @@ So:
   * depth prefix (layers 0-3: global, local, local, global): nRMS <= 5e-3,
     the pages' limit as written;
   * full depth: the GPU must be no farther from the fp64-summed oracle than
-    the fp32-summed oracle is (nRMS within 1.5x, max-abs within 2x), and
-    within 2x of that floor from the fp32 oracle.
+    the fp32-summed oracle is (nRMS within 1.5x; max-abs within 2x plus one
+    BF16 step of the largest reference magnitude), and within 2x of that
+    floor from the fp32 oracle;
+  * every layer alone, fed the GPU's own input state (tests/test_gpu_layers.py):
+    nRMS <= 5e-3 as written, on every row of every workload.
 The 2e-3 max-abs figure of "[RFC]: Native Laya inference with Rust and CUDA
 #14" bounded decision outputs; on BF16 hidden states of magnitude 2..8 a
 single BF16 step is 1.6e-2..3.1e-2, so it is reported, not asserted."""
@@ -30,7 +33,7 @@ import transformer_encoder_bf16_gb300 as te
 from transformer_encoder_bf16_gb300 import synth
 from transformer_encoder_bf16_gb300.synth import bf16_bits_to_f32
 
-from gpu_util import i32_dev, nrms, require_gpu, to_bits
+from gpu_util import i32_dev, nrms, require_gpu, to_bits, ulp_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -104,7 +107,10 @@ def check_full_depth(name, got_bits, model, w, ids, lengths):
     e64, m64 = report(name + " vs fp64 oracle", got_bits, r64, lengths)
     assert e64 <= 1.5 * floor + 1e-4, (name, e64, floor)
     assert e32 <= 2.0 * floor + 1e-4, (name, e32, floor)
-    assert m64 <= 2.0 * floor_abs + 1e-2, (name, m64, floor_abs)
+    # max-abs: twice the oracle pair's own, plus one BF16 step at the largest
+    # reference magnitude (one more flip of the largest element)
+    step = float(ulp_bf16(np.max(np.abs(valid_rows(r64, lengths)))))
+    assert m64 <= 2.0 * floor_abs + step, (name, m64, floor_abs, step)
 
 
 def test_reduced_1x48_matches_oracle():
@@ -122,10 +128,7 @@ def test_depth_prefix_within_page_limit(name, depth):
     model, B, S, seed, lr = synth.WORKLOADS[name]
     w, enc = encoder_for(model, seed, depth)
     ids, lengths = synth.make_inputs(model, B, S, seed, lr)
-    if name == "full_16x512":          # the GPU runs all 16 rows; the oracle the shortest two
-        rows = np.argsort(lengths)[:2]
-    else:
-        rows = np.arange(B)
+    rows = np.arange(B)
     got = run_gpu(enc, ids, lengths)
     for b in rows:
         L = int(lengths[b])
@@ -145,19 +148,16 @@ def test_full_depth_small(name):
     np.testing.assert_array_equal(got, run_gpu(enc, ids, lengths, graphs=False))  # eager == graph
 
 
-@pytest.mark.parametrize("name,rows", [("full_1x464", [0]), ("full_4x464", [2]),
-                                       ("full_16x512", "shortest_and_longest")])
-def test_full_depth_large_sampled_rows(name, rows):
+@pytest.mark.parametrize("name", ["full_1x464", "full_4x464", "full_16x512"])
+def test_full_depth_large_every_row(name):
     # the GPU runs the whole batch in the benchmarked configuration; the oracle
-    # recomputes sampled rows alone, truncated to their length (valid tokens do
-    # not depend on padding: pinned by the oracle's own invariant tests)
+    # recomputes every row alone, truncated to its length (valid tokens do not
+    # depend on padding: pinned by the oracle's own invariant tests)
     model, B, S, seed, lr = synth.WORKLOADS[name]
     w, enc = encoder_for(model, seed)
     ids, lengths = synth.make_inputs(model, B, S, seed, lr)
     got = run_gpu(enc, ids, lengths)
-    if rows == "shortest_and_longest":
-        rows = [int(np.argmin(lengths)), int(np.argmax(lengths))]
-    for b in rows:
+    for b in range(B):
         L = int(lengths[b])
         check_full_depth(f"{name} row {b} (len {L})", got[b:b + 1, :L], model, w,
                          ids[b:b + 1, :L], lengths[b:b + 1])

@@ -94,17 +94,6 @@ def test_fp32_output_reduced_packed_and_repeat_bitwise():
     assert e <= NRMS_LIMIT
 
 
-def test_fp32_output_keeps_the_fused_kernel_off():
-    model = synth.REDUCED
-    _, enc, enc32 = fp32_encoder(model, 0)
-    enc32.set_fused(True)
-    assert enc32.launch_count(1, 48) > 1
-    ids, lengths = synth.make_inputs(model, 1, 48, 0)
-    f = run_f32(enc32, ids, lengths)
-    enc32.set_fused(False)
-    np.testing.assert_array_equal(run_f32(enc32, ids, lengths), f)
-
-
 def test_fp32_output_rejects_a_bf16_buffer():
     torch = require_gpu()
     model = synth.REDUCED

@@ -11,13 +11,9 @@ import oracle
 import transformer_encoder_bf16_gb300 as te
 from transformer_encoder_bf16_gb300.synth import bf16_bits_to_f32, f32_to_bf16_bits
 
-from gpu_util import bf16_close, i32_dev, nrms, require_gpu, to_bits, to_dev, ulp_bf16
+from gpu_util import bf16_close, i32_dev, nrms, require_gpu, rnd_bits, to_bits, to_dev, ulp_bf16
 
 pytestmark = pytest.mark.gpu
-
-
-def rnd_bits(rng, shape, std=1.0, mean=0.0):
-    return f32_to_bf16_bits(rng.standard_normal(shape).astype(np.float32) * std + mean)
 
 
 # ------------------------------------------------------------------ GEMM --

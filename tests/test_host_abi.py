@@ -48,7 +48,7 @@ def test_cache_stats_rejects_null_handle(lib):
 
 
 def test_abi_version(lib):
-    assert te.abi_version() == 2
+    assert te.abi_version() == 3
 
 
 def test_validate_config(lib):

@@ -26,7 +26,7 @@ ERROR_NAMES = {E_INVAL: "LAYA_E_INVAL", E_NOMEM: "LAYA_E_NOMEM", E_CUDA: "LAYA_E
                E_DEVICE: "LAYA_E_DEVICE"}
 KIND_PLAIN, KIND_RESIDUAL, KIND_GEGLU = 0, 1, 2
 PROFILE_CLASSES = ("embed_norm", "norm", "qkv", "rope", "attention", "out_proj", "up_geglu",
-                   "down", "fused")
+                   "down", "output")
 
 
 class LayaError(RuntimeError):
@@ -84,7 +84,7 @@ _SIGNATURES = {
     "laya_enc_check": ([_P, _P], _I),
     "laya_enc_set_graphs": ([_P, _I], _I),
     "laya_enc_debug_fail_next_run": ([_P], _I),
-    "laya_enc_set_fused": ([_P, _I], _I),
+    "laya_enc_debug_capture": ([_P, _P, _P, _I, _I, _P, _P, _P], _I),
     "laya_enc_get_cache_stats": ([_P, _P], _I),
     "laya_enc_launch_count": ([_P, _I, _I], _I),
     "laya_enc_workspace_bytes": ([_P, _I, _I, ctypes.POINTER(_SZ)], _I),
@@ -98,6 +98,8 @@ _SIGNATURES = {
     "laya_op_rope": ([_P, _P, _P, _I, _I, _I, _I, _P], _I),
     "laya_op_attention": ([_P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "laya_op_attention_tc": ([_P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
+    "laya_op_attention_rows": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P], _I),
+    "laya_enc_run_markers": ([_P, _P, _P, _I, _I, _P, _I, _P, _P], _I),
     "laya_op_attention_rope": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "laya_op_linear": ([_P, _I, _I, _P, _I, _I, _P, _P, _P, _SZ, _I, _I, _P], _I),
     "laya_op_linear_noalloc": ([_P, _I, _I, _P, _I, _I, _P, _P, _I, _I, _P], _I),
@@ -207,6 +209,28 @@ class Encoder:
         _check(lib().laya_enc_run(self.handle, ids.ctypes.data, lengths.ctypes.data, B, S,
                                   _ptr(out), _stream_ptr(stream)), self.handle)
 
+    def run_markers(self, ids: np.ndarray, lengths: np.ndarray, marker_pos: np.ndarray, out,
+                    stream=None):
+        """The forward with the last layer at marker rows only.  marker_pos int32
+        [B, kmax] in HOST memory (a position in the row, or -1 for an empty
+        slot); out a device tensor [B * kmax, hidden] (bfloat16, float32 when
+        the model sets out_fp32)."""
+        import torch
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        lengths = np.ascontiguousarray(lengths, dtype=np.int32)
+        marker_pos = np.ascontiguousarray(marker_pos, dtype=np.int32)
+        B, S = ids.shape
+        if marker_pos.ndim != 2 or marker_pos.shape[0] != B:
+            raise LayaError(E_INVAL, "marker_pos must be an int32 [B, kmax] array")
+        kmax = marker_pos.shape[1]
+        want = torch.float32 if self._cfg.out_fp32 else torch.bfloat16
+        if out.dtype != want or not out.is_contiguous() or out.numel() < B * kmax * self._cfg.hidden:
+            raise LayaError(E_INVAL, f"out must be a contiguous {want} tensor of at least "
+                                     f"{B * kmax}x{self._cfg.hidden} elements")
+        _check(lib().laya_enc_run_markers(self.handle, ids.ctypes.data, lengths.ctypes.data, B, S,
+                                          marker_pos.ctypes.data, kmax, _ptr(out),
+                                          _stream_ptr(stream)), self.handle)
+
     def run_device(self, ids_dev, lengths_dev, out, stream=None):
         """ids_dev int32 [B, S] and lengths_dev int32 [B] device tensors."""
         check_device_inputs(ids_dev, lengths_dev)
@@ -233,9 +257,22 @@ class Encoder:
     def set_graphs(self, enabled: bool):
         _check(lib().laya_enc_set_graphs(self.handle, 1 if enabled else 0), self.handle)
 
-    def set_fused(self, enabled: bool):
-        """Short requests (batch * seq <= 128) as one persistent kernel (default off)."""
-        _check(lib().laya_enc_set_fused(self.handle, 1 if enabled else 0), self.handle)
+    def debug_capture(self, ids: np.ndarray, lengths: np.ndarray, out, states, stream=None):
+        """As run(), eagerly, also writing states [L, B, S, hidden] bfloat16:
+        the residual stream entering every layer (padded layout, padding 0)."""
+        import torch
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        lengths = np.ascontiguousarray(lengths, dtype=np.int32)
+        B, S = ids.shape
+        self._check_out(out, B, S)
+        L = self.model["n_encoder_layers"] + self.model["n_decision_layers"]
+        if (states.dtype != torch.bfloat16 or not states.is_contiguous() or not states.is_cuda
+                or states.numel() < L * B * S * self._cfg.hidden):
+            raise LayaError(E_INVAL, f"states must be a contiguous bfloat16 device tensor of at "
+                                     f"least {L}x{B}x{S}x{self._cfg.hidden} elements")
+        _check(lib().laya_enc_debug_capture(self.handle, ids.ctypes.data, lengths.ctypes.data, B, S,
+                                            _ptr(out), _ptr(states), _stream_ptr(stream)),
+               self.handle)
 
     def set_profiling(self, enabled: bool):
         _check(lib().laya_enc_set_profiling(self.handle, 1 if enabled else 0), self.handle)
@@ -323,6 +360,15 @@ def attention_tc(qkv, lengths_dev, B, S, heads, global_, half_window, ctx, head_
     _check(lib().laya_op_attention_tc(_ptr(qkv), _ptr(lengths_dev), B, S, heads, head_dim,
                                       1 if global_ else 0, half_window, _ptr(ctx),
                                       _stream_ptr(stream)))
+
+
+def attention_rows(qkv, lengths_dev, q_tok_dev, q_pos_dev, B, S, kmax, heads, global_,
+                   half_window, ctx_rows, head_dim=64, stream=None):
+    """Attention from the query slots q_tok_dev / q_pos_dev (int32 [B * kmax]) of each row."""
+    _check(lib().laya_op_attention_rows(_ptr(qkv), _ptr(lengths_dev), _ptr(q_tok_dev),
+                                        _ptr(q_pos_dev), B, S, kmax, heads, head_dim,
+                                        1 if global_ else 0, half_window, _ptr(ctx_rows),
+                                        _stream_ptr(stream)))
 
 
 def attention_rope(qkv, lengths_dev, cos_dev, sin_dev, B, S, heads, global_, half_window, ctx,

@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(128, 4) attention_kernel(const bf16* __restric
                                                         int half_window, bf16* __restrict__ ctx,
                                                         int* err, const float* __restrict__ cos_t,
                                                         const float* __restrict__ sin_t,
-                                                        int packed, int warm) {
+                                                        int packed, int warm, uint64_t* stamp) {
   __shared__ __align__(128) bf16 sQ[kQ * kLd];
   __shared__ __align__(128) bf16 sK[2][kKT * kLd];
   __shared__ __align__(128) bf16 sV[2][kKT * kLd];
@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(128, 4) attention_kernel(const bf16* __restric
   const bool live = pass == 1;
   if (live) {
     ptx::grid_dependency_wait();
+    if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) record_stamp(stamp);
     if (bad_len && tid == 0 && err != nullptr) atomicCAS(err, 0, kDevBadLength);
     if (pad_tile) {
       if (packed) return;  // no such tokens
@@ -333,6 +334,191 @@ __global__ void __launch_bounds__(128, 4) attention_kernel(const bf16* __restric
   }  // pass
 }
 
+
+// Attention over a subset of query rows ("perf(model): exact Metal speed-ups
+// of the forward pass - #45": the last layer attends only from its marker
+// rows, with the (b, 1, 1, s) key-padding row broadcast over them).  Slot
+// m = b * kmax + r (r < kmax) is query token q_tok[m] (its row in qkv) at
+// position q_pos[m] of row b; keys and values are row b's tokens.  One CTA per
+// (64 slots of one row, head, row): the gathered Q tile, every key tile of
+// the row (masked by the window on local layers), online softmax as above;
+// ctx_rows[m] receives the context of slot m.
+__global__ void __launch_bounds__(128) attention_rows_kernel(
+    const bf16* __restrict__ qkv, const int32_t* __restrict__ lengths,
+    const int32_t* __restrict__ q_tok, const int32_t* __restrict__ q_pos, int S, int kmax,
+    int heads, int global, int half_window, int packed, bf16* __restrict__ ctx_rows, int* err,
+    uint64_t* stamp) {
+  __shared__ __align__(128) bf16 sQ[kQ * kLd];
+  __shared__ __align__(128) bf16 sK[2][kKT * kLd];
+  __shared__ __align__(128) bf16 sV[2][kKT * kLd];
+  ptx::grid_launch_dependents();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r0 = blockIdx.x * kQ;  // first slot of this CTA within the row's kmax
+  const int n = blockIdx.y;
+  const int b = blockIdx.z;
+  if (r0 >= kmax) return;
+  const int nq = kmax - r0 < kQ ? kmax - r0 : kQ;
+  const int m0 = b * kmax + r0;
+  const int H = heads * 64;
+  const size_t ld = static_cast<size_t>(3) * H;
+  const int len_in = lengths[b];
+  const bool bad_len = len_in < 1 || len_in > S;
+  const int len = len_in < 1 ? 1 : (len_in > S ? S : len_in);
+  const size_t rb = packed ? static_cast<size_t>(packed_start(lengths, b, S))
+                           : static_cast<size_t>(b) * S;
+  const int rows = packed ? len : S;
+  const bf16* rowbase = qkv + rb * ld;
+  const int g = lane >> 2, c4 = lane & 3;
+  const int qr0 = warp * 16 + g;  // slot (within the CTA) of accumulator rows 0 and +8
+  const int pos0 = qr0 < nq ? q_pos[m0 + qr0] : 0;
+  const int pos1 = qr0 + 8 < nq ? q_pos[m0 + qr0 + 8] : 0;
+  const float scale_log2 = 0.125f * 1.4426950408889634f;
+  const uint32_t sq = ptx::smem_u32(sQ);
+  const uint32_t sk0 = ptx::smem_u32(sK[0]), sk1 = ptx::smem_u32(sK[1]);
+  const uint32_t sv0 = ptx::smem_u32(sV[0]), sv1 = ptx::smem_u32(sV[1]);
+
+  ptx::grid_dependency_wait();
+  if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) record_stamp(stamp);
+  if (bad_len && tid == 0 && err != nullptr) atomicCAS(err, 0, kDevBadLength);
+  // the gathered Q tile: slot rows past nq are zero
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int c = tid + 128 * r;
+    const int row = c >> 3, ch = c & 7;
+    const bool valid = row < nq;
+    const bf16* src = qkv + static_cast<size_t>(valid ? q_tok[m0 + row] : 0) * ld + n * 64 + ch * 8;
+    cp_async16(sq + static_cast<uint32_t>(row * kLd + ch * 8) * 2u, src, valid);
+  }
+  const int kt1 = (len + kKT - 1) / kKT;
+  load_tile(sk0, rowbase + H + n * 64, 0, rows, ld, tid);
+  load_tile(sv0, rowbase + 2 * H + n * 64, 0, rows, ld, tid);
+  cp_async_commit();
+
+  uint32_t qf[4][4];
+  float o[8][4];
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[j][e] = 0.f;
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+  for (int kt = 0; kt < kt1; ++kt) {
+    const int buf = kt & 1;
+    if (kt + 1 < kt1) {
+      load_tile(buf ? sk0 : sk1, rowbase + H + n * 64, (kt + 1) * kKT, rows, ld, tid);
+      load_tile(buf ? sv0 : sv1, rowbase + 2 * H + n * 64, (kt + 1) * kKT, rows, ld, tid);
+      cp_async_commit();
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    if (kt == 0) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const int row = warp * 16 + (lane & 15);
+        const int col = kk * 16 + (lane >> 4) * 8;
+        ldsm_x4(sq + static_cast<uint32_t>(row * kLd + col) * 2u, qf[kk][0], qf[kk][1],
+                qf[kk][2], qf[kk][3]);
+      }
+    }
+    const uint32_t skb = buf ? sk1 : sk0;
+    const uint32_t svb = buf ? sv1 : sv0;
+    float sc[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[j][e] = 0.f;
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t x0, x1, x2, x3;
+        const int key = j * 8 + (lane & 7);
+        const int dim = h2 * 32 + (lane >> 3) * 8;
+        ldsm_x4(skb + static_cast<uint32_t>(key * kLd + dim) * 2u, x0, x1, x2, x3);
+        mma16816(sc[j], qf[2 * h2], x0, x1);
+        mma16816(sc[j], qf[2 * h2 + 1], x2, x3);
+      }
+    }
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int qp = (e >> 1) ? pos1 : pos0;
+        const int kj = kt * kKT + j * 8 + 2 * c4 + (e & 1);
+        int dist = qp - kj;
+        dist = dist < 0 ? -dist : dist;
+        const bool vis = kj < len && (global || dist <= half_window);
+        sc[j][e] = vis ? sc[j][e] * scale_log2 : -INFINITY;
+        mx[e >> 1] = fmaxf(mx[e >> 1], sc[j][e]);
+      }
+    }
+    float alpha[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+      const float mnew = fmaxf(m[r], mx[r]);
+      alpha[r] = (mnew == -INFINITY) ? 1.f : exp2f(m[r] - mnew);
+      m[r] = mnew;
+    }
+    float ls[2] = {0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = e >> 1;
+        const float p = (m[r] == -INFINITY) ? 0.f : exp2f(sc[j][e] - m[r]);
+        sc[j][e] = p;
+        ls[r] += p;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) l[r] = l[r] * alpha[r] + ls[r];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      o[j][0] *= alpha[0];
+      o[j][1] *= alpha[0];
+      o[j][2] *= alpha[1];
+      o[j][3] *= alpha[1];
+    }
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      uint32_t pa[4];
+      pa[0] = pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
+      pa[1] = pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
+      pa[2] = pack_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+      pa[3] = pack_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+#pragma unroll
+      for (int jd = 0; jd < 8; jd += 2) {
+        uint32_t x0, x1, x2, x3;
+        const int key = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int dim = jd * 8 + (lane >> 4) * 8;
+        ldsm_x4_t(svb + static_cast<uint32_t>(key * kLd + dim) * 2u, x0, x1, x2, x3);
+        mma16816(o[jd], pa, x0, x1);
+        mma16816(o[jd + 1], pa, x2, x3);
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
+    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
+  }
+  const float inv0 = l[0] > 0.f ? 1.f / l[0] : 0.f;
+  const float inv1 = l[1] > 0.f ? 1.f / l[1] : 0.f;
+  bf16* out = ctx_rows + static_cast<size_t>(m0) * H + static_cast<size_t>(n) * 64;
+#pragma unroll
+  for (int jd = 0; jd < 8; ++jd) {
+    const int d = jd * 8 + 2 * c4;
+    if (qr0 < nq)
+      *reinterpret_cast<uint32_t*>(out + static_cast<size_t>(qr0) * H + d) =
+          pack_bf16(o[jd][0] * inv0, o[jd][1] * inv0);
+    if (qr0 + 8 < nq)
+      *reinterpret_cast<uint32_t*>(out + static_cast<size_t>(qr0 + 8) * H + d) =
+          pack_bf16(o[jd][2] * inv1, o[jd][3] * inv1);
+  }
+}
 }  // namespace
 
 cudaError_t launch_attention(const bf16* qkv, const int32_t* lengths, int B, int S, int heads,
@@ -354,7 +540,30 @@ cudaError_t launch_attention(const bf16* qkv, const int32_t* lengths, int B, int
   const long long ctas = static_cast<long long>(cfg.gridDim.x) * heads * B;
   const int warm = (l.pdl && ctas <= 4ll * device_sm_count()) ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, attention_kernel, qkv, lengths, S, heads, global, half_window,
-                            ctx, err, cos_t, sin_t, packed ? 1 : 0, warm);
+                            ctx, err, cos_t, sin_t, packed ? 1 : 0, warm, l.stamp);
+}
+
+}  // namespace laya
+
+namespace laya {
+
+cudaError_t launch_attention_rows(const bf16* qkv, const int32_t* lengths, const int32_t* q_tok,
+                                  const int32_t* q_pos, int B, int S, int kmax, int heads,
+                                  int global, int half_window, bool packed, bf16* ctx_rows,
+                                  int* err, Launch l) {
+  if (B <= 0 || S <= 0 || kmax <= 0 || heads <= 0 || half_window < 0)
+    return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((kmax + kQ - 1) / kQ, heads, B);
+  cfg.blockDim = dim3(128);
+  cfg.stream = l.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = l.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, attention_rows_kernel, qkv, lengths, q_tok, q_pos, S, kmax,
+                            heads, global, half_window, packed ? 1 : 0, ctx_rows, err, l.stamp);
 }
 
 }  // namespace laya

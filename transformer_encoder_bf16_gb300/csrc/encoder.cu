@@ -51,6 +51,14 @@ struct LayerMaps {
 
 struct Workspace {
   int B = 0, S = 0, M = 0;
+  // marker rows (laya_enc_run_markers): the last layer after its QKV runs on
+  // Mk = B * kmax slots only; kmax = 0 for the full forward
+  int kmax = 0, Mk = 0;
+  int32_t* mtok = nullptr;  // device staging [Mk]: each slot's token row in the activations
+  int32_t* mpos = nullptr;  // device staging [Mk]: each slot's position in its row
+  bf16 *xm = nullptr, *ctxm = nullptr, *hm = nullptr, *gm = nullptr;  // slot rows
+  GemmPlan p_mo, p_mup, p_mdn;
+  CUtensorMap tm_ctxm, tm_hm, tm_gm;
   void* block = nullptr;  // one device allocation for every buffer below
   size_t bytes = 0;
   bf16 *x = nullptr, *h = nullptr, *qkv = nullptr, *ctx = nullptr, *g = nullptr;
@@ -65,21 +73,18 @@ struct Workspace {
   GemmPlan p_qkv, p_o, p_up, p_dn;
   // activation operand of each GEMM; the TMA box height is that GEMM's own
   // token tile (plans may differ: a GeGLU split-K partial can force a smaller tile)
-  CUtensorMap tm_x_qkv, tm_h_qkv, tm_ctx_o, tm_h_up, tm_x_up, tm_g_dn;
-  // LayerNorm folded into the QKV / up GEMM (their plans are split-K): the
-  // GEMM normalises x on load and the LN kernel is not launched
-  bool ln_qkv = false, ln_up = false;
+  CUtensorMap tm_x_qkv, tm_h_qkv, tm_ctx_o, tm_h_up, tm_g_dn;
+  CUtensorMap tm_qkv_attn;  // the projection as the tcgen05 attention reads it (box 128 rows)
   // packed tokens (packing.cuh) for batches of several rows: the kernels skip
   // the padding and a last kernel writes the padded output
   bool packed = false;
-  // fused short forward (batch * seq <= 128): plan, slice statistics and the
-  // counters of its phase program (zeroed with the block, only ever grow)
-  bool fused_ok = false;
-  bool fused_now = false;  // this enqueue uses the fused kernel
-  FusedPlanOut fp;
-  CUtensorMap fm_x, fm_ctx, fm_g, fm_qkv;  // activation maps of the fused kernel
-  float* stats = nullptr;
-  uint32_t* counters = nullptr;
+  // profiling (laya_enc_set_profiling): one release time per launch plus the
+  // end mark, the class of each launch, and a graph of the stamped launches
+  uint64_t* stamps = nullptr;
+  std::vector<int> prof_class;
+  cudaGraphExec_t prof_exec = nullptr;
+  void* prof_out = nullptr;
+  bool prof_pending = false;  // a profiled forward is enqueued and not yet folded
   cudaGraphExec_t exec = nullptr;
   cudaGraph_t graph = nullptr;         // the template exec was instantiated from
   cudaGraphNode_t out_node = nullptr;  // its last launch, the one writing the output
@@ -107,17 +112,12 @@ struct laya_enc_handle {
   laya_enc_cache_stats stats = {};  // counters of the workspace / graph cache
   bool graphs = true;
   bool pdl = true;
-  bool fused = false;
-  int fused_clusters = 0;                    // clusters of the fused kernel (0: unavailable)
-  laya::FusedLayer* fused_layers = nullptr;  // device [L]
+  bool attn_tc = true;  // attention on tcgen05 (false: the mma.sync kernel, env LAYA_ATTN_MMA_SYNC=1)
   bool poisoned = false;
   std::string last_error;
-  // profiling: event pairs of the last run, per-class totals
   bool fail_next_run = false;  // test hook: the next run fails as a CUDA error would
+  // profiling: per-class totals of the stamped runs folded so far
   bool profiling = false;
-  std::vector<cudaEvent_t> prof_events;  // 2 per launch, reused
-  std::vector<int> prof_class;           // class of each recorded launch
-  size_t prof_used = 0;
   double prof_ms[LAYA_PROF_CLASSES] = {};
   int prof_count[LAYA_PROF_CLASSES] = {};
 };
@@ -151,6 +151,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 void free_workspace(Workspace* w) {
   if (!w) return;
   if (w->done) cudaEventSynchronize(w->done);
+  if (w->prof_exec) cudaGraphExecDestroy(w->prof_exec);
   if (w->exec) cudaGraphExecDestroy(w->exec);
   if (w->graph) cudaGraphDestroy(w->graph);
   if (w->staged) cudaEventDestroy(w->staged);
@@ -160,33 +161,40 @@ void free_workspace(Workspace* w) {
   delete w;
 }
 
-// Counters of the fused kernel: one per phase, then generation / finished
-// CTAs / abort word.
-size_t fused_counter_words(const laya_enc_handle* h) {
-  const laya_enc_config& c = h->cfg;
-  return fused_phase_count(h->L, c.n_encoder_layers, c.final_norm != 0) + 4;
+int kernel_count(const laya_enc_config& c, const Workspace& w) {
+  const int L = c.n_encoder_layers + c.n_decision_layers;
+  // per layer: attention norm (not at an identity layer 0), QKV, attention,
+  // out-proj, MLP norm, up, down
+  int n = 1 + 7 * L - (c.first_attn_norm_identity ? 1 : 0);
+  if (c.final_norm && c.n_decision_layers > 0) n += 1;
+  if (w.kmax > 0) n += 1;          // marker rows: the slot gather
+  else if (w.packed) n += 1;       // the padded output
+  return n;
 }
 
 // Activations, staging and split-K workspace for one (B, S) shape, and the
 // GEMM plans for it.
-int workspace_layout(const laya_enc_handle* h, int B, int S, Workspace* w, size_t* total) {
+int workspace_layout(const laya_enc_handle* h, int B, int S, int kmax, Workspace* w,
+                     size_t* total) {
   const laya_enc_config& c = h->cfg;
   const int M = B * S;
   const int H = c.hidden, I = c.intermediate;
   w->B = B;
   w->S = S;
   w->M = M;
+  w->kmax = kmax;
+  w->Mk = B * kmax;
+  const int Mk = w->Mk;
   w->packed = B > 1;
   if (!plan_gemm(M, 3 * H, H, kGemmPlain, h->num_sms, 0, 0, &w->p_qkv) ||
       !plan_gemm(M, H, H, kGemmResidual, h->num_sms, 0, 0, &w->p_o) ||
       !plan_gemm(M, I, H, kGemmGeglu, h->num_sms, 0, 0, &w->p_up) ||
       !plan_gemm(M, H, I, kGemmResidual, h->num_sms, 0, 0, &w->p_dn))
     return LAYA_E_INVAL;
-  // LayerNorm on load (laya_op_linear_ln) is not used here: measured on the
-  // GB300 it made 48- and 256-token requests slower (every split-K CTA
-  // recomputes the statistics of all its rows) than the LN kernel it replaces.
-  w->ln_qkv = false;
-  w->ln_up = false;
+  if (kmax > 0 && (!plan_gemm(Mk, H, H, kGemmResidual, h->num_sms, 0, 0, &w->p_mo) ||
+                   !plan_gemm(Mk, I, H, kGemmGeglu, h->num_sms, 0, 0, &w->p_mup) ||
+                   !plan_gemm(Mk, H, I, kGemmResidual, h->num_sms, 0, 0, &w->p_mdn)))
+    return LAYA_E_INVAL;
   size_t off = 0;
   auto take = [&](size_t n) {
     const size_t o = off;
@@ -198,18 +206,19 @@ int workspace_layout(const laya_enc_handle* h, int B, int S, Workspace* w, size_
   const size_t oq = take(static_cast<size_t>(M) * 3 * H * 2);
   const size_t oc = take(static_cast<size_t>(M) * H * 2);
   const size_t og = take(static_cast<size_t>(M) * I * 2);
-  const size_t oi = take(static_cast<size_t>(M + B) * 4);  // ids then lengths, adjacent
+  // ids, lengths, slot tokens, slot positions: adjacent, one upload
+  const size_t oi = take(static_cast<size_t>(M + B + 2 * Mk) * 4);
   const size_t opos = take(static_cast<size_t>(M) * 4);
-  const size_t pbytes = std::max(std::max(w->p_qkv.workspace_bytes, w->p_o.workspace_bytes),
-                                 std::max(w->p_up.workspace_bytes, w->p_dn.workspace_bytes));
-  // the fused kernel writes BF16 output only
-  w->fused_ok = h->fused_clusters > 0 && !c.out_fp32 &&
-                plan_fused(M, H, I, c.heads, h->fused_clusters, &w->fp);
-  size_t ost = 0, octr = 0;
-  if (w->fused_ok) {
-    ost = take(static_cast<size_t>(M) * (H / 128) * 2 * sizeof(float));
-    octr = take(fused_counter_words(h) * sizeof(uint32_t));
-  }
+  const size_t oxm = take(static_cast<size_t>(Mk) * H * 2);
+  const size_t ocm = take(static_cast<size_t>(Mk) * H * 2);
+  const size_t ohm = take(static_cast<size_t>(Mk) * H * 2);
+  const size_t ogm = take(static_cast<size_t>(Mk) * I * 2);
+  size_t pbytes = std::max(std::max(w->p_qkv.workspace_bytes, w->p_o.workspace_bytes),
+                           std::max(w->p_up.workspace_bytes, w->p_dn.workspace_bytes));
+  if (kmax > 0)
+    pbytes = std::max(pbytes, std::max(w->p_mo.workspace_bytes,
+                                       std::max(w->p_mup.workspace_bytes, w->p_mdn.workspace_bytes)));
+  const size_t ostamp = take(static_cast<size_t>(kernel_count(c, *w) + 1) * sizeof(uint64_t));
   const size_t op = take(pbytes);
   *total = off;
   if (w->block) {
@@ -221,152 +230,115 @@ int workspace_layout(const laya_enc_handle* h, int B, int S, Workspace* w, size_
     w->g = reinterpret_cast<bf16*>(base + og);
     w->ids = reinterpret_cast<int32_t*>(base + oi);
     w->lens = w->ids + M;
+    w->mtok = w->lens + B;
+    w->mpos = w->mtok + Mk;
     w->pos = reinterpret_cast<int32_t*>(base + opos);
+    if (kmax > 0) {
+      w->xm = reinterpret_cast<bf16*>(base + oxm);
+      w->ctxm = reinterpret_cast<bf16*>(base + ocm);
+      w->hm = reinterpret_cast<bf16*>(base + ohm);
+      w->gm = reinterpret_cast<bf16*>(base + ogm);
+    }
     w->partials = pbytes ? reinterpret_cast<float*>(base + op) : nullptr;
     w->partials_bytes = pbytes;
-    if (w->fused_ok) {
-      w->stats = reinterpret_cast<float*>(base + ost);
-      w->counters = reinterpret_cast<uint32_t*>(base + octr);
-    }
+    w->stamps = reinterpret_cast<uint64_t*>(base + ostamp);
   }
   return LAYA_OK;
 }
 
-int kernel_count(const laya_enc_config& c, const Workspace& w) {
-  if (w.fused_now) return 1;
-  const int L = c.n_encoder_layers + c.n_decision_layers;
-  // per layer: QKV, attention, out-proj, up, down, and the two norms unless folded
-  int n = 1 + 5 * L;
-  if (!w.ln_qkv) n += L - (c.first_attn_norm_identity ? 1 : 0);
-  if (!w.ln_up) n += L;
-  if (c.final_norm && c.n_decision_layers > 0) n += 1;
-  if (w.packed) n += 1;  // the padded output
-  return n;
-}
-
-// Records an event pair around one launch when profiling.
-struct Prof {
-  laya_enc_handle* h;
-  cudaStream_t s;
-  int cls = 0;
-  cudaError_t begin(int c) {
-    if (!h->profiling) return cudaSuccess;
-    cls = c;
-    const size_t i = 2 * h->prof_used;
-    while (h->prof_events.size() < i + 2) {
-      cudaEvent_t e;
-      cudaError_t r = cudaEventCreate(&e);
-      if (r != cudaSuccess) return r;
-      h->prof_events.push_back(e);
-    }
-    return cudaEventRecord(h->prof_events[i], s);
-  }
-  cudaError_t end(cudaError_t launched) {
-    if (!h->profiling || launched != cudaSuccess) return launched;
-    const size_t i = 2 * h->prof_used;
-    if (h->prof_class.size() <= h->prof_used) h->prof_class.resize(h->prof_used + 1);
-    h->prof_class[h->prof_used] = cls;
-    ++h->prof_used;
-    return cudaEventRecord(h->prof_events[i + 1], s);
-  }
-};
-
-cudaError_t prof_fold(laya_enc_handle* h) {
-  if (h->prof_used == 0) return cudaSuccess;
-  cudaError_t e = cudaEventSynchronize(h->prof_events[2 * h->prof_used - 1]);
+// Folds the stamps of the last profiled forward on workspace w into the
+// per-class totals: launch k is charged the time from its release (the
+// completion of launch k - 1) to the release of launch k + 1, so the charges
+// of one forward add up to its time from the first kernel's start to the
+// last kernel's completion, with the overlap the graph replay has.
+cudaError_t prof_fold(laya_enc_handle* h, Workspace* w) {
+  if (!w->prof_pending) return cudaSuccess;
+  cudaError_t e = cudaEventSynchronize(w->done);
   if (e != cudaSuccess) return e;
-  for (size_t i = 0; i < h->prof_used; ++i) {
-    float ms = 0.f;
-    e = cudaEventElapsedTime(&ms, h->prof_events[2 * i], h->prof_events[2 * i + 1]);
-    if (e != cudaSuccess) return e;
-    h->prof_ms[h->prof_class[i]] += ms;
-    h->prof_count[h->prof_class[i]] += 1;
+  const size_t n = w->prof_class.size();
+  std::vector<uint64_t> t(n + 1);
+  e = cudaMemcpy(t.data(), w->stamps, sizeof(uint64_t) * (n + 1), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return e;
+  for (size_t k = 0; k < n; ++k) {
+    const double ms = t[k + 1] > t[k] ? static_cast<double>(t[k + 1] - t[k]) * 1e-6 : 0.0;
+    h->prof_ms[w->prof_class[k]] += ms;
+    h->prof_count[w->prof_class[k]] += 1;
   }
-  h->prof_used = 0;
+  w->prof_pending = false;
   return cudaSuccess;
 }
 
-// out: BF16 [B, S, H], or fp32 when cfg.out_fp32 (written by the last
-// residual sum directly, or through the packed fp32 rows it leaves in the
-// qkv buffer, which that layer's attention no longer needs).
-cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, void* out, cudaStream_t stream) {
+cudaError_t prof_fold_all(laya_enc_handle* h) {
+  for (Workspace* w : h->cache) {
+    cudaError_t e = prof_fold(h, w);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// What one forward pass writes besides its workspace.
+struct RunOut {
+  void* out = nullptr;      // BF16 [B, S, H], or fp32 when cfg.out_fp32
+  bf16* capture = nullptr;  // debug: [L, B, S, H], the residual stream entering each layer
+};
+
+// Enqueues one forward pass.  out is written by the last residual sum
+// directly, or through the packed rows it leaves in x (fp32: in the qkv
+// buffer, which that layer's attention no longer needs).  profiling: every
+// launch records its release time in w->stamps (see prof_fold), and an end
+// mark follows the last launch.
+cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, const RunOut& ro,
+                            cudaStream_t stream, bool profiling) {
   const laya_enc_config& c = h->cfg;
   const int H = c.hidden;
   const int M = w->M;
-  const bool pdl = h->pdl && !h->profiling;
-  const Launch first{stream, false};
-  const Launch l{stream, pdl};
+  const bool pdl = h->pdl;
+  void* out = ro.out;
   const float* cos_g = h->rope;
   const float* sin_g = h->rope + static_cast<size_t>(c.max_seq) * 32;
   const float* cos_l = sin_g + static_cast<size_t>(c.max_seq) * 32;
   const float* sin_l = cos_l + static_cast<size_t>(c.max_seq) * 32;
-  Prof pr{h, stream};
+  if (profiling) w->prof_class.clear();
+  int idx = 0;
+  // launch options of the next launch; `cls` is its profiling class
+  auto next = [&](int cls, bool first = false) {
+    Launch l{stream, first ? false : pdl, nullptr};
+    if (profiling) {
+      l.stamp = w->stamps + idx;
+      w->prof_class.push_back(cls);
+    }
+    ++idx;
+    return l;
+  };
   cudaError_t e;
-#define LAYA_LAUNCH(cls, call)              \
-  do {                                      \
-    e = pr.begin(cls);                      \
-    if (e == cudaSuccess) e = pr.end(call); \
-    if (e != cudaSuccess) return e;         \
+#define LAYA_LAUNCH(call)             \
+  do {                                \
+    e = (call);                       \
+    if (e != cudaSuccess) return e;   \
   } while (0)
 
-  if (w->fused_now) {
-    FusedArgs a{};
-    a.tm_x = w->fm_x;
-    a.tm_ctx = w->fm_ctx;
-    a.tm_g = w->fm_g;
-    a.tm_qkv = w->fm_qkv;
-    a.M = M;
-    a.B = w->B;
-    a.S = w->S;
-    a.nt = w->fp.nt;
-    a.L = h->L;
-    a.n_enc = c.n_encoder_layers;
-    a.heads = c.heads;
-    a.H = H;
-    a.I = c.intermediate;
-    a.vocab = c.vocab;
-    a.half_window = c.local_half_window;
-    a.global_every = c.global_every;
-    a.max_seq = c.max_seq;
-    a.eps = c.ln_eps;
-    for (int i = 0; i < 4; ++i) a.plan[i] = w->fp.plan[i];
-    std::memcpy(a.cluster_tile, w->fp.cluster_tile, sizeof(a.cluster_tile));
-    a.layers = h->fused_layers;
-    a.ids = w->ids;
-    a.lens = w->lens;
-    a.emb = h->tok_emb;
-    a.emb_gamma = h->emb_norm;
-    a.final_gamma = c.final_norm ? h->final_norm : nullptr;
-    a.rope = h->rope;
-    a.x = w->x;
-    a.qkv = w->qkv;
-    a.ctx = w->ctx;
-    a.g = w->g;
-    a.out = static_cast<bf16*>(out);
-    a.stats = w->stats;
-    a.ready = w->counters;
-    a.sync = a.ready + fused_phase_count(h->L, c.n_encoder_layers, c.final_norm != 0);
-    a.err = h->err;
-    LAYA_LAUNCH(LAYA_PROF_FUSED, launch_fused(a, w->fp.n_clusters, stream));
-    return cudaSuccess;
-  }
   Packing pk;
-  if (w->packed) {
-    pk.lens = w->lens;
-    pk.B = w->B;
-    pk.S = w->S;
-    pk.pos = w->pos;
-  }
-  LAYA_LAUNCH(LAYA_PROF_EMBED_NORM,
-              launch_embed_layernorm(h->tok_emb, h->emb_norm, w->ids, M, H, c.vocab, c.ln_eps,
-                                     w->x, h->err, first, pk));
+  pk.lens = w->lens;
+  pk.B = w->B;
+  pk.S = w->S;
+  if (w->packed) pk.pos = w->pos;
+  else pk.lens = nullptr;
+  // debug capture of the stream entering each layer: padded layout, padding 0
+  auto capture = [&](int li) -> cudaError_t {
+    if (ro.capture == nullptr) return cudaSuccess;
+    bf16* dst = ro.capture + static_cast<size_t>(li) * w->B * w->S * H;
+    return launch_unpack_rows(w->x, w->lens, w->B, w->S, H * 2, dst, next(LAYA_PROF_OUTPUT));
+  };
+  LAYA_LAUNCH(launch_embed_layernorm(h->tok_emb, h->emb_norm, w->ids, M, H, c.vocab, c.ln_eps,
+                                     w->x, h->err, next(LAYA_PROF_EMBED_NORM, true), pk));
   for (int li = 0; li < h->L; ++li) {
     const LayerMaps& lw = h->layers[li];
     const bool dec = li >= c.n_encoder_layers;
     const bool glob = dec || (li % c.global_every == 0);
+    LAYA_LAUNCH(capture(li));
     if (li == c.n_encoder_layers && c.final_norm)
-      LAYA_LAUNCH(LAYA_PROF_NORM,
-                  launch_layernorm(w->x, h->final_norm, M, H, c.ln_eps, w->x, l, pk));
+      LAYA_LAUNCH(launch_layernorm(w->x, h->final_norm, M, H, c.ln_eps, w->x,
+                                   next(LAYA_PROF_NORM), pk));
     GemmOperands o;
     o.err = h->err;
     o.partials = w->partials;
@@ -378,14 +350,9 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, void* out, cudaStr
     const CUtensorMap* qkv_in = &w->tm_h_qkv;
     if (li == 0 && c.first_attn_norm_identity) {
       qkv_in = &w->tm_x_qkv;
-    } else if (w->ln_qkv) {
-      qkv_in = &w->tm_x_qkv;  // normalised on load
-      o.ln_x = w->x;
-      o.ln_gamma = lw.attn_norm;
-      o.ln_eps = c.ln_eps;
     } else {
-      LAYA_LAUNCH(LAYA_PROF_NORM,
-                  launch_layernorm(w->x, lw.attn_norm, M, H, c.ln_eps, w->h, l, pk));
+      LAYA_LAUNCH(launch_layernorm(w->x, lw.attn_norm, M, H, c.ln_eps, w->h,
+                                   next(LAYA_PROF_NORM), pk));
     }
     o.w = lw.wqkv;
     o.w2 = lw.wqkv;
@@ -397,36 +364,69 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, void* out, cudaStr
     o.rope_sin = glob ? sin_g : sin_l;
     o.rope_S = w->S;
     o.rope_cols = 2 * H;
-    LAYA_LAUNCH(LAYA_PROF_QKV, launch_gemm(w->p_qkv, o, l));
+    LAYA_LAUNCH(launch_gemm(w->p_qkv, o, next(LAYA_PROF_QKV)));
     o.rope_cos = o.rope_sin = nullptr;
-    o.ln_x = o.ln_gamma = nullptr;
-    LAYA_LAUNCH(LAYA_PROF_ATTN, launch_attention(w->qkv, w->lens, w->B, w->S, c.heads,
-                                                 glob ? 1 : 0, c.local_half_window, w->ctx,
-                                                 h->err, l, nullptr, nullptr, w->packed));
+    if (li == h->L - 1 && w->kmax > 0) {
+      // marker rows: everything after the keys and values is row-wise, so the
+      // rest of the last layer runs on the Mk slot rows alone
+      LAYA_LAUNCH(launch_gather_rows(w->x, w->mtok, w->Mk, H * 2, w->xm, next(LAYA_PROF_OUTPUT)));
+      LAYA_LAUNCH(launch_attention_rows(w->qkv, w->lens, w->mtok, w->mpos, w->B, w->S, w->kmax,
+                                        c.heads, glob ? 1 : 0, c.local_half_window, w->packed,
+                                        w->ctxm, h->err, next(LAYA_PROF_ATTN)));
+      GemmOperands om;
+      om.err = h->err;
+      om.partials = w->partials;
+      om.partials_bytes = w->partials_bytes;
+      om.w = lw.wo;
+      om.w2 = lw.wo;
+      om.x = w->tm_ctxm;
+      om.x_box_rows = w->p_mo.nt;
+      om.y = w->xm;
+      om.residual = w->xm;
+      LAYA_LAUNCH(launch_gemm(w->p_mo, om, next(LAYA_PROF_OUT)));
+      LAYA_LAUNCH(launch_layernorm(w->xm, lw.mlp_norm, w->Mk, H, c.ln_eps, w->hm,
+                                   next(LAYA_PROF_NORM)));
+      om.w = lw.wup_in;
+      om.w2 = lw.wup_gate;
+      om.x = w->tm_hm;
+      om.x_box_rows = w->p_mup.nt;
+      om.y = w->gm;
+      om.residual = nullptr;
+      LAYA_LAUNCH(launch_gemm(w->p_mup, om, next(LAYA_PROF_UP)));
+      om.w = lw.wdown;
+      om.w2 = lw.wdown;
+      om.x = w->tm_gm;
+      om.x_box_rows = w->p_mdn.nt;
+      om.y = static_cast<bf16*>(out);
+      om.residual = w->xm;
+      if (c.out_fp32) om.y_f32 = static_cast<float*>(out);
+      LAYA_LAUNCH(launch_gemm(w->p_mdn, om, next(LAYA_PROF_DOWN)));
+      break;
+    }
+    if (h->attn_tc)
+      LAYA_LAUNCH(launch_attention_tc(w->tm_qkv_attn, w->lens, w->B, w->S, c.heads, glob ? 1 : 0,
+                                      c.local_half_window, w->ctx, h->err, next(LAYA_PROF_ATTN),
+                                      w->packed));
+    else
+      LAYA_LAUNCH(launch_attention(w->qkv, w->lens, w->B, w->S, c.heads, glob ? 1 : 0,
+                                   c.local_half_window, w->ctx, h->err, next(LAYA_PROF_ATTN),
+                                   nullptr, nullptr, w->packed));
     o.w = lw.wo;
     o.w2 = lw.wo;
     o.x = w->tm_ctx_o;
     o.x_box_rows = w->p_o.nt;
     o.y = w->x;
     o.residual = w->x;
-    LAYA_LAUNCH(LAYA_PROF_OUT, launch_gemm(w->p_o, o, l));
+    LAYA_LAUNCH(launch_gemm(w->p_o, o, next(LAYA_PROF_OUT)));
+    LAYA_LAUNCH(launch_layernorm(w->x, lw.mlp_norm, M, H, c.ln_eps, w->h, next(LAYA_PROF_NORM),
+                                 pk));
     o.w = lw.wup_in;
     o.w2 = lw.wup_gate;
+    o.x = w->tm_h_up;
     o.x_box_rows = w->p_up.nt;
     o.y = w->g;
     o.residual = nullptr;
-    if (w->ln_up) {
-      o.x = w->tm_x_up;  // normalised on load
-      o.ln_x = w->x;
-      o.ln_gamma = lw.mlp_norm;
-      o.ln_eps = c.ln_eps;
-    } else {
-      LAYA_LAUNCH(LAYA_PROF_NORM,
-                  launch_layernorm(w->x, lw.mlp_norm, M, H, c.ln_eps, w->h, l, pk));
-      o.x = w->tm_h_up;
-    }
-    LAYA_LAUNCH(LAYA_PROF_UP, launch_gemm(w->p_up, o, l));
-    o.ln_x = o.ln_gamma = nullptr;
+    LAYA_LAUNCH(launch_gemm(w->p_up, o, next(LAYA_PROF_UP)));
     o.w = lw.wdown;
     o.w2 = lw.wdown;
     o.x = w->tm_g_dn;
@@ -436,19 +436,24 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, void* out, cudaStr
     o.residual = w->x;
     if (last && c.out_fp32)
       o.y_f32 = w->packed ? reinterpret_cast<float*>(w->qkv) : static_cast<float*>(out);
-    LAYA_LAUNCH(LAYA_PROF_DOWN, launch_gemm(w->p_dn, o, l));
+    LAYA_LAUNCH(launch_gemm(w->p_dn, o, next(LAYA_PROF_DOWN)));
   }
-  if (w->packed)
-    LAYA_LAUNCH(LAYA_PROF_EMBED_NORM,
-                launch_unpack_rows(c.out_fp32 ? static_cast<const void*>(w->qkv) : w->x, w->lens,
-                                   w->B, w->S, H * (c.out_fp32 ? 4 : 2), out, l));
+  if (w->packed && w->kmax == 0)
+    LAYA_LAUNCH(launch_unpack_rows(c.out_fp32 ? static_cast<const void*>(w->qkv) : w->x, w->lens,
+                                   w->B, w->S, H * (c.out_fp32 ? 4 : 2), out,
+                                   next(LAYA_PROF_OUTPUT)));
+  if (profiling) {
+    // the end mark: released when the last launch has completed
+    Launch l{stream, pdl, w->stamps + idx};
+    LAYA_LAUNCH(launch_stamp(l));
+  }
 #undef LAYA_LAUNCH
   return cudaSuccess;
 }
 
-int get_workspace(laya_enc_handle* h, int B, int S, Workspace** out) {
+int get_workspace(laya_enc_handle* h, int B, int S, int kmax, Workspace** out) {
   for (Workspace* w : h->cache) {
-    if (w->B == B && w->S == S) {
+    if (w->B == B && w->S == S && w->kmax == kmax) {
       w->last_use = ++h->tick;
       *out = w;
       return LAYA_OK;
@@ -458,7 +463,7 @@ int get_workspace(laya_enc_handle* h, int B, int S, Workspace** out) {
   Workspace* w = new (std::nothrow) Workspace();
   if (!w) return fail(h, LAYA_E_NOMEM, "workspace: host allocation failed");
   size_t bytes = 0;
-  if (workspace_layout(h, B, S, w, &bytes) != LAYA_OK) {
+  if (workspace_layout(h, B, S, kmax, w, &bytes) != LAYA_OK) {
     delete w;
     return fail(h, LAYA_E_INVAL, "no GEMM plan for this shape");
   }
@@ -482,8 +487,8 @@ int get_workspace(laya_enc_handle* h, int B, int S, Workspace** out) {
     return fail(h, LAYA_E_NOMEM, std::string("workspace: ") + cudaGetErrorString(e));
   }
   w->bytes = bytes;
-  workspace_layout(h, B, S, w, &bytes);
-  e = cudaHostAlloc(reinterpret_cast<void**>(&w->host), sizeof(int32_t) * (w->M + B),
+  workspace_layout(h, B, S, kmax, w, &bytes);
+  e = cudaHostAlloc(reinterpret_cast<void**>(&w->host), sizeof(int32_t) * (w->M + B + 2 * w->Mk),
                     cudaHostAllocDefault);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&w->staged, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&w->done, cudaEventDisableTiming);
@@ -500,14 +505,13 @@ int get_workspace(laya_enc_handle* h, int B, int S, Workspace** out) {
             make_tmap_bf16_2d(&w->tm_h_qkv, w->h, M, c.hidden, ldh, box(w->p_qkv)) &&
             make_tmap_bf16_2d(&w->tm_ctx_o, w->ctx, M, c.hidden, ldh, box(w->p_o)) &&
             make_tmap_bf16_2d(&w->tm_h_up, w->h, M, c.hidden, ldh, box(w->p_up)) &&
-            make_tmap_bf16_2d(&w->tm_x_up, w->x, M, c.hidden, ldh, box(w->p_up)) &&
-            make_tmap_bf16_2d(&w->tm_g_dn, w->g, M, c.intermediate, ldi, box(w->p_dn));
-  if (ok && w->fused_ok) {
-    const uint32_t nt = static_cast<uint32_t>(w->fp.nt);
-    ok = make_tmap_bf16_2d(&w->fm_x, w->x, M, c.hidden, ldh, nt) &&
-         make_tmap_bf16_2d(&w->fm_ctx, w->ctx, M, c.hidden, ldh, nt) &&
-         make_tmap_bf16_2d(&w->fm_g, w->g, M, c.intermediate, ldi, nt) &&
-         make_tmap_bf16_2d(&w->fm_qkv, w->qkv, M, 3ull * c.hidden, 3 * ldh, 128);
+            make_tmap_bf16_2d(&w->tm_g_dn, w->g, M, c.intermediate, ldi, box(w->p_dn)) &&
+            make_tmap_bf16_2d(&w->tm_qkv_attn, w->qkv, M, 3ull * c.hidden, 3 * ldh, 128);
+  if (ok && kmax > 0) {
+    const int Mk = w->Mk;
+    ok = make_tmap_bf16_2d(&w->tm_ctxm, w->ctxm, Mk, c.hidden, ldh, box(w->p_mo)) &&
+         make_tmap_bf16_2d(&w->tm_hm, w->hm, Mk, c.hidden, ldh, box(w->p_mup)) &&
+         make_tmap_bf16_2d(&w->tm_gm, w->gm, Mk, c.intermediate, ldi, box(w->p_mdn));
   }
   if (!ok) {
     free_workspace(w);
@@ -522,26 +526,82 @@ int get_workspace(laya_enc_handle* h, int B, int S, Workspace** out) {
   return LAYA_OK;
 }
 
-int run_common(laya_enc_handle* h, Workspace* w, void* out, cudaStream_t stream) {
+// Captures one forward pass of w into a graph.  sink: the capture's last
+// launch (the one writing out), null if it cannot be told.
+int capture_graph(laya_enc_handle* h, Workspace* w, void* out, bool profiling,
+                  cudaGraph_t* graph, cudaGraphExec_t* exec, cudaGraphNode_t* sink) {
+  *graph = nullptr;
+  *exec = nullptr;
+  *sink = nullptr;
+  cudaError_t e = cudaStreamBeginCapture(h->capture_stream, cudaStreamCaptureModeThreadLocal);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamBeginCapture");
+  RunOut ro;
+  ro.out = out;
+  cudaError_t el = enqueue_forward(h, w, ro, h->capture_stream, profiling);
+  // the capture's single open dependency is the last launch
+  if (el == cudaSuccess) {
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    const cudaGraphNode_t* deps = nullptr;
+    size_t nd = 0;
+    if (cudaStreamGetCaptureInfo(h->capture_stream, &st, nullptr, nullptr, &deps, nullptr, &nd) ==
+            cudaSuccess &&
+        nd == 1)
+      *sink = deps[0];
+    else
+      cudaGetLastError();
+  }
+  e = cudaStreamEndCapture(h->capture_stream, graph);
+  if (el != cudaSuccess) {
+    if (*graph) cudaGraphDestroy(*graph);
+    *graph = nullptr;
+    return cuda_fail(h, el, "launch during capture");
+  }
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamEndCapture");
+  e = cudaGraphInstantiate(exec, *graph, 0);
+  if (e != cudaSuccess) {
+    cudaGraphDestroy(*graph);
+    *graph = nullptr;
+    *exec = nullptr;
+    return cuda_fail(h, e, "cudaGraphInstantiate");
+  }
+  return LAYA_OK;
+}
+
+int run_common(laya_enc_handle* h, Workspace* w, const RunOut& ro, cudaStream_t stream) {
+  void* out = ro.out;
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   cudaError_t e = cudaStreamIsCapturing(stream, &cap);
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamIsCapturing");
-  if (h->profiling && cap == cudaStreamCaptureStatusNone) {
-    e = prof_fold(h);
-    if (e != cudaSuccess) return cuda_fail(h, e, "profiling events");
+  const bool profiling = h->profiling && cap == cudaStreamCaptureStatusNone && !ro.capture;
+  if (profiling) {
+    e = prof_fold_all(h);
+    if (e != cudaSuccess) return cuda_fail(h, e, "profiling stamps");
   }
-  // the fused kernel (a cooperative launch) runs eagerly, never inside a capture
-  w->fused_now = h->fused && w->fused_ok && cap == cudaStreamCaptureStatusNone;
-  if (!h->graphs || h->profiling || cap != cudaStreamCaptureStatusNone || w->fused_now) {
-    e = enqueue_forward(h, w, out, stream);
+  if (!h->graphs || cap != cudaStreamCaptureStatusNone || ro.capture != nullptr) {
+    e = enqueue_forward(h, w, ro, stream, profiling);
     if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");
+  } else if (profiling) {
+    // the same launches with release stamps, in a graph of their own
+    if (w->prof_exec == nullptr || w->prof_out != out) {
+      if (w->prof_exec) cudaGraphExecDestroy(w->prof_exec);
+      w->prof_exec = nullptr;
+      cudaGraph_t g = nullptr;
+      cudaGraphNode_t sink = nullptr;
+      const int rc = capture_graph(h, w, out, true, &g, &w->prof_exec, &sink);
+      if (rc != LAYA_OK) return rc;
+      cudaGraphDestroy(g);
+      w->prof_out = out;
+    }
+    e = cudaGraphLaunch(w->prof_exec, stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaGraphLaunch");
   } else {
     // a new output buffer for a captured shape: repoint the launch that
     // writes the output instead of capturing again
     if (w->exec != nullptr && w->graph_out != out && w->out_node != nullptr) {
       const cudaError_t er =
-          w->packed ? unpack_node_retarget(w->exec, w->out_node, w->graph_out, out)
-                    : gemm_node_retarget(w->exec, w->out_node, w->graph_out, out);
+          (w->packed && w->kmax == 0)
+              ? unpack_node_retarget(w->exec, w->out_node, w->graph_out, out)
+              : gemm_node_retarget(w->exec, w->out_node, w->graph_out, out);
       if (er == cudaSuccess) {
         w->graph_out = out;
         ++h->stats.retargets;
@@ -554,35 +614,12 @@ int run_common(laya_enc_handle* h, Workspace* w, void* out, cudaStream_t stream)
       if (w->exec == nullptr) {
         // two eager warm-up passes before the first capture of a shape
         for (int i = 0; i < 2; ++i) {
-          e = enqueue_forward(h, w, out, stream);
+          e = enqueue_forward(h, w, ro, stream, false);
           if (e != cudaSuccess) return cuda_fail(h, e, "warm-up launch");
         }
       }
       e = cudaStreamSynchronize(stream);
       if (e != cudaSuccess) return cuda_fail(h, e, "warm-up");
-      cudaGraph_t graph = nullptr;
-      e = cudaStreamBeginCapture(h->capture_stream, cudaStreamCaptureModeThreadLocal);
-      if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamBeginCapture");
-      cudaError_t el = enqueue_forward(h, w, out, h->capture_stream);
-      // the capture's single open dependency is the last launch: the output writer
-      cudaGraphNode_t sink = nullptr;
-      if (el == cudaSuccess) {
-        cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
-        const cudaGraphNode_t* deps = nullptr;
-        size_t nd = 0;
-        if (cudaStreamGetCaptureInfo(h->capture_stream, &st, nullptr, nullptr, &deps, nullptr,
-                                     &nd) == cudaSuccess &&
-            nd == 1)
-          sink = deps[0];
-        else
-          cudaGetLastError();
-      }
-      e = cudaStreamEndCapture(h->capture_stream, &graph);
-      if (el != cudaSuccess) {
-        if (graph) cudaGraphDestroy(graph);
-        return cuda_fail(h, el, "launch during capture");
-      }
-      if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamEndCapture");
       if (w->exec) {
         cudaGraphExecDestroy(w->exec);
         w->exec = nullptr;
@@ -592,13 +629,8 @@ int run_common(laya_enc_handle* h, Workspace* w, void* out, cudaStream_t stream)
         w->graph = nullptr;
         w->out_node = nullptr;
       }
-      e = cudaGraphInstantiate(&w->exec, graph, 0);
-      if (e != cudaSuccess) {
-        cudaGraphDestroy(graph);
-        return cuda_fail(h, e, "cudaGraphInstantiate");
-      }
-      w->graph = graph;
-      w->out_node = sink;
+      const int rc = capture_graph(h, w, out, false, &w->graph, &w->exec, &w->out_node);
+      if (rc != LAYA_OK) return rc;
       w->graph_out = out;
       ++h->stats.captures;
       h->stats.capture_ms += std::chrono::duration<double, std::milli>(
@@ -610,6 +642,7 @@ int run_common(laya_enc_handle* h, Workspace* w, void* out, cudaStream_t stream)
   e = cudaEventRecord(w->done, stream);
   if (e != cudaSuccess && cap == cudaStreamCaptureStatusNone)
     return cuda_fail(h, e, "cudaEventRecord");
+  if (profiling) w->prof_pending = true;
   return LAYA_OK;
 }
 
@@ -703,6 +736,7 @@ int laya_enc_create(const laya_enc_config* cfg, const laya_enc_weights* wts,
   h->num_sms = device_sm_count();
   h->graphs = !env_flag("LAYA_EAGER");
   h->pdl = !env_flag("LAYA_NO_PDL");
+  h->attn_tc = !env_flag("LAYA_ATTN_MMA_SYNC");
   h->tok_emb = static_cast<const bf16*>(wts->tok_emb);
   h->emb_norm = static_cast<const bf16*>(wts->emb_norm);
   h->final_norm = static_cast<const bf16*>(wts->final_norm);
@@ -726,8 +760,6 @@ int laya_enc_create(const laya_enc_config* cfg, const laya_enc_weights* wts,
     delete h;
     return fail(nullptr, LAYA_E_CUDA, "weight tensor map encoding failed");
   }
-  h->fused = env_flag("LAYA_FUSED");
-  h->fused_clusters = fused_max_clusters();
   const size_t tab = static_cast<size_t>(cfg->max_seq) * 32;
   std::vector<float> host(4 * tab);
   rope_table_host(cfg->theta_global, cfg->max_seq, 32, cfg->rope_table_bf16, host.data(),
@@ -740,23 +772,6 @@ int laya_enc_create(const laya_enc_config* cfg, const laya_enc_weights* wts,
   if (e == cudaSuccess) e = cudaMalloc(&h->err, 4 * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(h->err, 0, 4 * sizeof(int));
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->capture_stream, cudaStreamNonBlocking);
-  if (e == cudaSuccess && h->fused_clusters > 0) {
-    // the fused kernel reads every layer's tensor maps from device memory
-    std::vector<FusedLayer> fl(L);
-    for (int l = 0; l < L; ++l) {
-      const LayerMaps& m = h->layers[l];
-      fl[l].maps[0] = m.wqkv;
-      fl[l].maps[1] = m.wo;
-      fl[l].maps[2] = m.wup_in;
-      fl[l].maps[3] = m.wup_gate;
-      fl[l].maps[4] = m.wdown;
-      fl[l].attn_norm = (l == 0 && cfg->first_attn_norm_identity) ? nullptr : m.attn_norm;
-      fl[l].mlp_norm = m.mlp_norm;
-    }
-    e = cudaMalloc(&h->fused_layers, sizeof(FusedLayer) * L);
-    if (e == cudaSuccess)
-      e = cudaMemcpy(h->fused_layers, fl.data(), sizeof(FusedLayer) * L, cudaMemcpyHostToDevice);
-  }
   if (e != cudaSuccess) {
     std::string msg = std::string("create: ") + cudaGetErrorString(e);
     laya_enc_destroy(h);
@@ -768,9 +783,10 @@ int laya_enc_create(const laya_enc_config* cfg, const laya_enc_weights* wts,
 }
 
 static int run_impl(laya_enc_handle* h, const int32_t* ids, const int32_t* lengths, int B, int S,
-                    void* out, void* stream_v, bool device_inputs) {
+                    const int32_t* markers, int kmax, const laya::RunOut& ro, void* stream_v,
+                    bool device_inputs) {
   using namespace laya;
-  int rc = check_run_args(h, B, S, out);
+  int rc = check_run_args(h, B, S, ro.out);
   if (rc != LAYA_OK) return rc;
   if (!ids || !lengths) return fail(h, LAYA_E_INVAL, "null token_ids or lengths");
   if (!device_inputs) {
@@ -782,6 +798,18 @@ static int run_impl(laya_enc_handle* h, const int32_t* ids, const int32_t* lengt
       if (ids[t] < 0 || ids[t] >= h->cfg.vocab)
         return fail(h, LAYA_E_INVAL, "token id outside [0, vocab)");
   }
+  if (kmax > 0) {
+    if (!markers) return fail(h, LAYA_E_INVAL, "null marker_pos");
+    if (static_cast<int64_t>(B) * kmax > LAYA_ENC_MAX_MARKERS)
+      return fail(h, LAYA_E_INVAL, "batch * kmax exceeds LAYA_ENC_MAX_MARKERS");
+    for (int b = 0; b < B; ++b)
+      for (int j = 0; j < kmax; ++j) {
+        const int p = markers[b * kmax + j];
+        if (p < -1 || p >= lengths[b])
+          return fail(h, LAYA_E_INVAL, "marker_pos[" + std::to_string(b * kmax + j) +
+                                           "] is not a valid token of its row (nor -1)");
+      }
+  }
   if (h->fail_next_run) {
     h->fail_next_run = false;
     return cuda_fail(h, cudaErrorLaunchFailure, "injected failure (test hook)");
@@ -789,7 +817,7 @@ static int run_impl(laya_enc_handle* h, const int32_t* ids, const int32_t* lengt
   cudaError_t e = cudaSetDevice(h->device);
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaSetDevice");
   Workspace* w = nullptr;
-  rc = get_workspace(h, B, S, &w);
+  rc = get_workspace(h, B, S, kmax, &w);
   if (rc != LAYA_OK) return rc;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
   const size_t nid = static_cast<size_t>(w->M) * sizeof(int32_t);
@@ -804,8 +832,24 @@ static int run_impl(laya_enc_handle* h, const int32_t* ids, const int32_t* lengt
     if (e != cudaSuccess) return cuda_fail(h, e, "staging wait");
     std::memcpy(w->host, ids, nid);
     std::memcpy(w->host + w->M, lengths, nlen);
-    // ids and lengths are adjacent on both sides: one grouped upload
-    e = cudaMemcpyAsync(w->ids, w->host, nid + nlen, cudaMemcpyHostToDevice, stream);
+    // marker slots: the token row of each slot in the activations (packed
+    // rows start at the earlier rows' lengths summed) and its position; an
+    // empty slot reads its row's first token
+    int32_t* mtok = w->host + w->M + B;
+    int32_t* mpos = mtok + w->Mk;
+    int cu = 0;
+    for (int b = 0; b < B && kmax > 0; ++b) {
+      const int start = w->packed ? cu : b * S;
+      for (int j = 0; j < kmax; ++j) {
+        const int p = markers[b * kmax + j] < 0 ? 0 : markers[b * kmax + j];
+        mtok[b * kmax + j] = start + p;
+        mpos[b * kmax + j] = p;
+      }
+      cu += lengths[b];
+    }
+    // ids, lengths and marker slots are adjacent on both sides: one grouped upload
+    e = cudaMemcpyAsync(w->ids, w->host, nid + nlen + 2 * sizeof(int32_t) * w->Mk,
+                        cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) return cuda_fail(h, e, "input upload");
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
     cudaStreamIsCapturing(stream, &cap);
@@ -814,18 +858,44 @@ static int run_impl(laya_enc_handle* h, const int32_t* ids, const int32_t* lengt
       if (e != cudaSuccess) return cuda_fail(h, e, "cudaEventRecord");
     }
   }
-  return run_common(h, w, out, stream);
+  return run_common(h, w, ro, stream);
 }
 
 int laya_enc_run(laya_enc_handle* h, const int32_t* token_ids, const int32_t* lengths, int batch,
                  int seq, void* out_hidden, void* stream) {
-  return run_impl(h, token_ids, lengths, batch, seq, out_hidden, stream, false);
+  laya::RunOut ro;
+  ro.out = out_hidden;
+  return run_impl(h, token_ids, lengths, batch, seq, nullptr, 0, ro, stream, false);
 }
 
 int laya_enc_run_device(laya_enc_handle* h, const int32_t* token_ids_dev,
                         const int32_t* lengths_dev, int batch, int seq, void* out_hidden,
                         void* stream) {
-  return run_impl(h, token_ids_dev, lengths_dev, batch, seq, out_hidden, stream, true);
+  laya::RunOut ro;
+  ro.out = out_hidden;
+  return run_impl(h, token_ids_dev, lengths_dev, batch, seq, nullptr, 0, ro, stream, true);
+}
+
+int laya_enc_run_markers(laya_enc_handle* h, const int32_t* token_ids, const int32_t* lengths,
+                         int batch, int seq, const int32_t* marker_pos, int kmax,
+                         void* out_markers, void* stream) {
+  if (!h) return LAYA_E_INVAL;
+  if (kmax < 1 || kmax > LAYA_ENC_MAX_MARKERS)
+    return laya::fail(h, LAYA_E_INVAL, "kmax outside [1, LAYA_ENC_MAX_MARKERS]");
+  laya::RunOut ro;
+  ro.out = out_markers;
+  return run_impl(h, token_ids, lengths, batch, seq, marker_pos, kmax, ro, stream, false);
+}
+
+int laya_enc_debug_capture(laya_enc_handle* h, const int32_t* token_ids, const int32_t* lengths,
+                           int batch, int seq, void* out_hidden, void* states, void* stream) {
+  if (!h) return LAYA_E_INVAL;
+  if (!states || (reinterpret_cast<uintptr_t>(states) & 15u) != 0)
+    return laya::fail(h, LAYA_E_INVAL, "states must be a 16-byte aligned device pointer");
+  laya::RunOut ro;
+  ro.out = out_hidden;
+  ro.capture = static_cast<laya::bf16*>(states);
+  return run_impl(h, token_ids, lengths, batch, seq, nullptr, 0, ro, stream, false);
 }
 
 int laya_enc_check(laya_enc_handle* h, void* stream) {
@@ -864,17 +934,11 @@ int laya_enc_get_cache_stats(const laya_enc_handle* h, laya_enc_cache_stats* out
   return LAYA_OK;
 }
 
-int laya_enc_set_fused(laya_enc_handle* h, int enabled) {
-  if (!h) return LAYA_E_INVAL;
-  h->fused = enabled != 0;
-  return LAYA_OK;
-}
-
 int laya_enc_set_profiling(laya_enc_handle* h, int enabled) {
   if (!h) return LAYA_E_INVAL;
   if (!enabled && h->profiling) {
-    cudaError_t e = laya::prof_fold(h);
-    if (e != cudaSuccess) return laya::cuda_fail(h, e, "profiling events");
+    cudaError_t e = laya::prof_fold_all(h);
+    if (e != cudaSuccess) return laya::cuda_fail(h, e, "profiling stamps");
   }
   h->profiling = enabled != 0;
   return LAYA_OK;
@@ -882,8 +946,8 @@ int laya_enc_set_profiling(laya_enc_handle* h, int enabled) {
 
 int laya_enc_profile_read(laya_enc_handle* h, double* ms, int* launches, int n) {
   if (!h || !ms || !launches || n < 1 || n > LAYA_PROF_CLASSES) return LAYA_E_INVAL;
-  cudaError_t e = laya::prof_fold(h);
-  if (e != cudaSuccess) return laya::cuda_fail(h, e, "profiling events");
+  cudaError_t e = laya::prof_fold_all(h);
+  if (e != cudaSuccess) return laya::cuda_fail(h, e, "profiling stamps");
   for (int c = 0; c < n; ++c) {
     ms[c] = h->prof_ms[c];
     launches[c] = h->prof_count[c];
@@ -900,8 +964,7 @@ int laya_enc_launch_count(const laya_enc_handle* h, int batch, int seq) {
     return LAYA_E_INVAL;
   laya::Workspace w;
   size_t b = 0;
-  if (laya::workspace_layout(h, batch, seq, &w, &b) != LAYA_OK) return LAYA_E_INVAL;
-  w.fused_now = h->fused && w.fused_ok;
+  if (laya::workspace_layout(h, batch, seq, 0, &w, &b) != LAYA_OK) return LAYA_E_INVAL;
   return laya::kernel_count(h->cfg, w);
 }
 
@@ -910,7 +973,7 @@ int laya_enc_workspace_bytes(const laya_enc_handle* h, int batch, int seq, size_
     return LAYA_E_INVAL;
   laya::Workspace w;
   size_t b = 0;
-  if (laya::workspace_layout(h, batch, seq, &w, &b) != LAYA_OK) return LAYA_E_INVAL;
+  if (laya::workspace_layout(h, batch, seq, 0, &w, &b) != LAYA_OK) return LAYA_E_INVAL;
   *bytes = b;
   return LAYA_OK;
 }
@@ -919,11 +982,9 @@ int laya_enc_destroy(laya_enc_handle* h) {
   if (!h) return LAYA_OK;
   for (laya::Workspace* w : h->cache) laya::free_workspace(w);
   h->cache.clear();
-  for (cudaEvent_t e : h->prof_events) cudaEventDestroy(e);
   if (h->capture_stream) cudaStreamDestroy(h->capture_stream);
   if (h->rope) cudaFree(h->rope);
   if (h->err) cudaFree(h->err);
-  if (h->fused_layers) cudaFree(h->fused_layers);
   delete h;
   return LAYA_OK;
 }

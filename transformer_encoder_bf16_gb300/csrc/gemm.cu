@@ -95,6 +95,7 @@ struct GemmArgs {
   const bf16* ln_x;
   const bf16* ln_gamma;
   float ln_eps;
+  uint64_t* stamp;  // profiling: release time of the dependency wait (first CTA)
 };
 
 // Position in a ring of n stages, advanced without division (the stage
@@ -487,6 +488,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (NA == 2) ptx::tma_load_2d(st + kATileBytes, &tm_w2, fb, kc, f_tile * kBM, pol_w);
       }
       ptx::grid_dependency_wait();
+      if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) record_stamp(a.stamp);
       for (int i = 0; i < pre; ++i) {
         const uint32_t st = sbase + i * stage_bytes;
         ptx::tma_load_2d(st + NA * kATileBytes, &tm_x, full0 + 8u * i, (kb0 + i) * kBK,
@@ -849,6 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (NA == 2) ptx::tma_load_2d(st + kATileBytes, &tm_w2, full0 + 8u * i, i * kBK, f0 * kBM, pol_w);
         }
         ptx::grid_dependency_wait();
+        if (blockIdx.x == 0) record_stamp(a.stamp);
         const int t0 = first / a.feat_tiles;
         for (int i = 0; i < pre; ++i)
           ptx::tma_load_2d(sbase + i * stage_bytes + NA * kATileBytes, &tm_x, full0 + 8u * i,
@@ -1098,6 +1101,7 @@ cudaError_t launch_kind(const GemmPlan& p, const GemmOperands& o, Launch l) {
   a.ln_x = o.ln_x;
   a.ln_gamma = o.ln_gamma;
   a.ln_eps = o.ln_eps;
+  a.stamp = l.stamp;
 
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads);

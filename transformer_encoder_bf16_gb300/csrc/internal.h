@@ -33,7 +33,24 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 struct Launch {
   cudaStream_t stream = nullptr;
   bool pdl = false;  // programmatic dependent launch (overlap with the previous kernel)
+  // Profiling: non-null, the kernel's first CTA writes the %globaltimer value
+  // at which its dependency wait returned (the previous kernel's completion)
+  uint64_t* stamp = nullptr;
 };
+
+// Records the release time of a kernel (see Launch::stamp): called by one
+// thread of the kernel's first CTA right after its dependency wait.
+__device__ __forceinline__ void record_stamp(uint64_t* stamp) {
+  if (stamp != nullptr) {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    *stamp = t;
+  }
+}
+
+// A kernel that only records its release time: the end mark of a profiled
+// forward pass.
+cudaError_t launch_stamp(Launch l);
 
 // Packed tokens (packing.cuh): lens non-null selects them for B rows of S.
 struct Packing {
@@ -54,6 +71,9 @@ cudaError_t launch_unpack_rows(const void* x, const int32_t* lens, int B, int S,
                                void* out, Launch l);
 cudaError_t launch_rope(bf16* qkv, const float* cos_t, const float* sin_t, int B, int S,
                         int heads, Launch l);
+// out[m] = x[idx[m]] for m < n, rows of row_bytes (a multiple of 16).
+cudaError_t launch_gather_rows(const void* x, const int32_t* idx, int n, int row_bytes, void* out,
+                               Launch l);
 bool rowops_supported_hidden(int H);
 
 // ------------------------------------------------------------- attention ---
@@ -64,11 +84,19 @@ cudaError_t launch_attention(const bf16* qkv, const int32_t* lengths, int B, int
                              const float* cos_t = nullptr, const float* sin_t = nullptr,
                              bool packed = false);
 
-// tcgen05 attention: tm_qkv maps the packed projection [B*S, 3H] with a box of
-// 128 rows x 64 columns (make_tmap_bf16_2d(..., box_rows = 128)).
+// Attention from a subset of query rows: slot m = b * kmax + r is query token
+// q_tok[m] (its row in qkv) at position q_pos[m] of row b; ctx_rows [B*kmax, H].
+cudaError_t launch_attention_rows(const bf16* qkv, const int32_t* lengths, const int32_t* q_tok,
+                                  const int32_t* q_pos, int B, int S, int kmax, int heads,
+                                  int global, int half_window, bool packed, bf16* ctx_rows,
+                                  int* err, Launch l);
+
+// tcgen05 attention: tm_qkv maps the projection [rows, 3H] (padded: B*S rows;
+// packed: the packed tokens) with a box of 128 rows x 64 columns
+// (make_tmap_bf16_2d(..., box_rows = 128)).
 cudaError_t launch_attention_tc(const CUtensorMap& tm_qkv, const int32_t* lengths, int B, int S,
                                 int heads, int global, int half_window, bf16* ctx, int* err,
-                                Launch l);
+                                Launch l, bool packed = false);
 
 // ------------------------------------------------------------------ GEMM ---
 enum GemmKind : int { kGemmPlain = 0, kGemmResidual = 1, kGemmGeglu = 2 };
@@ -137,66 +165,6 @@ cudaError_t gemm_node_retarget(cudaGraphExec_t exec, cudaGraphNode_t node, const
                                void* new_y);
 cudaError_t unpack_node_retarget(cudaGraphExec_t exec, cudaGraphNode_t node, const void* old_out,
                                  void* new_out);
-
-// ------------------------------------------------ fused short forward ---
-// The whole forward of a request of at most 128 tokens as one persistent,
-// cooperatively launched kernel (fused.cu).
-
-// Weights of one layer as the fused kernel reads them (device memory).
-struct FusedLayer {
-  CUtensorMap maps[5];      // wqkv, wo, wup (GELU half), wup (gate half), wdown; boxes 64 x 128
-  const bf16* attn_norm;    // null: identity (encoder layer 0)
-  const bf16* mlp_norm;
-};
-
-struct FusedGemmPlan {
-  int tiles;  // 128-feature tiles
-  int kb;     // 64-wide k-blocks (split among the four CTAs of a cluster)
-};
-
-constexpr int kFusedMaxClusters = 64;
-
-struct FusedPlanOut {
-  int nt = 0;                  // token columns of the MMA (M rounded up to 16)
-  int n_clusters = 0;          // clusters of four CTAs launched
-  FusedGemmPlan plan[4] = {};  // QKV, out-projection, up (GeGLU), down
-  // tile of each projection each cluster computes (255: none)
-  uint8_t cluster_tile[4][kFusedMaxClusters] = {};
-};
-
-struct FusedArgs {
-  // activation tiles (boxes nt rows x 64) and the projection rows attention
-  // reads (boxes 128 rows x 64), over the workspace buffers
-  CUtensorMap tm_x, tm_ctx, tm_g, tm_qkv;
-  int M, B, S, nt;
-  int L, n_enc, heads, H, I, vocab, half_window, global_every, max_seq;
-  float eps;
-  FusedGemmPlan plan[4];
-  uint8_t cluster_tile[4][kFusedMaxClusters];
-  const FusedLayer* layers;    // [L]
-  const int32_t* ids;          // [M]
-  const int32_t* lens;         // [B]
-  const bf16* emb;             // [vocab, H]
-  const bf16* emb_gamma;
-  const bf16* final_gamma;     // null: no final norm before the decision layers
-  const float* rope;           // cos_g, sin_g, cos_l, sin_l, each [max_seq, 32]
-  bf16 *x, *qkv, *ctx, *g, *out;
-  float* stats;                // [M][H / 128] (mean, sum of squared deviations)
-  uint32_t* ready;             // [phases], zero-initialised, only grow
-  uint32_t* sync;              // [0] generation, [1] finished CTAs, [2] abort word
-  int* err;
-};
-
-// Number of ready counters the program of a configuration uses.
-inline int fused_phase_count(int L, int n_enc, bool final_norm) {
-  return 1 + 5 * L + ((final_norm && L > n_enc) ? 1 : 0);
-}
-
-bool plan_fused(int M, int H, int I, int heads, int n_clusters, FusedPlanOut* out);
-// Clusters of four CTAs (one per SM) that can be resident at once (at most
-// kFusedMaxClusters), 0 if the kernel cannot be launched.
-int fused_max_clusters();
-cudaError_t launch_fused(const FusedArgs& a, int n_clusters, cudaStream_t stream);
 
 // Host RoPE table (shared by create() and the op-level entry point).
 void rope_table_host(double theta, int max_seq, int half, int bf16_round, float* cos_t,

@@ -66,6 +66,21 @@ int laya_op_attention(const void* qkv, const int32_t* lengths_dev, int B, int S,
                                       nullptr, l));
 }
 
+int laya_op_attention_rows(const void* qkv, const int32_t* lengths_dev, const int32_t* q_tok_dev,
+                           const int32_t* q_pos_dev, int B, int S, int kmax, int heads,
+                           int head_dim, int global, int half_window, void* ctx_rows,
+                           void* stream) {
+  if (!al16(qkv) || !lengths_dev || !q_tok_dev || !q_pos_dev || !al16(ctx_rows) || B < 1 ||
+      S < 1 || kmax < 1 || static_cast<long long>(B) * kmax > LAYA_ENC_MAX_MARKERS || heads < 1 ||
+      head_dim != 64 || half_window < 0 || heads > 65535)
+    return LAYA_E_INVAL;
+  laya::Launch l{static_cast<cudaStream_t>(stream), false};
+  return rc_of(laya::launch_attention_rows(static_cast<const bf16*>(qkv), lengths_dev, q_tok_dev,
+                                           q_pos_dev, B, S, kmax, heads, global ? 1 : 0,
+                                           half_window, false, static_cast<bf16*>(ctx_rows),
+                                           nullptr, l));
+}
+
 int laya_op_attention_tc(const void* qkv, const int32_t* lengths_dev, int B, int S, int heads,
                          int head_dim, int global, int half_window, void* ctx, void* stream) {
   if (!al16(qkv) || !lengths_dev || !al16(ctx) || B < 1 || S < 1 || heads < 1 ||

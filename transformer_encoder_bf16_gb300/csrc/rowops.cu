@@ -56,7 +56,8 @@ __global__ void __launch_bounds__(128) layernorm_kernel(const bf16* src,
                                                         const int32_t* __restrict__ ids,
                                                         int vocab, int* err,
                                                         const int32_t* __restrict__ lens, int B,
-                                                        int S, int32_t* __restrict__ pos) {
+                                                        int S, int32_t* __restrict__ pos,
+                                                        uint64_t* stamp) {
   ptx::grid_launch_dependents();
   constexpr int H = 256 * V;
   const int row = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
@@ -68,6 +69,7 @@ __global__ void __launch_bounds__(128) layernorm_kernel(const bf16* src,
 #pragma unroll
   for (int c = 0; c < V; ++c) gr[c] = __ldg(g4 + lane + 32 * c);
   ptx::grid_dependency_wait();
+  if (blockIdx.x == 0 && threadIdx.x == 0) record_stamp(stamp);
   if (row >= M) return;
   int orow = row;  // output row
   if (lens != nullptr) {
@@ -138,9 +140,11 @@ __global__ void __launch_bounds__(256) rope_kernel(bf16* qkv, const float* __res
 __global__ void __launch_bounds__(128) unpack_rows_kernel(const uint4* __restrict__ x,
                                                           const int32_t* __restrict__ lens, int B,
                                                           int S, int chunks,
-                                                          uint4* __restrict__ out) {
+                                                          uint4* __restrict__ out,
+                                                          uint64_t* stamp) {
   ptx::grid_launch_dependents();
   ptx::grid_dependency_wait();
+  if (blockIdx.x == 0 && threadIdx.x == 0) record_stamp(stamp);
   const int row = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= B * S) return;
@@ -152,6 +156,22 @@ __global__ void __launch_bounds__(128) unpack_rows_kernel(const uint4* __restric
   } else {
     for (int c = lane; c < chunks; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
   }
+}
+
+// out[m] = x[idx[m]] for m < n: rows of `chunks` 16-byte units, one warp per row.
+__global__ void __launch_bounds__(128) gather_rows_kernel(const uint4* __restrict__ x,
+                                                          const int32_t* __restrict__ idx, int n,
+                                                          int chunks, uint4* __restrict__ out,
+                                                          uint64_t* stamp) {
+  ptx::grid_launch_dependents();
+  ptx::grid_dependency_wait();
+  if (blockIdx.x == 0 && threadIdx.x == 0) record_stamp(stamp);
+  const int row = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= n) return;
+  const uint4* src = x + static_cast<size_t>(idx[row]) * chunks;
+  uint4* dst = out + static_cast<size_t>(row) * chunks;
+  for (int c = lane; c < chunks; c += 32) dst[c] = src[c];
 }
 
 cudaError_t launch_cfg(const void* fn, dim3 grid, dim3 block, size_t smem, Launch l,
@@ -177,9 +197,10 @@ cudaError_t launch_ln_v(const bf16* src, const bf16* gamma, int M, float eps, bf
   const int32_t* lens = pk.lens;
   int B = pk.B, S = pk.S;
   int32_t* pos = pk.pos;
+  uint64_t* stamp = l.stamp;
   void* args[] = {(void*)&src, (void*)&gamma, (void*)&M,    (void*)&eps, (void*)&dst,
                   (void*)&ids, (void*)&vocab, (void*)&err,  (void*)&lens, (void*)&B,
-                  (void*)&S,   (void*)&pos};
+                  (void*)&S,   (void*)&pos,   (void*)&stamp};
   return launch_cfg(reinterpret_cast<const void*>(&layernorm_kernel<V>), grid, block, 0, l,
                     args);
 }
@@ -213,7 +234,20 @@ float bf16_round_host(float x) {
   return y;
 }
 
+// The end mark of a profiled forward pass: one thread records when the last
+// kernel before it has completed.
+__global__ void stamp_kernel(uint64_t* stamp) {
+  ptx::grid_dependency_wait();
+  record_stamp(stamp);
+}
+
 }  // namespace
+
+cudaError_t launch_stamp(Launch l) {
+  uint64_t* stamp = l.stamp;
+  void* args[] = {(void*)&stamp};
+  return launch_cfg(reinterpret_cast<const void*>(&stamp_kernel), dim3(1), dim3(32), 0, l, args);
+}
 
 bool rowops_supported_hidden(int H) { return H >= 256 && H <= 2048 && H % 256 == 0; }
 
@@ -237,8 +271,22 @@ cudaError_t launch_unpack_rows(const void* x, const int32_t* lens, int B, int S,
   const int rows_per_block = 4;
   const int chunks = row_bytes / 16;
   dim3 grid((B * S + rows_per_block - 1) / rows_per_block), block(32 * rows_per_block);
-  void* args[] = {(void*)&x, (void*)&lens, (void*)&B, (void*)&S, (void*)&chunks, (void*)&out};
+  uint64_t* stamp = l.stamp;
+  void* args[] = {(void*)&x,      (void*)&lens, (void*)&B,    (void*)&S,
+                  (void*)&chunks, (void*)&out,  (void*)&stamp};
   return launch_cfg(reinterpret_cast<const void*>(&unpack_rows_kernel), grid, block, 0, l, args);
+}
+
+cudaError_t launch_gather_rows(const void* x, const int32_t* idx, int n, int row_bytes, void* out,
+                               Launch l) {
+  if (n <= 0 || idx == nullptr || row_bytes <= 0 || row_bytes % 16 != 0)
+    return cudaErrorInvalidValue;
+  const int rows_per_block = 4;
+  const int chunks = row_bytes / 16;
+  dim3 grid((n + rows_per_block - 1) / rows_per_block), block(32 * rows_per_block);
+  uint64_t* stamp = l.stamp;
+  void* args[] = {(void*)&x, (void*)&idx, (void*)&n, (void*)&chunks, (void*)&out, (void*)&stamp};
+  return launch_cfg(reinterpret_cast<const void*>(&gather_rows_kernel), grid, block, 0, l, args);
 }
 
 cudaError_t unpack_node_retarget(cudaGraphExec_t exec, cudaGraphNode_t node, const void* old_out,
@@ -248,10 +296,10 @@ cudaError_t unpack_node_retarget(cudaGraphExec_t exec, cudaGraphNode_t node, con
   if (e != cudaSuccess) return e;
   if (p.func != reinterpret_cast<const void*>(&unpack_rows_kernel) || p.kernelParams == nullptr)
     return cudaErrorInvalidValue;
-  // arguments: x, lens, B, S, chunks, out
+  // arguments: x, lens, B, S, chunks, out, stamp
   if (*static_cast<void* const*>(p.kernelParams[5]) != old_out) return cudaErrorInvalidValue;
-  void* args[6] = {p.kernelParams[0], p.kernelParams[1], p.kernelParams[2],
-                   p.kernelParams[3], p.kernelParams[4], &new_out};
+  void* args[7] = {p.kernelParams[0], p.kernelParams[1], p.kernelParams[2], p.kernelParams[3],
+                   p.kernelParams[4], &new_out,          p.kernelParams[6]};
   p.kernelParams = args;
   p.extra = nullptr;
   e = cudaGraphExecKernelNodeSetParams(exec, node, &p);
