@@ -10,25 +10,33 @@
 // "Test Result" (queries whose visible keys are all padding: context 0 here).
 //
 // One CTA per (128-query tile, head, row); keys in tiles of 128.  Roles:
-//   warp 0     TMA: the Q tile once, K and V tiles into a two-stage ring;
+//   warp 0     TMA: the Q tile once, each K tile into one buffer (free as soon
+//              as its Q K^T is done), V tiles into a two-stage ring;
 //   warp 1     owns TMEM; one thread issues S_j = Q K_j^T (tcgen05.mma, fp32
-//              in TMEM, two S buffers) ahead of the softmax, and
-//              O_j = P_j V_j (V as an MN-major operand: its [keys][64 dims]
-//              tile is already that layout) into one of two O buffers;
+//              in TMEM) as soon as the softmax has read S_{j-1}, and
+//              O += P_j V_j into an fp32 accumulator in TMEM (V as an MN-major
+//              operand: its [keys][64 dims] tile is already that layout);
 //   warps 2-5  softmax, one thread per query row (its TMEM lane): the 128
-//              scores of S_j in one TMEM load, mask, running maximum and sum
-//              (exp2, fp32), the BF16 row of P_j into shared memory in the
-//              128-byte swizzled K-major layout (two buffers), then the
-//              previous tile's O_{j-1} folded into fp32 registers after
-//              rescaling.
-// So the QK^T of tile j + 1 and the PV of tile j - 1 run on the tensor cores
-// while the softmax of tile j runs.  P is rounded to BF16 for the PV product
-// (the row sums are not).  Local layers visit the two key tiles that cover
-// [q0 - w, q0 + 128 + w) (w = 64) inside the row; global layers the tiles
-// below len.  Query
-// rows outside the row (partial tiles of packed rows) are computed and not
-// stored; padded query rows of the padded layout are stored (0 where no key
-// is visible).  Every wait is bounded (ptx::mbar_wait): an expired wait raises the
+//              scores of S_j in one TMEM load, mask, running maximum, P_j =
+//              2^(s - m) rounded to BF16 into shared memory (128-byte swizzled
+//              K-major layout), fp32 row sum.
+// The QK^T of tile j + 1 runs on the tensor cores while the softmax of tile j
+// runs.  The maximum the exponents use is raised only when a row's running
+// maximum exceeds it by more than 8 (log2 units), and only then is that row of
+// O rescaled in TMEM (before the next P V): the normalisation divides by a sum
+// taken against the same maximum, so the result is the same softmax, with
+// probabilities below 2^8 before normalisation.  P is rounded to BF16 for the
+// P V product (the row sums are not).
+//
+// Shared memory (96 KB) and TMEM (256 columns: S 128, O 64) are sized so that
+// two CTAs share an SM: one CTA's softmax overlaps the other's loads and
+// products, and its start-up the other's tail.
+//
+// Local layers visit the key tiles of [q0 - w, q0 + 128 + w) inside the row
+// (two tiles when w <= 64); global layers the tiles below len.  Query rows
+// outside the row (partial tiles of packed rows) are computed and not stored;
+// padded query rows of the padded layout are stored (0 where no key is
+// visible).  Every wait is bounded (ptx::mbar_wait): an expired wait raises the
 // CTA's abort flag and the device error word, every role then leaves its loop,
 // the TMA and MMA threads wait (bounded) for their copies and products in
 // flight, and TMEM is released.
@@ -41,32 +49,35 @@ namespace laya {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kQT = 128;                    // queries per CTA (MMA M)
-constexpr int kKT = 128;                    // keys per tile (MMA N of Q K^T)
-constexpr uint32_t kTile = 128u * 128u;     // bytes of a [128 x 64] BF16 tile
-// shared memory (1024-byte aligned): Q | K[2] | V[2] | P[2] (two 64-key halves each) | barriers
+constexpr int kQT = 128;                 // queries per CTA (MMA M)
+constexpr int kKT = 128;                 // keys per tile (MMA N of Q K^T)
+constexpr uint32_t kTile = 128u * 128u;  // bytes of a [128 x 64] BF16 tile
+// shared memory (1024-byte aligned): Q | K | V[2] | P (two 64-key halves) | barriers
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kTile;
-constexpr uint32_t kOffV = kOffK + 2 * kTile;
+constexpr uint32_t kOffV = kOffK + kTile;
 constexpr uint32_t kOffP = kOffV + 2 * kTile;
-constexpr uint32_t kOffBar = kOffP + 4 * kTile;
+constexpr uint32_t kOffBar = kOffP + 2 * kTile;
 constexpr uint32_t kSmem = kOffBar + 256 + 1024;  // + alignment slack
-// TMEM: S[b] at columns 128 b, O[b] at 256 + 64 b
-constexpr uint32_t kTmemCols = 512;
+// TMEM: S at columns [0, 128), O at [128, 192)
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColO = 128;
+// the maximum the exponents use is raised only beyond this margin (log2)
+constexpr float kRescaleMargin = 8.f;
 
 // Barrier slots (8 bytes each) from kOffBar.
 enum : uint32_t {
   kBarQ = 0,
-  kBarKvFull = 1,   // + b
-  kBarKvEmpty = 3,  // + b
-  kBarSFull = 5,    // + b
-  kBarSEmpty = 7,   // + b
-  kBarPFull = 9,    // + b
-  kBarPEmpty = 11,  // + b
-  kBarOFull = 13,   // + b
-  kBarOEmpty = 15,  // + b
-  kBarDone = 17,    // every MMA of the CTA has completed
-  kBarCount = 18
+  kBarKFull = 1,
+  kBarKEmpty = 2,
+  kBarVFull = 3,   // + b
+  kBarVEmpty = 5,  // + b
+  kBarSFull = 7,
+  kBarSEmpty = 8,
+  kBarPFull = 9,
+  kBarPvDone = 10,  // P_j V_j has completed: P may be rewritten, O read or rescaled
+  kBarDone = 11,    // every MMA of the CTA has completed
+  kBarCount = 12
 };
 
 // Descriptor of a V tile as an MN-major operand (the 64 dims contiguous, keys
@@ -78,6 +89,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr) {
          (static_cast<uint64_t>(1) << 46) | (static_cast<uint64_t>(2) << 61);
 }
 
+// 2^x by the special-function unit (approximate, flush-to-zero; 2^-inf = 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 struct AttnArgs {
   const int32_t* lengths;
   int S, heads, global, half_window, packed;
@@ -86,7 +104,7 @@ struct AttnArgs {
   uint64_t* stamp;
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, const AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -127,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // first token of this row in the projection: packed rows start at cu(b)
   const int row0 = a.packed ? packed_start(a.lengths, b, S) : b * S;
   // key tiles of 128 from kbase: global, [0, len); local, the keys of
-  // [q0 - w, q0 + 128 + w) inside [0, len) (two tiles when w <= 64)
+  // [q0 - w, q0 + 128 + w) inside [0, len)
   const int kbase = a.global ? 0 : max(0, q0 - w);
   const int kend = a.global ? len : min(len, q0 + kQT + w);
   const int nk = (kend - kbase + kKT - 1) / kKT;
@@ -135,11 +153,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (uint32_t i = 0; i < kBarCount; ++i) ptx::mbar_init(bar(i), 1);
-    for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(bar(kBarSEmpty + i), 4);  // one arrival per softmax warp
-      ptx::mbar_init(bar(kBarPFull + i), 4);
-      ptx::mbar_init(bar(kBarOEmpty + i), 4);
-    }
+    ptx::mbar_init(bar(kBarSEmpty), 4);  // one arrival per softmax warp
+    ptx::mbar_init(bar(kBarPFull), 4);
     *abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tm_qkv);
@@ -162,26 +177,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (bad_len && a.err != nullptr) atomicCAS(a.err, 0, kDevBadLength);
       ptx::mbar_arrive_expect_tx(bar(kBarQ), kTile);
       ptx::tma_load_2d(sb + kOffQ, &tm_qkv, bar(kBarQ), n * 64, row0 + q0, pol);
-      int issued = 0;
+      int k_issued = 0, v_issued = 0;
       for (int j = 0; j < nk; ++j) {
-        const int s = j & 1;
-        if (j >= 2 && !ptx::mbar_wait(bar(kBarKvEmpty + s), ((j >> 1) - 1) & 1, abort_flag, a.err,
+        const int krow = row0 + kbase + j * kKT;
+        if (j >= 1 && !ptx::mbar_wait(bar(kBarKEmpty), (j - 1) & 1, abort_flag, a.err,
                                       kDevWaitEmpty, kWaitLimitNs))
           break;
-        const int krow = row0 + kbase + j * kKT;
-        ptx::mbar_arrive_expect_tx(bar(kBarKvFull + s), 2 * kTile);
-        ptx::tma_load_2d(sb + kOffK + s * kTile, &tm_qkv, bar(kBarKvFull + s), H + n * 64, krow,
-                         pol);
-        ptx::tma_load_2d(sb + kOffV + s * kTile, &tm_qkv, bar(kBarKvFull + s), 2 * H + n * 64,
+        ptx::mbar_arrive_expect_tx(bar(kBarKFull), kTile);
+        ptx::tma_load_2d(sb + kOffK, &tm_qkv, bar(kBarKFull), H + n * 64, krow, pol);
+        k_issued = j + 1;
+        const int s = j & 1;
+        if (j >= 2 && !ptx::mbar_wait(bar(kBarVEmpty + s), ((j >> 1) - 1) & 1, abort_flag, a.err,
+                                      kDevWaitEmpty, kWaitLimitNs))
+          break;
+        ptx::mbar_arrive_expect_tx(bar(kBarVFull + s), kTile);
+        ptx::tma_load_2d(sb + kOffV + s * kTile, &tm_qkv, bar(kBarVFull + s), 2 * H + n * 64,
                          krow, pol);
-        issued = j + 1;
+        v_issued = j + 1;
       }
       // no copy may still be in flight into shared memory at exit (a flag of
       // our own, so that an abort does not cut these waits short)
       volatile int drain = 0;
       ptx::mbar_wait(bar(kBarQ), 0, &drain, nullptr, 0, kWaitLimitNs);
-      for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
-        ptx::mbar_wait(bar(kBarKvFull + (j & 1)), (j >> 1) & 1, &drain, nullptr, 0, kWaitLimitNs);
+      if (k_issued > 0)
+        ptx::mbar_wait(bar(kBarKFull), (k_issued - 1) & 1, &drain, nullptr, 0, kWaitLimitNs);
+      for (int j = v_issued > 2 ? v_issued - 2 : 0; j < v_issued; ++j)
+        ptx::mbar_wait(bar(kBarVFull + (j & 1)), (j >> 1) & 1, &drain, nullptr, 0, kWaitLimitNs);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -190,41 +211,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_o = ptx::idesc_bf16(kQT, 64) | (1u << 16);   // P V: V MN-major
       auto issue_pv = [&](int t) -> bool {
         const int s = t & 1;
-        if (!ptx::mbar_wait(bar(kBarPFull + s), (t >> 1) & 1, abort_flag, a.err, kDevWaitFull,
+        if (!ptx::mbar_wait(bar(kBarPFull), t & 1, abort_flag, a.err, kDevWaitFull, kWaitLimitNs) ||
+            !ptx::mbar_wait(bar(kBarVFull + s), (t >> 1) & 1, abort_flag, a.err, kDevWaitFull,
                             kWaitLimitNs))
           return false;
-        if (t >= 2 && !ptx::mbar_wait(bar(kBarOEmpty + s), ((t >> 1) - 1) & 1, abort_flag, a.err,
-                                      kDevWaitAccum, kWaitLimitNs))
-          return false;
         ptx::tc_fence_after();
-        const uint32_t p = sb + kOffP + s * 2 * kTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          ptx::mma_bf16(tmem + 256 + 64 * s,
-                        ptx::sdesc_sw128(p + (kk >> 2) * kTile + (kk & 3) * 32),
+          ptx::mma_bf16(tmem + kColO, ptx::sdesc_sw128(sb + kOffP + (kk >> 2) * kTile + (kk & 3) * 32),
                         sdesc_sw128_mn(sb + kOffV + s * kTile + kk * 2048), idesc_o,
-                        kk > 0 ? 1u : 0u);
-        ptx::mma_commit(bar(kBarOFull + s));
-        ptx::mma_commit(bar(kBarPEmpty + s));
-        ptx::mma_commit(bar(kBarKvEmpty + s));
+                        (t > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_commit(bar(kBarPvDone));
+        ptx::mma_commit(bar(kBarVEmpty + s));
         return true;
       };
       bool ok = ptx::mbar_wait(bar(kBarQ), 0, abort_flag, a.err, kDevWaitFull, kWaitLimitNs);
       for (int j = 0; j < nk && ok; ++j) {
-        const int s = j & 1;
-        ok = ptx::mbar_wait(bar(kBarKvFull + s), (j >> 1) & 1, abort_flag, a.err, kDevWaitFull,
-                            kWaitLimitNs);
-        if (ok && j >= 2)
-          ok = ptx::mbar_wait(bar(kBarSEmpty + s), ((j >> 1) - 1) & 1, abort_flag, a.err,
-                              kDevWaitAccum, kWaitLimitNs);
+        ok = ptx::mbar_wait(bar(kBarKFull), j & 1, abort_flag, a.err, kDevWaitFull, kWaitLimitNs);
+        // S is single-buffered: the softmax must have read S_{j-1}
+        if (ok && j >= 1)
+          ok = ptx::mbar_wait(bar(kBarSEmpty), (j - 1) & 1, abort_flag, a.err, kDevWaitAccum,
+                              kWaitLimitNs);
         if (!ok) break;
         ptx::tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          ptx::mma_bf16(tmem + 128 * s, ptx::sdesc_sw128(sb + kOffQ + kk * 32),
-                        ptx::sdesc_sw128(sb + kOffK + s * kTile + kk * 32), idesc_s,
-                        kk > 0 ? 1u : 0u);
-        ptx::mma_commit(bar(kBarSFull + s));
+          ptx::mma_bf16(tmem, ptx::sdesc_sw128(sb + kOffQ + kk * 32),
+                        ptx::sdesc_sw128(sb + kOffK + kk * 32), idesc_s, kk > 0 ? 1u : 0u);
+        ptx::mma_commit(bar(kBarSFull));
+        ptx::mma_commit(bar(kBarKEmpty));
         if (j >= 1) ok = issue_pv(j - 1);
       }
       if (ok) issue_pv(nk - 1);
@@ -235,52 +250,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // -------------------------------------------------------------- softmax
+    // Scores stay in the raw domain until the exponent: p = 2^(s * scale - m)
+    // is one FFMA and one ex2 per score; maxima and sums use several
+    // independent accumulators.
     const int q4 = warp & 3;
     const int row = q4 * 32 + lane;  // this thread's query row and TMEM lane
     const int i = q0 + row;          // its position in the row
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
     const float scale_log2 = 0.125f * 1.4426950408889634f;
-    float o[64];
-#pragma unroll
-    for (int d = 0; d < 64; ++d) o[d] = 0.f;
-    float m = -INFINITY, l = 0.f;  // running maximum (scaled, log2 domain) and sum
-    float m_ref = -INFINITY;       // the maximum o is relative to
-    float m_tile[2] = {-INFINITY, -INFINITY};  // the maximum each O buffer's P used
+    float m = -INFINITY;  // the maximum the exponents use (scaled, log2 domain)
+    float l = 0.f;        // the row sum against m
     bool ok = true;
-    // adds O_t (relative to the maximum its P used) to o
-    auto fold = [&](int t) -> bool {
-      const int s = t & 1;
-      if (!ptx::mbar_wait(bar(kBarOFull + s), (t >> 1) & 1, abort_flag, a.err, kDevWaitAccum,
-                          kWaitLimitNs))
-        return false;
-      ptx::tc_fence_after();
-      float ot[64];
-      ptx::tmem_ld64(lane_base + 256 + 64 * s, ot);
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(kBarOEmpty + s));
-      const float mt = m_tile[s];
-      if (mt != -INFINITY) {
-        const float c = m_ref == -INFINITY ? 0.f : exp2f(m_ref - mt);
-#pragma unroll
-        for (int d = 0; d < 64; ++d) o[d] = o[d] * c + ot[d];
-        m_ref = mt;
-      }
-      return true;
-    };
     for (int j = 0; j < nk && ok; ++j) {
-      const int s = j & 1;
-      if (!ptx::mbar_wait(bar(kBarSFull + s), (j >> 1) & 1, abort_flag, a.err, kDevWaitAccum,
-                          kWaitLimitNs)) {
+      if (!ptx::mbar_wait(bar(kBarSFull), j & 1, abort_flag, a.err, kDevWaitAccum, kWaitLimitNs)) {
         ok = false;
         break;
       }
       ptx::tc_fence_after();
       float sc[128];
-      ptx::tmem_ld128(lane_base + 128 * s, sc);
+      ptx::tmem_ld128(lane_base, sc);
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(kBarSEmpty + s));
+      if (lane == 0) ptx::mbar_arrive(bar(kBarSEmpty));
       // visible columns of this row: [lo, hi) (keys kstart + c)
       const int kstart = kbase + j * kKT;
       int lo = -kstart, hi = len - kstart;
@@ -288,67 +279,89 @@ __global__ void __launch_bounds__(kThreads, 1)
         lo = max(lo, i - w - kstart);
         hi = min(hi, i + w + 1 - kstart);
       }
-      float mx = -INFINITY;
-      if (lo <= 0 && hi >= kKT) {
+      if (!(lo <= 0 && hi >= kKT)) {
+        const uint32_t span = static_cast<uint32_t>(max(hi - lo, 0));
 #pragma unroll
-        for (int c = 0; c < kKT; ++c) {
-          sc[c] *= scale_log2;
-          mx = fmaxf(mx, sc[c]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < kKT; ++c) {
-          sc[c] = (c >= lo && c < hi) ? sc[c] * scale_log2 : -INFINITY;
-          mx = fmaxf(mx, sc[c]);
-        }
+        for (int c = 0; c < kKT; ++c)
+          if (static_cast<uint32_t>(c - lo) >= span) sc[c] = -INFINITY;
       }
-      const float m_new = fmaxf(m, mx);
-      const float alpha = m_new == -INFINITY ? 1.f : exp2f(m - m_new);
-      m = m_new;
-      m_tile[s] = m_new;
-      if (j >= 2 && !ptx::mbar_wait(bar(kBarPEmpty + s), ((j >> 1) - 1) & 1, abort_flag, a.err,
-                                    kDevWaitAccum, kWaitLimitNs)) {
-        ok = false;
-        break;
+      float mxa[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mxa[k] = sc[k];
+#pragma unroll
+      for (int c = 8; c < kKT; ++c) mxa[c & 7] = fmaxf(mxa[c & 7], sc[c]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) mxa[k] = fmaxf(mxa[k], mxa[k + 4]);
+      const float mx = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])) * scale_log2;
+      // raise the exponents' maximum only when the row has gone beyond it by
+      // the margin (or had none): then O and l are rescaled to the new one
+      float alpha = 1.f;
+      if (mx > m + kRescaleMargin) {
+        alpha = m == -INFINITY ? 0.f : ex2(m - mx);
+        m = mx;
+      }
+      const float mu = m == -INFINITY ? 0.f : m;  // a fully masked row gives p = 0
+      // P_{j-1} V_{j-1} must have completed before P is rewritten and O read
+      if (j >= 1) {
+        if (!ptx::mbar_wait(bar(kBarPvDone), (j - 1) & 1, abort_flag, a.err, kDevWaitAccum,
+                            kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
       }
       // P row: keys [0, 64) in half 0, [64, 128) in half 1; 16-byte chunk c
       // of row r sits at chunk c ^ (r % 8)
-      uint8_t* prow = smem + kOffP + s * 2 * kTile + static_cast<uint32_t>(row) * 128u;
-      float ls = 0.f;
+      uint8_t* prow = smem + kOffP + static_cast<uint32_t>(row) * 128u;
+      float lsa[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c8 = 0; c8 < kKT / 8; ++c8) {
         uint4 pk;
         __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&pk);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float x0 = sc[c8 * 8 + 2 * e], x1 = sc[c8 * 8 + 2 * e + 1];
-          const float p0 = m_new == -INFINITY ? 0.f : exp2f(x0 - m_new);
-          const float p1 = m_new == -INFINITY ? 0.f : exp2f(x1 - m_new);
-          ls += p0 + p1;
+          const float p0 = ex2(fmaf(sc[c8 * 8 + 2 * e], scale_log2, -mu));
+          const float p1 = ex2(fmaf(sc[c8 * 8 + 2 * e + 1], scale_log2, -mu));
+          lsa[e] += p0 + p1;
           p2[e] = __floats2bfloat162_rn(p0, p1);
         }
         const int half = c8 >> 3, ch = c8 & 7;
         *reinterpret_cast<uint4*>(prow + half * kTile + ((ch ^ (row & 7)) << 4)) = pk;
       }
-      l = l * alpha + ls;
+      l = l * alpha + ((lsa[0] + lsa[1]) + (lsa[2] + lsa[3]));
+      // the scores are dead by now: rescale this warp's rows of O if any moved
+      if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        float ov[64];
+        ptx::tmem_ld64(lane_base + kColO, ov);
+#pragma unroll
+        for (int d = 0; d < 64; ++d) ov[d] *= alpha;
+        ptx::tmem_st64(lane_base + kColO, ov);
+      }
       ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(kBarPFull + s));
-      if (j >= 1) ok = fold(j - 1);
+      if (lane == 0) ptx::mbar_arrive(bar(kBarPFull));
     }
-    if (ok) ok = fold(nk - 1);
-    if (ok && *abort_flag == 0 && i < rows) {
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint4* o4 = reinterpret_cast<uint4*>(a.ctx + static_cast<size_t>(row0 + i) * H +
-                                           static_cast<size_t>(n) * 64);
+    if (ok)
+      ok = ptx::mbar_wait(bar(kBarPvDone), (nk - 1) & 1, abort_flag, a.err, kDevWaitAccum,
+                          kWaitLimitNs);
+    if (ok) {
+      ptx::tc_fence_after();
+      float ov[64];
+      ptx::tmem_ld64(lane_base + kColO, ov);
+      if (*abort_flag == 0 && i < rows) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint4* o4 = reinterpret_cast<uint4*>(a.ctx + static_cast<size_t>(row0 + i) * H +
+                                             static_cast<size_t>(n) * 64);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint4 pk;
-        __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&pk);
+        for (int c = 0; c < 8; ++c) {
+          uint4 pk;
+          __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&pk);
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          p2[e] = __floats2bfloat162_rn(o[c * 8 + 2 * e] * inv, o[c * 8 + 2 * e + 1] * inv);
-        o4[c] = pk;
+          for (int e = 0; e < 4; ++e)
+            p2[e] = __floats2bfloat162_rn(ov[c * 8 + 2 * e] * inv, ov[c * 8 + 2 * e + 1] * inv);
+          o4[c] = pk;
+        }
       }
     }
   }
