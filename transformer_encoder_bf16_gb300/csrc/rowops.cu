@@ -108,30 +108,42 @@ __global__ void __launch_bounds__(128) layernorm_kernel(const bf16* src,
   }
 }
 
-// threadIdx.x = pair i in [0, 32), threadIdx.y + 8 * blockIdx.x = head-part
-// (q heads then k heads), blockIdx.y = token.
+// threadIdx.x = group of 8 pairs (pairs 8 x .. 8 x + 7 of the 32), threadIdx.y
+// = head-part (q heads, then k heads), blockIdx.x = token: a (half-dim, head,
+// row) grid with 32-bit indices.  Each thread moves 16 bytes of each half of
+// its head (x1 = pairs' first members, x2 = second members) and two 32-byte
+// table rows, so a warp reads and writes whole 128-byte heads.
 __global__ void __launch_bounds__(256) rope_kernel(bf16* qkv, const float* __restrict__ cos_t,
                                                    const float* __restrict__ sin_t, int S,
                                                    int heads) {
   ptx::grid_launch_dependents();
   ptx::grid_dependency_wait();
-  const uint32_t i = threadIdx.x;
-  const uint32_t hp = blockIdx.x * blockDim.y + threadIdx.y;
+  const uint32_t i0 = threadIdx.x * 8u;
+  const uint32_t hp = threadIdx.y;
   if (hp >= 2u * static_cast<uint32_t>(heads)) return;
-  const uint32_t t = blockIdx.y;
+  const uint32_t t = blockIdx.x;
   const uint32_t s = t % static_cast<uint32_t>(S);
   const uint32_t H = static_cast<uint32_t>(heads) * 64u;
   const uint32_t part = hp / static_cast<uint32_t>(heads);
   const uint32_t n = hp - part * static_cast<uint32_t>(heads);
-  bf16* p = qkv + t * 3u * H + part * H + n * 64u + i;
-  const float x1 = __bfloat162float(p[0]);
-  const float x2 = __bfloat162float(p[32]);
-  const float c = cos_t[s * 32u + i];
-  const float sn = sin_t[s * 32u + i];
-  const float y1 = __fsub_rn(__fmul_rn(x1, c), __fmul_rn(x2, sn));
-  const float y2 = __fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, sn));
-  p[0] = __float2bfloat16_rn(y1);
-  p[32] = __float2bfloat16_rn(y2);
+  bf16* p = qkv + t * 3u * H + part * H + n * 64u + i0;
+  const uint4 a = *reinterpret_cast<const uint4*>(p);
+  const uint4 b = *reinterpret_cast<const uint4*>(p + 32);
+  const float4* c4 = reinterpret_cast<const float4*>(cos_t + s * 32u + i0);
+  const float4* s4 = reinterpret_cast<const float4*>(sin_t + s * 32u + i0);
+  const float4 ca = __ldg(c4), cb = __ldg(c4 + 1), sa = __ldg(s4), sb = __ldg(s4 + 1);
+  const float cv[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+  const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+  float x1[8], x2[8], y1[8], y2[8];
+  unpack8(a, x1);
+  unpack8(b, x2);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    y1[k] = __fsub_rn(__fmul_rn(x1[k], cv[k]), __fmul_rn(x2[k], sv[k]));
+    y2[k] = __fadd_rn(__fmul_rn(x2[k], cv[k]), __fmul_rn(x1[k], sv[k]));
+  }
+  *reinterpret_cast<uint4*>(p) = pack8(y1);
+  *reinterpret_cast<uint4*>(p + 32) = pack8(y2);
 }
 
 // Padded output from packed rows: out[b * S + s] = x[cu(b) + s] for s < len(b),
@@ -311,7 +323,8 @@ cudaError_t launch_rope(bf16* qkv, const float* cos_t, const float* sin_t, int B
                         int heads, Launch l) {
   const int M = B * S;
   if (M <= 0 || heads <= 0) return cudaErrorInvalidValue;
-  dim3 block(32, 8), grid((2 * heads + 7) / 8, M);
+  if (2 * heads > 64) return cudaErrorInvalidValue;
+  dim3 block(4, 2 * heads), grid(M);
   void* args[] = {(void*)&qkv, (void*)&cos_t, (void*)&sin_t, (void*)&S, (void*)&heads};
   return launch_cfg(reinterpret_cast<const void*>(&rope_kernel), grid, block, 0, l, args);
 }
