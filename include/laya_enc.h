@@ -180,6 +180,22 @@ int laya_enc_check(laya_enc_handle* h, void* stream);
  * LAYA_E_POISONED.  No device fault is involved. */
 int laya_enc_debug_fail_next_run(laya_enc_handle* h);
 
+/* Test hooks for the device-side failure path ("Laya native CUDA worker",
+ * "Start and check": a native failure stops the executor).  Every wait of a
+ * kernel on a barrier is bounded; when one runs out, the kernel raises its
+ * CTA's abort flag and the device error word, every role of the CTA leaves
+ * its loop, the copies and tensor-core products in flight are waited for and
+ * tensor memory is released, so the kernel returns and the context stays
+ * usable; laya_enc_check then returns LAYA_E_DEVICE and poisons the handle.
+ * set_wait_limit_ns: the bound of the projections' barrier waits, in [1 ms,
+ * 10 s]; 0 restores the default of 2 s.
+ * withhold_next_run: in the next laya_enc_run / _run_device on this handle
+ * (launched eagerly), the first CTA of the first projection never issues the
+ * copy of its first pipeline stage, so the wait for that stage runs out after
+ * the limit.  No trap, no fault, no invalid access is involved. */
+int laya_enc_debug_set_wait_limit_ns(laya_enc_handle* h, uint64_t ns);
+int laya_enc_debug_withhold_next_run(laya_enc_handle* h);
+
 /* 1: use CUDA Graphs (default, unless env LAYA_EAGER=1); 0: eager launches. */
 int laya_enc_set_graphs(laya_enc_handle* h, int enabled);
 
@@ -210,6 +226,14 @@ int laya_enc_get_cache_stats(const laya_enc_handle* h, laya_enc_cache_stats* out
 
 /* Number of kernel launches one forward pass of this shape makes. */
 int laya_enc_launch_count(const laya_enc_handle* h, int batch, int seq);
+
+/* The projection plans in use for a (batch, seq) shape that has a workspace
+ * (after its first run, which times the candidate plans): for QKV, out-proj,
+ * up and down in turn, four values each into out[16]: tokens per tile,
+ * split-K factor, pairing (0 none, 1 CTA pairs sharing the token tile, 2
+ * sharing the weight tiles), CTAs launched.  LAYA_E_INVAL if the shape has no
+ * workspace. */
+int laya_enc_get_plans(const laya_enc_handle* h, int batch, int seq, int32_t* out);
 
 /* Bytes of device workspace a (batch, seq) shape uses (activations, split-K
  * partials, staging). */

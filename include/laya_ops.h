@@ -53,8 +53,9 @@ int laya_op_rope_table(double theta, int max_seq, int half, int bf16,
  * Pairs (i, i + D/2); position of token (b, s) is s:
  *   y_i = bf16(x_i c - x_{i+D/2} s),  y_{i+D/2} = bf16(x_{i+D/2} c + x_i s)
  * with each product and the sum rounded to fp32 separately (no FMA).
- * cos_dev, sin_dev: fp32 [>= S, D/2] device tables.  One thread per
- * (pair, head, token) with 32-bit indices.
+ * cos_dev, sin_dev: fp32 [>= S, D/2] device tables, 16-byte aligned.  A
+ * (half-dim, head, row) grid with 32-bit indices: one thread per (8 pairs,
+ * head, token), 16-byte loads and stores; heads <= 32.
  * Sources: "[RFC]: Native Laya inference with Rust and CUDA #14", "Design"
  * (separate QKV, RoPE and attention launches); "perf(model): exact Metal
  * speed-ups of the forward pass - #45" (a (half-dim, head, row) grid with
@@ -97,11 +98,12 @@ int laya_op_attention_rows(const void* qkv, const int32_t* lengths_dev,
 
 /* laya_op_attention on the 5th-generation tensor cores: S = Q K^T and O = P V
  * by tcgen05.mma with fp32 accumulators in tensor memory, one CTA per 128
- * queries of one head and row, Q/K/V tiles brought in by TMA.  Same arguments,
- * layouts, mask and results contract as laya_op_attention; P is rounded to
- * BF16 for the P V product (the row sums are not).  qkv must be 16-byte
- * aligned with B*S rows of 3*heads*64 BF16 values.  Returns LAYA_E_INVAL for
- * bad arguments, LAYA_E_CUDA when the launch fails.
+ * queries of one head and row with warp-specialised roles (TMA, MMA issue,
+ * softmax), Q/K/V tiles brought in by TMA.  Same arguments, layouts, mask and
+ * results contract as laya_op_attention; P is rounded to BF16 for the P V
+ * product (the row sums are not).  qkv must be 16-byte aligned with B*S rows
+ * of 3*heads*64 BF16 values.  Returns LAYA_E_INVAL for bad arguments,
+ * LAYA_E_CUDA when the launch fails.
  * Sources: as laya_op_attention. */
 int laya_op_attention_tc(const void* qkv, const int32_t* lengths_dev, int B, int S,
                          int heads, int head_dim, int global, int half_window,
@@ -110,7 +112,9 @@ int laya_op_attention_tc(const void* qkv, const int32_t* lengths_dev, int B, int
 /* RoPE and attention in one kernel: the q and k of each tile are rotated in
  * shared memory (same arithmetic as laya_op_rope, bit-identical values) and
  * attended as in laya_op_attention; qkv in memory is not modified.  cos_dev,
- * sin_dev: fp32 [>= S, 32] device tables.  This is the form laya_enc_run uses.
+ * sin_dev: fp32 [>= S, 32] device tables.  (laya_enc_run rotates q and k once,
+ * in the QKV projection's epilogue, instead: every K tile would otherwise be
+ * rotated once per query tile.)
  * Sources: as laya_op_rope and laya_op_attention. */
 int laya_op_attention_rope(const void* qkv, const int32_t* lengths_dev,
                            const float* cos_dev, const float* sin_dev, int B,
@@ -139,6 +143,22 @@ int laya_op_linear(const void* x, int M, int K, const void* w, int N, int kind,
                    const void* residual, void* y, void* workspace,
                    size_t workspace_bytes, int splits, int tile_tokens,
                    void* stream);
+
+/* laya_op_linear with the choice of the persistent kernel's pairing (splits
+ * must be 1 when paired != 0): the one-CTA-per-SM kernel runs in clusters of
+ * two CTAs that share one operand tile of every pipeline stage, read from L2
+ * once and multicast by TMA into both (halving the L2-to-SM traffic of that
+ * operand).  paired = 1: the two CTAs take the two feature tiles of a pair
+ * with the same token tile (the token tile is shared); paired = 2: the two
+ * token tiles of a pair with the same feature tile (the weight tiles are
+ * shared).  laya_enc_run's first run of a shape may pick either by timing.
+ * Same arithmetic and results as paired = 0, bit for bit.
+ * LAYA_E_UNSUPPORTED if the device cannot hold such clusters.
+ * Sources: as laya_op_linear. */
+int laya_op_linear_ex(const void* x, int M, int K, const void* w, int N, int kind,
+                      const void* residual, void* y, void* workspace,
+                      size_t workspace_bytes, int splits, int tile_tokens, int paired,
+                      void* stream);
 
 /* Workspace bytes laya_op_linear (and the _ln / _rope forms) need for this
  * shape and plan; 0 when the plan does not split K. */

@@ -59,6 +59,39 @@ def test_linear_matches_oracle(kind, M, N, K, splits, nt):
     assert ok, msg
 
 
+@pytest.mark.parametrize("kind", [te.KIND_PLAIN, te.KIND_RESIDUAL, te.KIND_GEGLU])
+@pytest.mark.parametrize("M,N,K,nt", [
+    (2000, 1024, 1024, 224), (4117, 2624, 1024, 128), (1111, 520, 256, 64), (300, 3072, 1024, 48),
+    (8192, 1024, 2624, 224)])
+def test_linear_paired_equals_unpaired_and_oracle(kind, M, N, K, nt):
+    # the persistent kernel in clusters of two (the token tile, or the weight
+    # tiles, multicast into both CTAs) computes every tile exactly as the
+    # single-CTA kernel: bit for bit, twice in a row; odd feature- and
+    # token-tile counts (2624 / 128, 520 / 128, 4117 / 128 ...) leave the last
+    # pair's second tile past N or past the tokens
+    torch = require_gpu()
+    rng = np.random.default_rng(2000 + M + N + K + kind)
+    if kind == te.KIND_GEGLU:
+        nt = min(nt, 128)   # two accumulators, double-buffered: 4 x nt <= 512 TMEM columns
+    Nw = 2 * N if kind == te.KIND_GEGLU else N
+    xb = rnd_bits(rng, (M, K))
+    wb = rnd_bits(rng, (Nw, K), std=0.02)
+    rb = rnd_bits(rng, (M, N), std=2.0) if kind == te.KIND_RESIDUAL else None
+    r_dev = to_dev(rb) if rb is not None else None
+    outs = []
+    for paired in (0, 1, 1, 2, 2):
+        y = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+        te.linear(to_dev(xb), to_dev(wb), y, kind, residual=r_dev, splits=1, tile_tokens=nt,
+                  paired=paired)
+        torch.cuda.synchronize()
+        outs.append(to_bits(y))
+    for o in outs[1:]:
+        np.testing.assert_array_equal(o, outs[0])
+    if M <= 2000:
+        ok, msg = bf16_close(outs[1], oracle.linear(xb, wb, kind, rb), ulps=1.0, min_exact=0.97)
+        assert ok, msg
+
+
 def test_linear_residual_in_place_and_repeat():
     torch = require_gpu()
     rng = np.random.default_rng(7)

@@ -85,9 +85,12 @@ _SIGNATURES = {
     "laya_enc_set_graphs": ([_P, _I], _I),
     "laya_enc_debug_fail_next_run": ([_P], _I),
     "laya_enc_debug_capture": ([_P, _P, _P, _I, _I, _P, _P, _P], _I),
+    "laya_enc_debug_set_wait_limit_ns": ([_P, ctypes.c_uint64], _I),
+    "laya_enc_debug_withhold_next_run": ([_P], _I),
     "laya_enc_get_cache_stats": ([_P, _P], _I),
     "laya_enc_launch_count": ([_P, _I, _I], _I),
     "laya_enc_workspace_bytes": ([_P, _I, _I, ctypes.POINTER(_SZ)], _I),
+    "laya_enc_get_plans": ([_P, _I, _I, _P], _I),
     "laya_enc_set_profiling": ([_P, _I], _I),
     "laya_enc_profile_read": ([_P, ctypes.POINTER(_D), ctypes.POINTER(_I), _I], _I),
     "laya_enc_destroy": ([_P], _I),
@@ -103,6 +106,7 @@ _SIGNATURES = {
     "laya_op_attention_rope": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "laya_op_linear": ([_P, _I, _I, _P, _I, _I, _P, _P, _P, _SZ, _I, _I, _P], _I),
     "laya_op_linear_noalloc": ([_P, _I, _I, _P, _I, _I, _P, _P, _I, _I, _P], _I),
+    "laya_op_linear_ex": ([_P, _I, _I, _P, _I, _I, _P, _P, _P, _SZ, _I, _I, _I, _P], _I),
     "laya_op_linear_workspace_size": ([_I, _I, _I, _I, _I, _I, ctypes.POINTER(_SZ)], _I),
     "laya_op_linear_ln": ([_P, _P, _F, _I, _I, _P, _I, _I, _P, _P, _P, _SZ, _I, _I, _P], _I),
     "laya_op_linear_rope": ([_P, _I, _I, _P, _I, _P, _P, _I, _I, _P, _P, _SZ, _I, _I, _P], _I),
@@ -254,6 +258,15 @@ class Encoder:
         """Test hook: the next run fails like a CUDA launch failure (poisons the handle)."""
         _check(lib().laya_enc_debug_fail_next_run(self.handle), self.handle)
 
+    def debug_set_wait_limit_ns(self, ns: int):
+        """Bound of the projections' barrier waits (0: the default 2 s)."""
+        _check(lib().laya_enc_debug_set_wait_limit_ns(self.handle, int(ns)), self.handle)
+
+    def debug_withhold_next_run(self):
+        """Test hook: the next run's first projection withholds one pipeline
+        stage, so a bounded wait runs out (LAYA_E_DEVICE at check())."""
+        _check(lib().laya_enc_debug_withhold_next_run(self.handle), self.handle)
+
     def set_graphs(self, enabled: bool):
         _check(lib().laya_enc_set_graphs(self.handle, 1 if enabled else 0), self.handle)
 
@@ -293,6 +306,13 @@ class Encoder:
 
     def launch_count(self, B, S) -> int:
         return lib().laya_enc_launch_count(self.handle, B, S)
+
+    def plans(self, B, S) -> dict:
+        """{projection: (tokens per tile, split-K, pairing, CTAs)} of a shape that has run."""
+        out = (ctypes.c_int32 * 16)()
+        _check(lib().laya_enc_get_plans(self.handle, B, S, out), self.handle)
+        return {n: tuple(out[4 * g: 4 * g + 4])
+                for g, n in enumerate(("qkv", "out_proj", "up_geglu", "down"))}
 
     def workspace_bytes(self, B, S) -> int:
         n = ctypes.c_size_t()
@@ -379,15 +399,17 @@ def attention_rope(qkv, lengths_dev, cos_dev, sin_dev, B, S, heads, global_, hal
 
 
 def linear(x, w, y, kind=KIND_PLAIN, residual=None, splits=0, tile_tokens=0, stream=None,
-           workspace=None):
+           workspace=None, paired=0):
     """workspace: a device tensor of at least linear_workspace_size() bytes; a
-    fresh one is allocated when None (pass one when capturing a graph)."""
+    fresh one is allocated when None (pass one when capturing a graph).
+    paired: 0, or the persistent kernel in clusters of two sharing the token
+    tile (1) or the weight tiles (2) of every stage (splits must be 1)."""
     M, K = x.shape
     N = y.shape[1]
     ws = workspace if workspace is not None else _workspace(M, K, N, kind, splits, tile_tokens, y.device)
-    _check(lib().laya_op_linear(_ptr(x), M, K, _ptr(w), N, kind, _ptr(residual), _ptr(y), _ptr(ws),
-                                ws.numel() if ws is not None else 0, splits, tile_tokens,
-                                _stream_ptr(stream)))
+    _check(lib().laya_op_linear_ex(_ptr(x), M, K, _ptr(w), N, kind, _ptr(residual), _ptr(y),
+                                   _ptr(ws), ws.numel() if ws is not None else 0, splits,
+                                   tile_tokens, int(paired), _stream_ptr(stream)))
 
 
 def linear_noalloc(x, w, y, kind=KIND_PLAIN, residual=None, splits=0, tile_tokens=0, stream=None):

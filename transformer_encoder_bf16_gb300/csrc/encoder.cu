@@ -29,8 +29,11 @@
 #include <chrono>
 #include <cstdlib>
 #include <cstring>
+#include <map>
+#include <mutex>
 #include <new>
 #include <string>
+#include <tuple>
 #include <vector>
 
 #include "../../include/laya_ops.h"
@@ -71,6 +74,12 @@ struct Workspace {
   cudaEvent_t staged = nullptr;   // the last upload from `host` has been consumed
   cudaEvent_t done = nullptr;     // the last forward using this workspace has finished
   GemmPlan p_qkv, p_o, p_up, p_dn;
+  // plan tuning (tune_plans): candidate plans of each projection, timed on
+  // the first run of the shape; p_* above are the chosen ones
+  static constexpr int kMaxCand = 12;
+  GemmPlan cand[7][kMaxCand];
+  int ncand[7] = {};
+  bool tuned = false;
   // activation operand of each GEMM; the TMA box height is that GEMM's own
   // token tile (plans may differ: a GeGLU split-K partial can force a smaller tile)
   CUtensorMap tm_x_qkv, tm_h_qkv, tm_ctx_o, tm_h_up, tm_g_dn;
@@ -113,9 +122,14 @@ struct laya_enc_handle {
   bool graphs = true;
   bool pdl = true;
   bool attn_tc = true;  // attention on tcgen05 (false: the mma.sync kernel, env LAYA_ATTN_MMA_SYNC=1)
+  bool tune = true;     // time candidate projection plans on a shape's first run (env LAYA_NO_TUNE=1: off)
   bool poisoned = false;
   std::string last_error;
   bool fail_next_run = false;  // test hook: the next run fails as a CUDA error would
+  // failure-path test hooks on the device: the bound of the GEMM kernels'
+  // barrier waits, and the next run's first projection withholding a stage
+  uint64_t wait_ns = laya::kWaitLimitNs;
+  bool withhold_next_run = false;
   // profiling: per-class totals of the stamped runs folded so far
   bool profiling = false;
   double prof_ms[LAYA_PROF_CLASSES] = {};
@@ -161,6 +175,16 @@ void free_workspace(Workspace* w) {
   delete w;
 }
 
+// The projections of a workspace by slot: QKV, out, up, down, then the
+// marker-row out, up and down.
+enum GemmSlot : int { kGemmQkv = 0, kGemmOut, kGemmUp, kGemmDown, kGemmMarkerOut, kGemmMarkerUp,
+                      kGemmMarkerDown };
+
+GemmPlan* gemm_slot(Workspace* w, int g) {
+  GemmPlan* p[7] = {&w->p_qkv, &w->p_o, &w->p_up, &w->p_dn, &w->p_mo, &w->p_mup, &w->p_mdn};
+  return p[g];
+}
+
 int kernel_count(const laya_enc_config& c, const Workspace& w) {
   const int L = c.n_encoder_layers + c.n_decision_layers;
   // per layer: attention norm (not at an identity layer 0), QKV, attention,
@@ -195,6 +219,14 @@ int workspace_layout(const laya_enc_handle* h, int B, int S, int kmax, Workspace
                    !plan_gemm(Mk, I, H, kGemmGeglu, h->num_sms, 0, 0, &w->p_mup) ||
                    !plan_gemm(Mk, H, I, kGemmResidual, h->num_sms, 0, 0, &w->p_mdn)))
     return LAYA_E_INVAL;
+  // candidates for the timing on the first run (the model's choice first)
+  for (int g = 0; g < 7; ++g) {
+    GemmPlan* pg = gemm_slot(w, g);
+    w->ncand[g] = 0;
+    if (g >= kGemmMarkerOut && kmax == 0) continue;
+    w->ncand[g] = plan_candidates(pg->M, pg->N, pg->K, pg->kind, h->num_sms, w->cand[g],
+                                  Workspace::kMaxCand);
+  }
   size_t off = 0;
   auto take = [&](size_t n) {
     const size_t o = off;
@@ -213,11 +245,13 @@ int workspace_layout(const laya_enc_handle* h, int B, int S, int kmax, Workspace
   const size_t ocm = take(static_cast<size_t>(Mk) * H * 2);
   const size_t ohm = take(static_cast<size_t>(Mk) * H * 2);
   const size_t ogm = take(static_cast<size_t>(Mk) * I * 2);
-  size_t pbytes = std::max(std::max(w->p_qkv.workspace_bytes, w->p_o.workspace_bytes),
-                           std::max(w->p_up.workspace_bytes, w->p_dn.workspace_bytes));
-  if (kmax > 0)
-    pbytes = std::max(pbytes, std::max(w->p_mo.workspace_bytes,
-                                       std::max(w->p_mup.workspace_bytes, w->p_mdn.workspace_bytes)));
+  // split-K partials: room for the largest candidate of any projection
+  size_t pbytes = 0;
+  for (int g = 0; g < 7; ++g) {
+    if (g >= kGemmMarkerOut && kmax == 0) continue;
+    pbytes = std::max(pbytes, gemm_slot(w, g)->workspace_bytes);
+    for (int k = 0; k < w->ncand[g]; ++k) pbytes = std::max(pbytes, w->cand[g][k].workspace_bytes);
+  }
   const size_t ostamp = take(static_cast<size_t>(kernel_count(c, *w) + 1) * sizeof(uint64_t));
   const size_t op = take(pbytes);
   *total = off;
@@ -280,6 +314,7 @@ cudaError_t prof_fold_all(laya_enc_handle* h) {
 struct RunOut {
   void* out = nullptr;      // BF16 [B, S, H], or fp32 when cfg.out_fp32
   bf16* capture = nullptr;  // debug: [L, B, S, H], the residual stream entering each layer
+  bool withhold = false;    // failure-path test (laya_enc_debug_withhold_next_run)
 };
 
 // Enqueues one forward pass.  out is written by the last residual sum
@@ -341,6 +376,8 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, const RunOut& ro,
                                    next(LAYA_PROF_NORM), pk));
     GemmOperands o;
     o.err = h->err;
+    o.wait_ns = h->wait_ns;
+    o.withhold = ro.withhold && li == 0;  // the first projection of the forward
     o.partials = w->partials;
     o.partials_bytes = w->partials_bytes;
     o.lens = pk.lens;
@@ -365,6 +402,7 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, const RunOut& ro,
     o.rope_S = w->S;
     o.rope_cols = 2 * H;
     LAYA_LAUNCH(launch_gemm(w->p_qkv, o, next(LAYA_PROF_QKV)));
+    o.withhold = false;
     o.rope_cos = o.rope_sin = nullptr;
     if (li == h->L - 1 && w->kmax > 0) {
       // marker rows: everything after the keys and values is row-wise, so the
@@ -375,6 +413,7 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, const RunOut& ro,
                                         w->ctxm, h->err, next(LAYA_PROF_ATTN)));
       GemmOperands om;
       om.err = h->err;
+      om.wait_ns = h->wait_ns;
       om.partials = w->partials;
       om.partials_bytes = w->partials_bytes;
       om.w = lw.wo;
@@ -451,6 +490,149 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, const RunOut& ro,
   return cudaSuccess;
 }
 
+// TMA descriptors over the workspace activations; each GEMM's box height is
+// its plan's token tile.
+bool build_activation_maps(const laya_enc_handle* h, Workspace* w) {
+  const laya_enc_config& c = h->cfg;
+  const int M = w->M;
+  auto box = [](const GemmPlan& p) { return static_cast<uint32_t>(p.nt); };
+  const uint64_t ldh = c.hidden * 2ull, ldi = c.intermediate * 2ull;
+  bool ok = make_tmap_bf16_2d(&w->tm_x_qkv, w->x, M, c.hidden, ldh, box(w->p_qkv)) &&
+            make_tmap_bf16_2d(&w->tm_h_qkv, w->h, M, c.hidden, ldh, box(w->p_qkv)) &&
+            make_tmap_bf16_2d(&w->tm_ctx_o, w->ctx, M, c.hidden, ldh, box(w->p_o)) &&
+            make_tmap_bf16_2d(&w->tm_h_up, w->h, M, c.hidden, ldh, box(w->p_up)) &&
+            make_tmap_bf16_2d(&w->tm_g_dn, w->g, M, c.intermediate, ldi, box(w->p_dn)) &&
+            make_tmap_bf16_2d(&w->tm_qkv_attn, w->qkv, M, 3ull * c.hidden, 3 * ldh, 128);
+  if (ok && w->kmax > 0) {
+    const int Mk = w->Mk;
+    ok = make_tmap_bf16_2d(&w->tm_ctxm, w->ctxm, Mk, c.hidden, ldh, box(w->p_mo)) &&
+         make_tmap_bf16_2d(&w->tm_hm, w->hm, Mk, c.hidden, ldh, box(w->p_mup)) &&
+         make_tmap_bf16_2d(&w->tm_gm, w->gm, Mk, c.intermediate, ldi, box(w->p_mdn));
+  }
+  return ok;
+}
+
+// Plans chosen by timing, shared by every handle of the process so that two
+// handles running the same shape take the same plans (and give the same
+// bits): (M, N, K, kind, rows of the batch or 0 for marker slots) -> (token
+// tile, split-K factor, paired CTAs).
+std::mutex g_tuned_mu;
+std::map<std::tuple<int, int, int, int, int>, std::tuple<int, int, int>> g_tuned;
+
+// Times the candidate plans of each projection on the first run of a shape,
+// on `stream` after that run's input upload (the packed row lengths are real,
+// the activations are the workspace's), and keeps the fastest; the model's
+// choice stays unless another candidate is faster by more than 5 %.  Each
+// candidate is launched as in the forward (programmatic dependent launch,
+// layer-0 weights), into scratch outputs of the workspace.
+int marker_or_b(const Workspace* w, int g) { return g >= kGemmMarkerOut ? 0 : w->B; }
+
+int tune_plans(laya_enc_handle* h, Workspace* w, cudaStream_t stream) {
+  const laya_enc_config& c = h->cfg;
+  const int H = c.hidden;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  cudaError_t e = cudaEventCreate(&e0);
+  if (e == cudaSuccess) e = cudaEventCreate(&e1);
+  const LayerMaps& lw = h->layers[0];
+  const uint64_t ldh = H * 2ull, ldi = c.intermediate * 2ull;
+  for (int g = 0; g < 7 && e == cudaSuccess; ++g) {
+    if (w->ncand[g] <= 0) continue;
+    GemmPlan* slot = gemm_slot(w, g);
+    const auto key = std::make_tuple(slot->M, slot->N, slot->K, slot->kind, marker_or_b(w, g));
+    {
+      std::lock_guard<std::mutex> lk(g_tuned_mu);
+      auto it = g_tuned.find(key);
+      if (it != g_tuned.end()) {
+        for (int k = 0; k < w->ncand[g]; ++k)
+          if (w->cand[g][k].nt == std::get<0>(it->second) &&
+              w->cand[g][k].splits == std::get<1>(it->second) &&
+              w->cand[g][k].pair == std::get<2>(it->second))
+            *slot = w->cand[g][k];
+        continue;
+      }
+    }
+    const bool marker = g >= kGemmMarkerOut;
+    const int rows = marker ? w->Mk : w->M;
+    double best_ms = 0.0;
+    int best = 0;
+    for (int k = 0; k < w->ncand[g] && e == cudaSuccess; ++k) {
+      const GemmPlan& p = w->cand[g][k];
+      GemmOperands o;
+      o.err = h->err;
+      o.wait_ns = h->wait_ns;
+      o.partials = w->partials;
+      o.partials_bytes = w->partials_bytes;
+      if (!marker && w->packed) {
+        o.lens = w->lens;
+        o.lens_B = w->B;
+        o.lens_S = w->S;
+      }
+      o.x_box_rows = p.nt;
+      const uint32_t nt = static_cast<uint32_t>(p.nt);
+      bool ok = true;
+      switch (g) {
+        case kGemmQkv:
+          o.w = o.w2 = lw.wqkv;
+          ok = make_tmap_bf16_2d(&o.x, w->h, rows, H, ldh, nt);
+          o.y = w->qkv;
+          o.rope_cos = h->rope;
+          o.rope_sin = h->rope + static_cast<size_t>(c.max_seq) * 32;
+          o.rope_S = w->S;
+          o.rope_cols = 2 * H;
+          o.rope_pos = w->packed ? w->pos : nullptr;
+          break;
+        case kGemmOut:
+        case kGemmMarkerOut:
+          o.w = o.w2 = lw.wo;
+          ok = make_tmap_bf16_2d(&o.x, marker ? w->ctxm : w->ctx, rows, H, ldh, nt);
+          o.residual = marker ? w->xm : w->x;
+          o.y = marker ? w->hm : w->h;
+          break;
+        case kGemmUp:
+        case kGemmMarkerUp:
+          o.w = lw.wup_in;
+          o.w2 = lw.wup_gate;
+          ok = make_tmap_bf16_2d(&o.x, marker ? w->hm : w->h, rows, H, ldh, nt);
+          o.y = marker ? w->gm : w->g;
+          break;
+        default:
+          o.w = o.w2 = lw.wdown;
+          ok = make_tmap_bf16_2d(&o.x, marker ? w->gm : w->g, rows, c.intermediate, ldi, nt);
+          o.residual = marker ? w->xm : w->x;
+          o.y = marker ? w->hm : w->h;
+          break;
+      }
+      if (!ok) {
+        e = cudaErrorInvalidValue;
+        break;
+      }
+      const Launch l{stream, h->pdl, nullptr};
+      for (int r = 0; r < 2 && e == cudaSuccess; ++r) e = launch_gemm(p, o, l);
+      if (e == cudaSuccess) e = cudaEventRecord(e0, stream);
+      for (int r = 0; r < 6 && e == cudaSuccess; ++r) e = launch_gemm(p, o, l);
+      if (e == cudaSuccess) e = cudaEventRecord(e1, stream);
+      if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+      float ms = 0.f;
+      if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, e0, e1);
+      if (e != cudaSuccess) break;
+      if (k == 0 || ms < best_ms * (best == 0 ? 0.95 : 1.0)) {
+        best_ms = ms;
+        best = k;
+      }
+    }
+    if (e != cudaSuccess) break;
+    *slot = w->cand[g][best];
+    std::lock_guard<std::mutex> lk(g_tuned_mu);
+    g_tuned.emplace(key, std::make_tuple(slot->nt, slot->splits, slot->pair));
+  }
+  if (e0) cudaEventDestroy(e0);
+  if (e1) cudaEventDestroy(e1);
+  if (e != cudaSuccess) return cuda_fail(h, e, "plan tuning");
+  if (!build_activation_maps(h, w)) return fail(h, LAYA_E_CUDA, "tensor map encoding failed");
+  w->tuned = true;
+  return LAYA_OK;
+}
+
 int get_workspace(laya_enc_handle* h, int B, int S, int kmax, Workspace** out) {
   for (Workspace* w : h->cache) {
     if (w->B == B && w->S == S && w->kmax == kmax) {
@@ -497,22 +679,7 @@ int get_workspace(laya_enc_handle* h, int B, int S, int kmax, Workspace** out) {
     free_workspace(w);
     return fail(h, LAYA_E_NOMEM, std::string("workspace: ") + cudaGetErrorString(e));
   }
-  const laya_enc_config& c = h->cfg;
-  const int M = w->M;
-  auto box = [](const GemmPlan& p) { return static_cast<uint32_t>(p.nt); };
-  const uint64_t ldh = c.hidden * 2ull, ldi = c.intermediate * 2ull;
-  bool ok = make_tmap_bf16_2d(&w->tm_x_qkv, w->x, M, c.hidden, ldh, box(w->p_qkv)) &&
-            make_tmap_bf16_2d(&w->tm_h_qkv, w->h, M, c.hidden, ldh, box(w->p_qkv)) &&
-            make_tmap_bf16_2d(&w->tm_ctx_o, w->ctx, M, c.hidden, ldh, box(w->p_o)) &&
-            make_tmap_bf16_2d(&w->tm_h_up, w->h, M, c.hidden, ldh, box(w->p_up)) &&
-            make_tmap_bf16_2d(&w->tm_g_dn, w->g, M, c.intermediate, ldi, box(w->p_dn)) &&
-            make_tmap_bf16_2d(&w->tm_qkv_attn, w->qkv, M, 3ull * c.hidden, 3 * ldh, 128);
-  if (ok && kmax > 0) {
-    const int Mk = w->Mk;
-    ok = make_tmap_bf16_2d(&w->tm_ctxm, w->ctxm, Mk, c.hidden, ldh, box(w->p_mo)) &&
-         make_tmap_bf16_2d(&w->tm_hm, w->hm, Mk, c.hidden, ldh, box(w->p_mup)) &&
-         make_tmap_bf16_2d(&w->tm_gm, w->gm, Mk, c.intermediate, ldi, box(w->p_mdn));
-  }
+  const bool ok = build_activation_maps(h, w);
   if (!ok) {
     free_workspace(w);
     return fail(h, LAYA_E_CUDA, "workspace: tensor map encoding failed");
@@ -572,12 +739,22 @@ int run_common(laya_enc_handle* h, Workspace* w, const RunOut& ro, cudaStream_t 
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   cudaError_t e = cudaStreamIsCapturing(stream, &cap);
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamIsCapturing");
+  if (!w->tuned) {
+    if (cap == cudaStreamCaptureStatusNone && h->tune) {
+      const auto t_tune = std::chrono::steady_clock::now();
+      const int rc = tune_plans(h, w, stream);
+      if (rc != LAYA_OK) return rc;
+      h->stats.capture_ms += std::chrono::duration<double, std::milli>(
+                                 std::chrono::steady_clock::now() - t_tune).count();
+    }
+    w->tuned = true;  // inside a caller's capture: the model's plans stay
+  }
   const bool profiling = h->profiling && cap == cudaStreamCaptureStatusNone && !ro.capture;
   if (profiling) {
     e = prof_fold_all(h);
     if (e != cudaSuccess) return cuda_fail(h, e, "profiling stamps");
   }
-  if (!h->graphs || cap != cudaStreamCaptureStatusNone || ro.capture != nullptr) {
+  if (!h->graphs || cap != cudaStreamCaptureStatusNone || ro.capture != nullptr || ro.withhold) {
     e = enqueue_forward(h, w, ro, stream, profiling);
     if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");
   } else if (profiling) {
@@ -737,6 +914,7 @@ int laya_enc_create(const laya_enc_config* cfg, const laya_enc_weights* wts,
   h->graphs = !env_flag("LAYA_EAGER");
   h->pdl = !env_flag("LAYA_NO_PDL");
   h->attn_tc = !env_flag("LAYA_ATTN_MMA_SYNC");
+  h->tune = !env_flag("LAYA_NO_TUNE");
   h->tok_emb = static_cast<const bf16*>(wts->tok_emb);
   h->emb_norm = static_cast<const bf16*>(wts->emb_norm);
   h->final_norm = static_cast<const bf16*>(wts->final_norm);
@@ -820,6 +998,11 @@ static int run_impl(laya_enc_handle* h, const int32_t* ids, const int32_t* lengt
   rc = get_workspace(h, B, S, kmax, &w);
   if (rc != LAYA_OK) return rc;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  RunOut run = ro;
+  if (h->withhold_next_run) {
+    h->withhold_next_run = false;
+    run.withhold = true;
+  }
   const size_t nid = static_cast<size_t>(w->M) * sizeof(int32_t);
   const size_t nlen = static_cast<size_t>(B) * sizeof(int32_t);
   if (device_inputs) {
@@ -858,7 +1041,7 @@ static int run_impl(laya_enc_handle* h, const int32_t* ids, const int32_t* lengt
       if (e != cudaSuccess) return cuda_fail(h, e, "cudaEventRecord");
     }
   }
-  return run_common(h, w, ro, stream);
+  return run_common(h, w, run, stream);
 }
 
 int laya_enc_run(laya_enc_handle* h, const int32_t* token_ids, const int32_t* lengths, int batch,
@@ -917,6 +1100,21 @@ int laya_enc_debug_fail_next_run(laya_enc_handle* h) {
   return LAYA_OK;
 }
 
+int laya_enc_debug_set_wait_limit_ns(laya_enc_handle* h, uint64_t ns) {
+  if (!h) return LAYA_E_INVAL;
+  if (ns == 0) ns = laya::kWaitLimitNs;
+  if (ns < 1000000ull || ns > 10000000000ull)
+    return laya::fail(h, LAYA_E_INVAL, "wait limit outside [1 ms, 10 s]");
+  h->wait_ns = ns;
+  return LAYA_OK;
+}
+
+int laya_enc_debug_withhold_next_run(laya_enc_handle* h) {
+  if (!h) return LAYA_E_INVAL;
+  h->withhold_next_run = true;
+  return LAYA_OK;
+}
+
 int laya_enc_set_graphs(laya_enc_handle* h, int enabled) {
   if (!h) return LAYA_E_INVAL;
   h->graphs = enabled != 0;
@@ -966,6 +1164,22 @@ int laya_enc_launch_count(const laya_enc_handle* h, int batch, int seq) {
   size_t b = 0;
   if (laya::workspace_layout(h, batch, seq, 0, &w, &b) != LAYA_OK) return LAYA_E_INVAL;
   return laya::kernel_count(h->cfg, w);
+}
+
+int laya_enc_get_plans(const laya_enc_handle* h, int batch, int seq, int32_t* out) {
+  if (!h || !out) return LAYA_E_INVAL;
+  for (const laya::Workspace* w : h->cache) {
+    if (w->B != batch || w->S != seq || w->kmax != 0) continue;
+    const laya::GemmPlan* p[4] = {&w->p_qkv, &w->p_o, &w->p_up, &w->p_dn};
+    for (int g = 0; g < 4; ++g) {
+      out[4 * g + 0] = p[g]->nt;
+      out[4 * g + 1] = p[g]->splits;
+      out[4 * g + 2] = p[g]->pair;
+      out[4 * g + 3] = p[g]->ctas();
+    }
+    return LAYA_OK;
+  }
+  return LAYA_E_INVAL;
 }
 
 int laya_enc_workspace_bytes(const laya_enc_handle* h, int batch, int seq, size_t* bytes) {

@@ -96,6 +96,10 @@ struct GemmArgs {
   const bf16* ln_gamma;
   float ln_eps;
   uint64_t* stamp;  // profiling: release time of the dependency wait (first CTA)
+  uint64_t wait_ns;  // bound of every wait on a barrier
+  // failure-path test hook: the first CTA's producer never issues its first
+  // stage, so the MMA issuer's wait for it runs out (no fault, no trap)
+  int withhold;
 };
 
 // Position in a ring of n stages, advanced without division (the stage
@@ -188,6 +192,12 @@ __device__ __forceinline__ EpiOut epi_out(const GemmArgs& a) {
 struct RopeRow {
   float4 c0, c1, s0, s1;
 };
+
+__device__ __forceinline__ RopeRow rope_row_at(const EpiOut& e, int pos, int i0) {
+  const float4* ct = reinterpret_cast<const float4*>(e.rope_cos + static_cast<size_t>(pos) * 32 + i0);
+  const float4* st = reinterpret_cast<const float4*>(e.rope_sin + static_cast<size_t>(pos) * 32 + i0);
+  return RopeRow{__ldg(ct), __ldg(ct + 1), __ldg(st), __ldg(st + 1)};
+}
 
 __device__ __forceinline__ RopeRow rope_row(const EpiOut& e, int t, int i0, bool padded = false) {
   const int pos = (e.rope_pos != nullptr && !padded) ? e.rope_pos[t] : t % e.rope_S;
@@ -400,6 +410,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * a.stages + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t red_bar = full0 + 8u * (3 * a.stages + 2);  // split-K slices landed
+  const uint32_t done_bar = full0 + 8u * (3 * a.stages + 3);  // every MMA completed
   const bool ln = a.ln_x != nullptr;
 
   const int warp = threadIdx.x >> 5;
@@ -421,6 +432,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     ptx::mbar_init(accum_bar, 1);
     ptx::mbar_init(red_bar, 1);
+    ptx::mbar_init(done_bar, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -478,8 +490,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       const uint64_t pol_w = ptx::policy_evict_first();
       const uint64_t pol_x = ptx::policy_evict_last();
       const int pre = nkb < a.stages ? nkb : a.stages;
+      const bool wh = a.withhold && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
       // weights of the first stages do not depend on the previous kernel
       for (int i = 0; i < pre; ++i) {
+        if (wh && i == 0) continue;
         const uint32_t st = sbase + i * stage_bytes;
         const uint32_t fb = full0 + 8u * i;
         const int kc = (kb0 + i) * kBK;
@@ -490,6 +504,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       ptx::grid_dependency_wait();
       if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) record_stamp(a.stamp);
       for (int i = 0; i < pre; ++i) {
+        if (wh && i == 0) continue;
         const uint32_t st = sbase + i * stage_bytes;
         ptx::tma_load_2d(st + NA * kATileBytes, &tm_x, full0 + 8u * i, (kb0 + i) * kBK,
                          t_tile * a.nt, pol_x);
@@ -499,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int i = pre; i < nkb; ++i, rp.next()) {
         const int s = rp.s;
         if (!ptx::mbar_wait(empty0 + 8u * s, rp.ph ^ 1u, abort_flag, a.err, kDevWaitEmpty,
-                            kWaitLimitNs))
+                            a.wait_ns))
           break;
         const uint32_t st = sbase + s * stage_bytes;
         const uint32_t fb = full0 + 8u * s;
@@ -510,10 +525,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         ptx::tma_load_2d(st + NA * kATileBytes, &tm_x, fb, kc, t_tile * a.nt, pol_x);
         issued = i + 1;
       }
-      // no copy may still be in flight into this CTA's shared memory at exit
+      // no copy may still be in flight into this CTA's shared memory at exit:
+      // wait for the last stages issued, with a flag of our own so that an
+      // abort does not cut these waits short
+      volatile int drain = 0;
       for (int i = (issued > a.stages ? issued - a.stages : 0); i < issued; ++i)
-        ptx::mbar_wait(full0 + 8u * (i % a.stages), static_cast<uint32_t>(i / a.stages) & 1u,
-                       abort_flag, a.err, kDevWaitFull, kWaitLimitNs);
+        if (!(wh && i == 0))
+          ptx::mbar_wait(full0 + 8u * (i % a.stages), static_cast<uint32_t>(i / a.stages) & 1u,
+                         &drain, nullptr, 0, a.wait_ns);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -528,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int i = 0; i < nkb; ++i, rp.next()) {
         const int s = rp.s;
         if (!ptx::mbar_wait((ln ? xform0 : full0) + 8u * s, rp.ph, abort_flag, a.err, kDevWaitFull,
-                            kWaitLimitNs))
+                            a.wait_ns))
           break;
         ptx::tc_fence_after();
         const uint64_t da = da0 + static_cast<uint64_t>(s) * stage_units;
@@ -544,6 +563,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         ptx::mma_commit(empty0 + 8u * s);
       }
       ptx::mma_commit(accum_bar);
+      // every product issued has completed before TMEM is released (an abort
+      // may leave no other thread waiting for them)
+      ptx::mma_commit(done_bar);
+      volatile int drain = 0;
+      ptx::mbar_wait(done_bar, 0, &drain, nullptr, 0, a.wait_ns);
     }
   } else {
     // ------------------------------------------- epilogue phase 1: drain TMEM
@@ -582,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       RingPos rp(a.stages);
       for (int i = 0; i < nkb; ++i, rp.next()) {
         const int s = rp.s;
-        if (!ptx::mbar_wait(full0 + 8u * s, rp.ph, abort_flag, a.err, kDevWaitFull, kWaitLimitNs))
+        if (!ptx::mbar_wait(full0 + 8u * s, rp.ph, abort_flag, a.err, kDevWaitFull, a.wait_ns))
           break;
         // B tile: nt rows of 128 bytes; 16-byte chunk j of row r sits at j ^ (r % 8)
         uint8_t* bt = smem + static_cast<size_t>(s) * stage_bytes + NA * kATileBytes;
@@ -606,7 +630,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         ptx::mbar_arrive(xform0 + 8u * s);
       }
     }
-    epi_ok = ptx::mbar_wait(accum_bar, 0, abort_flag, a.err, kDevWaitAccum, kWaitLimitNs);
+    epi_ok = ptx::mbar_wait(accum_bar, 0, abort_flag, a.err, kDevWaitAccum, a.wait_ns);
+    // the TMEM loads below are warp-collective: after an abort, lanes that
+    // polled at different moments must still agree
+    epi_ok = __all_sync(0xffffffffu, epi_ok);
     ptx::tc_fence_after();
     if (epi_ok && a.splits > 1) {
       // partial tile to the workspace, this thread's row into its owner's slice
@@ -660,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           ptx::bulk_load(sbase + static_cast<uint32_t>(sp) * bytes, src + sp * pstride, bytes,
                          red_bar);
       }
-      if (!ptx::mbar_wait(red_bar, 0, abort_flag, a.err, kDevWaitReduce, kWaitLimitNs))
+      if (!ptx::mbar_wait(red_bar, 0, abort_flag, a.err, kDevWaitReduce, a.wait_ns))
         red_failed = true;
       else
         split_epilogue<KIND, NA>(eo, reinterpret_cast<const float*>(smem), red_width, red_sstride,
@@ -739,7 +766,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (red_failed && a.splits > 1 && threadIdx.x == 64) {
       // no bulk copy may still be landing in this CTA's shared memory at exit
       const uint64_t t0 = ptx::globaltimer_ns();
-      while (!ptx::mbar_try_wait(red_bar, 0) && ptx::globaltimer_ns() - t0 < kWaitLimitNs) {
+      while (!ptx::mbar_try_wait(red_bar, 0) && ptx::globaltimer_ns() - t0 < a.wait_ns) {
       }
     }
   }
@@ -776,7 +803,19 @@ EncodeTiledFn get_encode_fn() {
 // TMEM accumulators alternate, so the epilogue of one tile (drained 32 token
 // columns at a time through a double-buffered fp32 staging area) overlaps the
 // main loop of the next; the TMA ring runs continuously across tiles.
-template <int KIND>
+//
+// PAIR != 0: the CTAs run in clusters of two that share one operand tile of
+// every stage, brought in once by the first CTA and multicast by TMA into both
+// CTAs' shared memory (halving the L2-to-SM traffic of that operand); each
+// CTA's MMA issuer releases a stage in both CTAs (multicast commit), so a
+// stage is refilled only when both have consumed it.
+//   PAIR == 1: the two feature tiles of a pair with the same token tile (the
+//              token tile, B, is shared);
+//   PAIR == 2: the two token tiles of a pair with the same feature tile (the
+//              weight tiles, A, are shared).
+// With an odd tile count the last pair's second tile lies past N (its weight
+// rows load as zeros) or past the tokens; its outputs are not stored.
+template <int KIND, int PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_persistent_kernel(const __grid_constant__ CUtensorMap tm_w,
                            const __grid_constant__ CUtensorMap tm_w2,
@@ -795,26 +834,41 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t empty0 = full0 + 8u * a.stages;
   const uint32_t accf0 = empty0 + 8u * a.stages;  // accumulator b ready: accf0 + 8b
   const uint32_t acce0 = accf0 + 16u;             // accumulator b drained: acce0 + 8b
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * a.stages + 4);
+  const uint32_t done_bar = acce0 + 16u;          // every MMA completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * a.stages + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // tokens this launch covers (packed: the valid ones) and their tiles
+  // tokens this launch covers (packed: the valid ones) and their tiles.  The
+  // walk: work item w = first, first + step, ... < tiles; feature tile and
+  // token tile of an item from tile_of (PAIR: items are feature-tile pairs)
   const int Meff = a.lens != nullptr ? packed_total(a.lens, a.lens_B, a.lens_S) : a.M;
-  const int tiles = a.feat_tiles * ((Meff + a.nt - 1) / a.nt);
+  const int ttiles = (Meff + a.nt - 1) / a.nt;
+  const int fwalk = PAIR == 1 ? (a.feat_tiles + 1) / 2 : a.feat_tiles;
+  const int twalk = PAIR == 2 ? (ttiles + 1) / 2 : ttiles;
+  const int tiles = fwalk * twalk;
+  const int rank = PAIR ? static_cast<int>(ptx::cluster_ctarank()) : 0;
+  const int first = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int step = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  auto tile_of = [&](int item, int& ft, int& tt) {
+    const int f = item % fwalk, t = item / fwalk;
+    ft = PAIR == 1 ? 2 * f + rank : f;
+    tt = PAIR == 2 ? 2 * t + rank : t;
+  };
   const int KB = a.k_blocks;
   const uint32_t acc_cols = static_cast<uint32_t>(NA * a.nt);  // one accumulator's columns
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.stages; ++i) {
       ptx::mbar_init(full0 + 8u * i, 1);
-      ptx::mbar_init(empty0 + 8u * i, 1);
+      ptx::mbar_init(empty0 + 8u * i, PAIR ? 2 : 1);  // PAIR: both CTAs' MMAs release it
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(accf0 + 8u * b, 1);
       ptx::mbar_init(acce0 + 8u * b, kThreads - 64);
     }
+    ptx::mbar_init(done_bar, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -827,6 +881,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), a.tmem_cols);
     ptx::tmem_relinquish();
   }
+  // PAIR: both CTAs' barriers are initialised before either multicasts into the other
+  if (PAIR) ptx::cluster_sync();
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -838,51 +894,73 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------------- producer
       const uint64_t pol_w = ptx::policy_evict_first();
       const uint64_t pol_x = ptx::policy_evict_last();
+      // each operand tile: loaded by this CTA alone, or (the shared one of a
+      // pair) by the first CTA of the pair into both
+      const bool loads_a = PAIR != 2 || rank == 0;
+      const bool loads_b = PAIR != 1 || rank == 0;
+      auto load = [&](bool mc, uint32_t dst, const CUtensorMap* m, uint32_t fb, int kc, int row,
+                      uint64_t pol) {
+        if (mc)
+          ptx::tma_load_2d_mc(dst, m, fb, kc, row, static_cast<uint16_t>(0x3), pol);
+        else
+          ptx::tma_load_2d(dst, m, fb, kc, row, pol);
+      };
+      auto load_a = [&](uint32_t st, uint32_t fb, int kc, int f) {
+        load(PAIR == 2, st, &tm_w, fb, kc, f * kBM, pol_w);
+        if (NA == 2) load(PAIR == 2, st + kATileBytes, &tm_w2, fb, kc, f * kBM, pol_w);
+      };
+      auto load_b = [&](uint32_t dst, uint32_t fb, int kc, int t) {
+        load(PAIR == 1, dst, &tm_x, fb, kc, t, pol_x);
+      };
       int issued = 0;
-      const int first = blockIdx.x;
+      const bool wh = a.withhold && blockIdx.x == 0;
       if (first < tiles) {
         // weights of the first stages of the first tile before the dependency wait
         const int pre = KB < a.stages ? KB : a.stages;
-        const int f0 = first % a.feat_tiles;
+        int f0, t0;
+        tile_of(first, f0, t0);
         for (int i = 0; i < pre; ++i) {
+          if (wh && i == 0) continue;
           const uint32_t st = sbase + i * stage_bytes;
           ptx::mbar_arrive_expect_tx(full0 + 8u * i, stage_bytes);
-          ptx::tma_load_2d(st, &tm_w, full0 + 8u * i, i * kBK, f0 * kBM, pol_w);
-          if (NA == 2) ptx::tma_load_2d(st + kATileBytes, &tm_w2, full0 + 8u * i, i * kBK, f0 * kBM, pol_w);
+          if (loads_a) load_a(st, full0 + 8u * i, i * kBK, f0);
         }
         ptx::grid_dependency_wait();
         if (blockIdx.x == 0) record_stamp(a.stamp);
-        const int t0 = first / a.feat_tiles;
         for (int i = 0; i < pre; ++i)
-          ptx::tma_load_2d(sbase + i * stage_bytes + NA * kATileBytes, &tm_x, full0 + 8u * i,
-                           i * kBK, t0 * a.nt, pol_x);
+          if (!(wh && i == 0) && loads_b)
+            load_b(sbase + i * stage_bytes + NA * kATileBytes, full0 + 8u * i, i * kBK, t0 * a.nt);
         issued = pre;
         int it = 0;
         bool stop = false;
         RingPos rp(a.stages);
-        for (int tile = first; tile < tiles && !stop; tile += gridDim.x) {
-          const int ft = tile % a.feat_tiles, tt = tile / a.feat_tiles;
+        for (int item = first; item < tiles && !stop; item += step) {
+          int ft, tt;
+          tile_of(item, ft, tt);
           for (int kb = 0; kb < KB; ++kb, ++it, rp.next()) {
             if (it < pre) continue;  // issued above
             const int s = rp.s;
             if (!ptx::mbar_wait(empty0 + 8u * s, rp.ph ^ 1u, abort_flag, a.err, kDevWaitEmpty,
-                                kWaitLimitNs)) {
+                                a.wait_ns)) {
               stop = true;
               break;
             }
             const uint32_t st = sbase + s * stage_bytes;
             const uint32_t fb = full0 + 8u * s;
             ptx::mbar_arrive_expect_tx(fb, stage_bytes);
-            ptx::tma_load_2d(st, &tm_w, fb, kb * kBK, ft * kBM, pol_w);
-            if (NA == 2) ptx::tma_load_2d(st + kATileBytes, &tm_w2, fb, kb * kBK, ft * kBM, pol_w);
-            ptx::tma_load_2d(st + NA * kATileBytes, &tm_x, fb, kb * kBK, tt * a.nt, pol_x);
+            if (loads_a) load_a(st, fb, kb * kBK, ft);
+            if (loads_b) load_b(st + NA * kATileBytes, fb, kb * kBK, tt * a.nt);
             issued = it + 1;
           }
         }
       }
+      // no copy may still be in flight at exit (a flag of our own: an abort
+      // must not cut these waits short)
+      volatile int drain = 0;
       for (int i = (issued > a.stages ? issued - a.stages : 0); i < issued; ++i)
-        ptx::mbar_wait(full0 + 8u * (i % a.stages), static_cast<uint32_t>(i / a.stages) & 1u,
-                       abort_flag, a.err, kDevWaitFull, kWaitLimitNs);
+        if (!(wh && i == 0))
+          ptx::mbar_wait(full0 + 8u * (i % a.stages), static_cast<uint32_t>(i / a.stages) & 1u,
+                         &drain, nullptr, 0, a.wait_ns);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -894,17 +972,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       RingPos rp(a.stages);
       int it = 0, lt = 0;
       bool stop = false;
-      for (int tile = blockIdx.x; tile < tiles && !stop; tile += gridDim.x, ++lt) {
+      for (int item = first; item < tiles && !stop; item += step, ++lt) {
         const int b = lt & 1;
         const int use = lt >> 1;
         if (lt >= 2 && !ptx::mbar_wait(acce0 + 8u * b, static_cast<uint32_t>(use - 1) & 1u,
-                                       abort_flag, a.err, kDevWaitAccum, kWaitLimitNs))
+                                       abort_flag, a.err, kDevWaitAccum, a.wait_ns))
           break;
         ptx::tc_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>(b) * acc_cols;
         for (int kb = 0; kb < KB; ++kb, ++it, rp.next()) {
           const int s = rp.s;
-          if (!ptx::mbar_wait(full0 + 8u * s, rp.ph, abort_flag, a.err, kDevWaitFull, kWaitLimitNs)) {
+          if (!ptx::mbar_wait(full0 + 8u * s, rp.ph, abort_flag, a.err, kDevWaitFull, a.wait_ns)) {
             stop = true;
             break;
           }
@@ -919,48 +997,87 @@ __global__ void __launch_bounds__(kThreads, 1)
               ptx::mma_bf16(d + static_cast<uint32_t>(a.nt), da + (kATileBytes >> 4) + 2 * kk,
                             db + 2 * kk, idesc, acc);
           }
-          ptx::mma_commit(empty0 + 8u * s);
+          // PAIR: the stage is free only once both CTAs have consumed it
+          if (PAIR)
+            ptx::mma_commit_mc(empty0 + 8u * s, static_cast<uint16_t>(0x3));
+          else
+            ptx::mma_commit(empty0 + 8u * s);
         }
         ptx::mma_commit(accf0 + 8u * b);
       }
+      // every product issued has completed before TMEM is released
+      ptx::mma_commit(done_bar);
+      volatile int drain = 0;
+      ptx::mbar_wait(done_bar, 0, &drain, nullptr, 0, a.wait_ns);
     }
   } else {
     // ------------------------------------------------------------- epilogue
+    // Chunks of kChunk token columns: TMEM -> fp32 staging in shared memory
+    // -> 16-byte stores.  What a chunk reads from global memory (the
+    // residual, the RoPE table rows) is requested one chunk ahead, across
+    // tiles too, so that its latency overlaps the previous chunk's stores and
+    // this chunk's TMEM drain instead of adding to every chunk.
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const int tid_e = threadIdx.x - 64;
     const EpiOut eo = epi_out(a);
     ptx::grid_dependency_wait();  // residual written by earlier kernels
+    constexpr int kUnits = kChunk * (kBM / 8) / (kThreads - 64);  // units of 8 features per thread
+    static_assert(kUnits == kEpiBatch, "one batch of units per thread and chunk");
+    uint4 res_cur[kUnits], res_nxt[kUnits];
+    RopeRow rr_cur[kRopeUnits], rr_nxt[kRopeUnits];
+    // RoPE positions by arithmetic: packed tokens from the row starts, else t mod S
+    RowStarts rs;
+    const bool rope_packed = a.rope_pos != nullptr && a.lens != nullptr;
+    if (KIND == kGemmPlain && a.rope_cos != nullptr && rope_packed) rs.init(a.lens, a.lens_B, a.lens_S);
+    // global reads of chunk c0 of work item `item` into (res, rr)
+    auto prefetch = [&](int item, int c0, uint4 (&res)[kUnits], RopeRow (&rr)[kRopeUnits]) {
+      if (item >= tiles) return;
+      int ft, tt;
+      tile_of(item, ft, tt);
+      const int ncols = a.nt - c0 < kChunk ? a.nt - c0 : kChunk;
+      if (KIND == kGemmResidual) {
+#pragma unroll
+        for (int k = 0; k < kUnits; ++k) {
+          const int u = tid_e + (kThreads - 64) * k;
+          const int c = u / (kBM / 8), grp = u % (kBM / 8);
+          const int t = tt * a.nt + c0 + c;
+          const int f = ft * kBM + grp * 8;
+          if (u < ncols * (kBM / 8) && t < Meff && f < a.N)
+            res[k] = *reinterpret_cast<const uint4*>(a.residual + static_cast<size_t>(t) * a.N + f);
+        }
+      }
+      if (KIND == kGemmPlain && a.rope_cos != nullptr && ft * kBM < a.rope_cols) {
+#pragma unroll
+        for (int k = 0; k < kRopeUnits; ++k) {
+          const int u = tid_e + (kThreads - 64) * k;
+          const int c = u / (kBM / 16), pg = u % (kBM / 16);
+          const int t = tt * a.nt + c0 + c;
+          if (u < ncols * (kBM / 16) && t < Meff)
+            rr[k] = rope_row_at(eo, rope_packed ? rs.pos(t) : t % a.rope_S, 8 * (pg & 3));
+        }
+      }
+    };
+    prefetch(first, 0, res_cur, rr_cur);
     int lt = 0, cc = 0;
-    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++lt) {
+    for (int item = first; item < tiles; item += step, ++lt) {
       const int b = lt & 1;
       const int use = lt >> 1;
       ptx::mbar_wait(accf0 + 8u * b, static_cast<uint32_t>(use) & 1u, abort_flag, a.err,
-                     kDevWaitAccum, kWaitLimitNs);
+                     kDevWaitAccum, a.wait_ns);
       // all epilogue threads leave together: whoever gave up raised the flag
       // before this barrier, so everyone reads the same value after it
       ptx::named_barrier_sync(1, kThreads - 64);
       if (*abort_flag) break;
       ptx::tc_fence_after();
-      const int ft = tile % a.feat_tiles, tt = tile / a.feat_tiles;
+      int ft, tt;
+      tile_of(item, ft, tt);
       const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b) * acc_cols;
       const bool rope_tile =
           KIND == kGemmPlain && a.rope_cos != nullptr && ft * kBM < a.rope_cols;
       for (int c0 = 0; c0 < a.nt; c0 += kChunk, ++cc) {
         float* buf = staging + (cc & 1) * (kChunk * kSld);
         const int ncols = a.nt - c0 < kChunk ? a.nt - c0 : kChunk;
-        // RoPE tables of this chunk's units (two per thread), requested before
-        // the drain so that their L2 latency overlaps it
-        RopeRow rr[kRopeUnits];
-        if (rope_tile) {
-#pragma unroll
-          for (int k = 0; k < kRopeUnits; ++k) {
-            const int u = tid_e + (kThreads - 64) * k;
-            const int c = u / (kBM / 16), pg = u % (kBM / 16);
-            const int t = tt * a.nt + c0 + c;
-            if (u < ncols * (kBM / 16) && t < Meff) rr[k] = rope_row(eo, t, 8 * (pg & 3));
-          }
-        }
         for (int j0 = 0; j0 < ncols; j0 += 16) {
           float v[16];
           ptx::tmem_ld16(tq + c0 + j0, v);
@@ -979,6 +1096,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mbar_arrive(acce0 + 8u * b);
         }
         ptx::named_barrier_sync(1, kThreads - 64);
+        // the next chunk's global reads (of this tile, or the next tile's first)
+        if (c0 + kChunk < a.nt)
+          prefetch(item, c0 + kChunk, res_nxt, rr_nxt);
+        else
+          prefetch(item + step, 0, res_nxt, rr_nxt);
         // 16-byte vector stores: 8 features of one token per unit
         if (rope_tile) {
 #pragma unroll
@@ -991,61 +1113,46 @@ __global__ void __launch_bounds__(kThreads, 1)
               float v1[8], v2[8];
               load8_smem(buf + c * kSld + fo, v1);
               load8_smem(buf + c * kSld + fo + 32, v2);
-              rope_apply_store16(eo, t, ft * kBM + fo, rr[k], v1, v2);
+              rope_apply_store16(eo, t, ft * kBM + fo, rr_cur[k], v1, v2);
             }
           }
-          continue;
-        }
-        const int units = ncols * (kBM / 8);
-        for (int u0 = tid_e; u0 < units; u0 += (kThreads - 64) * kEpiBatch) {
-          float v[kEpiBatch][8];
-          uint4 res[kEpiBatch];
-          int tok[kEpiBatch], fea[kEpiBatch];
+        } else {
+          const int units = ncols * (kBM / 8);
 #pragma unroll
-          for (int bb = 0; bb < kEpiBatch; ++bb) {
-            const int u = u0 + (kThreads - 64) * bb;
-            tok[bb] = -1;
-            if (u < units) {
-              const int c = u / (kBM / 8), grp = u % (kBM / 8);
-              const float4* p4 = reinterpret_cast<const float4*>(buf + c * kSld + grp * 8);
-              const float4 lo = p4[0], hi = p4[1];
-              v[bb][0] = lo.x; v[bb][1] = lo.y; v[bb][2] = lo.z; v[bb][3] = lo.w;
-              v[bb][4] = hi.x; v[bb][5] = hi.y; v[bb][6] = hi.z; v[bb][7] = hi.w;
-              const int t = tt * a.nt + c0 + c;
-              const int f = ft * kBM + grp * 8;
-              if (t < Meff && f < a.N) {
-                tok[bb] = t;
-                fea[bb] = f;
-                if (KIND == kGemmResidual)
-                  res[bb] = *reinterpret_cast<const uint4*>(a.residual + static_cast<size_t>(t) * a.N + f);
-              }
-            }
-          }
-#pragma unroll
-          for (int bb = 0; bb < kEpiBatch; ++bb) {
-            if (tok[bb] < 0) continue;
+          for (int k = 0; k < kUnits; ++k) {
+            const int u = tid_e + (kThreads - 64) * k;
+            if (u >= units) continue;
+            const int c = u / (kBM / 8), grp = u % (kBM / 8);
+            const int t = tt * a.nt + c0 + c;
+            const int f = ft * kBM + grp * 8;
+            if (t >= Meff || f >= a.N) continue;
             float o[8];
+            load8_smem(buf + c * kSld + grp * 8, o);
             if (KIND == kGemmResidual) {
-              const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&res[bb]);
+              const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&res_cur[k]);
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
                 const float2 rf = __bfloat1622float2(r2[i]);
-                o[2 * i] = rf.x + v[bb][2 * i];
-                o[2 * i + 1] = rf.y + v[bb][2 * i + 1];
+                o[2 * i] = rf.x + o[2 * i];
+                o[2 * i + 1] = rf.y + o[2 * i + 1];
               }
-            } else {
-#pragma unroll
-              for (int i = 0; i < 8; ++i) o[i] = v[bb][i];
             }
-            store8<KIND>(eo, tok[bb], fea[bb], o);
+            store8<KIND>(eo, t, f, o);
           }
         }
+#pragma unroll
+        for (int k = 0; k < kUnits; ++k) res_cur[k] = res_nxt[k];
+#pragma unroll
+        for (int k = 0; k < kRopeUnits; ++k) rr_cur[k] = rr_nxt[k];
       }
     }
   }
 
   ptx::tc_fence_before();
   __syncthreads();
+  // PAIR: neither CTA leaves while the other may still multicast into it or
+  // arrive on its barriers
+  if (PAIR) ptx::cluster_sync();
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, a.tmem_cols);
@@ -1102,6 +1209,8 @@ cudaError_t launch_kind(const GemmPlan& p, const GemmOperands& o, Launch l) {
   a.ln_gamma = o.ln_gamma;
   a.ln_eps = o.ln_eps;
   a.stamp = l.stamp;
+  a.wait_ns = o.wait_ns;
+  a.withhold = o.withhold ? 1 : 0;
 
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads);
@@ -1111,6 +1220,13 @@ cudaError_t launch_kind(const GemmPlan& p, const GemmOperands& o, Launch l) {
   int n = 0;
   if (p.persistent) {
     cfg.gridDim = dim3(p.grid_ctas, 1, 1);
+    if (p.pair) {
+      attr[n].id = cudaLaunchAttributeClusterDimension;
+      attr[n].val.clusterDim.x = 2;
+      attr[n].val.clusterDim.y = 1;
+      attr[n].val.clusterDim.z = 1;
+      ++n;
+    }
   } else {
     cfg.gridDim = dim3(p.feat_tiles, p.token_tiles, p.splits);
     attr[n].id = cudaLaunchAttributeClusterDimension;
@@ -1126,8 +1242,12 @@ cudaError_t launch_kind(const GemmPlan& p, const GemmOperands& o, Launch l) {
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
+  if (p.persistent && p.pair == 1)
+    return cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<KIND, 1>, o.w, o.w2, o.x, a);
+  if (p.persistent && p.pair == 2)
+    return cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<KIND, 2>, o.w, o.w2, o.x, a);
   if (p.persistent)
-    return cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<KIND>, o.w, o.w2, o.x, a);
+    return cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<KIND, 0>, o.w, o.w2, o.x, a);
   return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<KIND>, o.w, o.w2, o.x, a);
 }
 
@@ -1143,20 +1263,39 @@ const void* kernel_ptr(int kind) {
   }
 }
 
+const void* persistent_ptr(int kind, int pair) {
+  switch (kind) {
+    case kGemmPlain:
+      return pair == 1   ? reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmPlain, 1>)
+             : pair == 2 ? reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmPlain, 2>)
+                         : reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmPlain, 0>);
+    case kGemmResidual:
+      return pair == 1   ? reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmResidual, 1>)
+             : pair == 2 ? reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmResidual, 2>)
+                         : reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmResidual, 0>);
+    default:
+      return pair == 1   ? reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmGeglu, 1>)
+             : pair == 2 ? reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmGeglu, 2>)
+                         : reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmGeglu, 0>);
+  }
+}
+
+// Clusters of two persistent CTAs with this shared memory that can be
+// resident at once; -1 when there is no device to ask.
+int max_active_pairs(int kind, size_t smem);
+
 // Opt every kernel variant into the full dynamic shared memory once.
 cudaError_t configure_kernels() {
   static cudaError_t status = cudaErrorNotReady;
   static std::once_flag once;
   std::call_once(once, [] {
     status = cudaSuccess;
-    const void* persistent[3] = {reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmPlain>),
-                                 reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmResidual>),
-                                 reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmGeglu>)};
     for (int k = kGemmPlain; k <= kGemmGeglu && status == cudaSuccess; ++k) {
       status = cudaFuncSetAttribute(kernel_ptr(k), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(kSmemLimit));
-      if (status == cudaSuccess)
-        status = cudaFuncSetAttribute(persistent[k], cudaFuncAttributeMaxDynamicSharedMemorySize,
+      for (int pair = 0; pair < 3 && status == cudaSuccess; ++pair)
+        status = cudaFuncSetAttribute(persistent_ptr(k, pair),
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(kSmemLimit));
     }
   });
@@ -1191,6 +1330,37 @@ int max_active_clusters(int kind, size_t smem, int splits) {
     if (cudaOccupancyMaxActiveClusters(&n, kernel_ptr(kind), &cfg) != cudaSuccess) n = -1;
   }
   cudaGetLastError();  // a failed query must not leave a sticky-looking error behind
+  std::lock_guard<std::mutex> g(mu);
+  cache[key] = n;
+  return n;
+}
+
+int max_active_pairs(int kind, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, size_t>, int> cache;
+  const auto key = std::make_tuple(kind, smem);
+  {
+    std::lock_guard<std::mutex> g(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  int n = -1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && configure_kernels() == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, persistent_ptr(kind, 1), &cfg) != cudaSuccess) n = -1;
+  }
+  cudaGetLastError();
   std::lock_guard<std::mutex> g(mu);
   cache[key] = n;
   return n;
@@ -1255,7 +1425,7 @@ bool finish_plan(GemmPlan* r) {
 }  // namespace
 
 bool plan_gemm(int M, int N, int K, int kind, int num_sms, int force_splits, int force_nt,
-               GemmPlan* p, bool allow_persistent) {
+               GemmPlan* p, bool allow_persistent, double split_cost) {
   if (M <= 0 || N <= 0 || K <= 0 || K % kBK != 0 || N % 8 != 0) return false;
   if (kind < kGemmPlain || kind > kGemmGeglu) return false;
   if (force_nt > 0 && (force_nt % 16 != 0 || force_nt > 256)) return false;
@@ -1268,7 +1438,8 @@ bool plan_gemm(int M, int N, int K, int kind, int num_sms, int force_splits, int
   // run one CTA per (tile, split) in clusters.  Cost in units of one 16 KB
   // weight tile streamed by one CTA:
   //   persistent: ceil(tiles / CTAs) x (K blocks x unit + 0.3) + 2
-  //   split:      waves x (K blocks per split x unit + 2 + partial round trip),
+  //   split:      waves x (K blocks per split x unit + split_cost + partial
+  //               round trip),
   // a wave being as many clusters as the device can hold at once.
   GemmPlan best;
   double best_cost = 0.0;
@@ -1308,7 +1479,7 @@ bool plan_gemm(int M, int N, int K, int kind, int num_sms, int force_splits, int
         // + the partial tile written to and read back from L2 (about half the
         //   cost of streaming the same bytes from HBM)
         const double partial = 0.5 * na * c.nt * kBM * 4.0 / kATileBytes;
-        cost = waves * (kb_per * unit + 2.0 + partial);
+        cost = waves * (kb_per * unit + split_cost + partial);
       }
       if (!found || cost < best_cost - 1e-9) {
         best = c;
@@ -1320,6 +1491,45 @@ bool plan_gemm(int M, int N, int K, int kind, int num_sms, int force_splits, int
   if (!found) return false;
   *p = best;
   return true;
+}
+
+bool make_pair_plan(GemmPlan* p, int mode) {
+  if (!p->persistent || p->pair != 0 || (mode != 1 && mode != 2)) return false;
+  const int pairs_max = max_active_pairs(p->kind, p->smem_bytes);
+  if (pairs_max <= 0) return false;
+  const int items = mode == 1 ? ((p->feat_tiles + 1) / 2) * p->token_tiles
+                              : p->feat_tiles * ((p->token_tiles + 1) / 2);
+  p->pair = mode;
+  p->grid_ctas = 2 * (items < pairs_max ? items : pairs_max);
+  return true;
+}
+
+int plan_candidates(int M, int N, int K, int kind, int num_sms, GemmPlan* out, int max_out) {
+  // the model's choice under a range of split-K overhead weights, and the
+  // best plan without split-K: distinct plans only
+  const double costs[] = {2.0, 8.0, 16.0, 32.0};
+  int n = 0;
+  auto add = [&](const GemmPlan& c) {
+    for (int i = 0; i < n; ++i)
+      if (out[i].nt == c.nt && out[i].splits == c.splits && out[i].persistent == c.persistent)
+        return;
+    if (n < max_out) out[n++] = c;
+  };
+  for (double sc : costs) {
+    GemmPlan c;
+    if (plan_gemm(M, N, K, kind, num_sms, 0, 0, &c, true, sc)) add(c);
+  }
+  GemmPlan c;
+  if (plan_gemm(M, N, K, kind, num_sms, 1, 0, &c, true)) add(c);
+  // the persistent candidates again in clusters of two with the token tile
+  // multicast (worth it when each CTA walks several tiles' operand traffic)
+  const int base = n;
+  for (int mode = 1; mode <= 2; ++mode)
+    for (int i = 0; i < base && n < max_out; ++i) {
+      GemmPlan pp = out[i];
+      if (pp.persistent && make_pair_plan(&pp, mode)) out[n++] = pp;
+    }
+  return n;
 }
 
 bool make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
@@ -1368,8 +1578,9 @@ cudaError_t gemm_node_retarget(cudaGraphExec_t exec, cudaGraphNode_t node, const
   cudaError_t e = cudaGraphKernelNodeGetParams(node, &p);
   if (e != cudaSuccess) return e;
   const void* split = reinterpret_cast<const void*>(&gemm_tc_kernel<kGemmResidual>);
-  const void* pers = reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmResidual>);
-  if ((p.func != split && p.func != pers) || p.kernelParams == nullptr)
+  if ((p.func != split && p.func != persistent_ptr(kGemmResidual, 0) &&
+       p.func != persistent_ptr(kGemmResidual, 1) && p.func != persistent_ptr(kGemmResidual, 2)) ||
+      p.kernelParams == nullptr)
     return cudaErrorInvalidValue;
   // arguments: weight map, gate map, activation map, GemmArgs
   GemmArgs a = *static_cast<const GemmArgs*>(p.kernelParams[3]);

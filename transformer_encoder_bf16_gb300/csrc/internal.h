@@ -109,6 +109,8 @@ struct GemmPlan {
   int splits = 1;        // split-K factor = cluster size along z
   int stages = 0;        // pipeline depth
   bool persistent = false;  // one CTA per SM walks the tiles (splits == 1)
+  int pair = 0;  // persistent CTAs in clusters of two sharing an operand tile by TMA multicast:
+                 // 1 the token tile (feature-tile pairs), 2 the weight tiles (token-tile pairs)
   int grid_ctas = 0;     // persistent: CTAs launched
   size_t workspace_bytes = 0;  // split-K partial tiles (0 when splits == 1)
   int k_blocks = 0;      // K / 64
@@ -120,7 +122,17 @@ struct GemmPlan {
 // Chooses tile and split for an M x N x K projection; force_* > 0 override.
 // Returns false if the shape is unsupported.
 bool plan_gemm(int M, int N, int K, int kind, int num_sms, int force_splits, int force_nt,
-               GemmPlan* p, bool allow_persistent = true);
+               GemmPlan* p, bool allow_persistent = true, double split_cost = 2.0);
+
+// A persistent plan run as clusters of two CTAs sharing an operand tile
+// (mode 1: the token tile; mode 2: the weight tiles); false if the device
+// cannot hold such clusters.
+bool make_pair_plan(GemmPlan* p, int mode);
+
+// Distinct plans worth timing for one projection shape (at most max_out):
+// the planner's choice under several weights of the split-K overhead, and the
+// best plan without split-K.  Returns how many were written.
+int plan_candidates(int M, int N, int K, int kind, int num_sms, GemmPlan* out, int max_out);
 
 // Tensor-map encoder (driver entry point resolved through the runtime).
 bool make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
@@ -152,6 +164,8 @@ struct GemmOperands {
   const int32_t* lens = nullptr;
   int lens_B = 0, lens_S = 0;
   const int32_t* rope_pos = nullptr;  // packed tokens: RoPE position of each token
+  uint64_t wait_ns = kWaitLimitNs;    // bound of every barrier wait
+  bool withhold = false;  // failure-path test: the first CTA never issues its first stage
 };
 
 cudaError_t launch_gemm(const GemmPlan& p, const GemmOperands& o, Launch l);

@@ -48,9 +48,10 @@ int laya_op_rope_table(double theta, int max_seq, int half, int bf16_round, floa
 
 int laya_op_rope(void* qkv, const float* cos_dev, const float* sin_dev, int B, int S, int heads,
                  int head_dim, void* stream) {
-  if (!al16(qkv) || !cos_dev || !sin_dev || B < 1 || S < 1 || heads < 1 || head_dim != 64)
+  if (!al16(qkv) || !al16(cos_dev) || !al16(sin_dev) || B < 1 || S < 1 || heads < 1 ||
+      heads > 32 || head_dim != 64)
     return LAYA_E_INVAL;
-  if (static_cast<long long>(B) * S > 65535) return LAYA_E_INVAL;
+  if (static_cast<long long>(B) * S > 0x7fffffffLL) return LAYA_E_INVAL;
   laya::Launch l{static_cast<cudaStream_t>(stream), false};
   return rc_of(laya::launch_rope(static_cast<bf16*>(qkv), cos_dev, sin_dev, B, S, heads, l));
 }
@@ -129,11 +130,20 @@ int laya_op_linear_workspace_size(int M, int K, int N, int kind, int splits, int
 int laya_op_linear(const void* x, int M, int K, const void* w, int N, int kind,
                    const void* residual, void* y, void* workspace, size_t workspace_bytes,
                    int splits, int tile_tokens, void* stream) {
+  return laya_op_linear_ex(x, M, K, w, N, kind, residual, y, workspace, workspace_bytes, splits,
+                           tile_tokens, 0, stream);
+}
+
+int laya_op_linear_ex(const void* x, int M, int K, const void* w, int N, int kind,
+                      const void* residual, void* y, void* workspace, size_t workspace_bytes,
+                      int splits, int tile_tokens, int paired, void* stream) {
   if (!al16(x) || !al16(w) || !al16(y)) return LAYA_E_INVAL;
   if (kind == laya::kGemmResidual && !al16(residual)) return LAYA_E_INVAL;
+  if (paired < 0 || paired > 2 || (paired && splits != 1)) return LAYA_E_INVAL;
   laya::GemmPlan p;
   if (!laya::plan_gemm(M, N, K, kind, laya::device_sm_count(), splits, tile_tokens, &p))
     return LAYA_E_INVAL;
+  if (paired && !laya::make_pair_plan(&p, paired)) return LAYA_E_UNSUPPORTED;
   laya::GemmOperands o;
   const uint64_t ldk = static_cast<uint64_t>(K) * 2;
   bool ok = laya::make_tmap_bf16_2d(&o.w, w, N, K, ldk, 128) &&

@@ -34,4 +34,26 @@ __device__ __forceinline__ int packed_total(const int32_t* lens, int B, int S) {
   return packed_start(lens, B, S);
 }
 
+// The first packed row of every batch row, held in registers, so that a
+// token's position in its row is found by compares alone (no dependent load
+// on the way to the RoPE table rows it selects).  B <= 16.
+struct RowStarts {
+  int cu[16];
+  __device__ __forceinline__ void init(const int32_t* lens, int B, int S) {
+    int c = 0;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      cu[k] = k < B ? c : 0x7fffffff;
+      if (k < B) c += packed_len(lens, k, S);
+    }
+  }
+  // index of packed token t in its row
+  __device__ __forceinline__ int pos(int t) const {
+    int base = 0;
+#pragma unroll
+    for (int k = 1; k < 16; ++k) base = cu[k] <= t ? cu[k] : base;
+    return t - base;
+  }
+};
+
 }  // namespace laya
