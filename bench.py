@@ -394,6 +394,7 @@ def measure(te, torch, enc, model, ids, lengths, steps, warmup, stream, world, c
     enc.check(stream)
     prof_step_ms = float(np.median([s.elapsed_time(e) for s, e in zip(pstarts, pends)]))
     return {"valid": valid, "B": B, "S": S, "total_ms": total_ms, "step_ms": step_ms,
+            "plans": enc.plans(B, S),
             "e2e_total_s": e2e_total, "e2e_times": e2e_times, "prof": prof,
             "prof_step_ms": prof_step_ms, "first_shape": first_shape, "clocks": clk,
             "launches": enc.launch_count(B, S)}
@@ -450,6 +451,61 @@ def analyse(model, r, steps, world, peaks):
             "M": M}
 
 
+def run_op(args):
+    """One step kernel alone at the workload's sizes (synthetic operands), for
+    per-kernel timing and ncu captures: prints one JSON line with the CUDA-
+    event time per launch and the achieved GB/s on the kernel's algorithmic
+    bytes."""
+    import torch
+    import transformer_encoder_bf16_gb300 as te
+    from transformer_encoder_bf16_gb300 import build as tebuild
+    tebuild.build()
+    torch.cuda.set_device(0)
+    model, B, S, seed, lr = synth.WORKLOADS[args.workload]
+    _, lengths = synth.make_inputs(model, B, S, seed, lr)
+    H, heads = model["hidden"], model["heads"]
+    rng = np.random.default_rng(seed)
+
+    def dev_bits(shape, std=1.0, mean=0.0):
+        x = synth.f32_to_bf16_bits(rng.standard_normal(shape).astype(np.float32) * std + mean)
+        return torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+
+    valid = int(np.sum(lengths))
+    M = valid if B > 1 else B * S   # the forward packs the tokens of several rows
+    if args.op == "layernorm":
+        x, g = dev_bits((M, H)), dev_bits((H,), 0.02, 1.0)
+        y = torch.empty_like(x)
+        fn = lambda: te.layernorm(x, g, model["ln_eps"], y)
+        nbytes = algorithmic(model, "norm", M)[0]
+    elif args.op == "rope":
+        qkv = dev_bits((B * S, 3 * H))
+        c, sn = te.rope_table(model["theta_global"], model["max_seq"], 32)
+        cd, sd = torch.from_numpy(c).cuda(), torch.from_numpy(sn).cuda()
+        fn = lambda: te.rope(qkv, cd, sd, B, S, heads)
+        nbytes = algorithmic(model, "rope", B * S)[0]
+    else:
+        qkv = dev_bits((B * S, 3 * H), 0.7)
+        ld = torch.from_numpy(lengths).cuda()
+        ctx = torch.empty((B * S, H), dtype=torch.bfloat16, device="cuda")
+        glob = args.op == "attention"
+        fn = lambda: te.attention_tc(qkv, ld, B, S, heads, glob, model["local_half_window"], ctx)
+        nbytes = algorithmic(model, "attention", B * S)[0]
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    st = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    en = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        st[i].record()
+        fn()
+        en[i].record()
+    torch.cuda.synchronize()
+    us = float(np.median([a.elapsed_time(b) for a, b in zip(st, en)])) * 1000
+    print(json.dumps({"op": args.op, "workload": args.workload, "us_per_launch": us,
+                      "algorithmic_bytes": nbytes, "GB_s": nbytes / us / 1e3,
+                      "frac_of_hbm": nbytes / us / 1e3 / peak_value(load_peaks()[0], "hbm_gbs")}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -462,8 +518,13 @@ def main():
                     help="time the headline workload only")
     ap.add_argument("--per-config-steps", type=int, default=50)
     ap.add_argument("--reference-budget", type=float, default=150.0)
+    ap.add_argument("--op", choices=["layernorm", "rope", "attention", "attention_local"],
+                    help="time one step kernel alone at the workload's sizes instead")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.op:
+        run_op(args)
+        return
 
     rank, local_rank, world = dist_env()
     model, B, S, seed, lr = synth.WORKLOADS[args.workload]
@@ -539,6 +600,7 @@ def main():
                     "e2e_p50_ms", "launches_per_forward", "forward_roofline", "gemm_tflops_valid",
                     "class_sum_over_p50")},
                 "kernel_ms_per_step": {k: v["ms_per_step"] for k, v in a2["kernel_classes"].items()},
+                "gemm_plans": {k: list(v) for k, v in r2["plans"].items()},
                 "h800_rust_cuda_event_p50_ms": pub}
             torch.cuda.empty_cache()
 
@@ -576,6 +638,8 @@ def main():
             "gpu_launches": a["launches_per_forward"] * args.steps,
             "roofline": roof,
             "gemm_tflops_valid": a["gemm_tflops_valid"],
+            "gemm_plans": {k: {"tokens_per_tile": v[0], "splits": v[1], "pairing": v[2], "ctas": v[3]}
+                           for k, v in r["plans"].items()},
             "forward_roofline": a["forward_roofline"],
             "kernel_classes": a["kernel_classes"],
             "class_sum_over_p50": a["class_sum_over_p50"],

@@ -289,3 +289,43 @@ def test_failure_poisons_the_handle_and_enqueues_nothing():
     fresh.run(ids, lengths, out)
     fresh.check()
     fresh.close()
+
+
+def test_device_wait_runs_out_returns_device_error_and_fresh_handle_works():
+    # "Laya native CUDA worker", "Start and check": a native failure stops the
+    # executor.  The first projection's first CTA withholds one pipeline
+    # stage, so its MMA issuer's bounded wait runs out (limit 50 ms): the
+    # kernels return, laya_enc_check reports LAYA_E_DEVICE and poisons the
+    # handle; a fresh handle on the same device then runs and matches the
+    # oracle.  No trap, fault or invalid access is involved.
+    torch = require_gpu()
+    model, B, S, seed, lr = synth.WORKLOADS["reduced_1x48"]
+    w = synth.make_weights(model, seed)
+    ids, lengths = synth.make_inputs(model, B, S, seed, lr)
+    dev = te.upload_weights(w)
+    enc = te.Encoder(model, dev)
+    out = torch.empty((B, S, model["hidden"]), dtype=torch.bfloat16, device="cuda")
+    try:
+        enc.debug_set_wait_limit_ns(50_000_000)
+        enc.debug_withhold_next_run()
+        t0 = time.time()
+        enc.run(ids, lengths, out)
+        with pytest.raises(te.LayaError) as ex:
+            enc.check()
+        assert ex.value.code == te.E_DEVICE, ex.value
+        assert time.time() - t0 < 30.0
+        with pytest.raises(te.LayaError) as ex:
+            enc.run(ids, lengths, out)
+        assert ex.value.code == te.E_POISONED
+    finally:
+        enc.close()
+    fresh = te.Encoder(model, dev)
+    try:
+        got = run_gpu(fresh, ids, lengths)
+        e, _ = report("reduced 1x48 after a device error on another handle", got,
+                      oracle.forward(model, w, ids, lengths), lengths)
+        assert e <= NRMS_LIMIT
+        with pytest.raises(te.LayaError):
+            fresh.debug_set_wait_limit_ns(10)        # below 1 ms
+    finally:
+        fresh.close()
