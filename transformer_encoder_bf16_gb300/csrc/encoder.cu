@@ -76,7 +76,7 @@ struct Workspace {
   GemmPlan p_qkv, p_o, p_up, p_dn;
   // plan tuning (tune_plans): candidate plans of each projection, timed on
   // the first run of the shape; p_* above are the chosen ones
-  static constexpr int kMaxCand = 12;
+  static constexpr int kMaxCand = 20;
   GemmPlan cand[7][kMaxCand];
   int ncand[7] = {};
   bool tuned = false;

@@ -29,9 +29,11 @@
 // partials in shared memory and reading them through DSMEM, and pushing the
 // slices into the reducers' shared memory with DSMEM bulk copies.)
 //
-// Roles (192 threads): warp 0 lane 0 issues TMA, warp 1 owns TMEM and its lane
-// 0 issues the MMAs, warps 2-5 drain TMEM (warp w reads TMEM lanes
-// 32 * (w % 4) .. + 31).  Every wait is bounded (see ptx::mbar_wait).
+// Roles: warp 0 lane 0 issues TMA, warp 1 owns TMEM and its lane 0 issues the
+// MMAs, the other warps drain TMEM (warp w reads TMEM lanes 32 * (w % 4) ..
+// + 31): warps 2-5 of the 192-thread split kernel, warps 2-9 of the 320-thread
+// persistent kernel (two warps per lane quarter, each taking half of a
+// chunk's token columns).  Every wait is bounded (see ptx::mbar_wait).
 //
 // With programmatic dependent launch the producer loads the first pipeline
 // stages of WEIGHTS before waiting for the previous kernel, so weight streaming
@@ -61,8 +63,14 @@ constexpr size_t kCtrlBytes = 256;
 constexpr size_t kLnStatsBytes = 256 * 8;  // [nt <= 256][mean, rstd] for LayerNorm on load
 constexpr int kEpiBatch = 4;             // epilogue units whose loads are issued together
 constexpr int kChunk = 32;               // persistent epilogue: token columns per drain step
-// RoPE units (token, 8 pairs) of a chunk per epilogue thread: kChunk * 8 / 128
-constexpr int kRopeUnits = kChunk * 8 / 128;
+constexpr int kPThreads = 320;           // persistent kernel: 2 issuing warps + 8 epilogue warps
+constexpr int kPEpi = kPThreads - 64;    // its epilogue threads
+// per epilogue thread and chunk: units of (token, 8 features) and RoPE units
+// of (token, 8 pairs)
+constexpr int kPUnits = kChunk * (kBM / 8) / kPEpi;
+constexpr int kRopeUnits = kChunk * (kBM / 16) / kPEpi;
+static_assert(kPUnits * kPEpi == kChunk * (kBM / 8) && kRopeUnits * kPEpi == kChunk * (kBM / 16),
+              "a chunk divides evenly among the epilogue threads");
 // fp32 staging tiles are token-major with a padded row of kSld floats: the
 // padding spreads the rows of consecutive tokens over different banks for
 // the 16-byte reads of the vector phase (and the DSMEM reads of split-K).
@@ -816,7 +824,7 @@ EncodeTiledFn get_encode_fn() {
 // With an odd tile count the last pair's second tile lies past N (its weight
 // rows load as zeros) or past the tokens; its outputs are not stored.
 template <int KIND, int PAIR>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kPThreads, 1)
     gemm_persistent_kernel(const __grid_constant__ CUtensorMap tm_w,
                            const __grid_constant__ CUtensorMap tm_w2,
                            const __grid_constant__ CUtensorMap tm_x, const GemmArgs a) {
@@ -866,7 +874,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(accf0 + 8u * b, 1);
-      ptx::mbar_init(acce0 + 8u * b, kThreads - 64);
+      ptx::mbar_init(acce0 + 8u * b, kPEpi);
     }
     ptx::mbar_init(done_bar, 1);
     *abort_flag = 0;
@@ -1013,33 +1021,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------- epilogue
     // Chunks of kChunk token columns: TMEM -> fp32 staging in shared memory
-    // -> 16-byte stores.  What a chunk reads from global memory (the
-    // residual, the RoPE table rows) is requested one chunk ahead, across
-    // tiles too, so that its latency overlaps the previous chunk's stores and
-    // this chunk's TMEM drain instead of adding to every chunk.
+    // -> 16-byte stores.  The two warps of a TMEM lane quarter drain 16
+    // columns each.  What a chunk reads from global memory (the residual, the
+    // RoPE table rows) is requested when the chunk before it starts, across
+    // tiles too, so that its latency overlaps that whole chunk.
     const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row = q * 32 + lane;
     const int tid_e = threadIdx.x - 64;
     const EpiOut eo = epi_out(a);
     ptx::grid_dependency_wait();  // residual written by earlier kernels
-    constexpr int kUnits = kChunk * (kBM / 8) / (kThreads - 64);  // units of 8 features per thread
-    static_assert(kUnits == kEpiBatch, "one batch of units per thread and chunk");
-    uint4 res_cur[kUnits], res_nxt[kUnits];
+    uint4 res_cur[kPUnits], res_nxt[kPUnits];
     RopeRow rr_cur[kRopeUnits], rr_nxt[kRopeUnits];
     // RoPE positions by arithmetic: packed tokens from the row starts, else t mod S
     RowStarts rs;
     const bool rope_packed = a.rope_pos != nullptr && a.lens != nullptr;
     if (KIND == kGemmPlain && a.rope_cos != nullptr && rope_packed) rs.init(a.lens, a.lens_B, a.lens_S);
     // global reads of chunk c0 of work item `item` into (res, rr)
-    auto prefetch = [&](int item, int c0, uint4 (&res)[kUnits], RopeRow (&rr)[kRopeUnits]) {
+    auto prefetch = [&](int item, int c0, uint4 (&res)[kPUnits], RopeRow (&rr)[kRopeUnits]) {
       if (item >= tiles) return;
       int ft, tt;
       tile_of(item, ft, tt);
       const int ncols = a.nt - c0 < kChunk ? a.nt - c0 : kChunk;
       if (KIND == kGemmResidual) {
 #pragma unroll
-        for (int k = 0; k < kUnits; ++k) {
-          const int u = tid_e + (kThreads - 64) * k;
+        for (int k = 0; k < kPUnits; ++k) {
+          const int u = tid_e + kPEpi * k;
           const int c = u / (kBM / 8), grp = u % (kBM / 8);
           const int t = tt * a.nt + c0 + c;
           const int f = ft * kBM + grp * 8;
@@ -1050,7 +1057,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (KIND == kGemmPlain && a.rope_cos != nullptr && ft * kBM < a.rope_cols) {
 #pragma unroll
         for (int k = 0; k < kRopeUnits; ++k) {
-          const int u = tid_e + (kThreads - 64) * k;
+          const int u = tid_e + kPEpi * k;
           const int c = u / (kBM / 16), pg = u % (kBM / 16);
           const int t = tt * a.nt + c0 + c;
           if (u < ncols * (kBM / 16) && t < Meff)
@@ -1067,7 +1074,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      kDevWaitAccum, a.wait_ns);
       // all epilogue threads leave together: whoever gave up raised the flag
       // before this barrier, so everyone reads the same value after it
-      ptx::named_barrier_sync(1, kThreads - 64);
+      ptx::named_barrier_sync(1, kPEpi);
       if (*abort_flag) break;
       ptx::tc_fence_after();
       int ft, tt;
@@ -1078,14 +1085,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c0 = 0; c0 < a.nt; c0 += kChunk, ++cc) {
         float* buf = staging + (cc & 1) * (kChunk * kSld);
         const int ncols = a.nt - c0 < kChunk ? a.nt - c0 : kChunk;
-        for (int j0 = 0; j0 < ncols; j0 += 16) {
+        // the next chunk's global reads (of this tile, or the next tile's first)
+        if (c0 + kChunk < a.nt)
+          prefetch(item, c0 + kChunk, res_nxt, rr_nxt);
+        else
+          prefetch(item + step, 0, res_nxt, rr_nxt);
+        const int j0 = 16 * half;  // ncols is a multiple of 16
+        if (j0 < ncols) {
           float v[16];
-          ptx::tmem_ld16(tq + c0 + j0, v);
           if (NA == 2) {
             float g[16];
-            ptx::tmem_ld16(tq + a.nt + c0 + j0, g);
+            ptx::tmem_ld16x2(tq + c0 + j0, tq + a.nt + c0 + j0, v, g);
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = gelu_erf(v[j]) * g[j];
+          } else {
+            ptx::tmem_ld16(tq + c0 + j0, v);
           }
 #pragma unroll
           for (int j = 0; j < 16; ++j) buf[(j0 + j) * kSld + row] = v[j];
@@ -1095,17 +1109,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tc_fence_before();
           ptx::mbar_arrive(acce0 + 8u * b);
         }
-        ptx::named_barrier_sync(1, kThreads - 64);
-        // the next chunk's global reads (of this tile, or the next tile's first)
-        if (c0 + kChunk < a.nt)
-          prefetch(item, c0 + kChunk, res_nxt, rr_nxt);
-        else
-          prefetch(item + step, 0, res_nxt, rr_nxt);
+        ptx::named_barrier_sync(1, kPEpi);
         // 16-byte vector stores: 8 features of one token per unit
         if (rope_tile) {
 #pragma unroll
           for (int k = 0; k < kRopeUnits; ++k) {
-            const int u = tid_e + (kThreads - 64) * k;
+            const int u = tid_e + kPEpi * k;
             const int c = u / (kBM / 16), pg = u % (kBM / 16);
             const int fo = 64 * (pg >> 2) + 8 * (pg & 3);
             const int t = tt * a.nt + c0 + c;
@@ -1119,8 +1128,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           const int units = ncols * (kBM / 8);
 #pragma unroll
-          for (int k = 0; k < kUnits; ++k) {
-            const int u = tid_e + (kThreads - 64) * k;
+          for (int k = 0; k < kPUnits; ++k) {
+            const int u = tid_e + kPEpi * k;
             if (u >= units) continue;
             const int c = u / (kBM / 8), grp = u % (kBM / 8);
             const int t = tt * a.nt + c0 + c;
@@ -1141,7 +1150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
 #pragma unroll
-        for (int k = 0; k < kUnits; ++k) res_cur[k] = res_nxt[k];
+        for (int k = 0; k < kPUnits; ++k) res_cur[k] = res_nxt[k];
 #pragma unroll
         for (int k = 0; k < kRopeUnits; ++k) rr_cur[k] = rr_nxt[k];
       }
@@ -1213,7 +1222,7 @@ cudaError_t launch_kind(const GemmPlan& p, const GemmOperands& o, Launch l) {
   a.withhold = o.withhold ? 1 : 0;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(p.persistent ? kPThreads : kThreads);
   cfg.dynamicSmemBytes = p.smem_bytes;
   cfg.stream = l.stream;
   cudaLaunchAttribute attr[2];
@@ -1349,7 +1358,7 @@ int max_active_pairs(int kind, size_t smem) {
   if (cudaGetDevice(&dev) == cudaSuccess && configure_kernels() == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kPThreads);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1521,6 +1530,22 @@ int plan_candidates(int M, int N, int K, int kind, int num_sms, GemmPlan* out, i
   }
   GemmPlan c;
   if (plan_gemm(M, N, K, kind, num_sms, 1, 0, &c, true)) add(c);
+  // persistent plans with more, smaller tiles per CTA: the largest token tile
+  // that gives each CTA k tiles, k = 2..4 (the last tile's epilogue is the
+  // part no main loop hides, and it shrinks with the tile)
+  const int sms = num_sms > 0 ? num_sms : 148;
+  const int ftiles = (N + kBM - 1) / kBM;
+  for (int k = 2; k <= 4; ++k) {
+    int pick = 0;
+    for (int nt = 16; nt <= 256; nt += 16) {
+      const int tiles = ((M + nt - 1) / nt) * ftiles;
+      if ((tiles + sms - 1) / sms <= k) {
+        pick = nt;
+        break;
+      }
+    }
+    if (pick > 0 && plan_gemm(M, N, K, kind, num_sms, 1, pick, &c, true)) add(c);
+  }
   // the persistent candidates again in clusters of two with the token tile
   // multicast (worth it when each CTA walks several tiles' operand traffic)
   const int base = n;
