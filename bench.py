@@ -638,7 +638,8 @@ def main():
             "gpu_launches": a["launches_per_forward"] * args.steps,
             "roofline": roof,
             "gemm_tflops_valid": a["gemm_tflops_valid"],
-            "gemm_plans": {k: {"tokens_per_tile": v[0], "splits": v[1], "pairing": v[2], "ctas": v[3]}
+            "gemm_plans": {k: {"tokens_per_tile": v[0], "splits": v[1], "pairing": v[2], "ctas": v[3],
+                               "kind": v[4]}
                            for k, v in r["plans"].items()},
             "forward_roofline": a["forward_roofline"],
             "kernel_classes": a["kernel_classes"],

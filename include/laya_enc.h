@@ -229,10 +229,11 @@ int laya_enc_launch_count(const laya_enc_handle* h, int batch, int seq);
 
 /* The projection plans in use for a (batch, seq) shape that has a workspace
  * (after its first run, which times the candidate plans): for QKV, out-proj,
- * up and down in turn, four values each into out[16]: tokens per tile,
+ * up and down in turn, five values each into out[20]: tokens per tile,
  * split-K factor, pairing (0 none, 1 CTA pairs sharing the token tile, 2
- * sharing the weight tiles), CTAs launched.  LAYA_E_INVAL if the shape has no
- * workspace. */
+ * sharing the weight tiles), CTAs launched, and the kernel kind as
+ * laya_op_linear numbers it (the up-projection: 2, or 3 for the interleaved
+ * weight tiles).  LAYA_E_INVAL if the shape has no workspace. */
 int laya_enc_get_plans(const laya_enc_handle* h, int batch, int seq, int32_t* out);
 
 /* Bytes of device workspace a (batch, seq) shape uses (activations, split-K

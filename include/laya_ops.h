@@ -127,6 +127,10 @@ int laya_op_attention_rope(const void* qkv, const int32_t* lengths_dev,
  * kind 1 (residual): y [M, N] = bf16(residual + a),  N_w = N; residual may be y
  * kind 2 (GeGLU):    y [M, N] = bf16(gelu(a[:, :N]) * a[:, N:]), N_w = 2N,
  *                    gelu(z) = z/2 (1 + erf(z / sqrt 2))
+ * kind 3 (GeGLU, interleaved tiles): the kind 2 result bit for bit, from the
+ *                    same w, computed with 64 rows of each half in one
+ *                    128-row weight tile (one MMA per K step); N a multiple
+ *                    of 64, unsplit plans only (splits <= 1)
  * K a multiple of 64; N a multiple of 8.  splits <= 0 and tile_tokens <= 0
  * pick the library's plan; positive values force them (tile_tokens a multiple
  * of 16, at most 256; splits at most 8 and at most K/64).  workspace: device

@@ -92,6 +92,53 @@ def test_linear_paired_equals_unpaired_and_oracle(kind, M, N, K, nt):
         assert ok, msg
 
 
+@pytest.mark.parametrize("M,N,K,nt", [
+    (4117, 2624, 1024, 240), (4117, 2624, 1024, 128), (1111, 576, 256, 64), (300, 3072, 1024, 48),
+    (48, 2624, 1024, 48), (8192, 1024, 2624, 256), (1, 64, 64, 16)])
+def test_linear_geglu_interleaved_equals_geglu(M, N, K, nt):
+    # one 128-row weight tile holding 64 rows of each half (read through a 4-D
+    # tensor map) gives the two-tile GeGLU's values bit for bit: the same fp32
+    # accumulators meet in the same epilogue arithmetic; also in both pairings
+    torch = require_gpu()
+    rng = np.random.default_rng(3000 + M + N + K)
+    xb = rnd_bits(rng, (M, K))
+    wb = rnd_bits(rng, (2 * N, K), std=0.02)
+    x_dev, w_dev = to_dev(xb), to_dev(wb)
+    y = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+    te.linear(x_dev, w_dev, y, te.KIND_GEGLU, splits=1, tile_tokens=min(nt, 128))
+    torch.cuda.synchronize()
+    ref = to_bits(y)
+    for paired in (0, 0, 1, 2):
+        y = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+        te.linear(x_dev, w_dev, y, te.KIND_GEGLU_IL, splits=1, tile_tokens=nt, paired=paired)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(to_bits(y), ref)
+    y = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+    te.linear_noalloc(x_dev, w_dev, y, te.KIND_GEGLU_IL, splits=1, tile_tokens=nt)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to_bits(y), ref)
+    if M <= 1111:
+        ok, msg = bf16_close(ref, oracle.linear(xb, wb, te.KIND_GEGLU, None), ulps=1.0,
+                             min_exact=0.97)
+        assert ok, msg
+
+
+def test_linear_geglu_interleaved_rejects_what_it_cannot_run():
+    torch = require_gpu()
+    x = torch.zeros((64, 256), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((2 * 96, 256), dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros((64, 96), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(te.LayaError):   # N not a multiple of 64
+        te.linear(x, w, y, te.KIND_GEGLU_IL, splits=1)
+    w = torch.zeros((2 * 128, 256), dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros((64, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(te.LayaError):   # split-K is not offered
+        te.linear(x, w, y, te.KIND_GEGLU_IL, splits=2)
+    with pytest.raises(te.LayaError):   # nor LayerNorm on load (split kernel only)
+        te.linear_ln(x, torch.ones(256, dtype=torch.bfloat16, device="cuda"), 1e-5, w, y,
+                     te.KIND_GEGLU_IL)
+
+
 def test_linear_residual_in_place_and_repeat():
     torch = require_gpu()
     rng = np.random.default_rng(7)

@@ -25,6 +25,9 @@ ERROR_NAMES = {E_INVAL: "LAYA_E_INVAL", E_NOMEM: "LAYA_E_NOMEM", E_CUDA: "LAYA_E
                E_POISONED: "LAYA_E_POISONED", E_UNSUPPORTED: "LAYA_E_UNSUPPORTED",
                E_DEVICE: "LAYA_E_DEVICE"}
 KIND_PLAIN, KIND_RESIDUAL, KIND_GEGLU = 0, 1, 2
+# GeGLU from interleaved 128-row weight tiles (64 rows of each half): the
+# KIND_GEGLU result bit for bit, same weight layout; N % 64 == 0, unsplit
+KIND_GEGLU_IL = 3
 PROFILE_CLASSES = ("embed_norm", "norm", "qkv", "rope", "attention", "out_proj", "up_geglu",
                    "down", "output")
 
@@ -308,10 +311,10 @@ class Encoder:
         return lib().laya_enc_launch_count(self.handle, B, S)
 
     def plans(self, B, S) -> dict:
-        """{projection: (tokens per tile, split-K, pairing, CTAs)} of a shape that has run."""
-        out = (ctypes.c_int32 * 16)()
+        """{projection: (tokens per tile, split-K, pairing, CTAs, kind)} of a shape that has run."""
+        out = (ctypes.c_int32 * 20)()
         _check(lib().laya_enc_get_plans(self.handle, B, S, out), self.handle)
-        return {n: tuple(out[4 * g: 4 * g + 4])
+        return {n: tuple(out[5 * g: 5 * g + 5])
                 for g, n in enumerate(("qkv", "out_proj", "up_geglu", "down"))}
 
     def workspace_bytes(self, B, S) -> int:

@@ -48,6 +48,7 @@ constexpr size_t kMaxWorkspaceBytes = 512ull << 20;
 
 struct LayerMaps {
   CUtensorMap wqkv, wo, wup_in, wup_gate, wdown;
+  CUtensorMap wup_il;  // the up-projection as interleaved 128-row tiles (kGemmGegluIl)
   const bf16* attn_norm;
   const bf16* mlp_norm;
 };
@@ -123,6 +124,7 @@ struct laya_enc_handle {
   bool pdl = true;
   bool attn_tc = true;  // attention on tcgen05 (false: the mma.sync kernel, env LAYA_ATTN_MMA_SYNC=1)
   bool tune = true;     // time candidate projection plans on a shape's first run (env LAYA_NO_TUNE=1: off)
+  bool geglu_il = false;  // the up-projection can also run as interleaved tiles (I % 64 == 0)
   bool poisoned = false;
   std::string last_error;
   bool fail_next_run = false;  // test hook: the next run fails as a CUDA error would
@@ -226,6 +228,10 @@ int workspace_layout(const laya_enc_handle* h, int B, int S, int kmax, Workspace
     if (g >= kGemmMarkerOut && kmax == 0) continue;
     w->ncand[g] = plan_candidates(pg->M, pg->N, pg->K, pg->kind, h->num_sms, w->cand[g],
                                   Workspace::kMaxCand);
+    // the up-projection also as one interleaved weight tile per 64 features
+    if (pg->kind == kGemmGeglu && h->geglu_il && w->ncand[g] < Workspace::kMaxCand)
+      w->ncand[g] += plan_candidates(pg->M, pg->N, pg->K, kGemmGegluIl, h->num_sms,
+                                     w->cand[g] + w->ncand[g], Workspace::kMaxCand - w->ncand[g]);
   }
   size_t off = 0;
   auto take = [&](size_t n) {
@@ -425,7 +431,7 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, const RunOut& ro,
       LAYA_LAUNCH(launch_gemm(w->p_mo, om, next(LAYA_PROF_OUT)));
       LAYA_LAUNCH(launch_layernorm(w->xm, lw.mlp_norm, w->Mk, H, c.ln_eps, w->hm,
                                    next(LAYA_PROF_NORM)));
-      om.w = lw.wup_in;
+      om.w = w->p_mup.kind == kGemmGegluIl ? lw.wup_il : lw.wup_in;
       om.w2 = lw.wup_gate;
       om.x = w->tm_hm;
       om.x_box_rows = w->p_mup.nt;
@@ -459,7 +465,7 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, const RunOut& ro,
     LAYA_LAUNCH(launch_gemm(w->p_o, o, next(LAYA_PROF_OUT)));
     LAYA_LAUNCH(launch_layernorm(w->x, lw.mlp_norm, M, H, c.ln_eps, w->h, next(LAYA_PROF_NORM),
                                  pk));
-    o.w = lw.wup_in;
+    o.w = w->p_up.kind == kGemmGegluIl ? lw.wup_il : lw.wup_in;
     o.w2 = lw.wup_gate;
     o.x = w->tm_h_up;
     o.x_box_rows = w->p_up.nt;
@@ -515,9 +521,9 @@ bool build_activation_maps(const laya_enc_handle* h, Workspace* w) {
 // Plans chosen by timing, shared by every handle of the process so that two
 // handles running the same shape take the same plans (and give the same
 // bits): (M, N, K, kind, rows of the batch or 0 for marker slots) -> (token
-// tile, split-K factor, paired CTAs).
+// tile, split-K factor, paired CTAs, kind run).
 std::mutex g_tuned_mu;
-std::map<std::tuple<int, int, int, int, int>, std::tuple<int, int, int>> g_tuned;
+std::map<std::tuple<int, int, int, int, int>, std::tuple<int, int, int, int>> g_tuned;
 
 // Times the candidate plans of each projection on the first run of a shape,
 // on `stream` after that run's input upload (the packed row lengths are real,
@@ -546,7 +552,8 @@ int tune_plans(laya_enc_handle* h, Workspace* w, cudaStream_t stream) {
         for (int k = 0; k < w->ncand[g]; ++k)
           if (w->cand[g][k].nt == std::get<0>(it->second) &&
               w->cand[g][k].splits == std::get<1>(it->second) &&
-              w->cand[g][k].pair == std::get<2>(it->second))
+              w->cand[g][k].pair == std::get<2>(it->second) &&
+              w->cand[g][k].kind == std::get<3>(it->second))
             *slot = w->cand[g][k];
         continue;
       }
@@ -590,7 +597,7 @@ int tune_plans(laya_enc_handle* h, Workspace* w, cudaStream_t stream) {
           break;
         case kGemmUp:
         case kGemmMarkerUp:
-          o.w = lw.wup_in;
+          o.w = p.kind == kGemmGegluIl ? lw.wup_il : lw.wup_in;
           o.w2 = lw.wup_gate;
           ok = make_tmap_bf16_2d(&o.x, marker ? w->hm : w->h, rows, H, ldh, nt);
           o.y = marker ? w->gm : w->g;
@@ -623,7 +630,7 @@ int tune_plans(laya_enc_handle* h, Workspace* w, cudaStream_t stream) {
     if (e != cudaSuccess) break;
     *slot = w->cand[g][best];
     std::lock_guard<std::mutex> lk(g_tuned_mu);
-    g_tuned.emplace(key, std::make_tuple(slot->nt, slot->splits, slot->pair));
+    g_tuned.emplace(key, std::make_tuple(slot->nt, slot->splits, slot->pair, slot->kind));
   }
   if (e0) cudaEventDestroy(e0);
   if (e1) cudaEventDestroy(e1);
@@ -915,6 +922,7 @@ int laya_enc_create(const laya_enc_config* cfg, const laya_enc_weights* wts,
   h->pdl = !env_flag("LAYA_NO_PDL");
   h->attn_tc = !env_flag("LAYA_ATTN_MMA_SYNC");
   h->tune = !env_flag("LAYA_NO_TUNE");
+  h->geglu_il = cfg->intermediate % 64 == 0;
   h->tok_emb = static_cast<const bf16*>(wts->tok_emb);
   h->emb_norm = static_cast<const bf16*>(wts->emb_norm);
   h->final_norm = static_cast<const bf16*>(wts->final_norm);
@@ -933,6 +941,7 @@ int laya_enc_create(const laya_enc_config* cfg, const laya_enc_weights* wts,
          make_tmap_bf16_2d(&m.wup_gate, up + static_cast<size_t>(I) * H * 2, I, H, H * 2ull,
                            128) &&
          make_tmap_bf16_2d(&m.wdown, lw.wdown, H, I, I * 2ull, 128);
+    if (ok && h->geglu_il) h->geglu_il = make_tmap_geglu_il(&m.wup_il, lw.wup, I, H);
   }
   if (!ok) {
     delete h;
@@ -1172,10 +1181,11 @@ int laya_enc_get_plans(const laya_enc_handle* h, int batch, int seq, int32_t* ou
     if (w->B != batch || w->S != seq || w->kmax != 0) continue;
     const laya::GemmPlan* p[4] = {&w->p_qkv, &w->p_o, &w->p_up, &w->p_dn};
     for (int g = 0; g < 4; ++g) {
-      out[4 * g + 0] = p[g]->nt;
-      out[4 * g + 1] = p[g]->splits;
-      out[4 * g + 2] = p[g]->pair;
-      out[4 * g + 3] = p[g]->ctas();
+      out[5 * g + 0] = p[g]->nt;
+      out[5 * g + 1] = p[g]->splits;
+      out[5 * g + 2] = p[g]->pair;
+      out[5 * g + 3] = p[g]->ctas();
+      out[5 * g + 4] = p[g]->kind;
     }
     return LAYA_OK;
   }

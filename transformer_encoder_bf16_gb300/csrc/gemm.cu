@@ -17,6 +17,11 @@
 //   residual  y = bf16(r + acc)                attention output, MLP down (in place)
 //   GeGLU     y = bf16(gelu(acc_in) * acc_gate) MLP up: two weight tiles (rows f and
 //             I + f of the up-projection) feed two TMEM accumulators
+//   GeGLU-il  the same values from ONE 128-row weight tile holding 64 rows of
+//             each half (TMEM lanes f and 64 + f meet in the epilogue's
+//             staging tile): one MMA per K step instead of two, an
+//             accumulator of nt columns instead of 2 nt (so token tiles up to
+//             256 still double-buffer), a third less shared-memory traffic
 //
 // Split-K for short sequences, where the weights are the traffic and too few
 // tiles exist to occupy every SM ("Implementation priorities": smaller tiles
@@ -69,7 +74,10 @@ constexpr int kPEpi = kPThreads - 64;    // its epilogue threads
 // of (token, 8 pairs)
 constexpr int kPUnits = kChunk * (kBM / 8) / kPEpi;
 constexpr int kRopeUnits = kChunk * (kBM / 16) / kPEpi;
-static_assert(kPUnits * kPEpi == kChunk * (kBM / 8) && kRopeUnits * kPEpi == kChunk * (kBM / 16),
+// GeGLU-il: units of (token, 8 of the tile's 64 output features)
+constexpr int kIlUnits = kChunk * 8 / kPEpi;
+static_assert(kPUnits * kPEpi == kChunk * (kBM / 8) && kRopeUnits * kPEpi == kChunk * (kBM / 16) &&
+                  kIlUnits * kPEpi == kChunk * 8,
               "a chunk divides evenly among the epilogue threads");
 // fp32 staging tiles are token-major with a padded row of kSld floats: the
 // padding spreads the rows of consecutive tokens over different banks for
@@ -914,6 +922,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
           ptx::tma_load_2d(dst, m, fb, kc, row, pol);
       };
       auto load_a = [&](uint32_t st, uint32_t fb, int kc, int f) {
+        if (KIND == kGemmGegluIl) {
+          // 64 rows of block f of each half: (k, row, block, half) from (kc, 0, f, 0)
+          if (PAIR == 2)
+            ptx::tma_load_4d_mc(st, &tm_w, fb, kc, 0, f, 0, static_cast<uint16_t>(0x3), pol_w);
+          else
+            ptx::tma_load_4d(st, &tm_w, fb, kc, 0, f, 0, pol_w);
+          return;
+        }
         load(PAIR == 2, st, &tm_w, fb, kc, f * kBM, pol_w);
         if (NA == 2) load(PAIR == 2, st + kATileBytes, &tm_w2, fb, kc, f * kBM, pol_w);
       };
@@ -1125,6 +1141,23 @@ __global__ void __launch_bounds__(kPThreads, 1)
               rope_apply_store16(eo, t, ft * kBM + fo, rr_cur[k], v1, v2);
             }
           }
+        } else if (KIND == kGemmGegluIl) {
+          // unit: 8 output features of one token; the GELU half sits in
+          // staging rows grp * 8 .., the gate half 64 rows further
+#pragma unroll
+          for (int k = 0; k < kIlUnits; ++k) {
+            const int u = tid_e + kPEpi * k;
+            const int c = u / 8, grp = u % 8;
+            const int t = tt * a.nt + c0 + c;
+            if (u < ncols * 8 && t < Meff && ft * 64 < a.N) {
+              float hv[8], gv[8];
+              load8_smem(buf + c * kSld + grp * 8, hv);
+              load8_smem(buf + c * kSld + 64 + grp * 8, gv);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) hv[i] = gelu_erf(hv[i]) * gv[i];
+              store8<KIND>(eo, t, ft * 64 + grp * 8, hv);
+            }
+          }
         } else {
           const int units = ncols * (kBM / 8);
 #pragma unroll
@@ -1257,7 +1290,11 @@ cudaError_t launch_kind(const GemmPlan& p, const GemmOperands& o, Launch l) {
     return cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<KIND, 2>, o.w, o.w2, o.x, a);
   if (p.persistent)
     return cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<KIND, 0>, o.w, o.w2, o.x, a);
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<KIND>, o.w, o.w2, o.x, a);
+  if constexpr (KIND == kGemmGegluIl) {
+    return cudaErrorInvalidValue;  // persistent plans only
+  } else {
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<KIND>, o.w, o.w2, o.x, a);
+  }
 }
 
 }  // namespace
@@ -1282,10 +1319,14 @@ const void* persistent_ptr(int kind, int pair) {
       return pair == 1   ? reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmResidual, 1>)
              : pair == 2 ? reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmResidual, 2>)
                          : reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmResidual, 0>);
-    default:
+    case kGemmGeglu:
       return pair == 1   ? reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmGeglu, 1>)
              : pair == 2 ? reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmGeglu, 2>)
                          : reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmGeglu, 0>);
+    default:
+      return pair == 1   ? reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmGegluIl, 1>)
+             : pair == 2 ? reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmGegluIl, 2>)
+                         : reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmGegluIl, 0>);
   }
 }
 
@@ -1299,9 +1340,10 @@ cudaError_t configure_kernels() {
   static std::once_flag once;
   std::call_once(once, [] {
     status = cudaSuccess;
-    for (int k = kGemmPlain; k <= kGemmGeglu && status == cudaSuccess; ++k) {
-      status = cudaFuncSetAttribute(kernel_ptr(k), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(kSmemLimit));
+    for (int k = kGemmPlain; k <= kGemmGegluIl && status == cudaSuccess; ++k) {
+      if (k <= kGemmGeglu)
+        status = cudaFuncSetAttribute(kernel_ptr(k), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(kSmemLimit));
       for (int pair = 0; pair < 3 && status == cudaSuccess; ++pair)
         status = cudaFuncSetAttribute(persistent_ptr(k, pair),
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1436,7 +1478,9 @@ bool finish_plan(GemmPlan* r) {
 bool plan_gemm(int M, int N, int K, int kind, int num_sms, int force_splits, int force_nt,
                GemmPlan* p, bool allow_persistent, double split_cost) {
   if (M <= 0 || N <= 0 || K <= 0 || K % kBK != 0 || N % 8 != 0) return false;
-  if (kind < kGemmPlain || kind > kGemmGeglu) return false;
+  if (kind < kGemmPlain || kind > kGemmGegluIl) return false;
+  // the interleaved GeGLU: persistent (unsplit) plans over 64-feature tiles
+  if (kind == kGemmGegluIl && (!allow_persistent || N % 64 != 0 || force_splits > 1)) return false;
   if (force_nt > 0 && (force_nt % 16 != 0 || force_nt > 256)) return false;
   if (force_splits > 0 && (force_splits > kMaxSplits || force_splits > K / kBK)) return false;
   if (num_sms <= 0) num_sms = 148;
@@ -1464,11 +1508,13 @@ bool plan_gemm(int M, int N, int K, int kind, int num_sms, int force_splits, int
     r.k_blocks = K / kBK;
     r.nt = nt;
     r.token_tiles = (M + nt - 1) / nt;
-    r.feat_tiles = (N + kBM - 1) / kBM;
+    r.feat_tiles = kind == kGemmGegluIl ? N / 64 : (N + kBM - 1) / kBM;
     const int tiles = r.token_tiles * r.feat_tiles;
     const double unit = (na * kATileBytes + static_cast<double>(nt) * 128.0) / kATileBytes;
     const int s_lo = force_splits > 0 ? force_splits : 1;
-    const int s_hi = force_splits > 0 ? force_splits : (tiles >= num_sms ? 1 : kMaxSplits);
+    const int s_hi = force_splits > 0                   ? force_splits
+                     : (tiles >= num_sms || kind == kGemmGegluIl) ? 1
+                                                                   : kMaxSplits;
     for (int S = s_lo; S <= s_hi && S <= r.k_blocks; ++S) {
       GemmPlan c = r;
       c.splits = S;
@@ -1534,7 +1580,7 @@ int plan_candidates(int M, int N, int K, int kind, int num_sms, GemmPlan* out, i
   // that gives each CTA k tiles, k = 2..4 (the last tile's epilogue is the
   // part no main loop hides, and it shrinks with the tile)
   const int sms = num_sms > 0 ? num_sms : 148;
-  const int ftiles = (N + kBM - 1) / kBM;
+  const int ftiles = kind == kGemmGegluIl ? N / 64 : (N + kBM - 1) / kBM;
   for (int k = 2; k <= 4; ++k) {
     int pick = 0;
     for (int nt = 16; nt <= 256; nt += 16) {
@@ -1574,6 +1620,22 @@ bool make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_geglu_il(CUtensorMap* m, const void* w, uint64_t N, uint64_t K) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr || w == nullptr || N == 0 || N % 64 != 0 || K == 0 || (K * 2) % 16 != 0)
+    return false;
+  if ((reinterpret_cast<uintptr_t>(w) & 15u) != 0) return false;
+  std::memset(m, 0, sizeof(*m));
+  const cuuint64_t dims[4] = {K, 64, N / 64, 2};
+  const cuuint64_t strides[3] = {K * 2, 64 * K * 2, N * K * 2};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(kBK), 64, 1, 2};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(w), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 cudaError_t launch_gemm(const GemmPlan& p, const GemmOperands& o, Launch l) {
   // the TMA box must match the shared-memory stage the plan reserves for it
   if (o.x_box_rows != p.nt) return cudaErrorInvalidValue;
@@ -1593,6 +1655,7 @@ cudaError_t launch_gemm(const GemmPlan& p, const GemmOperands& o, Launch l) {
     case kGemmPlain: return launch_kind<kGemmPlain>(p, o, l);
     case kGemmResidual: return launch_kind<kGemmResidual>(p, o, l);
     case kGemmGeglu: return launch_kind<kGemmGeglu>(p, o, l);
+    case kGemmGegluIl: return launch_kind<kGemmGegluIl>(p, o, l);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -99,13 +99,17 @@ cudaError_t launch_attention_tc(const CUtensorMap& tm_qkv, const int32_t* length
                                 Launch l, bool packed = false);
 
 // ------------------------------------------------------------------ GEMM ---
-enum GemmKind : int { kGemmPlain = 0, kGemmResidual = 1, kGemmGeglu = 2 };
+// kGemmGegluIl: GeGLU with both halves in one 128-row weight tile (rows
+// 0..63 the GELU half, 64..127 the gate half of the same 64 output features),
+// read from the unchanged [2N, K] weight through a 4-D tensor map
+// (make_tmap_geglu_il); persistent plans only, N a multiple of 64.
+enum GemmKind : int { kGemmPlain = 0, kGemmResidual = 1, kGemmGeglu = 2, kGemmGegluIl = 3 };
 
 struct GemmPlan {
   int M = 0, N = 0, K = 0, kind = 0;
   int nt = 0;            // tokens per tile (MMA N)
   int token_tiles = 0;   // ceil(M / nt)
-  int feat_tiles = 0;    // ceil(N / 128)
+  int feat_tiles = 0;    // ceil(N / 128) (kGemmGegluIl: N / 64)
   int splits = 1;        // split-K factor = cluster size along z
   int stages = 0;        // pipeline depth
   bool persistent = false;  // one CTA per SM walks the tiles (splits == 1)
@@ -138,8 +142,13 @@ int plan_candidates(int M, int N, int K, int kind, int num_sms, GemmPlan* out, i
 bool make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
                        uint64_t row_stride_bytes, uint32_t box_rows);
 
+// The [2N, K] GeGLU weight (rows [0, N) the GELU half, [N, 2N) the gate) as
+// 4-D (k, row in block, block of 64, half): a box of (64, 64, 1, 2) is the
+// 128-row tile of kGemmGegluIl.  N a multiple of 64.
+bool make_tmap_geglu_il(CUtensorMap* m, const void* w, uint64_t N, uint64_t K);
+
 struct GemmOperands {
-  CUtensorMap w;       // weights [N, K] (GeGLU: the GELU half)
+  CUtensorMap w;       // weights [N, K] (GeGLU: the GELU half; kGemmGegluIl: make_tmap_geglu_il)
   CUtensorMap w2;      // GeGLU gate half [N, K]; unused otherwise
   CUtensorMap x;       // activations [M, K], box rows = plan.nt
   int x_box_rows = 0;  // the box height x was encoded with; launch_gemm checks it

@@ -146,13 +146,18 @@ int laya_op_linear_ex(const void* x, int M, int K, const void* w, int N, int kin
   if (paired && !laya::make_pair_plan(&p, paired)) return LAYA_E_UNSUPPORTED;
   laya::GemmOperands o;
   const uint64_t ldk = static_cast<uint64_t>(K) * 2;
-  bool ok = laya::make_tmap_bf16_2d(&o.w, w, N, K, ldk, 128) &&
-            laya::make_tmap_bf16_2d(&o.x, x, M, K, ldk, static_cast<uint32_t>(p.nt));
-  if (kind == laya::kGemmGeglu) {
-    const char* gate = static_cast<const char*>(w) + static_cast<size_t>(N) * K * 2;
-    ok = ok && laya::make_tmap_bf16_2d(&o.w2, gate, N, K, ldk, 128);
-  } else {
+  bool ok = laya::make_tmap_bf16_2d(&o.x, x, M, K, ldk, static_cast<uint32_t>(p.nt));
+  if (kind == laya::kGemmGegluIl) {
+    ok = ok && laya::make_tmap_geglu_il(&o.w, w, N, K);
     o.w2 = o.w;
+  } else {
+    ok = ok && laya::make_tmap_bf16_2d(&o.w, w, N, K, ldk, 128);
+    if (kind == laya::kGemmGeglu) {
+      const char* gate = static_cast<const char*>(w) + static_cast<size_t>(N) * K * 2;
+      ok = ok && laya::make_tmap_bf16_2d(&o.w2, gate, N, K, ldk, 128);
+    } else {
+      o.w2 = o.w;
+    }
   }
   if (!ok) return LAYA_E_INVAL;
   o.x_box_rows = p.nt;
