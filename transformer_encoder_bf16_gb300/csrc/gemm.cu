@@ -18,10 +18,11 @@
 //   GeGLU     y = bf16(gelu(acc_in) * acc_gate) MLP up: two weight tiles (rows f and
 //             I + f of the up-projection) feed two TMEM accumulators
 //   GeGLU-il  the same values from ONE 128-row weight tile holding 64 rows of
-//             each half (TMEM lanes f and 64 + f meet in the epilogue's
-//             staging tile): one MMA per K step instead of two, an
-//             accumulator of nt columns instead of 2 nt (so token tiles up to
-//             256 still double-buffer), a third less shared-memory traffic
+//             each half, interleaved 16 by 16 (so that a feature's two values
+//             sit 16 lanes apart in one warp): one MMA per K step instead of
+//             two, an accumulator of nt columns instead of 2 nt (so token
+//             tiles up to 256 still double-buffer), a third less shared-memory
+//             traffic
 //
 // Split-K for short sequences, where the weights are the traffic and too few
 // tiles exist to occupy every SM ("Implementation priorities": smaller tiles
@@ -67,23 +68,22 @@ constexpr size_t kSmemLimit = 227 * 1024;
 constexpr size_t kCtrlBytes = 256;
 constexpr size_t kLnStatsBytes = 256 * 8;  // [nt <= 256][mean, rstd] for LayerNorm on load
 constexpr int kEpiBatch = 4;             // epilogue units whose loads are issued together
-constexpr int kChunk = 32;               // persistent epilogue: token columns per drain step
+constexpr int kChunk = 32;               // staging epilogue: token columns per drain step
 constexpr int kPThreads = 320;           // persistent kernel: 2 issuing warps + 8 epilogue warps
 constexpr int kPEpi = kPThreads - 64;    // its epilogue threads
 // per epilogue thread and chunk: units of (token, 8 features) and RoPE units
 // of (token, 8 pairs)
 constexpr int kPUnits = kChunk * (kBM / 8) / kPEpi;
 constexpr int kRopeUnits = kChunk * (kBM / 16) / kPEpi;
-// GeGLU-il: units of (token, 8 of the tile's 64 output features)
-constexpr int kIlUnits = kChunk * 8 / kPEpi;
-static_assert(kPUnits * kPEpi == kChunk * (kBM / 8) && kRopeUnits * kPEpi == kChunk * (kBM / 16) &&
-                  kIlUnits * kPEpi == kChunk * 8,
+static_assert(kPUnits * kPEpi == kChunk * (kBM / 8) && kRopeUnits * kPEpi == kChunk * (kBM / 16),
               "a chunk divides evenly among the epilogue threads");
 // fp32 staging tiles are token-major with a padded row of kSld floats: the
 // padding spreads the rows of consecutive tokens over different banks for
 // the 16-byte reads of the vector phase (and the DSMEM reads of split-K).
 constexpr int kSld = kBM + 4;
-constexpr size_t kStagingBytes = 2ull * kChunk * kSld * 4;  // double-buffered fp32 staging
+// the persistent kernel's double-buffered fp32 staging (plain and residual kinds)
+constexpr size_t kStagingBytes = 2ull * kChunk * kSld * 4;
+constexpr bool staged_epilogue(int kind) { return kind == kGemmPlain || kind == kGemmResidual; }
 
 struct GemmArgs {
   int M, N, k_blocks, nt, splits, stages;
@@ -816,9 +816,23 @@ EncodeTiledFn get_encode_fn() {
 
 // Persistent variant for splits == 1: one CTA per SM walks the output tiles
 // (tile = feature tile + feat_tiles * token tile, strided by gridDim.x).  Two
-// TMEM accumulators alternate, so the epilogue of one tile (drained 32 token
-// columns at a time through a double-buffered fp32 staging area) overlaps the
-// main loop of the next; the TMA ring runs continuously across tiles.
+// TMEM accumulators alternate, so the epilogue of one tile overlaps the main
+// loop of the next; the TMA ring runs continuously across tiles.
+//
+// Two epilogues.  Plain and residual kinds stage the accumulator through
+// shared memory (32 token columns at a time, fp32) and store 16-byte
+// vectors, reading the residual and the RoPE table rows as 16-byte vectors
+// too.  The GeGLU kinds, which read nothing from global memory, go from TMEM
+// straight to global memory: shared-memory bandwidth is what the main loop's
+// TMA writes and MMA reads already use up, and staging there slowed their
+// MMAs by a third.  There a thread owns one accumulator row (an output
+// feature) and loads 16 token columns at a time; for each token the warp's
+// lanes store consecutive features.  GeGLU-il's two rows of a feature (GELU
+// and gate half) are loaded as lanes l and l + 16 of one warp (a 4-D tensor
+// map interleaves the weight rows 16 by 16): one shuffle brings them together.
+// (Stores of 2 bytes per lane were measured slower than the staged 16-byte
+// vectors for the plain and residual kinds, whose reads of the residual and
+// the RoPE tables then become 2- and 4-byte loads per lane and token.)
 //
 // PAIR != 0: the CTAs run in clusters of two that share one operand tile of
 // every stage, brought in once by the first CTA and multicast by TMA into both
@@ -923,11 +937,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
       };
       auto load_a = [&](uint32_t st, uint32_t fb, int kc, int f) {
         if (KIND == kGemmGegluIl) {
-          // 64 rows of block f of each half: (k, row, block, half) from (kc, 0, f, 0)
+          // blocks 4f .. 4f + 3 of 16 features, each as GELU rows then gate
+          // rows: (k, row, half, block) from (kc, 0, 0, 4f)
           if (PAIR == 2)
-            ptx::tma_load_4d_mc(st, &tm_w, fb, kc, 0, f, 0, static_cast<uint16_t>(0x3), pol_w);
+            ptx::tma_load_4d_mc(st, &tm_w, fb, kc, 0, 0, 4 * f, static_cast<uint16_t>(0x3), pol_w);
           else
-            ptx::tma_load_4d(st, &tm_w, fb, kc, 0, f, 0, pol_w);
+            ptx::tma_load_4d(st, &tm_w, fb, kc, 0, 0, 4 * f, pol_w);
           return;
         }
         load(PAIR == 2, st, &tm_w, fb, kc, f * kBM, pol_w);
@@ -1035,157 +1050,198 @@ __global__ void __launch_bounds__(kPThreads, 1)
       ptx::mbar_wait(done_bar, 0, &drain, nullptr, 0, a.wait_ns);
     }
   } else {
-    // ------------------------------------------------------------- epilogue
-    // Chunks of kChunk token columns: TMEM -> fp32 staging in shared memory
-    // -> 16-byte stores.  The two warps of a TMEM lane quarter drain 16
-    // columns each.  What a chunk reads from global memory (the residual, the
-    // RoPE table rows) is requested when the chunk before it starts, across
-    // tiles too, so that its latency overlaps that whole chunk.
-    const int q = warp & 3;
-    const int half = (warp - 2) >> 2;
-    const int row = q * 32 + lane;
-    const int tid_e = threadIdx.x - 64;
-    const EpiOut eo = epi_out(a);
-    ptx::grid_dependency_wait();  // residual written by earlier kernels
-    uint4 res_cur[kPUnits], res_nxt[kPUnits];
-    RopeRow rr_cur[kRopeUnits], rr_nxt[kRopeUnits];
-    // RoPE positions by arithmetic: packed tokens from the row starts, else t mod S
-    RowStarts rs;
-    const bool rope_packed = a.rope_pos != nullptr && a.lens != nullptr;
-    if (KIND == kGemmPlain && a.rope_cos != nullptr && rope_packed) rs.init(a.lens, a.lens_B, a.lens_S);
-    // global reads of chunk c0 of work item `item` into (res, rr)
-    auto prefetch = [&](int item, int c0, uint4 (&res)[kPUnits], RopeRow (&rr)[kRopeUnits]) {
-      if (item >= tiles) return;
-      int ft, tt;
-      tile_of(item, ft, tt);
-      const int ncols = a.nt - c0 < kChunk ? a.nt - c0 : kChunk;
-      if (KIND == kGemmResidual) {
-#pragma unroll
-        for (int k = 0; k < kPUnits; ++k) {
-          const int u = tid_e + kPEpi * k;
-          const int c = u / (kBM / 8), grp = u % (kBM / 8);
-          const int t = tt * a.nt + c0 + c;
-          const int f = ft * kBM + grp * 8;
-          if (u < ncols * (kBM / 8) && t < Meff && f < a.N)
-            res[k] = *reinterpret_cast<const uint4*>(a.residual + static_cast<size_t>(t) * a.N + f);
-        }
-      }
-      if (KIND == kGemmPlain && a.rope_cos != nullptr && ft * kBM < a.rope_cols) {
-#pragma unroll
-        for (int k = 0; k < kRopeUnits; ++k) {
-          const int u = tid_e + kPEpi * k;
-          const int c = u / (kBM / 16), pg = u % (kBM / 16);
-          const int t = tt * a.nt + c0 + c;
-          if (u < ncols * (kBM / 16) && t < Meff)
-            rr[k] = rope_row_at(eo, rope_packed ? rs.pos(t) : t % a.rope_S, 8 * (pg & 3));
-        }
-      }
-    };
-    prefetch(first, 0, res_cur, rr_cur);
-    int lt = 0, cc = 0;
-    for (int item = first; item < tiles; item += step, ++lt) {
-      const int b = lt & 1;
-      const int use = lt >> 1;
-      ptx::mbar_wait(accf0 + 8u * b, static_cast<uint32_t>(use) & 1u, abort_flag, a.err,
-                     kDevWaitAccum, a.wait_ns);
-      // all epilogue threads leave together: whoever gave up raised the flag
-      // before this barrier, so everyone reads the same value after it
-      ptx::named_barrier_sync(1, kPEpi);
-      if (*abort_flag) break;
-      ptx::tc_fence_after();
-      int ft, tt;
-      tile_of(item, ft, tt);
-      const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b) * acc_cols;
-      const bool rope_tile =
-          KIND == kGemmPlain && a.rope_cos != nullptr && ft * kBM < a.rope_cols;
-      for (int c0 = 0; c0 < a.nt; c0 += kChunk, ++cc) {
-        float* buf = staging + (cc & 1) * (kChunk * kSld);
+    if constexpr (staged_epilogue(KIND)) {
+      // ------------------------------------------------ epilogue (staged)
+      // Chunks of kChunk token columns: TMEM -> fp32 staging in shared memory
+      // -> 16-byte stores.  The two warps of a TMEM lane quarter drain 16
+      // columns each.  What a chunk reads from global memory (the residual, the
+      // RoPE table rows) is requested when the chunk before it starts, across
+      // tiles too, so that its latency overlaps that whole chunk.
+      const int q = warp & 3;
+      const int half = (warp - 2) >> 2;
+      const int row = q * 32 + lane;
+      const int tid_e = threadIdx.x - 64;
+      const EpiOut eo = epi_out(a);
+      ptx::grid_dependency_wait();  // residual written by earlier kernels
+      uint4 res_cur[kPUnits], res_nxt[kPUnits];
+      RopeRow rr_cur[kRopeUnits], rr_nxt[kRopeUnits];
+      // RoPE positions by arithmetic: packed tokens from the row starts, else t mod S
+      RowStarts rs;
+      const bool rope_packed = a.rope_pos != nullptr && a.lens != nullptr;
+      if (KIND == kGemmPlain && a.rope_cos != nullptr && rope_packed) rs.init(a.lens, a.lens_B, a.lens_S);
+      // global reads of chunk c0 of work item `item` into (res, rr)
+      auto prefetch = [&](int item, int c0, uint4 (&res)[kPUnits], RopeRow (&rr)[kRopeUnits]) {
+        if (item >= tiles) return;
+        int ft, tt;
+        tile_of(item, ft, tt);
         const int ncols = a.nt - c0 < kChunk ? a.nt - c0 : kChunk;
-        // the next chunk's global reads (of this tile, or the next tile's first)
-        if (c0 + kChunk < a.nt)
-          prefetch(item, c0 + kChunk, res_nxt, rr_nxt);
-        else
-          prefetch(item + step, 0, res_nxt, rr_nxt);
-        const int j0 = 16 * half;  // ncols is a multiple of 16
-        if (j0 < ncols) {
-          float v[16];
-          if (NA == 2) {
-            float g[16];
-            ptx::tmem_ld16x2(tq + c0 + j0, tq + a.nt + c0 + j0, v, g);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = gelu_erf(v[j]) * g[j];
-          } else {
-            ptx::tmem_ld16(tq + c0 + j0, v);
-          }
-#pragma unroll
-          for (int j = 0; j < 16; ++j) buf[(j0 + j) * kSld + row] = v[j];
-        }
-        if (c0 + kChunk >= a.nt) {
-          // every TMEM read of this tile is complete: hand the accumulator back
-          ptx::tc_fence_before();
-          ptx::mbar_arrive(acce0 + 8u * b);
-        }
-        ptx::named_barrier_sync(1, kPEpi);
-        // 16-byte vector stores: 8 features of one token per unit
-        if (rope_tile) {
-#pragma unroll
-          for (int k = 0; k < kRopeUnits; ++k) {
-            const int u = tid_e + kPEpi * k;
-            const int c = u / (kBM / 16), pg = u % (kBM / 16);
-            const int fo = 64 * (pg >> 2) + 8 * (pg & 3);
-            const int t = tt * a.nt + c0 + c;
-            if (u < ncols * (kBM / 16) && t < Meff) {
-              float v1[8], v2[8];
-              load8_smem(buf + c * kSld + fo, v1);
-              load8_smem(buf + c * kSld + fo + 32, v2);
-              rope_apply_store16(eo, t, ft * kBM + fo, rr_cur[k], v1, v2);
-            }
-          }
-        } else if (KIND == kGemmGegluIl) {
-          // unit: 8 output features of one token; the GELU half sits in
-          // staging rows grp * 8 .., the gate half 64 rows further
-#pragma unroll
-          for (int k = 0; k < kIlUnits; ++k) {
-            const int u = tid_e + kPEpi * k;
-            const int c = u / 8, grp = u % 8;
-            const int t = tt * a.nt + c0 + c;
-            if (u < ncols * 8 && t < Meff && ft * 64 < a.N) {
-              float hv[8], gv[8];
-              load8_smem(buf + c * kSld + grp * 8, hv);
-              load8_smem(buf + c * kSld + 64 + grp * 8, gv);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) hv[i] = gelu_erf(hv[i]) * gv[i];
-              store8<KIND>(eo, t, ft * 64 + grp * 8, hv);
-            }
-          }
-        } else {
-          const int units = ncols * (kBM / 8);
-#pragma unroll
+        if (KIND == kGemmResidual) {
+  #pragma unroll
           for (int k = 0; k < kPUnits; ++k) {
             const int u = tid_e + kPEpi * k;
-            if (u >= units) continue;
             const int c = u / (kBM / 8), grp = u % (kBM / 8);
             const int t = tt * a.nt + c0 + c;
             const int f = ft * kBM + grp * 8;
-            if (t >= Meff || f >= a.N) continue;
-            float o[8];
-            load8_smem(buf + c * kSld + grp * 8, o);
-            if (KIND == kGemmResidual) {
-              const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&res_cur[k]);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const float2 rf = __bfloat1622float2(r2[i]);
-                o[2 * i] = rf.x + o[2 * i];
-                o[2 * i + 1] = rf.y + o[2 * i + 1];
-              }
-            }
-            store8<KIND>(eo, t, f, o);
+            if (u < ncols * (kBM / 8) && t < Meff && f < a.N)
+              res[k] = *reinterpret_cast<const uint4*>(a.residual + static_cast<size_t>(t) * a.N + f);
           }
         }
-#pragma unroll
-        for (int k = 0; k < kPUnits; ++k) res_cur[k] = res_nxt[k];
-#pragma unroll
-        for (int k = 0; k < kRopeUnits; ++k) rr_cur[k] = rr_nxt[k];
+        if (KIND == kGemmPlain && a.rope_cos != nullptr && ft * kBM < a.rope_cols) {
+  #pragma unroll
+          for (int k = 0; k < kRopeUnits; ++k) {
+            const int u = tid_e + kPEpi * k;
+            const int c = u / (kBM / 16), pg = u % (kBM / 16);
+            const int t = tt * a.nt + c0 + c;
+            if (u < ncols * (kBM / 16) && t < Meff)
+              rr[k] = rope_row_at(eo, rope_packed ? rs.pos(t) : t % a.rope_S, 8 * (pg & 3));
+          }
+        }
+      };
+      prefetch(first, 0, res_cur, rr_cur);
+      int lt = 0, cc = 0;
+      for (int item = first; item < tiles; item += step, ++lt) {
+        const int b = lt & 1;
+        const int use = lt >> 1;
+        ptx::mbar_wait(accf0 + 8u * b, static_cast<uint32_t>(use) & 1u, abort_flag, a.err,
+                       kDevWaitAccum, a.wait_ns);
+        // all epilogue threads leave together: whoever gave up raised the flag
+        // before this barrier, so everyone reads the same value after it
+        ptx::named_barrier_sync(1, kPEpi);
+        if (*abort_flag) break;
+        ptx::tc_fence_after();
+        int ft, tt;
+        tile_of(item, ft, tt);
+        const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b) * acc_cols;
+        const bool rope_tile =
+            KIND == kGemmPlain && a.rope_cos != nullptr && ft * kBM < a.rope_cols;
+        for (int c0 = 0; c0 < a.nt; c0 += kChunk, ++cc) {
+          float* buf = staging + (cc & 1) * (kChunk * kSld);
+          const int ncols = a.nt - c0 < kChunk ? a.nt - c0 : kChunk;
+          // the next chunk's global reads (of this tile, or the next tile's first)
+          if (c0 + kChunk < a.nt)
+            prefetch(item, c0 + kChunk, res_nxt, rr_nxt);
+          else
+            prefetch(item + step, 0, res_nxt, rr_nxt);
+          const int j0 = 16 * half;  // ncols is a multiple of 16
+          if (j0 < ncols) {
+            float v[16];
+            ptx::tmem_ld16(tq + c0 + j0, v);
+  #pragma unroll
+            for (int j = 0; j < 16; ++j) buf[(j0 + j) * kSld + row] = v[j];
+          }
+          if (c0 + kChunk >= a.nt) {
+            // every TMEM read of this tile is complete: hand the accumulator back
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(acce0 + 8u * b);
+          }
+          ptx::named_barrier_sync(1, kPEpi);
+          // 16-byte vector stores: 8 features of one token per unit
+          if (rope_tile) {
+  #pragma unroll
+            for (int k = 0; k < kRopeUnits; ++k) {
+              const int u = tid_e + kPEpi * k;
+              const int c = u / (kBM / 16), pg = u % (kBM / 16);
+              const int fo = 64 * (pg >> 2) + 8 * (pg & 3);
+              const int t = tt * a.nt + c0 + c;
+              if (u < ncols * (kBM / 16) && t < Meff) {
+                float v1[8], v2[8];
+                load8_smem(buf + c * kSld + fo, v1);
+                load8_smem(buf + c * kSld + fo + 32, v2);
+                rope_apply_store16(eo, t, ft * kBM + fo, rr_cur[k], v1, v2);
+              }
+            }
+          } else {
+            const int units = ncols * (kBM / 8);
+  #pragma unroll
+            for (int k = 0; k < kPUnits; ++k) {
+              const int u = tid_e + kPEpi * k;
+              if (u >= units) continue;
+              const int c = u / (kBM / 8), grp = u % (kBM / 8);
+              const int t = tt * a.nt + c0 + c;
+              const int f = ft * kBM + grp * 8;
+              if (t >= Meff || f >= a.N) continue;
+              float o[8];
+              load8_smem(buf + c * kSld + grp * 8, o);
+              if (KIND == kGemmResidual) {
+                const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&res_cur[k]);
+  #pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const float2 rf = __bfloat1622float2(r2[i]);
+                  o[2 * i] = rf.x + o[2 * i];
+                  o[2 * i + 1] = rf.y + o[2 * i + 1];
+                }
+              }
+              store8<KIND>(eo, t, f, o);
+            }
+          }
+  #pragma unroll
+          for (int k = 0; k < kPUnits; ++k) res_cur[k] = res_nxt[k];
+  #pragma unroll
+          for (int k = 0; k < kRopeUnits; ++k) rr_cur[k] = rr_nxt[k];
+        }
+      }
+    } else {
+      // ------------------------------------------------ epilogue (direct)
+      // The two warps of a TMEM lane quarter take alternate blocks of 16 token
+      // columns.
+      const int q = warp & 3;
+      const int half = (warp - 2) >> 2;
+      const int lrow = q * 32 + lane;         // accumulator row (TMEM lane)
+      const bool upper = (lane & 16) != 0;    // GeGLU-il: the gate row of the pair
+      ptx::grid_dependency_wait();            // the output may be read by earlier kernels
+      int lt = 0;
+      for (int item = first; item < tiles; item += step, ++lt) {
+        const int b = lt & 1;
+        const int use = lt >> 1;
+        ptx::mbar_wait(accf0 + 8u * b, static_cast<uint32_t>(use) & 1u, abort_flag, a.err,
+                       kDevWaitAccum, a.wait_ns);
+        // all epilogue threads leave together: whoever gave up raised the flag
+        // before this barrier, so everyone reads the same value after it
+        ptx::named_barrier_sync(1, kPEpi);
+        if (*abort_flag) break;
+        ptx::tc_fence_after();
+        int ft, tt;
+        tile_of(item, ft, tt);
+        const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b) * acc_cols;
+        // the output feature of this accumulator row
+        const int f = KIND == kGemmGegluIl ? ft * 64 + (lrow >> 5) * 16 + (lrow & 15) : ft * kBM + lrow;
+        const bool f_ok = f < a.N;
+        unsigned short* yb = reinterpret_cast<unsigned short*>(a.y);
+        for (int c = 16 * half; c < a.nt; c += 32) {
+          const int t0 = tt * a.nt + c;
+          float v[16];
+          if (NA == 2) {
+            float g[16];
+            ptx::tmem_ld16x2(tq + c, tq + a.nt + c, v, g);
+  #pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int t = t0 + j;
+              const float val = gelu_erf(v[j]) * g[j];
+              if (t < Meff && f_ok)
+                yb[static_cast<size_t>(t) * a.N + f] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+            }
+          } else {
+            // lanes l < 16 hold the GELU half, l + 16 the gate half of the same
+            // feature: the lower lanes finish even tokens, the upper odd ones
+            ptx::tmem_ld16(tq + c, v);
+            float o[16];
+  #pragma unroll
+            for (int j = 0; j < 16; ++j) o[j] = __shfl_xor_sync(0xffffffffu, v[j], 16);
+  #pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+              const float h = upper ? o[2 * jj + 1] : v[2 * jj];
+              const float gt = upper ? v[2 * jj + 1] : o[2 * jj];
+              const int t = t0 + 2 * jj + (upper ? 1 : 0);
+              const float val = gelu_erf(h) * gt;
+              if (t < Meff && f_ok)
+                yb[static_cast<size_t>(t) * a.N + f] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+            }
+          }
+        }
+        // every TMEM read of this tile by this thread is complete: its share
+        // of the accumulator goes back to the MMA issuer
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(acce0 + 8u * b);
       }
     }
   }
@@ -1227,7 +1283,7 @@ cudaError_t launch_kind(const GemmPlan& p, const GemmOperands& o, Launch l) {
   const size_t stage_bytes = static_cast<size_t>(na) * kATileBytes + static_cast<size_t>(p.nt) * 128;
   size_t data = stage_bytes * p.stages;
   if (p.persistent) {
-    data += kStagingBytes;
+    if (staged_epilogue(KIND)) data += kStagingBytes;
   } else {
     const size_t part = p.splits == 1 ? static_cast<size_t>(p.nt) * kSld * 4
                                       : split_reduce_bytes(na, p.nt, p.splits);
@@ -1428,15 +1484,16 @@ bool finish_plan(GemmPlan* r) {
   const size_t stage_bytes = static_cast<size_t>(na) * kATileBytes + static_cast<size_t>(r->nt) * 128;
   const size_t budget = kSmemLimit - kCtrlBytes - kLnStatsBytes - 1024;
   if (r->persistent) {
-    // ring of stages + double-buffered staging; two accumulators in TMEM
-    const size_t avail = budget - kStagingBytes;
-    int stages = static_cast<int>(avail / stage_bytes);
+    // ring of stages (+ the staging of the plain and residual epilogues); two
+    // accumulators in TMEM
+    const size_t staging = staged_epilogue(r->kind) ? kStagingBytes : 0;
+    int stages = static_cast<int>((budget - staging) / stage_bytes);
     if (stages > 8) stages = 8;
     if (stages > r->k_blocks) stages = r->k_blocks;
     if (stages < 2 && r->k_blocks >= 2) return false;
     if (stages < 1) return false;
     r->stages = stages;
-    r->smem_bytes = stage_bytes * stages + kStagingBytes + kCtrlBytes + 1024;
+    r->smem_bytes = stage_bytes * stages + staging + kCtrlBytes + 1024;
     r->tmem_cols = pow2_cols(static_cast<uint32_t>(2 * na * r->nt));
     return r->tmem_cols <= 512 && r->smem_bytes <= kSmemLimit;
   }
@@ -1626,9 +1683,11 @@ bool make_tmap_geglu_il(CUtensorMap* m, const void* w, uint64_t N, uint64_t K) {
     return false;
   if ((reinterpret_cast<uintptr_t>(w) & 15u) != 0) return false;
   std::memset(m, 0, sizeof(*m));
-  const cuuint64_t dims[4] = {K, 64, N / 64, 2};
-  const cuuint64_t strides[3] = {K * 2, 64 * K * 2, N * K * 2};
-  const cuuint32_t box[4] = {static_cast<cuuint32_t>(kBK), 64, 1, 2};
+  // (k, row in a block of 16, half, block): a box of 4 blocks is 128 rows,
+  // 16 GELU rows then the 16 gate rows of the same features, four times
+  const cuuint64_t dims[4] = {K, 16, 2, N / 16};
+  const cuuint64_t strides[3] = {K * 2, N * K * 2, 16 * K * 2};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(kBK), 16, 2, 4};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(w), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -143,8 +143,9 @@ bool make_tmap_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t
                        uint64_t row_stride_bytes, uint32_t box_rows);
 
 // The [2N, K] GeGLU weight (rows [0, N) the GELU half, [N, 2N) the gate) as
-// 4-D (k, row in block, block of 64, half): a box of (64, 64, 1, 2) is the
-// 128-row tile of kGemmGegluIl.  N a multiple of 64.
+// 4-D (k, row in a block of 16, half, block): a box of (64, 16, 2, 4) is the
+// 128-row tile of kGemmGegluIl, the 16 GELU rows of a block of features
+// followed by its 16 gate rows.  N a multiple of 64.
 bool make_tmap_geglu_il(CUtensorMap* m, const void* w, uint64_t N, uint64_t K);
 
 struct GemmOperands {
