@@ -155,8 +155,11 @@ int laya_op_linear(const void* x, int M, int K, const void* w, int N, int kind,
  * operand).  paired = 1: the two CTAs take the two feature tiles of a pair
  * with the same token tile (the token tile is shared); paired = 2: the two
  * token tiles of a pair with the same feature tile (the weight tiles are
- * shared).  laya_enc_run's first run of a shape may pick either by timing.
- * Same arithmetic and results as paired = 0, bit for bit.
+ * shared); paired = 3: the pair computes one 256-feature tile with one
+ * two-CTA MMA (tcgen05 cta_group::2), each CTA loading its 128 weight rows
+ * and half of the token tile.  laya_enc_run's first run of a shape may pick
+ * any of them by timing.  Same arithmetic and results as paired = 0, bit for
+ * bit.
  * LAYA_E_UNSUPPORTED if the device cannot hold such clusters.
  * Sources: as laya_op_linear. */
 int laya_op_linear_ex(const void* x, int M, int K, const void* w, int N, int kind,

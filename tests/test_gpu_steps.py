@@ -79,7 +79,7 @@ def test_linear_paired_equals_unpaired_and_oracle(kind, M, N, K, nt):
     rb = rnd_bits(rng, (M, N), std=2.0) if kind == te.KIND_RESIDUAL else None
     r_dev = to_dev(rb) if rb is not None else None
     outs = []
-    for paired in (0, 1, 1, 2, 2):
+    for paired in (0, 1, 1, 2, 2, 3, 3):
         y = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
         te.linear(to_dev(xb), to_dev(wb), y, kind, residual=r_dev, splits=1, tile_tokens=nt,
                   paired=paired)
@@ -108,7 +108,7 @@ def test_linear_geglu_interleaved_equals_geglu(M, N, K, nt):
     te.linear(x_dev, w_dev, y, te.KIND_GEGLU, splits=1, tile_tokens=min(nt, 128))
     torch.cuda.synchronize()
     ref = to_bits(y)
-    for paired in (0, 0, 1, 2):
+    for paired in (0, 0, 1, 2, 3):
         y = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
         te.linear(x_dev, w_dev, y, te.KIND_GEGLU_IL, splits=1, tile_tokens=nt, paired=paired)
         torch.cuda.synchronize()

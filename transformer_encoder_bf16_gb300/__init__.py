@@ -406,7 +406,8 @@ def linear(x, w, y, kind=KIND_PLAIN, residual=None, splits=0, tile_tokens=0, str
     """workspace: a device tensor of at least linear_workspace_size() bytes; a
     fresh one is allocated when None (pass one when capturing a graph).
     paired: 0, or the persistent kernel in clusters of two sharing the token
-    tile (1) or the weight tiles (2) of every stage (splits must be 1)."""
+    tile (1) or the weight tiles (2) of every stage, or issuing one two-CTA
+    MMA per pair of feature tiles (3) (splits must be 1)."""
     M, K = x.shape
     N = y.shape[1]
     ws = workspace if workspace is not None else _workspace(M, K, N, kind, splits, tile_tokens, y.device)

@@ -77,7 +77,7 @@ struct Workspace {
   GemmPlan p_qkv, p_o, p_up, p_dn;
   // plan tuning (tune_plans): candidate plans of each projection, timed on
   // the first run of the shape; p_* above are the chosen ones
-  static constexpr int kMaxCand = 20;
+  static constexpr int kMaxCand = 32;
   GemmPlan cand[7][kMaxCand];
   int ncand[7] = {};
   bool tuned = false;
@@ -226,12 +226,28 @@ int workspace_layout(const laya_enc_handle* h, int B, int S, int kmax, Workspace
     GemmPlan* pg = gemm_slot(w, g);
     w->ncand[g] = 0;
     if (g >= kGemmMarkerOut && kmax == 0) continue;
-    w->ncand[g] = plan_candidates(pg->M, pg->N, pg->K, pg->kind, h->num_sms, w->cand[g],
-                                  Workspace::kMaxCand);
+    // the model's choice first (kept unless another candidate is clearly faster)
+    w->cand[g][0] = *pg;
+    w->ncand[g] = 1;
     // the up-projection also as one interleaved weight tile per 64 features
-    if (pg->kind == kGemmGeglu && h->geglu_il && w->ncand[g] < Workspace::kMaxCand)
+    if (pg->kind == kGemmGeglu && h->geglu_il)
       w->ncand[g] += plan_candidates(pg->M, pg->N, pg->K, kGemmGegluIl, h->num_sms,
-                                     w->cand[g] + w->ncand[g], Workspace::kMaxCand - w->ncand[g]);
+                                     w->cand[g] + w->ncand[g], 12);
+    w->ncand[g] += plan_candidates(pg->M, pg->N, pg->K, pg->kind, h->num_sms,
+                                   w->cand[g] + w->ncand[g], Workspace::kMaxCand - w->ncand[g]);
+    // distinct plans only
+    int n = 0;
+    for (int k = 0; k < w->ncand[g]; ++k) {
+      const GemmPlan& c = w->cand[g][k];
+      bool dup = false;
+      for (int j = 0; j < n && !dup; ++j) {
+        const GemmPlan& d = w->cand[g][j];
+        dup = d.kind == c.kind && d.nt == c.nt && d.splits == c.splits &&
+              d.persistent == c.persistent && d.pair == c.pair;
+      }
+      if (!dup) w->cand[g][n++] = c;
+    }
+    w->ncand[g] = n;
   }
   size_t off = 0;
   auto take = [&](size_t n) {
@@ -400,7 +416,7 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, const RunOut& ro,
     o.w = lw.wqkv;
     o.w2 = lw.wqkv;
     o.x = *qkv_in;
-    o.x_box_rows = w->p_qkv.nt;
+    o.x_box_rows = w->p_qkv.x_box();
     o.y = w->qkv;
     // RoPE in the QKV epilogue: q and k columns [0, 2H) leave the GEMM rotated
     o.rope_cos = glob ? cos_g : cos_l;
@@ -425,7 +441,7 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, const RunOut& ro,
       om.w = lw.wo;
       om.w2 = lw.wo;
       om.x = w->tm_ctxm;
-      om.x_box_rows = w->p_mo.nt;
+      om.x_box_rows = w->p_mo.x_box();
       om.y = w->xm;
       om.residual = w->xm;
       LAYA_LAUNCH(launch_gemm(w->p_mo, om, next(LAYA_PROF_OUT)));
@@ -434,14 +450,14 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, const RunOut& ro,
       om.w = w->p_mup.kind == kGemmGegluIl ? lw.wup_il : lw.wup_in;
       om.w2 = lw.wup_gate;
       om.x = w->tm_hm;
-      om.x_box_rows = w->p_mup.nt;
+      om.x_box_rows = w->p_mup.x_box();
       om.y = w->gm;
       om.residual = nullptr;
       LAYA_LAUNCH(launch_gemm(w->p_mup, om, next(LAYA_PROF_UP)));
       om.w = lw.wdown;
       om.w2 = lw.wdown;
       om.x = w->tm_gm;
-      om.x_box_rows = w->p_mdn.nt;
+      om.x_box_rows = w->p_mdn.x_box();
       om.y = static_cast<bf16*>(out);
       om.residual = w->xm;
       if (c.out_fp32) om.y_f32 = static_cast<float*>(out);
@@ -459,7 +475,7 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, const RunOut& ro,
     o.w = lw.wo;
     o.w2 = lw.wo;
     o.x = w->tm_ctx_o;
-    o.x_box_rows = w->p_o.nt;
+    o.x_box_rows = w->p_o.x_box();
     o.y = w->x;
     o.residual = w->x;
     LAYA_LAUNCH(launch_gemm(w->p_o, o, next(LAYA_PROF_OUT)));
@@ -468,14 +484,14 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, const RunOut& ro,
     o.w = w->p_up.kind == kGemmGegluIl ? lw.wup_il : lw.wup_in;
     o.w2 = lw.wup_gate;
     o.x = w->tm_h_up;
-    o.x_box_rows = w->p_up.nt;
+    o.x_box_rows = w->p_up.x_box();
     o.y = w->g;
     o.residual = nullptr;
     LAYA_LAUNCH(launch_gemm(w->p_up, o, next(LAYA_PROF_UP)));
     o.w = lw.wdown;
     o.w2 = lw.wdown;
     o.x = w->tm_g_dn;
-    o.x_box_rows = w->p_dn.nt;
+    o.x_box_rows = w->p_dn.x_box();
     const bool last = li == h->L - 1;
     o.y = (last && !w->packed) ? static_cast<bf16*>(out) : w->x;
     o.residual = w->x;
@@ -501,7 +517,7 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, const RunOut& ro,
 bool build_activation_maps(const laya_enc_handle* h, Workspace* w) {
   const laya_enc_config& c = h->cfg;
   const int M = w->M;
-  auto box = [](const GemmPlan& p) { return static_cast<uint32_t>(p.nt); };
+  auto box = [](const GemmPlan& p) { return static_cast<uint32_t>(p.x_box()); };
   const uint64_t ldh = c.hidden * 2ull, ldi = c.intermediate * 2ull;
   bool ok = make_tmap_bf16_2d(&w->tm_x_qkv, w->x, M, c.hidden, ldh, box(w->p_qkv)) &&
             make_tmap_bf16_2d(&w->tm_h_qkv, w->h, M, c.hidden, ldh, box(w->p_qkv)) &&
@@ -574,8 +590,8 @@ int tune_plans(laya_enc_handle* h, Workspace* w, cudaStream_t stream) {
         o.lens_B = w->B;
         o.lens_S = w->S;
       }
-      o.x_box_rows = p.nt;
-      const uint32_t nt = static_cast<uint32_t>(p.nt);
+      o.x_box_rows = p.x_box();
+      const uint32_t nt = static_cast<uint32_t>(p.x_box());  // activation box rows
       bool ok = true;
       switch (g) {
         case kGemmQkv:

@@ -843,6 +843,13 @@ EncodeTiledFn get_encode_fn() {
 //              token tile, B, is shared);
 //   PAIR == 2: the two token tiles of a pair with the same feature tile (the
 //              weight tiles, A, are shared).
+//   PAIR == 3: one MMA for the pair (tcgen05 cta_group::2, 256 weight rows):
+//              each CTA loads its 128 weight rows and HALF of the shared token
+//              tile (halving that operand's traffic into each SM, not only
+//              out of L2), the first CTA issues the MMAs for both, and each
+//              CTA's TMEM holds its 128 features x nt tokens.  Both CTAs'
+//              loads count on the first CTA's full barriers; both CTAs'
+//              epilogues hand the accumulator back on its barriers.
 // With an odd tile count the last pair's second tile lies past N (its weight
 // rows load as zeros) or past the tokens; its outputs are not stored.
 template <int KIND, int PAIR>
@@ -851,11 +858,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
                            const __grid_constant__ CUtensorMap tm_w2,
                            const __grid_constant__ CUtensorMap tm_x, const GemmArgs a) {
   constexpr int NA = (KIND == kGemmGeglu) ? 2 : 1;
+  constexpr bool TWO = PAIR == 3;  // one cta_group::2 MMA per pair
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = ptx::smem_u32(smem);
-  const uint32_t b_bytes = static_cast<uint32_t>(a.nt) * kBK * 2;
+  // this CTA's token rows of a stage (TWO: half the tile)
+  const uint32_t b_bytes = static_cast<uint32_t>(TWO ? a.nt / 2 : a.nt) * kBK * 2;
   const uint32_t stage_bytes = NA * kATileBytes + b_bytes;
   float* staging = reinterpret_cast<float*>(smem + static_cast<size_t>(a.stages) * stage_bytes);
 
@@ -875,7 +884,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   // token tile of an item from tile_of (PAIR: items are feature-tile pairs)
   const int Meff = a.lens != nullptr ? packed_total(a.lens, a.lens_B, a.lens_S) : a.M;
   const int ttiles = (Meff + a.nt - 1) / a.nt;
-  const int fwalk = PAIR == 1 ? (a.feat_tiles + 1) / 2 : a.feat_tiles;
+  const int fwalk = (PAIR == 1 || TWO) ? (a.feat_tiles + 1) / 2 : a.feat_tiles;
   const int twalk = PAIR == 2 ? (ttiles + 1) / 2 : ttiles;
   const int tiles = fwalk * twalk;
   const int rank = PAIR ? static_cast<int>(ptx::cluster_ctarank()) : 0;
@@ -883,7 +892,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   const int step = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   auto tile_of = [&](int item, int& ft, int& tt) {
     const int f = item % fwalk, t = item / fwalk;
-    ft = PAIR == 1 ? 2 * f + rank : f;
+    ft = (PAIR == 1 || TWO) ? 2 * f + rank : f;
     tt = PAIR == 2 ? 2 * t + rank : t;
   };
   const int KB = a.k_blocks;
@@ -892,11 +901,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.stages; ++i) {
       ptx::mbar_init(full0 + 8u * i, 1);
-      ptx::mbar_init(empty0 + 8u * i, PAIR ? 2 : 1);  // PAIR: both CTAs' MMAs release it
+      // PAIR 1, 2: both CTAs' MMAs release it; TWO: the first CTA's MMA for both
+      ptx::mbar_init(empty0 + 8u * i, (PAIR == 1 || PAIR == 2) ? 2 : 1);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(accf0 + 8u * b, 1);
-      ptx::mbar_init(acce0 + 8u * b, kPEpi);
+      ptx::mbar_init(acce0 + 8u * b, TWO ? 2 * kPEpi : kPEpi);  // TWO: both CTAs' epilogues
     }
     ptx::mbar_init(done_bar, 1);
     *abort_flag = 0;
@@ -908,8 +918,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
     ptx::prefetch_tmap(&tm_x);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), a.tmem_cols);
-    ptx::tmem_relinquish();
+    if (TWO) {
+      ptx::tmem_alloc_cg2(ptx::smem_u32(tmem_slot), a.tmem_cols);
+      ptx::tmem_relinquish_cg2();
+    } else {
+      ptx::tmem_alloc(ptx::smem_u32(tmem_slot), a.tmem_cols);
+      ptx::tmem_relinquish();
+    }
   }
   // PAIR: both CTAs' barriers are initialised before either multicasts into the other
   if (PAIR) ptx::cluster_sync();
@@ -918,6 +933,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
   ptx::tc_fence_after();
   ptx::grid_launch_dependents();
   const uint32_t tmem = *tmem_slot;
+  // an epilogue thread hands accumulator b back to the MMA issuer (TWO: to
+  // the first CTA's barrier, from both CTAs)
+  auto release_acc = [&](int b) {
+    if (TWO)
+      ptx::mbar_arrive_cluster(ptx::mapa(acce0 + 8u * b, 0));
+    else
+      ptx::mbar_arrive(acce0 + 8u * b);
+  };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -930,16 +953,27 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const bool loads_b = PAIR != 1 || rank == 0;
       auto load = [&](bool mc, uint32_t dst, const CUtensorMap* m, uint32_t fb, int kc, int row,
                       uint64_t pol) {
-        if (mc)
+        if (TWO)
+          ptx::tma_load_2d_cg2(dst, m, fb, kc, row, pol);
+        else if (mc)
           ptx::tma_load_2d_mc(dst, m, fb, kc, row, static_cast<uint16_t>(0x3), pol);
         else
           ptx::tma_load_2d(dst, m, fb, kc, row, pol);
       };
+      // the barrier a stage's bytes count on (TWO: the first CTA's) and the
+      // bytes it expects (TWO: both CTAs'; only the first CTA arms it)
+      auto fbar = [&](int s) {
+        return TWO ? ptx::mapa(full0 + 8u * s, 0) : full0 + 8u * s;
+      };
+      const bool arms = !TWO || rank == 0;
+      const uint32_t expect = TWO ? 2 * stage_bytes : stage_bytes;
       auto load_a = [&](uint32_t st, uint32_t fb, int kc, int f) {
         if (KIND == kGemmGegluIl) {
           // blocks 4f .. 4f + 3 of 16 features, each as GELU rows then gate
           // rows: (k, row, half, block) from (kc, 0, 0, 4f)
-          if (PAIR == 2)
+          if (TWO)
+            ptx::tma_load_4d_cg2(st, &tm_w, fb, kc, 0, 0, 4 * f, pol_w);
+          else if (PAIR == 2)
             ptx::tma_load_4d_mc(st, &tm_w, fb, kc, 0, 0, 4 * f, static_cast<uint16_t>(0x3), pol_w);
           else
             ptx::tma_load_4d(st, &tm_w, fb, kc, 0, 0, 4 * f, pol_w);
@@ -948,8 +982,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
         load(PAIR == 2, st, &tm_w, fb, kc, f * kBM, pol_w);
         if (NA == 2) load(PAIR == 2, st + kATileBytes, &tm_w2, fb, kc, f * kBM, pol_w);
       };
+      // token rows from t (TWO: this CTA's half of the tile)
       auto load_b = [&](uint32_t dst, uint32_t fb, int kc, int t) {
-        load(PAIR == 1, dst, &tm_x, fb, kc, t, pol_x);
+        load(PAIR == 1, dst, &tm_x, fb, kc, TWO ? t + rank * (a.nt / 2) : t, pol_x);
       };
       int issued = 0;
       const bool wh = a.withhold && blockIdx.x == 0;
@@ -961,14 +996,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
         for (int i = 0; i < pre; ++i) {
           if (wh && i == 0) continue;
           const uint32_t st = sbase + i * stage_bytes;
-          ptx::mbar_arrive_expect_tx(full0 + 8u * i, stage_bytes);
-          if (loads_a) load_a(st, full0 + 8u * i, i * kBK, f0);
+          if (arms) ptx::mbar_arrive_expect_tx(full0 + 8u * i, expect);
+          if (loads_a) load_a(st, fbar(i), i * kBK, f0);
         }
         ptx::grid_dependency_wait();
         if (blockIdx.x == 0) record_stamp(a.stamp);
         for (int i = 0; i < pre; ++i)
           if (!(wh && i == 0) && loads_b)
-            load_b(sbase + i * stage_bytes + NA * kATileBytes, full0 + 8u * i, i * kBK, t0 * a.nt);
+            load_b(sbase + i * stage_bytes + NA * kATileBytes, fbar(i), i * kBK, t0 * a.nt);
         issued = pre;
         int it = 0;
         bool stop = false;
@@ -985,8 +1020,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
               break;
             }
             const uint32_t st = sbase + s * stage_bytes;
-            const uint32_t fb = full0 + 8u * s;
-            ptx::mbar_arrive_expect_tx(fb, stage_bytes);
+            const uint32_t fb = fbar(s);
+            if (arms) ptx::mbar_arrive_expect_tx(full0 + 8u * s, expect);
             if (loads_a) load_a(st, fb, kb * kBK, ft);
             if (loads_b) load_b(st + NA * kATileBytes, fb, kb * kBK, tt * a.nt);
             issued = it + 1;
@@ -994,17 +1029,21 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
       }
       // no copy may still be in flight at exit (a flag of our own: an abort
-      // must not cut these waits short)
+      // must not cut these waits short).  TWO: the second CTA's copies count
+      // on the first CTA's barriers, which the first CTA waits for, and
+      // neither CTA leaves before the final cluster barrier.
       volatile int drain = 0;
-      for (int i = (issued > a.stages ? issued - a.stages : 0); i < issued; ++i)
-        if (!(wh && i == 0))
-          ptx::mbar_wait(full0 + 8u * (i % a.stages), static_cast<uint32_t>(i / a.stages) & 1u,
-                         &drain, nullptr, 0, a.wait_ns);
+      if (arms)
+        for (int i = (issued > a.stages ? issued - a.stages : 0); i < issued; ++i)
+          if (!(wh && i == 0))
+            ptx::mbar_wait(full0 + 8u * (i % a.stages), static_cast<uint32_t>(i / a.stages) & 1u,
+                           &drain, nullptr, 0, a.wait_ns);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    // TWO: the pair's MMAs are issued by the first CTA alone
+    if (lane == 0 && (!TWO || rank == 0)) {
       // ---------------------------------------------------------- MMA issuer
-      const uint32_t idesc = ptx::idesc_bf16(kBM, a.nt);
+      const uint32_t idesc = ptx::idesc_bf16(TWO ? 2 * kBM : kBM, a.nt);
       const uint64_t da0 = ptx::sdesc_sw128(sbase);
       const uint64_t db0 = ptx::sdesc_sw128(sbase + NA * kATileBytes);
       const uint64_t stage_units = stage_bytes >> 4;
@@ -1014,9 +1053,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
       for (int item = first; item < tiles && !stop; item += step, ++lt) {
         const int b = lt & 1;
         const int use = lt >> 1;
-        if (lt >= 2 && !ptx::mbar_wait(acce0 + 8u * b, static_cast<uint32_t>(use - 1) & 1u,
-                                       abort_flag, a.err, kDevWaitAccum, a.wait_ns))
-          break;
+        if (lt >= 2) {
+          const uint32_t par = static_cast<uint32_t>(use - 1) & 1u;
+          const bool ok = TWO ? ptx::mbar_wait_cluster(acce0 + 8u * b, par, abort_flag, a.err,
+                                                       kDevWaitAccum, a.wait_ns)
+                              : ptx::mbar_wait(acce0 + 8u * b, par, abort_flag, a.err,
+                                               kDevWaitAccum, a.wait_ns);
+          if (!ok) break;
+        }
         ptx::tc_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>(b) * acc_cols;
         for (int kb = 0; kb < KB; ++kb, ++it, rp.next()) {
@@ -1031,21 +1075,37 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-            ptx::mma_bf16(d, da + 2 * kk, db + 2 * kk, idesc, acc);
-            if (NA == 2)
-              ptx::mma_bf16(d + static_cast<uint32_t>(a.nt), da + (kATileBytes >> 4) + 2 * kk,
-                            db + 2 * kk, idesc, acc);
+            if (TWO) {
+              ptx::mma_bf16_cg2(d, da + 2 * kk, db + 2 * kk, idesc, acc);
+              if (NA == 2)
+                ptx::mma_bf16_cg2(d + static_cast<uint32_t>(a.nt), da + (kATileBytes >> 4) + 2 * kk,
+                                  db + 2 * kk, idesc, acc);
+            } else {
+              ptx::mma_bf16(d, da + 2 * kk, db + 2 * kk, idesc, acc);
+              if (NA == 2)
+                ptx::mma_bf16(d + static_cast<uint32_t>(a.nt), da + (kATileBytes >> 4) + 2 * kk,
+                              db + 2 * kk, idesc, acc);
+            }
           }
           // PAIR: the stage is free only once both CTAs have consumed it
-          if (PAIR)
+          // (TWO: once the pair's MMA has, in both CTAs)
+          if (TWO)
+            ptx::mma_commit_cg2_mc(empty0 + 8u * s, static_cast<uint16_t>(0x3));
+          else if (PAIR)
             ptx::mma_commit_mc(empty0 + 8u * s, static_cast<uint16_t>(0x3));
           else
             ptx::mma_commit(empty0 + 8u * s);
         }
-        ptx::mma_commit(accf0 + 8u * b);
+        if (TWO)
+          ptx::mma_commit_cg2_mc(accf0 + 8u * b, static_cast<uint16_t>(0x3));
+        else
+          ptx::mma_commit(accf0 + 8u * b);
       }
       // every product issued has completed before TMEM is released
-      ptx::mma_commit(done_bar);
+      if (TWO)
+        ptx::mma_commit_cg2(done_bar);
+      else
+        ptx::mma_commit(done_bar);
       volatile int drain = 0;
       ptx::mbar_wait(done_bar, 0, &drain, nullptr, 0, a.wait_ns);
     }
@@ -1132,7 +1192,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           if (c0 + kChunk >= a.nt) {
             // every TMEM read of this tile is complete: hand the accumulator back
             ptx::tc_fence_before();
-            ptx::mbar_arrive(acce0 + 8u * b);
+            release_acc(b);
           }
           ptx::named_barrier_sync(1, kPEpi);
           // 16-byte vector stores: 8 features of one token per unit
@@ -1241,7 +1301,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // every TMEM read of this tile by this thread is complete: its share
         // of the accumulator goes back to the MMA issuer
         ptx::tc_fence_before();
-        ptx::mbar_arrive(acce0 + 8u * b);
+        release_acc(b);
       }
     }
   }
@@ -1253,7 +1313,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
   if (PAIR) ptx::cluster_sync();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, a.tmem_cols);
+    if (TWO)
+      ptx::tmem_dealloc_cg2(tmem, a.tmem_cols);
+    else
+      ptx::tmem_dealloc(tmem, a.tmem_cols);
   }
 }
 
@@ -1280,7 +1343,8 @@ cudaError_t launch_kind(const GemmPlan& p, const GemmOperands& o, Launch l) {
   a.token_tiles = p.token_tiles;
   a.tmem_cols = p.tmem_cols;
   const int na = KIND == kGemmGeglu ? 2 : 1;
-  const size_t stage_bytes = static_cast<size_t>(na) * kATileBytes + static_cast<size_t>(p.nt) * 128;
+  const size_t stage_bytes =
+      static_cast<size_t>(na) * kATileBytes + static_cast<size_t>(p.x_box()) * 128;
   size_t data = stage_bytes * p.stages;
   if (p.persistent) {
     if (staged_epilogue(KIND)) data += kStagingBytes;
@@ -1344,6 +1408,8 @@ cudaError_t launch_kind(const GemmPlan& p, const GemmOperands& o, Launch l) {
     return cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<KIND, 1>, o.w, o.w2, o.x, a);
   if (p.persistent && p.pair == 2)
     return cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<KIND, 2>, o.w, o.w2, o.x, a);
+  if (p.persistent && p.pair == 3)
+    return cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<KIND, 3>, o.w, o.w2, o.x, a);
   if (p.persistent)
     return cudaLaunchKernelEx(&cfg, gemm_persistent_kernel<KIND, 0>, o.w, o.w2, o.x, a);
   if constexpr (KIND == kGemmGegluIl) {
@@ -1370,25 +1436,29 @@ const void* persistent_ptr(int kind, int pair) {
     case kGemmPlain:
       return pair == 1   ? reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmPlain, 1>)
              : pair == 2 ? reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmPlain, 2>)
+             : pair == 3 ? reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmPlain, 3>)
                          : reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmPlain, 0>);
     case kGemmResidual:
       return pair == 1   ? reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmResidual, 1>)
              : pair == 2 ? reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmResidual, 2>)
+             : pair == 3 ? reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmResidual, 3>)
                          : reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmResidual, 0>);
     case kGemmGeglu:
       return pair == 1   ? reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmGeglu, 1>)
              : pair == 2 ? reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmGeglu, 2>)
+             : pair == 3 ? reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmGeglu, 3>)
                          : reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmGeglu, 0>);
     default:
       return pair == 1   ? reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmGegluIl, 1>)
              : pair == 2 ? reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmGegluIl, 2>)
+             : pair == 3 ? reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmGegluIl, 3>)
                          : reinterpret_cast<const void*>(&gemm_persistent_kernel<kGemmGegluIl, 0>);
   }
 }
 
 // Clusters of two persistent CTAs with this shared memory that can be
 // resident at once; -1 when there is no device to ask.
-int max_active_pairs(int kind, size_t smem);
+int max_active_pairs(int kind, size_t smem, int mode);
 
 // Opt every kernel variant into the full dynamic shared memory once.
 cudaError_t configure_kernels() {
@@ -1400,7 +1470,7 @@ cudaError_t configure_kernels() {
       if (k <= kGemmGeglu)
         status = cudaFuncSetAttribute(kernel_ptr(k), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(kSmemLimit));
-      for (int pair = 0; pair < 3 && status == cudaSuccess; ++pair)
+      for (int pair = 0; pair < 4 && status == cudaSuccess; ++pair)
         status = cudaFuncSetAttribute(persistent_ptr(k, pair),
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(kSmemLimit));
@@ -1442,10 +1512,10 @@ int max_active_clusters(int kind, size_t smem, int splits) {
   return n;
 }
 
-int max_active_pairs(int kind, size_t smem) {
+int max_active_pairs(int kind, size_t smem, int mode) {
   static std::mutex mu;
-  static std::map<std::tuple<int, size_t>, int> cache;
-  const auto key = std::make_tuple(kind, smem);
+  static std::map<std::tuple<int, size_t, int>, int> cache;
+  const auto key = std::make_tuple(kind, smem, mode);
   {
     std::lock_guard<std::mutex> g(mu);
     auto it = cache.find(key);
@@ -1465,7 +1535,7 @@ int max_active_pairs(int kind, size_t smem) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, persistent_ptr(kind, 1), &cfg) != cudaSuccess) n = -1;
+    if (cudaOccupancyMaxActiveClusters(&n, persistent_ptr(kind, mode), &cfg) != cudaSuccess) n = -1;
   }
   cudaGetLastError();
   std::lock_guard<std::mutex> g(mu);
@@ -1481,7 +1551,7 @@ namespace {
 // tile does not fit in shared memory or TMEM.
 bool finish_plan(GemmPlan* r) {
   const int na = r->kind == kGemmGeglu ? 2 : 1;
-  const size_t stage_bytes = static_cast<size_t>(na) * kATileBytes + static_cast<size_t>(r->nt) * 128;
+  const size_t stage_bytes = static_cast<size_t>(na) * kATileBytes + static_cast<size_t>(r->x_box()) * 128;
   const size_t budget = kSmemLimit - kCtrlBytes - kLnStatsBytes - 1024;
   if (r->persistent) {
     // ring of stages (+ the staging of the plain and residual epilogues); two
@@ -1606,13 +1676,17 @@ bool plan_gemm(int M, int N, int K, int kind, int num_sms, int force_splits, int
 }
 
 bool make_pair_plan(GemmPlan* p, int mode) {
-  if (!p->persistent || p->pair != 0 || (mode != 1 && mode != 2)) return false;
-  const int pairs_max = max_active_pairs(p->kind, p->smem_bytes);
+  if (!p->persistent || p->pair != 0 || mode < 1 || mode > 3) return false;
+  GemmPlan q = *p;
+  q.pair = mode;
+  // mode 3: a CTA's stage holds half the token tile (more stages fit)
+  if (mode == 3 && !finish_plan(&q)) return false;
+  const int pairs_max = max_active_pairs(q.kind, q.smem_bytes, mode);
   if (pairs_max <= 0) return false;
-  const int items = mode == 1 ? ((p->feat_tiles + 1) / 2) * p->token_tiles
-                              : p->feat_tiles * ((p->token_tiles + 1) / 2);
-  p->pair = mode;
-  p->grid_ctas = 2 * (items < pairs_max ? items : pairs_max);
+  const int items = mode == 2 ? q.feat_tiles * ((q.token_tiles + 1) / 2)
+                              : ((q.feat_tiles + 1) / 2) * q.token_tiles;
+  q.grid_ctas = 2 * (items < pairs_max ? items : pairs_max);
+  *p = q;
   return true;
 }
 
@@ -1649,10 +1723,10 @@ int plan_candidates(int M, int N, int K, int kind, int num_sms, GemmPlan* out, i
     }
     if (pick > 0 && plan_gemm(M, N, K, kind, num_sms, 1, pick, &c, true)) add(c);
   }
-  // the persistent candidates again in clusters of two with the token tile
-  // multicast (worth it when each CTA walks several tiles' operand traffic)
+  // the persistent candidates again in clusters of two: one two-CTA MMA per
+  // pair first, then the multicast pairings
   const int base = n;
-  for (int mode = 1; mode <= 2; ++mode)
+  for (int mode : {3, 1, 2})
     for (int i = 0; i < base && n < max_out; ++i) {
       GemmPlan pp = out[i];
       if (pp.persistent && make_pair_plan(&pp, mode)) out[n++] = pp;
@@ -1697,7 +1771,7 @@ bool make_tmap_geglu_il(CUtensorMap* m, const void* w, uint64_t N, uint64_t K) {
 
 cudaError_t launch_gemm(const GemmPlan& p, const GemmOperands& o, Launch l) {
   // the TMA box must match the shared-memory stage the plan reserves for it
-  if (o.x_box_rows != p.nt) return cudaErrorInvalidValue;
+  if (o.x_box_rows != p.x_box()) return cudaErrorInvalidValue;
   // split-K needs its workspace, 16-byte aligned
   if (p.splits > 1 && (o.partials == nullptr || o.partials_bytes < p.workspace_bytes ||
                        (reinterpret_cast<uintptr_t>(o.partials) & 15u) != 0))
@@ -1726,7 +1800,8 @@ cudaError_t gemm_node_retarget(cudaGraphExec_t exec, cudaGraphNode_t node, const
   if (e != cudaSuccess) return e;
   const void* split = reinterpret_cast<const void*>(&gemm_tc_kernel<kGemmResidual>);
   if ((p.func != split && p.func != persistent_ptr(kGemmResidual, 0) &&
-       p.func != persistent_ptr(kGemmResidual, 1) && p.func != persistent_ptr(kGemmResidual, 2)) ||
+       p.func != persistent_ptr(kGemmResidual, 1) && p.func != persistent_ptr(kGemmResidual, 2) &&
+       p.func != persistent_ptr(kGemmResidual, 3)) ||
       p.kernelParams == nullptr)
     return cudaErrorInvalidValue;
   // arguments: weight map, gate map, activation map, GemmArgs

@@ -114,13 +114,16 @@ struct GemmPlan {
   int stages = 0;        // pipeline depth
   bool persistent = false;  // one CTA per SM walks the tiles (splits == 1)
   int pair = 0;  // persistent CTAs in clusters of two sharing an operand tile by TMA multicast:
-                 // 1 the token tile (feature-tile pairs), 2 the weight tiles (token-tile pairs)
+                 // 1 the token tile (feature-tile pairs), 2 the weight tiles (token-tile pairs);
+                 // 3 one cta_group::2 MMA per feature-tile pair, each CTA loading half the tokens
   int grid_ctas = 0;     // persistent: CTAs launched
   size_t workspace_bytes = 0;  // split-K partial tiles (0 when splits == 1)
   int k_blocks = 0;      // K / 64
   uint32_t tmem_cols = 0;
   size_t smem_bytes = 0;
   int ctas() const { return persistent ? grid_ctas : feat_tiles * token_tiles * splits; }
+  // rows of the activation box a CTA loads per stage (pair 3: half the token tile)
+  int x_box() const { return pair == 3 ? nt / 2 : nt; }
 };
 
 // Chooses tile and split for an M x N x K projection; force_* > 0 override.
@@ -129,8 +132,9 @@ bool plan_gemm(int M, int N, int K, int kind, int num_sms, int force_splits, int
                GemmPlan* p, bool allow_persistent = true, double split_cost = 2.0);
 
 // A persistent plan run as clusters of two CTAs sharing an operand tile
-// (mode 1: the token tile; mode 2: the weight tiles); false if the device
-// cannot hold such clusters.
+// (mode 1: the token tile; mode 2: the weight tiles; mode 3: one two-CTA MMA
+// per pair of feature tiles, each CTA loading half of the token tile); false
+// if the device cannot hold such clusters.
 bool make_pair_plan(GemmPlan* p, int mode);
 
 // Distinct plans worth timing for one projection shape (at most max_out):
@@ -152,7 +156,7 @@ struct GemmOperands {
   CUtensorMap w;       // weights [N, K] (GeGLU: the GELU half; kGemmGegluIl: make_tmap_geglu_il)
   CUtensorMap w2;      // GeGLU gate half [N, K]; unused otherwise
   CUtensorMap x;       // activations [M, K], box rows = plan.nt
-  int x_box_rows = 0;  // the box height x was encoded with; launch_gemm checks it
+  int x_box_rows = 0;  // the box height x was encoded with (plan.x_box()); launch_gemm checks it
   bf16* y = nullptr;   // output [M, N]
   const bf16* residual = nullptr;
   float* y_f32 = nullptr;  // residual kind: fp32 output [M, N] in place of y (16-byte aligned)

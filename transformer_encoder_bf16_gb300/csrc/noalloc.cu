@@ -82,7 +82,7 @@ int laya_op_linear_noalloc(const void* x, int M, int K, const void* w, int N, in
     }
   }
   if (!ok) return LAYA_E_INVAL;
-  o.x_box_rows = p.nt;
+  o.x_box_rows = p.x_box();
   o.y = static_cast<laya::bf16*>(y);
   o.residual = static_cast<const laya::bf16*>(residual);
   if (p.workspace_bytes > 0) {

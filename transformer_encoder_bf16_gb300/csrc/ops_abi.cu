@@ -139,14 +139,14 @@ int laya_op_linear_ex(const void* x, int M, int K, const void* w, int N, int kin
                       int splits, int tile_tokens, int paired, void* stream) {
   if (!al16(x) || !al16(w) || !al16(y)) return LAYA_E_INVAL;
   if (kind == laya::kGemmResidual && !al16(residual)) return LAYA_E_INVAL;
-  if (paired < 0 || paired > 2 || (paired && splits != 1)) return LAYA_E_INVAL;
+  if (paired < 0 || paired > 3 || (paired && splits != 1)) return LAYA_E_INVAL;
   laya::GemmPlan p;
   if (!laya::plan_gemm(M, N, K, kind, laya::device_sm_count(), splits, tile_tokens, &p))
     return LAYA_E_INVAL;
   if (paired && !laya::make_pair_plan(&p, paired)) return LAYA_E_UNSUPPORTED;
   laya::GemmOperands o;
   const uint64_t ldk = static_cast<uint64_t>(K) * 2;
-  bool ok = laya::make_tmap_bf16_2d(&o.x, x, M, K, ldk, static_cast<uint32_t>(p.nt));
+  bool ok = laya::make_tmap_bf16_2d(&o.x, x, M, K, ldk, static_cast<uint32_t>(p.x_box()));
   if (kind == laya::kGemmGegluIl) {
     ok = ok && laya::make_tmap_geglu_il(&o.w, w, N, K);
     o.w2 = o.w;
@@ -160,7 +160,7 @@ int laya_op_linear_ex(const void* x, int M, int K, const void* w, int N, int kin
     }
   }
   if (!ok) return LAYA_E_INVAL;
-  o.x_box_rows = p.nt;
+  o.x_box_rows = p.x_box();
   o.y = static_cast<bf16*>(y);
   o.residual = static_cast<const bf16*>(residual);
   o.err = nullptr;
@@ -193,7 +193,7 @@ int laya_op_linear_ln(const void* x_raw, const void* gamma, float eps, int M, in
     o.w2 = o.w;
   }
   if (!ok) return LAYA_E_INVAL;
-  o.x_box_rows = p.nt;
+  o.x_box_rows = p.x_box();
   o.y = static_cast<bf16*>(y);
   o.residual = static_cast<const bf16*>(residual);
   o.ln_x = static_cast<const bf16*>(x_raw);
@@ -223,7 +223,7 @@ int laya_op_linear_rope(const void* x, int M, int K, const void* w, int N, const
       !laya::make_tmap_bf16_2d(&o.x, x, M, K, ldk, static_cast<uint32_t>(p.nt)))
     return LAYA_E_INVAL;
   o.w2 = o.w;
-  o.x_box_rows = p.nt;
+  o.x_box_rows = p.x_box();
   o.y = static_cast<bf16*>(y);
   o.rope_cos = cos_dev;
   o.rope_sin = sin_dev;
