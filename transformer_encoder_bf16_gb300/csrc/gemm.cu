@@ -906,7 +906,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(accf0 + 8u * b, 1);
-      ptx::mbar_init(acce0 + 8u * b, TWO ? 2 * kPEpi : kPEpi);  // TWO: both CTAs' epilogues
+      // every epilogue thread arrives (TWO: both CTAs')
+      ptx::mbar_init(acce0 + 8u * b, (TWO ? 2 : 1) * kPEpi);
     }
     ptx::mbar_init(done_bar, 1);
     *abort_flag = 0;
@@ -1242,7 +1243,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
     } else {
       // ------------------------------------------------ epilogue (direct)
-      // The two warps of a TMEM lane quarter take alternate blocks of 16 token
+      // The two warps of a TMEM lane quarter take alternate blocks of token
       // columns.
       const int q = warp & 3;
       const int half = (warp - 2) >> 2;
@@ -1267,7 +1268,39 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const int f = KIND == kGemmGegluIl ? ft * 64 + (lrow >> 5) * 16 + (lrow & 15) : ft * kBM + lrow;
         const bool f_ok = f < a.N;
         unsigned short* yb = reinterpret_cast<unsigned short*>(a.y);
-        for (int c = 16 * half; c < a.nt; c += 32) {
+        // GeGLU-il, 16 token columns from t0: lanes l < 16 hold the GELU half,
+        // l + 16 the gate half of the same feature; the lower lanes finish
+        // even tokens, the upper odd ones
+        auto il16 = [&](const float* v, int t0) {
+          float o[16];
+  #pragma unroll
+          for (int j = 0; j < 16; ++j) o[j] = __shfl_xor_sync(0xffffffffu, v[j], 16);
+  #pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const float h = upper ? o[2 * jj + 1] : v[2 * jj];
+            const float gt = upper ? v[2 * jj + 1] : o[2 * jj];
+            const int t = t0 + 2 * jj + (upper ? 1 : 0);
+            const float val = gelu_erf(h) * gt;
+            if (t < Meff && f_ok)
+              yb[static_cast<size_t>(t) * a.N + f] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+          }
+        };
+        int c_first = 16 * half;
+        if (KIND == kGemmGegluIl) {
+          // whole blocks of 64 columns in one TMEM load each (one wait per 64
+          // columns instead of per 16: the load latency under the main loop's
+          // TMEM traffic is what bounds this epilogue); the two warps of a
+          // lane quarter alternate blocks, the last partial block goes 16 by 16
+          const int full64 = a.nt / 64;
+          for (int blk = half; blk < full64; blk += 2) {
+            float v64[64];
+            ptx::tmem_ld64(tq + blk * 64, v64);
+  #pragma unroll
+            for (int g4 = 0; g4 < 4; ++g4) il16(v64 + 16 * g4, tt * a.nt + blk * 64 + 16 * g4);
+          }
+          c_first = full64 * 64 + 16 * half;
+        }
+        for (int c = c_first; c < a.nt; c += 32) {
           const int t0 = tt * a.nt + c;
           float v[16];
           if (NA == 2) {
@@ -1281,21 +1314,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 yb[static_cast<size_t>(t) * a.N + f] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
             }
           } else {
-            // lanes l < 16 hold the GELU half, l + 16 the gate half of the same
-            // feature: the lower lanes finish even tokens, the upper odd ones
             ptx::tmem_ld16(tq + c, v);
-            float o[16];
-  #pragma unroll
-            for (int j = 0; j < 16; ++j) o[j] = __shfl_xor_sync(0xffffffffu, v[j], 16);
-  #pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-              const float h = upper ? o[2 * jj + 1] : v[2 * jj];
-              const float gt = upper ? v[2 * jj + 1] : o[2 * jj];
-              const int t = t0 + 2 * jj + (upper ? 1 : 0);
-              const float val = gelu_erf(h) * gt;
-              if (t < Meff && f_ok)
-                yb[static_cast<size_t>(t) * a.N + f] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
-            }
+            il16(v, t0);
           }
         }
         // every TMEM read of this tile by this thread is complete: its share
