@@ -472,6 +472,31 @@ def run_op(args):
 
     valid = int(np.sum(lengths))
     M = valid if B > 1 else B * S   # the forward packs the tokens of several rows
+    if args.op == "forward":
+        ids, _ = synth.make_inputs(model, B, S, seed, lr)
+        enc = te.Encoder(model, te.upload_weights(synth.make_weights(model, seed)))
+        out = torch.empty((B, S, H), dtype=torch.bfloat16, device="cuda")
+        ids_dev, len_dev = torch.from_numpy(ids).cuda(), torch.from_numpy(lengths).cuda()
+        stream = torch.cuda.current_stream()
+        for _ in range(args.warmup):   # the first run also times the candidate plans
+            enc.run_device(ids_dev, len_dev, out, stream)
+        enc.check(stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.nvtx.range_push("laya_forward")
+        e0.record()
+        for _ in range(args.steps):
+            enc.run_device(ids_dev, len_dev, out, stream)
+        e1.record()
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize()
+        enc.check(stream)
+        us = e0.elapsed_time(e1) / args.steps * 1000
+        print(json.dumps({"op": "forward", "workload": args.workload, "us_per_forward": us,
+                          "launches_per_forward": enc.launch_count(B, S),
+                          "tokens_per_s": valid / us * 1e6}))
+        enc.close()
+        return
     if args.op == "layernorm":
         x, g = dev_bits((M, H)), dev_bits((H,), 0.02, 1.0)
         y = torch.empty_like(x)
@@ -518,8 +543,10 @@ def main():
                     help="time the headline workload only")
     ap.add_argument("--per-config-steps", type=int, default=50)
     ap.add_argument("--reference-budget", type=float, default=150.0)
-    ap.add_argument("--op", choices=["layernorm", "rope", "attention", "attention_local"],
-                    help="time one step kernel alone at the workload's sizes instead")
+    ap.add_argument("--op", choices=["layernorm", "rope", "attention", "attention_local", "forward"],
+                    help="time one step kernel alone at the workload's sizes instead (forward: "
+                         "the whole forward only, its timed steps inside the NVTX range "
+                         "laya_forward, for ncu --nvtx --nvtx-include laya_forward/)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.op:
