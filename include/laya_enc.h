@@ -130,8 +130,11 @@ int laya_enc_create(const laya_enc_config* cfg, const laya_enc_weights* weights,
  * finite values of no meaning.  The host arrays are copied into library-owned
  * pinned memory before the call returns and may be reused at once.  The call
  * is asynchronous; synchronise `stream` before reading out_hidden.
- * The first call of a (batch, seq) shape allocates its workspace, runs two
- * eager warm-up passes and captures a CUDA Graph (unless graphs are off); later
+ * The first call of a (batch, seq) shape allocates its workspace, times the
+ * candidate plans of each projection once per process (unless env
+ * LAYA_NO_TUNE=1; env LAYA_PLAN_CACHE=<file> keeps the chosen plans in a text
+ * file that later processes read instead of timing again), runs two eager
+ * warm-up passes and captures a CUDA Graph (unless graphs are off); later
  * calls replay it.  If `stream` is itself capturing, the kernels are launched
  * into the caller's capture instead. */
 int laya_enc_run(laya_enc_handle* h, const int32_t* token_ids,

@@ -29,6 +29,7 @@
 #include <chrono>
 #include <cstdlib>
 #include <cstring>
+#include <fstream>
 #include <map>
 #include <mutex>
 #include <new>
@@ -544,6 +545,41 @@ bool build_activation_maps(const laya_enc_handle* h, Workspace* w) {
 std::mutex g_tuned_mu;
 std::map<std::tuple<int, int, int, int, int>, std::tuple<int, int, int, int>> g_tuned;
 
+// The choices can also live in a text file named by the environment variable
+// LAYA_PLAN_CACHE (one line per shape: M N K kind rows, then token tile,
+// split-K, pairing, kind run), read once per process before the first
+// tuning and rewritten after every tuning that adds a shape: a second
+// process (a profiler's run, say, whose timings would differ) then runs the
+// plans the first one chose.  A line whose plan is not among a shape's
+// candidates is ignored (the model's plan runs, untimed).
+const char* plan_cache_path() {
+  const char* p = std::getenv("LAYA_PLAN_CACHE");
+  return (p != nullptr && p[0] != '\0') ? p : nullptr;
+}
+
+void load_plan_cache() {  // with g_tuned_mu held
+  static bool loaded = false;
+  if (loaded) return;
+  loaded = true;
+  const char* path = plan_cache_path();
+  if (path == nullptr) return;
+  std::ifstream in(path);
+  int M, N, K, kind, rows, nt, splits, pair, krun;
+  while (in >> M >> N >> K >> kind >> rows >> nt >> splits >> pair >> krun)
+    g_tuned.emplace(std::make_tuple(M, N, K, kind, rows), std::make_tuple(nt, splits, pair, krun));
+}
+
+void save_plan_cache() {  // with g_tuned_mu held
+  const char* path = plan_cache_path();
+  if (path == nullptr) return;
+  std::ofstream out(path, std::ios::trunc);
+  for (const auto& e : g_tuned)
+    out << std::get<0>(e.first) << ' ' << std::get<1>(e.first) << ' ' << std::get<2>(e.first)
+        << ' ' << std::get<3>(e.first) << ' ' << std::get<4>(e.first) << ' '
+        << std::get<0>(e.second) << ' ' << std::get<1>(e.second) << ' ' << std::get<2>(e.second)
+        << ' ' << std::get<3>(e.second) << '\n';
+}
+
 // Times the candidate plans of each projection on the first run of a shape,
 // on `stream` after that run's input upload (the packed row lengths are real,
 // the activations are the workspace's), and keeps the fastest; the model's
@@ -566,6 +602,7 @@ int tune_plans(laya_enc_handle* h, Workspace* w, cudaStream_t stream) {
     const auto key = std::make_tuple(slot->M, slot->N, slot->K, slot->kind, marker_or_b(w, g));
     {
       std::lock_guard<std::mutex> lk(g_tuned_mu);
+      load_plan_cache();
       auto it = g_tuned.find(key);
       if (it != g_tuned.end()) {
         for (int k = 0; k < w->ncand[g]; ++k)
@@ -650,6 +687,7 @@ int tune_plans(laya_enc_handle* h, Workspace* w, cudaStream_t stream) {
     *slot = w->cand[g][best];
     std::lock_guard<std::mutex> lk(g_tuned_mu);
     g_tuned.emplace(key, std::make_tuple(slot->nt, slot->splits, slot->pair, slot->kind));
+    save_plan_cache();
   }
   if (e0) cudaEventDestroy(e0);
   if (e1) cudaEventDestroy(e1);
