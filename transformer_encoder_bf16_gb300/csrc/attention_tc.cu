@@ -10,16 +10,18 @@
 // "Test Result" (queries whose visible keys are all padding: context 0 here).
 //
 // One CTA per (128-query tile, head, row); keys in tiles of 128.  Roles:
-//   warp 0     TMA: the Q tile once, each K tile into one buffer (free as soon
-//              as its Q K^T is done), V tiles into a two-stage ring;
+//   warp 0     TMA: the Q tile once, K tiles into a two-stage ring (the next
+//              K tile loads while Q K^T of the current one runs), V tiles into
+//              a two-stage ring;
 //   warp 1     owns TMEM; one thread issues S_j = Q K_j^T (tcgen05.mma, fp32
 //              in TMEM) as soon as the softmax has read S_{j-1}, and
-//              O += P_j V_j into an fp32 accumulator in TMEM (V as an MN-major
-//              operand: its [keys][64 dims] tile is already that layout);
+//              O += P_j V_j into an fp32 accumulator in TMEM, with P_j read
+//              from TMEM as the A operand (V as an MN-major operand: its
+//              [keys][64 dims] tile is already that layout);
 //   warps 2-5  softmax, one thread per query row (its TMEM lane): the 128
 //              scores of S_j in one TMEM load, mask, running maximum, P_j =
-//              2^(s - m) rounded to BF16 into shared memory (128-byte swizzled
-//              K-major layout), fp32 row sum.
+//              2^(s - m) rounded to BF16 and stored into TMEM (one row per
+//              lane, two keys per 32-bit column), fp32 row sum.
 // The QK^T of tile j + 1 runs on the tensor cores while the softmax of tile j
 // runs.  The maximum the exponents use is raised only when a row's running
 // maximum exceeds it by more than 8 (log2 units), and only then is that row of
@@ -28,9 +30,9 @@
 // probabilities below 2^8 before normalisation.  P is rounded to BF16 for the
 // P V product (the row sums are not).
 //
-// Shared memory (96 KB) and TMEM (256 columns: S 128, O 64) are sized so that
-// two CTAs share an SM: one CTA's softmax overlaps the other's loads and
-// products, and its start-up the other's tail.
+// Shared memory (80 KB) and TMEM (256 columns: S 128, O 64, P 64) are sized
+// so that two CTAs share an SM: one CTA's softmax overlaps the other's loads
+// and products, and its start-up the other's tail.
 //
 // Local layers visit the key tiles of [q0 - w, q0 + 128 + w) inside the row
 // (two tiles when w <= 64); global layers the tiles below len.  Query rows
@@ -52,32 +54,32 @@ constexpr int kThreads = 192;
 constexpr int kQT = 128;                 // queries per CTA (MMA M)
 constexpr int kKT = 128;                 // keys per tile (MMA N of Q K^T)
 constexpr uint32_t kTile = 128u * 128u;  // bytes of a [128 x 64] BF16 tile
-// shared memory (1024-byte aligned): Q | K | V[2] | P (two 64-key halves) | barriers
+// shared memory (1024-byte aligned): Q | K[2] | V[2] | barriers
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kTile;
-constexpr uint32_t kOffV = kOffK + kTile;
-constexpr uint32_t kOffP = kOffV + 2 * kTile;
-constexpr uint32_t kOffBar = kOffP + 2 * kTile;
+constexpr uint32_t kOffV = kOffK + 2 * kTile;
+constexpr uint32_t kOffBar = kOffV + 2 * kTile;
 constexpr uint32_t kSmem = kOffBar + 256 + 1024;  // + alignment slack
-// TMEM: S at columns [0, 128), O at [128, 192)
+// TMEM: S at columns [0, 128), O at [128, 192), P (BF16 pairs) at [192, 256)
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColO = 128;
+constexpr uint32_t kColP = 192;
 // the maximum the exponents use is raised only beyond this margin (log2)
 constexpr float kRescaleMargin = 8.f;
 
 // Barrier slots (8 bytes each) from kOffBar.
 enum : uint32_t {
   kBarQ = 0,
-  kBarKFull = 1,
-  kBarKEmpty = 2,
-  kBarVFull = 3,   // + b
-  kBarVEmpty = 5,  // + b
-  kBarSFull = 7,
-  kBarSEmpty = 8,
-  kBarPFull = 9,
-  kBarPvDone = 10,  // P_j V_j has completed: P may be rewritten, O read or rescaled
-  kBarDone = 11,    // every MMA of the CTA has completed
-  kBarCount = 12
+  kBarKFull = 1,   // + b
+  kBarKEmpty = 3,  // + b
+  kBarVFull = 5,   // + b
+  kBarVEmpty = 7,  // + b
+  kBarSFull = 9,
+  kBarSEmpty = 10,
+  kBarPFull = 11,
+  kBarPvDone = 12,  // P_j V_j has completed: P may be rewritten, O read or rescaled
+  kBarDone = 13,    // every MMA of the CTA has completed
+  kBarCount = 14
 };
 
 // Descriptor of a V tile as an MN-major operand (the 64 dims contiguous, keys
@@ -94,6 +96,13 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float m;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
+  return m;
 }
 
 struct AttnArgs {
@@ -180,13 +189,13 @@ __global__ void __launch_bounds__(kThreads, 2)
       int k_issued = 0, v_issued = 0;
       for (int j = 0; j < nk; ++j) {
         const int krow = row0 + kbase + j * kKT;
-        if (j >= 1 && !ptx::mbar_wait(bar(kBarKEmpty), (j - 1) & 1, abort_flag, a.err,
+        const int s = j & 1;
+        if (j >= 2 && !ptx::mbar_wait(bar(kBarKEmpty + s), ((j >> 1) - 1) & 1, abort_flag, a.err,
                                       kDevWaitEmpty, kWaitLimitNs))
           break;
-        ptx::mbar_arrive_expect_tx(bar(kBarKFull), kTile);
-        ptx::tma_load_2d(sb + kOffK, &tm_qkv, bar(kBarKFull), H + n * 64, krow, pol);
+        ptx::mbar_arrive_expect_tx(bar(kBarKFull + s), kTile);
+        ptx::tma_load_2d(sb + kOffK + s * kTile, &tm_qkv, bar(kBarKFull + s), H + n * 64, krow, pol);
         k_issued = j + 1;
-        const int s = j & 1;
         if (j >= 2 && !ptx::mbar_wait(bar(kBarVEmpty + s), ((j >> 1) - 1) & 1, abort_flag, a.err,
                                       kDevWaitEmpty, kWaitLimitNs))
           break;
@@ -199,8 +208,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       // our own, so that an abort does not cut these waits short)
       volatile int drain = 0;
       ptx::mbar_wait(bar(kBarQ), 0, &drain, nullptr, 0, kWaitLimitNs);
-      if (k_issued > 0)
-        ptx::mbar_wait(bar(kBarKFull), (k_issued - 1) & 1, &drain, nullptr, 0, kWaitLimitNs);
+      for (int j = k_issued > 2 ? k_issued - 2 : 0; j < k_issued; ++j)
+        ptx::mbar_wait(bar(kBarKFull + (j & 1)), (j >> 1) & 1, &drain, nullptr, 0, kWaitLimitNs);
       for (int j = v_issued > 2 ? v_issued - 2 : 0; j < v_issued; ++j)
         ptx::mbar_wait(bar(kBarVFull + (j & 1)), (j >> 1) & 1, &drain, nullptr, 0, kWaitLimitNs);
     }
@@ -217,17 +226,18 @@ __global__ void __launch_bounds__(kThreads, 2)
           return false;
         ptx::tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          ptx::mma_bf16(tmem + kColO, ptx::sdesc_sw128(sb + kOffP + (kk >> 2) * kTile + (kk & 3) * 32),
-                        sdesc_sw128_mn(sb + kOffV + s * kTile + kk * 2048), idesc_o,
-                        (t > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk)  // keys 16 kk ..: P columns 8 kk .. (two keys a column)
+          ptx::mma_bf16_ta(tmem + kColO, tmem + kColP + 8 * kk,
+                           sdesc_sw128_mn(sb + kOffV + s * kTile + kk * 2048), idesc_o,
+                           (t > 0 || kk > 0) ? 1u : 0u);
         ptx::mma_commit(bar(kBarPvDone));
         ptx::mma_commit(bar(kBarVEmpty + s));
         return true;
       };
       bool ok = ptx::mbar_wait(bar(kBarQ), 0, abort_flag, a.err, kDevWaitFull, kWaitLimitNs);
       for (int j = 0; j < nk && ok; ++j) {
-        ok = ptx::mbar_wait(bar(kBarKFull), j & 1, abort_flag, a.err, kDevWaitFull, kWaitLimitNs);
+        ok = ptx::mbar_wait(bar(kBarKFull + (j & 1)), (j >> 1) & 1, abort_flag, a.err, kDevWaitFull,
+                            kWaitLimitNs);
         // S is single-buffered: the softmax must have read S_{j-1}
         if (ok && j >= 1)
           ok = ptx::mbar_wait(bar(kBarSEmpty), (j - 1) & 1, abort_flag, a.err, kDevWaitAccum,
@@ -237,9 +247,10 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           ptx::mma_bf16(tmem, ptx::sdesc_sw128(sb + kOffQ + kk * 32),
-                        ptx::sdesc_sw128(sb + kOffK + kk * 32), idesc_s, kk > 0 ? 1u : 0u);
+                        ptx::sdesc_sw128(sb + kOffK + (j & 1) * kTile + kk * 32), idesc_s,
+                        kk > 0 ? 1u : 0u);
         ptx::mma_commit(bar(kBarSFull));
-        ptx::mma_commit(bar(kBarKEmpty));
+        ptx::mma_commit(bar(kBarKEmpty + (j & 1)));
         if (j >= 1) ok = issue_pv(j - 1);
       }
       if (ok) issue_pv(nk - 1);
@@ -285,14 +296,17 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int c = 0; c < kKT; ++c)
           if (static_cast<uint32_t>(c - lo) >= span) sc[c] = -INFINITY;
       }
+      // row maximum with three-input max: eight independent accumulators
       float mxa[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mxa[k] = sc[k];
+      for (int k = 0; k < 8; ++k) mxa[k] = fmaxf(sc[k], sc[k + 8]);
 #pragma unroll
-      for (int c = 8; c < kKT; ++c) mxa[c & 7] = fmaxf(mxa[c & 7], sc[c]);
+      for (int c = 16; c < kKT; c += 16)
 #pragma unroll
-      for (int k = 0; k < 4; ++k) mxa[k] = fmaxf(mxa[k], mxa[k + 4]);
-      const float mx = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])) * scale_log2;
+        for (int k = 0; k < 8; ++k) mxa[k] = fmax3(mxa[k], sc[c + k], sc[c + 8 + k]);
+      const float mx =
+          fmax3(fmax3(mxa[0], mxa[1], mxa[2]), fmax3(mxa[3], mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])) *
+          scale_log2;
       // raise the exponents' maximum only when the row has gone beyond it by
       // the margin (or had none): then O and l are rescaled to the new one
       float alpha = 1.f;
@@ -310,23 +324,21 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         ptx::tc_fence_after();
       }
-      // P row: keys [0, 64) in half 0, [64, 128) in half 1; 16-byte chunk c
-      // of row r sits at chunk c ^ (r % 8)
-      uint8_t* prow = smem + kOffP + static_cast<uint32_t>(row) * 128u;
+      // the P row into TMEM: keys 2c and 2c + 1 as the BF16 pair of column c,
+      // in two halves of 32 columns
       float lsa[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c8 = 0; c8 < kKT / 8; ++c8) {
-        uint4 pk;
-        __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&pk);
+      for (int h2 = 0; h2 < 2; ++h2) {
+        float pk[32];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = ex2(fmaf(sc[c8 * 8 + 2 * e], scale_log2, -mu));
-          const float p1 = ex2(fmaf(sc[c8 * 8 + 2 * e + 1], scale_log2, -mu));
-          lsa[e] += p0 + p1;
-          p2[e] = __floats2bfloat162_rn(p0, p1);
+        for (int c = 0; c < 32; ++c) {
+          const float p0 = ex2(fmaf(sc[64 * h2 + 2 * c], scale_log2, -mu));
+          const float p1 = ex2(fmaf(sc[64 * h2 + 2 * c + 1], scale_log2, -mu));
+          lsa[c & 3] += p0 + p1;
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+          pk[c] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&b2));
         }
-        const int half = c8 >> 3, ch = c8 & 7;
-        *reinterpret_cast<uint4*>(prow + half * kTile + ((ch ^ (row & 7)) << 4)) = pk;
+        ptx::tmem_st32(lane_base + kColP + 32 * h2, pk);
       }
       l = l * alpha + ((lsa[0] + lsa[1]) + (lsa[2] + lsa[3]));
       // the scores are dead by now: rescale this warp's rows of O if any moved
@@ -337,7 +349,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int d = 0; d < 64; ++d) ov[d] *= alpha;
         ptx::tmem_st64(lane_base + kColO, ov);
       }
-      ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar(kBarPFull));

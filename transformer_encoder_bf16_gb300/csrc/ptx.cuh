@@ -306,6 +306,20 @@ __device__ __forceinline__ void mma_bf16_cg2(uint32_t d_tmem, uint64_t a_desc, u
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T, BF16, fp32 accumulate, one CTA: A (M rows
+// in TMEM lanes, two BF16 of K per 32-bit column) read from tensor memory.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      " .reg .pred p;\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive on the barrier at `bar`'s offset in every CTA of `mask` once this
 // thread's earlier cta_group::2 MMAs have completed.
 __device__ __forceinline__ void mma_commit_cg2_mc(uint32_t bar, uint16_t mask) {
@@ -429,6 +443,49 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
       : "memory");
 #pragma unroll
   for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Store 32 consecutive 32-bit columns into this warp's 32 TMEM lanes (one
+// lane per thread) and wait until the stores have completed.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n"
+      "tcgen05.wait::st.sync.aligned;\n"
+      :
+      : "r"(taddr),
+        "r"(__float_as_uint(v[0])),
+        "r"(__float_as_uint(v[1])),
+        "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])),
+        "r"(__float_as_uint(v[4])),
+        "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])),
+        "r"(__float_as_uint(v[7])),
+        "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])),
+        "r"(__float_as_uint(v[10])),
+        "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])),
+        "r"(__float_as_uint(v[13])),
+        "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])),
+        "r"(__float_as_uint(v[16])),
+        "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])),
+        "r"(__float_as_uint(v[19])),
+        "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])),
+        "r"(__float_as_uint(v[22])),
+        "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])),
+        "r"(__float_as_uint(v[25])),
+        "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])),
+        "r"(__float_as_uint(v[28])),
+        "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])),
+        "r"(__float_as_uint(v[31]))
+      : "memory");
 }
 
 // Store 64 consecutive fp32 columns into this warp's 32 TMEM lanes (one lane
