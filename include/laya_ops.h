@@ -176,9 +176,8 @@ int laya_op_linear_workspace_size(int M, int K, int N, int kind, int splits,
  * x_raw [M, K] and computes h = bf16(LN(x_raw) * gamma) in shared memory with
  * exactly the arithmetic of laya_op_layernorm, so y equals laya_op_layernorm
  * followed by laya_op_linear bit for bit; kinds as laya_op_linear.  The
- * split-K kernel is used (short sequences: laya_enc_run folds the attention
- * and MLP norms this way when its plan for the shape is split-K).  K a
- * multiple of 256, at most 2048.  Sources: as laya_op_layernorm and
+ * split-K kernel is used (laya_enc_run launches its norms as separate
+ * kernels).  K a multiple of 256, at most 2048.  Sources: as laya_op_layernorm and
  * laya_op_linear. */
 int laya_op_linear_ln(const void* x_raw, const void* gamma, float eps, int M,
                       int K, const void* w, int N, int kind,

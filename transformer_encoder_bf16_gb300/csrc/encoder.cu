@@ -7,13 +7,12 @@
 //   for each of the n_enc encoder and n_dec decision layers l:
 //     if l == n_enc and final_norm:  x = LN_final(x)
 //     h   = (l == 0 and first_attn_norm_identity) ? x : LN_attn(x)
-//           (short sequences: the QKV GEMM normalises x on load instead)
 //     qkv = RoPE(h Wqkv^T)            GEMM, plain epilogue with RoPE on q and k
 //                                     (RoPE of q and k in the same epilogue: global table
 //                                     iff decision layer or l % global_every == 0)
 //     ctx = attention(qkv, lengths)   sliding window on local layers
 //     x   = x + ctx Wo^T              GEMM, residual epilogue (in place)
-//     h   = LN_mlp(x)                  (short sequences: folded into the up GEMM)
+//     h   = LN_mlp(x)
 //     g   = gelu(h Wup_in^T) * (h Wup_gate^T)   GEMM, GeGLU epilogue
 //     x   = x + g Wdown^T             GEMM, residual epilogue (last layer: into out)
 // Sources: "Run Laya encoder and decision layers on CUDA" ("Purpose",
