@@ -494,7 +494,8 @@ def run_op(args):
         us = e0.elapsed_time(e1) / args.steps * 1000
         print(json.dumps({"op": "forward", "workload": args.workload, "us_per_forward": us,
                           "launches_per_forward": enc.launch_count(B, S),
-                          "tokens_per_s": valid / us * 1e6}))
+                          "tokens_per_s": valid / us * 1e6,
+                          "gemm_plans": {k: list(v) for k, v in enc.plans(B, S).items()}}))
         enc.close()
         return
     if args.op == "layernorm":

@@ -133,7 +133,7 @@ int laya_op_attention_rope(const void* qkv, const int32_t* lengths_dev,
  *                    of 64, unsplit plans only (splits <= 1)
  * K a multiple of 64; N a multiple of 8.  splits <= 0 and tile_tokens <= 0
  * pick the library's plan; positive values force them (tile_tokens a multiple
- * of 16, at most 256; splits at most 8 and at most K/64).  workspace: device
+ * of 16, at most 256; splits at most 16 and at most K/64).  workspace: device
  * scratch of at least laya_op_linear_workspace_size() bytes, 16-byte aligned,
  * caller-owned (NULL allowed when that size is 0): split-K writes its fp32
  * partial tiles there and the CTAs of each cluster sum them in split order,

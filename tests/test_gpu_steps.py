@@ -42,7 +42,8 @@ def test_linear_exact_integers(M, N, K, splits, nt):
 @pytest.mark.parametrize("M,N,K,splits,nt", [
     (48, 3072, 1024, 0, 0), (48, 1024, 2624, 0, 0), (1, 2624, 1024, 0, 0), (256, 1024, 1024, 0, 0),
     (464, 1024, 1024, 3, 0), (600, 640, 256, 1, 128), (130, 2624, 1024, 2, 48),
-    (1200, 3072, 1024, 1, 0), (1000, 1024, 2624, 1, 112)])
+    (1200, 3072, 1024, 1, 0), (1000, 1024, 2624, 1, 112), (48, 1024, 2624, 16, 48),
+    (48, 1024, 1024, 12, 48), (100, 640, 1024, 16, 64)])
 def test_linear_matches_oracle(kind, M, N, K, splits, nt):
     torch = require_gpu()
     rng = np.random.default_rng(1000 + M + N + K + kind)
@@ -299,6 +300,8 @@ def test_attention_with_fused_rope_matches_oracle(B, S, heads, lengths, glob, th
 @pytest.mark.parametrize("B,S,splits,nt,theta", [
     (1, 48, 0, 0, 160000.0),        # library plan (split-K clusters at 48 tokens)
     (4, 64, 4, 64, 10000.0),        # forced split-K
+    (1, 48, 16, 48, 10000.0),       # split-K cluster of 16 (RoPE tiles: some ranks reduce nothing)
+    (1, 48, 12, 48, 160000.0),      # uneven slices
     (2, 300, 1, 112, 10000.0),      # persistent kernel, several tiles per CTA
     (16, 512, 0, 0, 160000.0),      # library plan at 8192 tokens
 ])
@@ -325,7 +328,7 @@ def test_qkv_with_rope_epilogue_bit_exact(B, S, splits, nt, theta):
 
 @pytest.mark.parametrize("kind", [te.KIND_PLAIN, te.KIND_GEGLU])
 @pytest.mark.parametrize("M,N,splits,nt", [(48, 3072, 4, 48), (48, 2624, 6, 48), (256, 1024, 2, 128),
-                                           (100, 640, 3, 112), (48, 1024, 1, 48)])
+                                           (100, 640, 3, 112), (48, 1024, 1, 48), (48, 1024, 16, 48)])
 def test_linear_with_layernorm_on_load_bit_exact(kind, M, N, splits, nt):
     # the GEMM normalising its input tiles on load equals the LayerNorm kernel
     # followed by the same GEMM plan, byte for byte

@@ -81,7 +81,7 @@ def test_linear_plan_invariants(lib, M, N, K, kind):
         assert nt % 16 == 0 and 16 <= nt <= 256
         tiles_t = -(-M // nt)
         assert tiles_t * nt >= M and (tiles_t - 1) * nt < M
-        assert 1 <= splits <= min(8, K // 64)
+        assert 1 <= splits <= min(16, K // 64)
         tiles = tiles_t * -(-N // 128)
         if splits == 1:
             assert ctas == min(tiles, sms)             # persistent: one CTA per SM walks the tiles

@@ -63,7 +63,7 @@ constexpr int kThreads = 192;
 constexpr int kBM = 128;                 // features per tile
 constexpr int kBK = 64;                  // K per stage: one 128-byte swizzle row of BF16
 constexpr uint32_t kATileBytes = kBM * kBK * 2;
-constexpr int kMaxSplits = 8;            // portable cluster size
+constexpr int kMaxSplits = 16;           // split-K cluster size (above 8: non-portable, opted in)
 constexpr size_t kSmemLimit = 227 * 1024;
 constexpr size_t kCtrlBytes = 256;
 constexpr size_t kLnStatsBytes = 256 * 8;  // [nt <= 256][mean, rstd] for LayerNorm on load
@@ -1487,9 +1487,14 @@ cudaError_t configure_kernels() {
   std::call_once(once, [] {
     status = cudaSuccess;
     for (int k = kGemmPlain; k <= kGemmGegluIl && status == cudaSuccess; ++k) {
-      if (k <= kGemmGeglu)
+      if (k <= kGemmGeglu) {
         status = cudaFuncSetAttribute(kernel_ptr(k), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(kSmemLimit));
+        // split-K clusters of up to 16 CTAs (the portable limit is 8)
+        if (status == cudaSuccess)
+          status = cudaFuncSetAttribute(kernel_ptr(k),
+                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      }
       for (int pair = 0; pair < 4 && status == cudaSuccess; ++pair)
         status = cudaFuncSetAttribute(persistent_ptr(k, pair),
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
