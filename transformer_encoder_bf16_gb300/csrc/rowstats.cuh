@@ -36,20 +36,24 @@ __device__ __forceinline__ void row_stats(const uint4* row, int lane, float eps,
                                           float& mean, float& rstd) {
 #pragma unroll
   for (int c = 0; c < V; ++c) bf16x8_to_f32(row[lane + 32 * c], v[c]);
-  float s = 0.f;
+  // four independent partial sums per lane (short dependency chains), added
+  // in a fixed order, then across the warp
+  float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int c = 0; c < V; ++c)
 #pragma unroll
-    for (int i = 0; i < 8; ++i) s = __fadd_rn(s, v[c][i]);
+    for (int i = 0; i < 8; ++i) s4[i & 3] = __fadd_rn(s4[i & 3], v[c][i]);
+  const float s = __fadd_rn(__fadd_rn(s4[0], s4[1]), __fadd_rn(s4[2], s4[3]));
   mean = __fdiv_rn(warp_allsum(s), static_cast<float>(256 * V));
-  float q = 0.f;
+  float q4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int c = 0; c < V; ++c)
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const float d = __fsub_rn(v[c][i], mean);
-      q = __fadd_rn(q, __fmul_rn(d, d));
+      q4[i & 3] = __fadd_rn(q4[i & 3], __fmul_rn(d, d));
     }
+  const float q = __fadd_rn(__fadd_rn(q4[0], q4[1]), __fadd_rn(q4[2], q4[3]));
   const float var = __fdiv_rn(warp_allsum(q), static_cast<float>(256 * V));
   rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, eps)));
 }
