@@ -133,7 +133,10 @@ int laya_enc_create(const laya_enc_config* cfg, const laya_enc_weights* weights,
  * The first call of a (batch, seq) shape allocates its workspace, times the
  * candidate plans of each projection once per process (unless env
  * LAYA_NO_TUNE=1; env LAYA_PLAN_CACHE=<file> keeps the chosen plans in a text
- * file that later processes read instead of timing again), runs two eager
+ * file that later processes read instead of timing again; the file is not
+ * locked: processes sharing one file at the same time may each time a shape,
+ * the last writer's lines stand, and reading stops at the first line that
+ * does not parse), runs two eager
  * warm-up passes and captures a CUDA Graph (unless graphs are off); later
  * calls replay it.  If `stream` is itself capturing, the kernels are launched
  * into the caller's capture instead. */
