@@ -105,6 +105,22 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return m;
 }
 
+// Two fp32 lanes in one instruction (sm_100 f32x2 arithmetic).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n"
+      " .reg .b64 ra, rb, rc, rd;\n"
+      " mov.b64 ra, {%2, %3};\n"
+      " mov.b64 rb, {%4, %5};\n"
+      " mov.b64 rc, {%6, %7};\n"
+      " fma.rn.f32x2 rd, ra, rb, rc;\n"
+      " mov.b64 {%0, %1}, rd;\n"
+      "}\n"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
 struct AttnArgs {
   const int32_t* lengths;
   int S, heads, global, half_window, packed;
@@ -325,15 +341,18 @@ __global__ void __launch_bounds__(kThreads, 2)
         ptx::tc_fence_after();
       }
       // the P row into TMEM: keys 2c and 2c + 1 as the BF16 pair of column c,
-      // in two halves of 32 columns
+      // in two halves of 32 columns; exponents' arguments and the row sum two
+      // keys per instruction
       float lsa[4] = {0.f, 0.f, 0.f, 0.f};
+      const float2 sc2 = make_float2(scale_log2, scale_log2);
+      const float2 nmu2 = make_float2(-mu, -mu);
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
         float pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          const float p0 = ex2(fmaf(sc[64 * h2 + 2 * c], scale_log2, -mu));
-          const float p1 = ex2(fmaf(sc[64 * h2 + 2 * c + 1], scale_log2, -mu));
+          const float2 x = ffma2(make_float2(sc[64 * h2 + 2 * c], sc[64 * h2 + 2 * c + 1]), sc2, nmu2);
+          const float p0 = ex2(x.x), p1 = ex2(x.y);
           lsa[c & 3] += p0 + p1;
           const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
           pk[c] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&b2));
