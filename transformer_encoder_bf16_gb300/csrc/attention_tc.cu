@@ -306,7 +306,17 @@ __global__ void __launch_bounds__(kThreads, 2)
         lo = max(lo, i - w - kstart);
         hi = min(hi, i + w + 1 - kstart);
       }
-      if (!(lo <= 0 && hi >= kKT)) {
+      // (one-sided where one bound is outside the tile: the usual case, the
+      // lower bound in a window's first tile, the upper one in its last)
+      if (lo > 0 && hi >= kKT) {
+#pragma unroll
+        for (int c = 0; c < kKT; ++c)
+          if (c < lo) sc[c] = -INFINITY;
+      } else if (lo <= 0 && hi < kKT) {
+#pragma unroll
+        for (int c = 0; c < kKT; ++c)
+          if (c >= hi) sc[c] = -INFINITY;
+      } else if (lo > 0) {
         const uint32_t span = static_cast<uint32_t>(max(hi - lo, 0));
 #pragma unroll
         for (int c = 0; c < kKT; ++c)
