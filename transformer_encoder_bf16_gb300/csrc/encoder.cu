@@ -669,9 +669,9 @@ int tune_plans(laya_enc_handle* h, Workspace* w, cudaStream_t stream) {
         break;
       }
       const Launch l{stream, h->pdl, nullptr};
-      for (int r = 0; r < 2 && e == cudaSuccess; ++r) e = launch_gemm(p, o, l);
+      for (int r = 0; r < 3 && e == cudaSuccess; ++r) e = launch_gemm(p, o, l);
       if (e == cudaSuccess) e = cudaEventRecord(e0, stream);
-      for (int r = 0; r < 6 && e == cudaSuccess; ++r) e = launch_gemm(p, o, l);
+      for (int r = 0; r < 12 && e == cudaSuccess; ++r) e = launch_gemm(p, o, l);
       if (e == cudaSuccess) e = cudaEventRecord(e1, stream);
       if (e == cudaSuccess) e = cudaEventSynchronize(e1);
       float ms = 0.f;
