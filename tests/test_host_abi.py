@@ -74,7 +74,8 @@ def test_rope_table_equals_oracle_bitwise(lib, orc, theta, bf16):
 
 @pytest.mark.parametrize("M", [1, 7, 48, 100, 256, 257, 464, 1856, 8192])
 @pytest.mark.parametrize("N,K,kind", [(3072, 1024, 0), (1024, 1024, 1), (2624, 1024, 2),
-                                      (1024, 2624, 1), (768, 256, 0), (640, 256, 2)])
+                                      (1024, 2624, 1), (768, 256, 0), (640, 256, 2),
+                                      (2624, 1024, 3), (640, 256, 3)])
 def test_linear_plan_invariants(lib, M, N, K, kind):
     for sms in (148, 152):
         nt, splits, ctas = te.linear_plan(M, K, N, kind, sms)
@@ -82,16 +83,23 @@ def test_linear_plan_invariants(lib, M, N, K, kind):
         tiles_t = -(-M // nt)
         assert tiles_t * nt >= M and (tiles_t - 1) * nt < M
         assert 1 <= splits <= min(16, K // 64)
-        tiles = tiles_t * -(-N // 128)
+        if kind == te.KIND_GEGLU_IL:
+            assert splits == 1                         # interleaved GeGLU: unsplit plans only
+        tiles = tiles_t * (N // 64 if kind == te.KIND_GEGLU_IL else -(-N // 128))
         if splits == 1:
             assert ctas == min(tiles, sms)             # persistent: one CTA per SM walks the tiles
         else:
             assert ctas == tiles * splits              # one CTA per (tile, split), clusters of `splits`
-        if M <= 512 and K >= 1024:
-            assert ctas >= sms // 3                    # short sequences keep the GPU busy
+        if M <= 512 and K >= 1024 and kind != te.KIND_GEGLU_IL:
+            # short sequences keep the GPU busy (the interleaved GeGLU has no
+            # split-K: at a handful of tokens its 41 tiles are what it has, and
+            # the forward's timing then picks the split two-tile GeGLU)
+            assert ctas >= sms // 3
 
 
 def test_linear_plan_rejects_bad_shapes(lib):
+    with pytest.raises(te.LayaError):   # interleaved GeGLU needs N a multiple of 64
+        te.linear_plan(48, 1024, 2600, te.KIND_GEGLU_IL, 152)
     with pytest.raises(te.LayaError):
         te.linear_plan(48, 100, 1024, 0, 148)      # K not a multiple of 64
     with pytest.raises(te.LayaError):
