@@ -92,7 +92,7 @@ def test_every_layer_teacher_forced(name):
     print(f"\n[layers] {name}: embedding nRMS {e0:.2e}")
     assert e0 <= NRMS_LIMIT
     worst = (0.0, 0.0, 0.0, 0.0)
-    failures = []   # every layer is checked and printed before the verdict
+    failures = []   # every layer is checked and printed before the assertion
     for l in range(L):
         got_all = states[l + 1] if l + 1 < L else final
         gots, refs, ins, row_steps = [], [], [], []
