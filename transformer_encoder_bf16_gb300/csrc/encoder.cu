@@ -44,7 +44,6 @@ namespace laya {
 namespace {
 
 constexpr int kMaxShapes = 4;
-constexpr int kAttnTcMinSeq = 128;  // sequences longer than this use the tcgen05 attention
 constexpr size_t kMaxWorkspaceBytes = 512ull << 20;
 
 struct LayerMaps {
@@ -123,7 +122,7 @@ struct laya_enc_handle {
   laya_enc_cache_stats stats = {};  // counters of the workspace / graph cache
   bool graphs = true;
   bool pdl = true;
-  bool attn_tc = true;  // attention on tcgen05 for S > kAttnTcMinSeq (false: always the mma.sync kernel, env LAYA_ATTN_MMA_SYNC=1)
+  bool attn_tc = true;  // attention on tcgen05 (false: the mma.sync kernel, env LAYA_ATTN_MMA_SYNC=1)
   bool tune = true;     // time candidate projection plans on a shape's first run (env LAYA_NO_TUNE=1: off)
   bool geglu_il = false;  // the up-projection can also run as interleaved tiles (I % 64 == 0)
   bool poisoned = false;
@@ -465,9 +464,7 @@ cudaError_t enqueue_forward(laya_enc_handle* h, Workspace* w, const RunOut& ro,
       LAYA_LAUNCH(launch_gemm(w->p_mdn, om, next(LAYA_PROF_DOWN)));
       break;
     }
-    // rows of at most one 128-query tile: the mma.sync kernel (less set-up
-    // per CTA; measured faster at 48 and 64 tokens, slower from 464 on)
-    if (h->attn_tc && w->S > kAttnTcMinSeq)
+    if (h->attn_tc)
       LAYA_LAUNCH(launch_attention_tc(w->tm_qkv_attn, w->lens, w->B, w->S, c.heads, glob ? 1 : 0,
                                       c.local_half_window, w->ctx, h->err, next(LAYA_PROF_ATTN),
                                       w->packed));
