@@ -163,6 +163,22 @@ def test_full_depth_large_every_row(name):
                          ids[b:b + 1, :L], lengths[b:b + 1])
 
 
+def test_full_depth_maximum_shape():
+    # the largest request the library takes: max_batch rows of max_seq tokens,
+    # every token valid (8192 tokens, no padding to skip); the first and the
+    # last row against the oracle, every element finite
+    model = synth.FULL
+    B, S, seed = model["max_batch"], model["max_seq"], 4
+    w, enc = encoder_for(model, seed)
+    ids, lengths = synth.make_inputs(model, B, S, seed)
+    assert int(lengths.sum()) == B * S
+    got = run_gpu(enc, ids, lengths)
+    assert np.all(np.isfinite(bf16_bits_to_f32(got)))
+    for b in (0, B - 1):
+        check_full_depth(f"max {B}x{S} row {b}", got[b:b + 1], model, w, ids[b:b + 1],
+                         lengths[b:b + 1])
+
+
 def test_invariants_bitwise():
     model, B, S, seed, lr = synth.WORKLOADS["full_4x64"]
     w, enc = encoder_for(model, seed)
