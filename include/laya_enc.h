@@ -117,6 +117,11 @@ int laya_enc_validate_config(const laya_enc_config* cfg);
 /* Creates a handle on the current CUDA device: checks the device (10.3),
  * builds the global and local RoPE tables on the host and uploads them, and
  * builds TMA descriptors over the caller's weights (no weight copy).
+ * Switches read from the environment here: LAYA_EAGER=1 (no CUDA Graphs),
+ * LAYA_NO_PDL=1 (no programmatic dependent launch), LAYA_NO_TUNE=1 (see
+ * laya_enc_run), LAYA_ATTN_MMA_SYNC=1 (attention on the mma.sync kernel
+ * instead of the tcgen05 one).  Results stay within the same tolerances
+ * under each of them.
  * *out is set to NULL on failure. */
 int laya_enc_create(const laya_enc_config* cfg, const laya_enc_weights* weights,
                     laya_enc_handle** out);
